@@ -1,0 +1,202 @@
+"""fp64 CPU oracle for block verification -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The GPU library neither imports nor
+links it, and the two share no code: the only thing both sides see are the
+seeded inputs from ``serving_sd_verify_gb300.workloads``.
+
+The arithmetic lives in ``sd_oracle.c`` (plain C99, fp64, single thread);
+this module only marshals numpy arrays through ctypes.  See that file's
+header for the passages each routine follows.
+
+Pins (tests/test_oracle_*.py) fix every routine to something other than
+itself: Philox known-answer vectors, textbook decode attention, closed forms
+(constant keys, one key), brute force on tiny shapes, the worked cycle of the
+VFlash-FM project page, the autoregressive-equivalence invariant and a
+chi-square test of the sampled rule.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_sd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_ip = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_lp = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_up = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+
+
+def build(force: bool = False) -> str:
+    """Compile sd_oracle.c into _sd_oracle.so beside it (gcc, no fast-math)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+               "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    lib.oracle_philox4x32_10_batch.argtypes = [_up, _up, _up, ctypes.c_long]
+    lib.oracle_philox4x32_10_batch.restype = None
+    lib.oracle_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                   ctypes.c_uint32, ctypes.c_uint32]
+    lib.oracle_uniform.restype = ctypes.c_double
+    lib.oracle_attention_rows.argtypes = [
+        _dp, _dp, _dp, ctypes.c_void_p, ctypes.c_void_p, _ip, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_double, ctypes.c_long, ctypes.c_long, ctypes.c_void_p, ctypes.c_long,
+        _dp, ctypes.c_void_p]
+    lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_lse_merge.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_int, _dp]
+    lib.oracle_lse_merge.restype = ctypes.c_double
+    lib.oracle_accept_greedy.argtypes = [_ip, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         _ip, _ip, ctypes.c_void_p]
+    lib.oracle_accept_greedy.restype = ctypes.c_int
+    lib.oracle_accept_sample.argtypes = [_ip, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32,
+                                         _ip, _ip, ctypes.c_void_p]
+    lib.oracle_accept_sample.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact fp64 copy of a numpy array or a CPU torch tensor (bf16 / fp32 values)."""
+    if hasattr(x, "detach"):  # torch tensor: widen on the CPU, exactly
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# --------------------------------------------------------------------------
+# Philox4x32-10
+# --------------------------------------------------------------------------
+
+def philox4x32_10(counters, key) -> np.ndarray:
+    """counters [n, 4] uint32, key [2] uint32 -> [n, 4] uint32."""
+    ctr = np.ascontiguousarray(counters, dtype=np.uint32).reshape(-1, 4)
+    k = np.ascontiguousarray(key, dtype=np.uint32).reshape(2)
+    out = np.empty_like(ctr)
+    _load().oracle_philox4x32_10_batch(ctr, k, out, ctr.shape[0])
+    return out
+
+
+def uniform(seed: int, row: int, batch: int, stream: int, offset: int) -> float:
+    return _load().oracle_uniform(seed, row, batch, stream, offset)
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def attention_rows(q, k, v, nctx, scale, *, mode=0, kb=None, vb=None, rows=None,
+                   key_range=None, return_lse=False):
+    """Exact fp64 attention for the selected flat rows (b*T + j)*Hq + h.
+
+    q [B,T,Hq,D]; k, v [B,Sc,Hkv,D]; nctx [B]; mode 0 = target verify (row j
+    sees cache keys [0, nctx+j)), mode 1 = drafter (cache keys [0, nctx) then
+    the T block keys kb, vb [B,T,Hkv,D]).  Returns out [n_rows, D] (and lse).
+    """
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    B, T, Hq, D = qd.shape
+    _, Sc, Hkv, _ = kd.shape
+    n = _i32(nctx).reshape(B)
+    kbd = _f64(kb) if kb is not None else None
+    vbd = _f64(vb) if vb is not None else None
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+    n_rows = B * T * Hq if rows_a is None else rows_a.size
+    out = np.zeros((n_rows, D), dtype=np.float64)
+    lse = np.zeros(n_rows, dtype=np.float64)
+    lo, hi = (-1, -1) if key_range is None else key_range
+    rc = _load().oracle_attention_rows(qd, kd, vd, _ptr(kbd), _ptr(vbd), n, int(mode),
+                                       B, T, Hq, Hkv, D, Sc, float(scale), int(lo), int(hi),
+                                       _ptr(rows_a), n_rows, out, _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attention_rows rejected its arguments")
+    return (out, lse) if return_lse else out
+
+
+def lse_merge(o_parts, lse_parts):
+    """o_parts [S, D], lse_parts [S] -> (out [D], merged lse)."""
+    o = _f64(o_parts)
+    l = _f64(lse_parts).reshape(-1)
+    S, D = o.shape
+    out = np.zeros(D, dtype=np.float64)
+    m = _load().oracle_lse_merge(o, l, S, D, out)
+    return out, m
+
+
+# --------------------------------------------------------------------------
+# Acceptance
+# --------------------------------------------------------------------------
+
+def accept_greedy(draft_ids, logits, return_argmax=False):
+    """draft [B,T-1] int, logits [B,T,V] -> (n_accepted [B], correction [B])."""
+    lg = _f64(logits)
+    B, T, V = lg.shape
+    d = _i32(draft_ids).reshape(B, max(T - 1, 0))
+    d = np.ascontiguousarray(d) if d.size else np.zeros(1, dtype=np.int32)
+    n = np.zeros(B, dtype=np.int32)
+    c = np.zeros(B, dtype=np.int32)
+    am = np.zeros((B, T), dtype=np.int32)
+    rc = _load().oracle_accept_greedy(d, lg, B, T, V, n, c, _ptr(am))
+    if rc != 0:
+        raise ValueError("oracle_accept_greedy rejected its arguments")
+    return (n, c, am) if return_argmax else (n, c)
+
+
+def accept_sample(draft_ids, draft_probs, logits, temperature, seed, offset=0,
+                  return_diag=False):
+    """Speculative accept / residual resample; returns (n_accepted, next_id[, diag])."""
+    lg = _f64(logits)
+    B, T, V = lg.shape
+    q = _f64(draft_probs).reshape(B, T, V)
+    d = _i32(draft_ids).reshape(B, max(T - 1, 0))
+    d = np.ascontiguousarray(d) if d.size else np.zeros(1, dtype=np.int32)
+    n = np.zeros(B, dtype=np.int32)
+    nx = np.zeros(B, dtype=np.int32)
+    diag = np.zeros((B, 2 * (T - 1) + 6), dtype=np.float64)
+    rc = _load().oracle_accept_sample(d, q, lg, B, T, V, float(temperature), int(seed),
+                                      int(offset), n, nx, _ptr(diag))
+    if rc != 0:
+        raise ValueError("oracle_accept_sample rejected its arguments")
+    return (n, nx, diag) if return_diag else (n, nx)
+
+
+def split_diag(diag, T):
+    """Name the columns of accept_sample's diag array."""
+    t1 = T - 1
+    return {
+        "u": diag[:, :t1], "ratio": diag[:, t1:2 * t1],
+        "x": diag[:, 2 * t1], "S": diag[:, 2 * t1 + 1], "c_prev": diag[:, 2 * t1 + 2],
+        "c_at": diag[:, 2 * t1 + 3], "mode": diag[:, 2 * t1 + 4], "u2": diag[:, 2 * t1 + 5],
+    }
