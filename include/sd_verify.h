@@ -1,0 +1,210 @@
+/*
+ * sd_verify.h -- C ABI of libsdverify.so: the GPU hot path of block
+ * verification in lossless draft-then-verify speculative decoding.
+ *
+ * The method ("VFlash-FM: Flow-Trained One-Pass Drafting for Video Language
+ * Models", project page, section "How VFlash-FM works" and the worked cycle
+ * in its figure): a drafter proposes a block of 16 slots -- the anchor (the
+ * last committed token) and 15 proposals -- in one forward; the frozen target
+ * scores all 16 slots in one forward over its KV cache; the proposals equal to
+ * the target's greedy picks are kept up to the first mismatch, where the
+ * target's own pick is committed instead.  The sampled variant applies the
+ * usual speculative accept/reject test ("SpecFLASH" README, inference
+ * section), so the output follows the target distribution exactly.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing and keeps no per-call state.  `workspace` is caller
+ *    memory of at least the size the matching *_workspace_size() returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work and return; SD_OK means "validated and launched".  Faults
+ *    of launched kernels surface at the caller's next synchronisation.
+ *  - Argument errors are detected on the host before anything is launched
+ *    and return SD_ERR_INVALID_ARG / SD_ERR_UNSUPPORTED / SD_ERR_WORKSPACE;
+ *    sd_last_error() then holds a one-line reason (thread-local).  No C++
+ *    exception crosses this boundary.
+ *  - Device-side guards (bounded waits, index checks) never trap: they set
+ *    the library's fault word, read with sd_fault_word().
+ *  - Tensors are row-major and contiguous unless strides are passed.
+ *  - Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef SD_VERIFY_H
+#define SD_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SD_OK = 0,
+    SD_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shape */
+    SD_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. D = 96)     */
+    SD_ERR_WORKSPACE = 3,     /* workspace missing or too small              */
+    SD_ERR_CUDA = 4           /* a CUDA runtime call failed (see sd_last_error) */
+} sd_status;
+
+typedef enum {
+    SD_BF16 = 0,              /* bfloat16 storage, fp32 arithmetic */
+    SD_FP32 = 1               /* float32 storage, fp32 arithmetic  */
+} sd_dtype;
+
+/* element strides of a [B, S, H, D] tensor whose D axis is contiguous */
+typedef struct {
+    int64_t b, s, h;
+} sd_strides;
+
+/* ------------------------------------------------------------------------
+ * Target block-verify attention (split-KV, log-sum-exp merge)
+ *
+ * Source: "VFlash-FM" project page, "How VFlash-FM works": the target
+ * verifies all 16 block slots in one forward with grouped-query attention
+ * over a KV cache allocated up front.  Slot j of the block may only see what
+ * precedes it, so row j attends to cache keys [0, ctx_len[b] + j): ctx_len
+ * counts the anchor, whose K/V sits at slot ctx_len-1; block row j's own K/V
+ * is at slot ctx_len-1+j and must already be written by the caller.  T = 1
+ * is ordinary one-token decode attention.
+ *
+ *   q        [B, T, Hq, D]  contiguous, rotary embedding already applied
+ *   k_cache, v_cache  [B, S_max, Hkv, D] with element strides `kv`; the D
+ *            axis contiguous; base addresses 16-byte aligned
+ *   ctx_len  device int32 [B], each in [1, max_ctx]
+ *   max_ctx  host upper bound of ctx_len; the cache must hold at least
+ *            max_ctx + T - 1 slots per sequence (caller's contract: slots
+ *            beyond a sequence's ctx_len + T - 1 are never read into the
+ *            result, whatever they hold)
+ *   out      device fp32 [B, T, Hq, D] contiguous
+ *   query head h reads kv head h / (Hq / Hkv)
+ *   logits are scale * q.k; softmax and accumulation in fp32
+ *   T in [1, 16]; D in {64, 128}; Hq % Hkv == 0; (Hq / Hkv) * T <= 256
+ * ------------------------------------------------------------------------ */
+sd_status sd_verify_attention(const void *q, const void *k_cache, const void *v_cache,
+                              sd_strides kv, const int32_t *ctx_len, int max_ctx,
+                              float *out, int B, int T, int Hq, int Hkv, int D,
+                              sd_dtype dtype, float scale,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+size_t sd_verify_attention_workspace_size(int B, int T, int Hq, int Hkv, int D,
+                                          int max_ctx, sd_dtype dtype);
+
+/* ------------------------------------------------------------------------
+ * Drafter block attention
+ *
+ * Source: "VFlash-FM" project page, "How VFlash-FM works" and its figure:
+ * the drafter never reads the video; its keys and values are a linear map of
+ * the hidden states the target cached for every context position, and its
+ * block (anchor + 15 mask slots) is filled in one forward, so every block
+ * query sees every context key and every block key (no causal mask).
+ *
+ *   q            [B, T, Hq, D] contiguous
+ *   k_ctx, v_ctx [B, S_ctx, Hkv, D] projected context keys / values, strides `ctx`
+ *   n_ctx        device int32 [B], context keys per sequence, each in [1, max_ctx]
+ *   k_blk, v_blk [B, T, Hkv, D] contiguous keys / values of the block slots
+ *   out          fp32 [B, T, Hq, D]
+ *   every row attends to context keys [0, n_ctx[b]) followed by the T block keys
+ *   limits as for sd_verify_attention
+ * ------------------------------------------------------------------------ */
+sd_status sd_draft_block_attention(const void *q, const void *k_ctx, const void *v_ctx,
+                                   sd_strides ctx, const int32_t *n_ctx, int max_ctx,
+                                   const void *k_blk, const void *v_blk, float *out,
+                                   int B, int T, int Hq, int Hkv, int D, sd_dtype dtype,
+                                   float scale, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, int D,
+                                               int max_ctx, sd_dtype dtype);
+
+/* ------------------------------------------------------------------------
+ * Greedy acceptance
+ *
+ * Source: "VFlash-FM" project page, worked cycle: the target keeps the
+ * proposals that equal its own greedy picks up to the first mismatch and
+ * commits its own pick there (7 accepted + 1 correction = 8 tokens).
+ *
+ *   draft_ids     device int32 [B, T-1]; draft_ids[b][j] is the proposal for
+ *                 the slot after block row j, checked against logits row j
+ *   target_logits device [B, T, V] (bf16 or fp32), contiguous
+ *   n_accepted    device int32 [B]: first j in [0, T-2] whose proposal is not
+ *                 the row's argmax, else T-1
+ *   correction_id device int32 [B]: argmax of row n_accepted (the target's
+ *                 token at the first mismatch, or the bonus token)
+ *   argmax ties go to the lowest index; values compare exactly in fp32
+ *   workspace: its first 256 bytes must be zero before the first call on it;
+ *   each completed call leaves them zero again.
+ * ------------------------------------------------------------------------ */
+sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits,
+                           int B, int T, int V, sd_dtype dtype,
+                           int32_t *n_accepted, int32_t *correction_id,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype);
+
+/* ------------------------------------------------------------------------
+ * Sampled (lossless) acceptance
+ *
+ * Source: "SpecFLASH" README, inference section: the drafted tokens are
+ * checked under the standard speculative accept/reject rule, which leaves
+ * the output distributed exactly as the target's.
+ *
+ *   p_j = softmax(target_logits[b, j] / temperature), fp32
+ *   for j = 0 .. T-2:  u = U(seed; j, b, 0, offset);
+ *                      accept draft_ids[b][j] = d iff u * q_j(d) < p_j(d)
+ *   first reject at n: u' = U(seed; n, b, 1, offset); next_id = the smallest i
+ *                      whose ascending inclusive cumulative sum of
+ *                      r = max(p_n - q_n, 0) exceeds u' * sum(r)
+ *                      (if sum(r) == 0: the same draw from p_n)
+ *   all accepted:      next_id drawn the same way from p_{T-1} with u' from row T-1
+ *   U(seed; c0, c1, c2, c3) = (word0 of Philox4x32-10 with key (seed lo32,
+ *   seed hi32) and counter (c0, c1, c2, c3)) >> 8, times 2^-24.
+ *
+ *   draft_probs  device fp32 [B, T, V], rows 0..T-2 read (the drafter's
+ *                normalised distributions)
+ *   temperature  > 0 (temperature 0 is sd_accept_greedy)
+ *   n_accepted, next_id  device int32 [B]
+ *   workspace: first 256 bytes zero before the first call; left zero.
+ * ------------------------------------------------------------------------ */
+sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs,
+                           const void *target_logits, int B, int T, int V, sd_dtype dtype,
+                           float temperature, uint64_t philox_seed, uint32_t philox_offset,
+                           int32_t *n_accepted, int32_t *next_id,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype);
+
+/* ------------------------------------------------------------------------
+ * Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
+ * 3", SC'11), the generator behind sd_accept_sample, exposed so callers can
+ * check it: counters device uint32 [n, 4], out device uint32 [n, 4],
+ * key = (key lo32, key hi32).
+ * ------------------------------------------------------------------------ */
+sd_status sd_philox4x32_10(const uint32_t *counters, uint64_t key, uint32_t *out,
+                           int64_t n, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Utilities
+ * ------------------------------------------------------------------------ */
+const char *sd_status_string(sd_status s);
+const char *sd_last_error(void);        /* reason for the last non-OK status on this thread */
+int sd_version(void);                   /* 100 * major + minor */
+
+/* Device fault word: 0 while no kernel guard fired.  Reading synchronises the
+ * current device; `clear` resets it to 0. */
+sd_status sd_fault_word(uint32_t *out, int clear);
+
+/* Attention kernel selection, process-wide, for tests and measurement:
+ * 0 = automatic (tensor-core kernel where it applies), 1 = force the
+ * CUDA-core kernel, 2 = require the tensor-core kernel (calls it cannot
+ * serve return SD_ERR_UNSUPPORTED).  Returns the previous setting. */
+int sd_set_attention_path(int path);
+
+/* Which kernel the last attention call on this thread launched:
+ * 1 = CUDA-core split kernel, 2 = tensor-core split kernel; and its split count. */
+int sd_last_attention_path(int *n_splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_VERIFY_H */

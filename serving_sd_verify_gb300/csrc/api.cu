@@ -1,0 +1,368 @@
+// C-ABI layer of libsdverify: argument validation on the host, workspace
+// layout, kernel selection and launch.  Declarations and the passages each
+// call follows are in include/sd_verify.h.
+#include <cuda_runtime.h>
+
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "internal.h"
+
+// device fault word, set by kernel guards (never a trap)
+__device__ unsigned int g_sd_fault_word;
+
+namespace sdv {
+
+namespace {
+
+thread_local char g_err[512] = "";
+thread_local int g_last_path = 0;
+thread_local int g_last_splits = 0;
+std::atomic<int> g_force_path{0};
+
+constexpr size_t kHeader = 256;  // counters; zero between calls
+constexpr int kMaxDevices = 64;
+
+sd_status fail(sd_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+sd_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(SD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+unsigned int *fault_ptr() {
+    static unsigned int *ptrs[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_sd_fault_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned int *>(p);
+    }
+    return ptrs[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t esize(sd_dtype dt) { return dt == SD_BF16 ? 2 : 4; }
+
+// ----------------------------------------------------------------------------
+// attention planning
+// ----------------------------------------------------------------------------
+struct AttnPlan {
+    int path;           // 1 CUDA-core, 2 tensor-core
+    int n_splits, keys_per_split;
+};
+
+// keys of the longest sequence's key space
+int max_keys(int mode, int max_ctx, int T) { return mode == 0 ? max_ctx + T - 1 : max_ctx + T; }
+
+AttnPlan plan_attention(const AttnParams &p, int path) {
+    const int sms = device_sm_count();
+    const int N = max_keys(p.mode, p.max_ctx, p.T);
+    const int units = p.B * p.Hkv;
+    AttnPlan pl;
+    pl.path = path;
+    int ctas_per_sm, min_keys, gran;
+    if (path == 2) { ctas_per_sm = 1; min_keys = 4 * kTileKeys; gran = kTileKeys; }
+    else { ctas_per_sm = 2; min_keys = 128; gran = 32; }
+    const int target = std::max(1, sms * ctas_per_sm);
+    int splits = (target + units - 1) / units;
+    splits = std::max(1, std::min(splits, (N + min_keys - 1) / min_keys));
+    int kps = (N + splits - 1) / splits;
+    kps = (kps + gran - 1) / gran * gran;
+    pl.keys_per_split = kps;
+    pl.n_splits = (N + kps - 1) / kps;
+    return pl;
+}
+
+size_t attn_workspace(int B, int T, int Hq, int D, int n_splits) {
+    const size_t rows = (size_t)B * T * Hq;
+    return kHeader + align_up((size_t)n_splits * rows * D * sizeof(float), 256) +
+           align_up((size_t)n_splits * rows * sizeof(float), 256);
+}
+
+sd_status validate_attention(const AttnParams &p) {
+    if (!p.q || !p.kc || !p.vc || !p.nctx || !p.out)
+        return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (p.mode == 1 && (!p.kb || !p.vb)) return fail(SD_ERR_INVALID_ARG, "null block key/value pointer");
+    if (p.B < 1 || p.T < 1 || p.T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    if (p.Hq < 1 || p.Hkv < 1 || p.Hq % p.Hkv) return fail(SD_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+    if (p.D != 64 && p.D != 128) return fail(SD_ERR_UNSUPPORTED, "D must be 64 or 128");
+    if (p.dt != SD_BF16 && p.dt != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if ((p.Hq / p.Hkv) * p.T > 256) return fail(SD_ERR_UNSUPPORTED, "(Hq/Hkv)*T must be <= 256");
+    if (p.max_ctx < 1) return fail(SD_ERR_INVALID_ARG, "max_ctx must be >= 1");
+    if (!(p.scale == p.scale)) return fail(SD_ERR_INVALID_ARG, "scale is NaN");
+    const size_t es = esize(p.dt);
+    if (!aligned16(p.q) || !aligned16(p.kc) || !aligned16(p.vc) || !aligned16(p.out) ||
+        (p.mode == 1 && (!aligned16(p.kb) || !aligned16(p.vb))))
+        return fail(SD_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+    if (p.kv.s < p.D || p.kv.h < p.D || p.kv.b < 1)
+        return fail(SD_ERR_INVALID_ARG, "cache strides must not overlap the D axis");
+    if (((size_t)p.kv.b * es) % 16 || ((size_t)p.kv.s * es) % 16 || ((size_t)p.kv.h * es) % 16)
+        return fail(SD_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+    return SD_OK;
+}
+
+sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t st) {
+    sd_status v = validate_attention(p);
+    if (v != SD_OK) return v;
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    const int force = g_force_path.load();
+    int path;
+    if (force == 1) path = 1;
+    else if (attn_tc_supported(p)) path = 2;
+    else if (force == 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
+    else path = 1;
+    AttnPlan pl = plan_attention(p, path);
+    const size_t need = attn_workspace(p.B, p.T, p.Hq, p.D, pl.n_splits);
+    if (!ws || ws_bytes < need)
+        return fail(SD_ERR_WORKSPACE, "attention workspace too small: need %zu bytes, got %zu", need, ws_bytes);
+    if (!aligned16(ws)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const size_t rows = (size_t)p.B * p.T * p.Hq;
+    char *w = static_cast<char *>(ws) + kHeader;
+    p.o_part = reinterpret_cast<float *>(w);
+    p.lse_part = reinterpret_cast<float *>(w + align_up((size_t)pl.n_splits * rows * p.D * sizeof(float), 256));
+    p.n_splits = pl.n_splits;
+    p.keys_per_split = pl.keys_per_split;
+    cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
+    e = launch_lse_merge(p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attention merge kernel launch");
+    g_last_path = path;
+    g_last_splits = pl.n_splits;
+    return SD_OK;
+}
+
+size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max_ctx, sd_dtype dt) {
+    if (B < 1 || T < 1 || T > kMaxT || Hq < 1 || Hkv < 1 || max_ctx < 1 || (D != 64 && D != 128)) return 0;
+    AttnParams p = {};
+    p.mode = mode; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dt; p.max_ctx = max_ctx;
+    size_t need = attn_workspace(B, T, Hq, D, plan_attention(p, 1).n_splits);
+    need = std::max(need, attn_workspace(B, T, Hq, D, plan_attention(p, 2).n_splits));
+    return need;
+}
+
+// ----------------------------------------------------------------------------
+// acceptance planning
+// ----------------------------------------------------------------------------
+int accept_chunk(int rows, int V) {
+    const int sms = device_sm_count();
+    const long target = 4L * sms;  // CTAs
+    long chunk = ((long)rows * V + target - 1) / target;
+    chunk = std::max(2048L, std::min(chunk, 16384L));
+    chunk = (chunk + 7) / 8 * 8;
+    return (int)std::min<long>(chunk, (long)V);
+}
+
+size_t greedy_ws(int B, int T, int V, int chunk) {
+    const size_t parts = (size_t)B * T * ((V + chunk - 1) / chunk);
+    return kHeader + align_up(parts * sizeof(float), 256) + align_up(parts * sizeof(int), 256);
+}
+
+size_t sample_ws(int B, int T, int V, int chunk) {
+    const int nc = (V + chunk - 1) / chunk;
+    const size_t parts = (size_t)B * T * nc;
+    return kHeader + 2 * align_up(parts * sizeof(float), 256) + align_up((size_t)B * sizeof(float4), 256) +
+           2 * align_up((size_t)B * nc * sizeof(double), 256);
+}
+
+}  // namespace
+
+int device_sm_count() {
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace sdv
+
+using namespace sdv;
+
+extern "C" {
+
+const char *sd_status_string(sd_status s) {
+    switch (s) {
+        case SD_OK: return "SD_OK";
+        case SD_ERR_INVALID_ARG: return "SD_ERR_INVALID_ARG";
+        case SD_ERR_UNSUPPORTED: return "SD_ERR_UNSUPPORTED";
+        case SD_ERR_WORKSPACE: return "SD_ERR_WORKSPACE";
+        case SD_ERR_CUDA: return "SD_ERR_CUDA";
+    }
+    return "SD_ERR_UNKNOWN";
+}
+
+const char *sd_last_error(void) { return g_err; }
+
+int sd_version(void) { return 100; }
+
+int sd_set_attention_path(int path) {
+    if (path < 0 || path > 2) path = 0;
+    return g_force_path.exchange(path);
+}
+
+int sd_last_attention_path(int *n_splits) {
+    if (n_splits) *n_splits = g_last_splits;
+    return g_last_path;
+}
+
+sd_status sd_fault_word(uint32_t *out, int clear) {
+    if (!out) return fail(SD_ERR_INVALID_ARG, "null output pointer");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_sd_fault_word, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the fault word");
+    *out = v;
+    if (clear) {
+        const unsigned int z = 0;
+        e = cudaMemcpyToSymbol(g_sd_fault_word, &z, sizeof z);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the fault word");
+    }
+    return SD_OK;
+}
+
+sd_status sd_verify_attention(const void *q, const void *k_cache, const void *v_cache, sd_strides kv,
+                              const int32_t *ctx_len, int max_ctx, float *out, int B, int T, int Hq,
+                              int Hkv, int D, sd_dtype dtype, float scale, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    AttnParams p = {};
+    p.q = q; p.kc = k_cache; p.vc = v_cache; p.kv = kv; p.nctx = ctx_len; p.mode = 0;
+    p.out = out; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dtype; p.scale = scale;
+    p.max_ctx = max_ctx;
+    p.fault = fault_ptr();
+    return run_attention(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t sd_verify_attention_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_ctx, sd_dtype dtype) {
+    return attention_ws_size(0, B, T, Hq, Hkv, D, max_ctx, dtype);
+}
+
+sd_status sd_draft_block_attention(const void *q, const void *k_ctx, const void *v_ctx, sd_strides ctx,
+                                   const int32_t *n_ctx, int max_ctx, const void *k_blk, const void *v_blk,
+                                   float *out, int B, int T, int Hq, int Hkv, int D, sd_dtype dtype,
+                                   float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    AttnParams p = {};
+    p.q = q; p.kc = k_ctx; p.vc = v_ctx; p.kv = ctx; p.nctx = n_ctx; p.mode = 1;
+    p.kb = k_blk; p.vb = v_blk;
+    p.out = out; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dtype; p.scale = scale;
+    p.max_ctx = max_ctx;
+    p.fault = fault_ptr();
+    return run_attention(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_ctx,
+                                               sd_dtype dtype) {
+    return attention_ws_size(1, B, T, Hq, Hkv, D, max_ctx, dtype);
+}
+
+size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
+    (void)dtype;
+    if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
+    return greedy_ws(B, T, V, accept_chunk(B * T, V));
+}
+
+sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, int B, int T, int V,
+                           sd_dtype dtype, int32_t *n_accepted, int32_t *correction_id, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (B < 1 || T < 1 || T > kMaxT || V < 1) return fail(SD_ERR_INVALID_ARG, "need B >= 1, T in [1, 16], V >= 1");
+    if (!target_logits || !n_accepted || !correction_id || (T > 1 && !draft_ids))
+        return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (dtype != SD_BF16 && dtype != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if ((reinterpret_cast<uintptr_t>(target_logits) % esize(dtype)) != 0)
+        return fail(SD_ERR_INVALID_ARG, "logits pointer not aligned to its element size");
+    GreedyParams p = {};
+    p.draft = draft_ids; p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
+    p.n_acc = n_accepted; p.corr = correction_id;
+    p.chunk = accept_chunk(B * T, V);
+    p.n_chunks = (V + p.chunk - 1) / p.chunk;
+    const size_t need = greedy_ws(B, T, V, p.chunk);
+    if (!workspace || workspace_bytes < need)
+        return fail(SD_ERR_WORKSPACE, "greedy workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    char *w = static_cast<char *>(workspace);
+    const size_t parts = (size_t)B * T * p.n_chunks;
+    p.counter = reinterpret_cast<unsigned int *>(w);
+    p.pval = reinterpret_cast<float *>(w + kHeader);
+    p.pidx = reinterpret_cast<int *>(w + kHeader + align_up(parts * sizeof(float), 256));
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_accept_greedy(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "greedy accept launch");
+    return SD_OK;
+}
+
+size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype) {
+    (void)dtype;
+    if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
+    return sample_ws(B, T, V, accept_chunk(B * T, V));
+}
+
+sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, const void *target_logits,
+                           int B, int T, int V, sd_dtype dtype, float temperature, uint64_t philox_seed,
+                           uint32_t philox_offset, int32_t *n_accepted, int32_t *next_id, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (B < 1 || T < 1 || T > kMaxT || V < 1) return fail(SD_ERR_INVALID_ARG, "need B >= 1, T in [1, 16], V >= 1");
+    if (!target_logits || !draft_probs || !n_accepted || !next_id || (T > 1 && !draft_ids))
+        return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (dtype != SD_BF16 && dtype != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if (!(temperature > 0.f) || temperature == INFINITY)
+        return fail(SD_ERR_INVALID_ARG, "temperature must be finite and > 0 (use sd_accept_greedy for 0)");
+    if ((reinterpret_cast<uintptr_t>(target_logits) % esize(dtype)) != 0 ||
+        (reinterpret_cast<uintptr_t>(draft_probs) % 4) != 0)
+        return fail(SD_ERR_INVALID_ARG, "tensor pointer not aligned to its element size");
+    SampleParams p = {};
+    p.draft = draft_ids; p.q = draft_probs; p.logits = target_logits; p.B = B; p.T = T; p.V = V;
+    p.dt = dtype; p.inv_tau = 1.0f / temperature; p.seed = philox_seed; p.offset = philox_offset;
+    p.n_acc = n_accepted; p.next_id = next_id;
+    p.chunk = accept_chunk(B * T, V);
+    p.n_chunks = (V + p.chunk - 1) / p.chunk;
+    const size_t need = sample_ws(B, T, V, p.chunk);
+    if (!workspace || workspace_bytes < need)
+        return fail(SD_ERR_WORKSPACE, "sample workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    char *w = static_cast<char *>(workspace);
+    const size_t parts = (size_t)B * T * p.n_chunks;
+    size_t off = kHeader;
+    p.counters = reinterpret_cast<unsigned int *>(w);
+    p.pm = reinterpret_cast<float *>(w + off); off += align_up(parts * sizeof(float), 256);
+    p.pz = reinterpret_cast<float *>(w + off); off += align_up(parts * sizeof(float), 256);
+    p.state = reinterpret_cast<float4 *>(w + off); off += align_up((size_t)B * sizeof(float4), 256);
+    p.rs = reinterpret_cast<double *>(w + off); off += align_up((size_t)B * p.n_chunks * sizeof(double), 256);
+    p.ps = reinterpret_cast<double *>(w + off);
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_accept_sample(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sampled accept launch");
+    return SD_OK;
+}
+
+sd_status sd_philox4x32_10(const uint32_t *counters, uint64_t key, uint32_t *out, int64_t n, void *stream) {
+    if (n < 0) return fail(SD_ERR_INVALID_ARG, "n must be >= 0");
+    if (n == 0) return SD_OK;
+    if (!counters || !out) return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(counters) || !aligned16(out)) return fail(SD_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    if (n > (int64_t)1 << 40) return fail(SD_ERR_INVALID_ARG, "n too large");
+    cudaError_t e = launch_philox(counters, key, out, n, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "philox launch");
+    return SD_OK;
+}
+
+}  // extern "C"

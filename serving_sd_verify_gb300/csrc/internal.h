@@ -1,0 +1,95 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+// Not installed; callers use include/sd_verify.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sd_verify.h"
+
+namespace sdv {
+
+// Fault word bits set by device-side guards (never a trap).
+enum FaultBits : unsigned int {
+    FAULT_BAD_CTX = 1u << 0,        // ctx_len / n_ctx outside [1, max_ctx]
+    FAULT_BAD_DRAFT_ID = 1u << 1,   // draft id outside [0, V)
+    FAULT_NAN_ROW = 1u << 2,        // argmax row without any ordered value (NaN)
+    FAULT_WAIT_TIMEOUT = 1u << 3,   // a bounded mbarrier wait gave up
+    FAULT_TMEM_ALLOC = 1u << 4,     // tensor-memory allocation returned out of range
+};
+
+constexpr int kMaxT = 16;           // block rows (anchor + 15 proposals)
+constexpr int kTileKeys = 64;       // keys per tile, shared by both attention kernels
+
+// Attention launch description (both the target verify and the drafter).
+//  key index space of sequence b:
+//   mode 0 (verify):  N_b = nctx[b] + T - 1 cache keys; row j sees [0, nctx[b] + j)
+//   mode 1 (drafter): N_b = nctx[b] + T; keys [0, nctx[b]) from the cache,
+//                     [nctx[b], N_b) from the block tensors; every row sees all
+//  split s covers keys [s * keys_per_split, (s + 1) * keys_per_split) of that space.
+struct AttnParams {
+    const void *q;                  // [B, T, Hq, D]
+    const void *kc, *vc;            // [B, S, Hkv, D] with strides kv
+    sd_strides kv;
+    const int32_t *nctx;            // [B]
+    int mode;
+    const void *kb, *vb;            // [B, T, Hkv, D] (mode 1)
+    float *out;                     // [B, T, Hq, D]
+    int B, T, Hq, Hkv, D;
+    sd_dtype dt;
+    float scale;
+    int max_ctx;                    // host bound of nctx
+    int s_rows;                     // cache slots available per sequence (derived bound)
+    int n_splits, keys_per_split;
+    float *o_part;                  // [n_splits, B*T*Hq, D]
+    float *lse_part;                // [n_splits, B*T*Hq]
+    unsigned int *fault;
+};
+
+// kernel launchers: return the launch error (cudaSuccess when enqueued)
+cudaError_t launch_attn_generic(const AttnParams &p, cudaStream_t st);
+cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
+cudaError_t launch_lse_merge(const AttnParams &p, cudaStream_t st);
+bool attn_tc_supported(const AttnParams &p);
+size_t attn_tc_smem_bytes(const AttnParams &p);
+
+struct GreedyParams {
+    const int32_t *draft;
+    const void *logits;
+    int B, T, V;
+    sd_dtype dt;
+    int32_t *n_acc, *corr;
+    int chunk, n_chunks;
+    unsigned int *counter;
+    float *pval;
+    int *pidx;
+    unsigned int *fault;
+};
+cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st);
+
+struct SampleParams {
+    const int32_t *draft;
+    const float *q;
+    const void *logits;
+    int B, T, V;
+    sd_dtype dt;
+    float inv_tau;
+    uint64_t seed;
+    uint32_t offset;
+    int32_t *n_acc, *next_id;
+    int chunk, n_chunks;
+    unsigned int *counters;         // [2]
+    float *pm, *pz;                 // [B*T, n_chunks] chunk max and sum of exp
+    float4 *state;                  // [B]: (n as int bits, M, Z, unused)
+    double *rs, *ps;                // [B, n_chunks] residual / p chunk sums
+    unsigned int *fault;
+};
+cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);
+
+cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int64_t n,
+                          cudaStream_t st);
+
+int device_sm_count();              // SMs of the current device (cached)
+
+}  // namespace sdv

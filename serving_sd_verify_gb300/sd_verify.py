@@ -1,0 +1,246 @@
+"""Thin Python binding of libsdverify.so (ctypes).
+
+Argument marshalling only: every function reads shapes, strides and device
+pointers off torch tensors and calls the C entry point of the same name (see
+include/sd_verify.h for what each computes and its contract).  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.  If
+the shared library has not been built, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdverify.so")
+
+SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_WORKSPACE, SD_ERR_CUDA = range(5)
+SD_BF16, SD_FP32 = 0, 1
+
+# exported symbols, in header order
+SYMBOLS = [
+    "sd_verify_attention", "sd_verify_attention_workspace_size",
+    "sd_draft_block_attention", "sd_draft_block_attention_workspace_size",
+    "sd_accept_greedy", "sd_accept_greedy_workspace_size",
+    "sd_accept_sample", "sd_accept_sample_workspace_size",
+    "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
+    "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path",
+]
+
+
+class SdError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_status_name(status)}: {msg}")
+        self.status = status
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("s", ctypes.c_int64), ("h", ctypes.c_int64)]
+
+
+_lib = None
+_vp, _i, _sz, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+
+
+def load():
+    """Load the shared library (raises if it is missing: build it with build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: run serving_sd_verify_gb300.build.build() "
+                           "(nvcc, sm_103a) first; there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.sd_verify_attention.argtypes = [_vp, _vp, _vp, Strides, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                        _f, _vp, _sz, _vp]
+    lib.sd_verify_attention.restype = _i
+    lib.sd_verify_attention_workspace_size.argtypes = [_i] * 7
+    lib.sd_verify_attention_workspace_size.restype = _sz
+    lib.sd_draft_block_attention.argtypes = [_vp, _vp, _vp, Strides, _vp, _i, _vp, _vp, _vp,
+                                             _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+    lib.sd_draft_block_attention.restype = _i
+    lib.sd_draft_block_attention_workspace_size.argtypes = [_i] * 7
+    lib.sd_draft_block_attention_workspace_size.restype = _sz
+    lib.sd_accept_greedy.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]
+    lib.sd_accept_greedy.restype = _i
+    lib.sd_accept_greedy_workspace_size.argtypes = [_i] * 4
+    lib.sd_accept_greedy_workspace_size.restype = _sz
+    lib.sd_accept_sample.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, ctypes.c_uint64,
+                                     ctypes.c_uint32, _vp, _vp, _vp, _sz, _vp]
+    lib.sd_accept_sample.restype = _i
+    lib.sd_accept_sample_workspace_size.argtypes = [_i] * 4
+    lib.sd_accept_sample_workspace_size.restype = _sz
+    lib.sd_philox4x32_10.argtypes = [_vp, ctypes.c_uint64, _vp, ctypes.c_int64, _vp]
+    lib.sd_philox4x32_10.restype = _i
+    lib.sd_status_string.argtypes = [_i]
+    lib.sd_status_string.restype = ctypes.c_char_p
+    lib.sd_last_error.argtypes = []
+    lib.sd_last_error.restype = ctypes.c_char_p
+    lib.sd_version.argtypes = []
+    lib.sd_version.restype = _i
+    lib.sd_fault_word.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i]
+    lib.sd_fault_word.restype = _i
+    lib.sd_set_attention_path.argtypes = [_i]
+    lib.sd_set_attention_path.restype = _i
+    lib.sd_last_attention_path.argtypes = [ctypes.POINTER(_i)]
+    lib.sd_last_attention_path.restype = _i
+    _lib = lib
+    return lib
+
+
+def _status_name(s: int) -> str:
+    try:
+        return load().sd_status_string(s).decode()
+    except Exception:  # library not loadable: still name the code
+        return f"status {s}"
+
+
+def _check(status: int):
+    if status != SD_OK:
+        raise SdError(status, load().sd_last_error().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SD_BF16
+    if t.dtype == torch.float32:
+        return SD_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (device memory)")
+
+
+def _kv_strides(k: torch.Tensor) -> Strides:
+    if k.stride(3) != 1:
+        raise ValueError("the D axis of the cache must be contiguous")
+    return Strides(k.stride(0), k.stride(1), k.stride(2))
+
+
+# --------------------------------------------------------------------------
+# workspace sizes
+# --------------------------------------------------------------------------
+
+def sd_verify_attention_workspace_size(B, T, Hq, Hkv, D, max_ctx, dtype=SD_BF16) -> int:
+    return load().sd_verify_attention_workspace_size(B, T, Hq, Hkv, D, max_ctx, dtype)
+
+
+def sd_draft_block_attention_workspace_size(B, T, Hq, Hkv, D, max_ctx, dtype=SD_BF16) -> int:
+    return load().sd_draft_block_attention_workspace_size(B, T, Hq, Hkv, D, max_ctx, dtype)
+
+
+def sd_accept_greedy_workspace_size(B, T, V, dtype=SD_BF16) -> int:
+    return load().sd_accept_greedy_workspace_size(B, T, V, dtype)
+
+
+def sd_accept_sample_workspace_size(B, T, V, dtype=SD_BF16) -> int:
+    return load().sd_accept_sample_workspace_size(B, T, V, dtype)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled device workspace (the acceptance calls need the first 256 bytes zero)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------
+
+def sd_verify_attention(q, k_cache, v_cache, ctx_len, max_ctx, out, scale, ws, stream=None):
+    """q [B,T,Hq,D]; k_cache/v_cache [B,S,Hkv,D]; ctx_len int32 [B]; out fp32 [B,T,Hq,D]."""
+    _need_cuda(q, k_cache, v_cache, ctx_len, out, ws)
+    B, T, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    if not q.is_contiguous() or not out.is_contiguous() or out.dtype != torch.float32:
+        raise ValueError("q and out must be contiguous; out fp32")
+    if ctx_len.dtype != torch.int32 or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("ctx_len int32; q, k_cache, v_cache of one dtype")
+    if k_cache.stride() != v_cache.stride():
+        raise ValueError("k_cache and v_cache must share strides")
+    _check(load().sd_verify_attention(_p(q), _p(k_cache), _p(v_cache), _kv_strides(k_cache), _p(ctx_len),
+                                      int(max_ctx), _p(out), B, T, Hq, Hkv, D, _dt(q), float(scale),
+                                      _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sd_draft_block_attention(q, k_ctx, v_ctx, n_ctx, max_ctx, k_blk, v_blk, out, scale, ws,
+                             stream=None):
+    """q [B,T,Hq,D]; k_ctx/v_ctx [B,S,Hkv,D]; n_ctx int32 [B]; k_blk/v_blk [B,T,Hkv,D]."""
+    _need_cuda(q, k_ctx, v_ctx, n_ctx, k_blk, v_blk, out, ws)
+    B, T, Hq, D = q.shape
+    Hkv = k_ctx.shape[2]
+    if not (q.is_contiguous() and out.is_contiguous() and k_blk.is_contiguous() and v_blk.is_contiguous()):
+        raise ValueError("q, out, k_blk, v_blk must be contiguous")
+    if out.dtype != torch.float32 or n_ctx.dtype != torch.int32:
+        raise ValueError("out fp32, n_ctx int32")
+    if k_ctx.stride() != v_ctx.stride():
+        raise ValueError("k_ctx and v_ctx must share strides")
+    _check(load().sd_draft_block_attention(_p(q), _p(k_ctx), _p(v_ctx), _kv_strides(k_ctx), _p(n_ctx),
+                                           int(max_ctx), _p(k_blk), _p(v_blk), _p(out), B, T, Hq, Hkv,
+                                           D, _dt(q), float(scale), _p(ws), ws.numel() * ws.element_size(),
+                                           _stream(stream)))
+
+
+def sd_accept_greedy(draft_ids, target_logits, n_accepted, correction_id, ws, stream=None):
+    """draft_ids int32 [B,T-1]; target_logits [B,T,V]; outputs int32 [B]."""
+    _need_cuda(draft_ids, target_logits, n_accepted, correction_id, ws)
+    B, T, V = target_logits.shape
+    if not target_logits.is_contiguous() or not draft_ids.is_contiguous():
+        raise ValueError("logits and draft ids must be contiguous")
+    if draft_ids.dtype != torch.int32 or n_accepted.dtype != torch.int32 or correction_id.dtype != torch.int32:
+        raise ValueError("ids are int32")
+    _check(load().sd_accept_greedy(_p(draft_ids), _p(target_logits), B, T, V, _dt(target_logits),
+                                   _p(n_accepted), _p(correction_id), _p(ws), ws.numel() * ws.element_size(),
+                                   _stream(stream)))
+
+
+def sd_accept_sample(draft_ids, draft_probs, target_logits, temperature, philox_seed, philox_offset,
+                     n_accepted, next_id, ws, stream=None):
+    """draft_ids int32 [B,T-1]; draft_probs fp32 [B,T,V]; target_logits [B,T,V]."""
+    _need_cuda(draft_ids, draft_probs, target_logits, n_accepted, next_id, ws)
+    B, T, V = target_logits.shape
+    if not (target_logits.is_contiguous() and draft_ids.is_contiguous() and draft_probs.is_contiguous()):
+        raise ValueError("inputs must be contiguous")
+    if draft_probs.dtype != torch.float32 or draft_ids.dtype != torch.int32:
+        raise ValueError("draft_probs fp32, draft_ids int32")
+    _check(load().sd_accept_sample(_p(draft_ids), _p(draft_probs), _p(target_logits), B, T, V,
+                                   _dt(target_logits), float(temperature), int(philox_seed),
+                                   int(philox_offset), _p(n_accepted), _p(next_id), _p(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sd_philox4x32_10(counters, key, out, stream=None):
+    """counters uint32-as-int32 [n,4] device, out same shape."""
+    _need_cuda(counters, out)
+    n = counters.shape[0]
+    _check(load().sd_philox4x32_10(_p(counters), int(key), _p(out), n, _stream(stream)))
+
+
+def sd_fault_word(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _check(load().sd_fault_word(ctypes.byref(v), 1 if clear else 0))
+    return v.value
+
+
+def sd_set_attention_path(path: int) -> int:
+    return load().sd_set_attention_path(int(path))
+
+
+def sd_last_attention_path():
+    n = ctypes.c_int(0)
+    path = load().sd_last_attention_path(ctypes.byref(n))
+    return path, n.value

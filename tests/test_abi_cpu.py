@@ -1,0 +1,118 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports
+every entry point include/*.h declares, and rejects bad arguments on the host
+(status codes, no launch).  No compute call is made here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def S():
+    from serving_sd_verify_gb300 import build, sd_verify
+    build.build()
+    sd_verify.load()
+    return sd_verify
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"(?:^|\n)\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(sd_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("sd_verify_attention", "sd_draft_block_attention", "sd_accept_greedy", "sd_accept_sample"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(S):
+    lib = ctypes.CDLL(S.LIB_PATH)
+    missing = [n for n in sorted(declared_functions()) if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(S.SYMBOLS) == declared_functions()
+
+
+def test_status_strings_and_version(S):
+    lib = S.load()
+    assert lib.sd_version() >= 100
+    for code, name in enumerate(["SD_OK", "SD_ERR_INVALID_ARG", "SD_ERR_UNSUPPORTED",
+                                 "SD_ERR_WORKSPACE", "SD_ERR_CUDA"]):
+        assert lib.sd_status_string(code).decode() == name
+
+
+def test_host_validation_rejects_bad_arguments(S):
+    lib = S.load()
+    st = S.Strides(100 * 4 * 128, 4 * 128, 128)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    # null q
+    r = lib.sd_verify_attention(None, fake, fake, st, fake, 100, fake, 1, 16, 28, 4, 128, 0, 1.0, fake,
+                                1 << 30, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # T out of range
+    r = lib.sd_verify_attention(fake, fake, fake, st, fake, 100, fake, 1, 17, 28, 4, 128, 0, 1.0, fake,
+                                1 << 30, None)
+    assert r == S.SD_ERR_INVALID_ARG and b"T in [1, 16]" in lib.sd_last_error()
+    # Hq not a multiple of Hkv
+    r = lib.sd_verify_attention(fake, fake, fake, st, fake, 100, fake, 1, 16, 27, 4, 128, 0, 1.0, fake,
+                                1 << 30, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # unsupported head dim
+    r = lib.sd_verify_attention(fake, fake, fake, st, fake, 100, fake, 1, 16, 28, 4, 96, 0, 1.0, fake,
+                                1 << 30, None)
+    assert r == S.SD_ERR_UNSUPPORTED
+    # misaligned cache stride (bf16, 8 bytes)
+    bad = S.Strides(100 * 4 * 128, 4, 128)
+    r = lib.sd_verify_attention(fake, fake, fake, bad, fake, 100, fake, 1, 16, 28, 4, 128, 0, 1.0, fake,
+                                1 << 30, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # drafter without block tensors
+    r = lib.sd_draft_block_attention(fake, fake, fake, st, fake, 100, None, None, fake, 1, 16, 28, 4, 128, 0,
+                                     1.0, fake, 1 << 30, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # greedy: V < 1, null logits
+    assert lib.sd_accept_greedy(fake, fake, 1, 16, 0, 0, fake, fake, fake, 1 << 20, None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_accept_greedy(fake, None, 1, 16, 10, 0, fake, fake, fake, 1 << 20, None) == S.SD_ERR_INVALID_ARG
+    # sample: temperature must be > 0
+    assert lib.sd_accept_sample(fake, fake, fake, 1, 16, 10, 0, 0.0, 1, 0, fake, fake, fake, 1 << 20,
+                                None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_accept_sample(fake, fake, fake, 1, 16, 10, 0, float("nan"), 1, 0, fake, fake, fake, 1 << 20,
+                                None) == S.SD_ERR_INVALID_ARG
+    # philox: negative n
+    assert lib.sd_philox4x32_10(fake, 1, fake, -1, None) == S.SD_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_are_positive_and_monotone(S):
+    a = S.sd_verify_attention_workspace_size(1, 16, 28, 4, 128, 25_119)
+    b = S.sd_verify_attention_workspace_size(8, 16, 28, 4, 128, 32_768)
+    assert 256 < a <= b
+    assert S.sd_draft_block_attention_workspace_size(1, 16, 28, 4, 128, 25_119) > 256
+    assert S.sd_accept_greedy_workspace_size(1, 16, 152_064) > 256
+    assert S.sd_accept_sample_workspace_size(4, 16, 152_064) > 256
+    assert S.sd_verify_attention_workspace_size(1, 17, 28, 4, 128, 100) == 0
+
+
+def test_binding_refuses_cpu_tensors(S):
+    import torch
+    q = torch.zeros(1, 16, 28, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        S.sd_verify_attention(q, q, q, torch.zeros(1, dtype=torch.int32), 10, q.float(), 1.0,
+                              torch.zeros(8, dtype=torch.uint8))
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    from serving_sd_verify_gb300 import sd_verify
+    monkeypatch.setattr(sd_verify, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(sd_verify, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        sd_verify.load()

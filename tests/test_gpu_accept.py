@@ -1,0 +1,209 @@
+"""GPU parity of the acceptance kernels and Philox against the fp64 oracle.
+
+Greedy: accept lengths and correction ids bit-exact (argmax compared on the
+exact stored values, ties to the lowest index).  Sampled: ids and lengths
+bit-exact except where the oracle's own diagnostics show the decision sits
+within 1e-6 of a threshold (|u - p/q| < 1e-6, or u'*S within 1e-6*S of a
+cumulative-sum boundary).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from serving_sd_verify_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+EXCUSE = 1e-6
+
+
+@pytest.fixture(scope="module")
+def S():
+    from serving_sd_verify_gb300 import build, sd_verify
+    build.build()
+    sd_verify.load()
+    return sd_verify
+
+
+def run_greedy(S, draft, logits):
+    B, T, V = logits.shape
+    dl = logits.cuda()
+    dd = draft.to(torch.int32).cuda().contiguous()
+    n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    c = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    ws = S.workspace(S.sd_accept_greedy_workspace_size(B, T, V, S._dt(logits)))
+    S.sd_accept_greedy(dd, dl, n, c, ws)
+    torch.cuda.synchronize()
+    assert int(ws[:256].abs().sum()) == 0, "counter block not returned to zero"
+    return n.cpu().numpy(), c.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,T,V,dtype", [
+    (1, 16, 1000, torch.float32),
+    (1, 16, 152_064, torch.bfloat16),
+    (3, 16, 5_001, torch.bfloat16),     # odd V: rows not 16-byte aligned
+    (2, 7, 777, torch.float32),
+    (20, 16, 3_000, torch.bfloat16),    # more rows than one finisher window
+    (5, 1, 4_096, torch.bfloat16),      # block of one = greedy decode
+    (4, 3, 13, torch.bfloat16),         # tiny vocab, ragged window
+])
+def test_greedy_matches_oracle(S, B, T, V, dtype):
+    inp = W.greedy_inputs(B=B, T=T, V=V, dtype=dtype, seed=B * 1000 + T)
+    n, c = run_greedy(S, inp["draft"], inp["logits"])
+    on, oc = oracle.accept_greedy(inp["draft"], inp["logits"])
+    assert n.tolist() == on.tolist()
+    assert c.tolist() == oc.tolist()
+    assert n.tolist() == [min(k, T - 1) for k in inp["k"]]
+
+
+def test_greedy_ties_lowest_index(S):
+    V = 10_000
+    lg = torch.zeros(2, 16, V, dtype=torch.bfloat16)
+    lg[:, :, [17, 5000, 9999]] = 3.0  # triple tie in every row
+    lg[1, 4, 9999] = 3.5
+    draft = torch.full((2, 15), 17, dtype=torch.int32)
+    n, c = run_greedy(S, draft, lg)
+    on, oc = oracle.accept_greedy(draft, lg)
+    assert n.tolist() == on.tolist() == [15, 4]
+    assert c.tolist() == oc.tolist() == [17, 9999]
+
+
+def test_greedy_all_accepted_and_worked_cycle(S):
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_cycle.json")))
+    lg = torch.zeros(1, 16, g["vocab"], dtype=torch.float32)
+    for j, t in enumerate(g["target_choice"]):
+        lg[0, j, t] = 1.0
+    n, c = run_greedy(S, torch.tensor([g["draft"]], dtype=torch.int32), lg)
+    assert int(n[0]) == g["expect"]["n_accepted"] and int(c[0]) == g["expect"]["correction"]
+
+
+@pytest.mark.parametrize("n", [2, 3])
+def test_greedy_full_size_workloads(S, n):
+    cfg = W.config(n)
+    g = cfg["greedy"]
+    got_n, got_c = run_greedy(S, g["draft"], g["logits"])
+    on, oc = oracle.accept_greedy(g["draft"], g["logits"])
+    assert got_n.tolist() == on.tolist() == g["k"]
+    assert got_c.tolist() == oc.tolist()
+
+
+def test_greedy_workload1(S):
+    g = W.config(1)["greedy"]
+    got_n, got_c = run_greedy(S, g["draft"], g["logits"])
+    on, oc = oracle.accept_greedy(g["draft"], g["logits"])
+    assert got_n.tolist() == on.tolist() == [5]
+    assert got_c.tolist() == oc.tolist()
+
+
+def test_greedy_repeated_calls_share_workspace(S):
+    inp = W.greedy_inputs(B=2, T=16, V=50_000, seed=5)
+    B, T, V = inp["logits"].shape
+    ws = S.workspace(S.sd_accept_greedy_workspace_size(B, T, V, S.SD_BF16))
+    dl, dd = inp["logits"].cuda(), inp["draft"].cuda()
+    on, oc = oracle.accept_greedy(inp["draft"], inp["logits"])
+    for _ in range(5):
+        n = torch.zeros(B, dtype=torch.int32, device="cuda")
+        c = torch.zeros(B, dtype=torch.int32, device="cuda")
+        S.sd_accept_greedy(dd, dl, n, c, ws)
+        assert n.cpu().tolist() == on.tolist() and c.cpu().tolist() == oc.tolist()
+
+
+# --------------------------------------------------------------------------
+# sampled
+# --------------------------------------------------------------------------
+
+def run_sample(S, inp, tau, seed, offset=0, ws=None):
+    lg, q, d = inp["logits"], inp["q"], inp["draft"]
+    B, T, V = lg.shape
+    n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    nx = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    if ws is None:
+        ws = S.workspace(S.sd_accept_sample_workspace_size(B, T, V, S._dt(lg)))
+    S.sd_accept_sample(d.cuda(), q.cuda(), lg.cuda(), tau, seed, offset, n, nx, ws)
+    torch.cuda.synchronize()
+    assert int(ws[:256].abs().sum()) == 0, "counter block not returned to zero"
+    return n.cpu().numpy(), nx.cpu().numpy()
+
+
+def assert_sample_parity(inp, n, nx, tau, seed, offset=0):
+    T = inp["logits"].shape[1]
+    on, onx, diag = oracle.accept_sample(inp["draft"], inp["q"], inp["logits"], tau, seed, offset,
+                                         return_diag=True)
+    d = oracle.split_diag(diag, T)
+    excused = 0
+    for b in range(len(on)):
+        if n[b] != on[b]:
+            j = min(n[b], on[b])
+            assert abs(d["u"][b, j] - d["ratio"][b, j]) < EXCUSE, (b, n[b], on[b])
+            excused += 1
+            continue
+        if nx[b] != onx[b]:
+            S_ = d["S"][b]
+            near = min(abs(d["x"][b] - d["c_prev"][b]), abs(d["x"][b] - d["c_at"][b]))
+            assert near < EXCUSE * S_, (b, nx[b], onx[b])
+            excused += 1
+    return on, onx, excused
+
+
+@pytest.mark.parametrize("B,T,V,tau,dtype", [
+    (4, 16, 152_064, 1.0, torch.bfloat16),
+    (8, 16, 1_000, 0.7, torch.bfloat16),
+    (3, 5, 5_003, 1.3, torch.float32),
+    (64, 4, 2_000, 1.0, torch.bfloat16),
+    (2, 1, 3_000, 1.0, torch.bfloat16),
+])
+def test_sample_matches_oracle(S, B, T, V, tau, dtype):
+    inp = W.sample_inputs(B=B, T=T, V=V, seed=B + V, dtype=dtype)
+    for offset in (0, 7):
+        n, nx = run_sample(S, inp, tau, 1234, offset)
+        on, onx, exc = assert_sample_parity(inp, n, nx, tau, 1234, offset)
+        assert exc <= max(1, B // 20)
+
+
+def test_sample_workload5(S):
+    cfg = W.config(5)
+    n, nx = run_sample(S, cfg["sample"], cfg["temperature"], cfg["philox_seed"])
+    on, onx, exc = assert_sample_parity(cfg["sample"], n, nx, cfg["temperature"], cfg["philox_seed"])
+    assert exc == 0
+    assert (n == on).all() and (nx == onx).all()
+
+
+def test_sample_p_equals_q_accepts_all(S):
+    B, T, V = 6, 16, 4_000
+    g = torch.Generator().manual_seed(3)
+    lg = (torch.randn(B, T, V, generator=g) * 2).to(torch.bfloat16)
+    q = torch.softmax(lg.double(), -1).float()
+    draft = torch.multinomial(q[:, :-1].reshape(-1, V).double(), 1, generator=g).reshape(B, T - 1).int()
+    inp = {"logits": lg, "q": q, "draft": draft}
+    n, nx = run_sample(S, inp, 1.0, 42)
+    on, onx, _ = assert_sample_parity(inp, n, nx, 1.0, 42)
+    assert (n >= 14).all()
+
+
+def test_philox_word_for_word(S):
+    n = 1 << 20
+    rng = np.random.default_rng(9)
+    ctr = rng.integers(0, 2**32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    key = 0x9E3779B97F4A7C15
+    out = torch.zeros(n, 4, dtype=torch.int32, device="cuda")
+    S.sd_philox4x32_10(torch.from_numpy(ctr.view(np.int32)).cuda(), key, out)
+    got = out.cpu().numpy().view(np.uint32)
+    want = oracle.philox4x32_10(ctr, np.array([key & 0xFFFFFFFF, key >> 32], dtype=np.uint32))
+    assert np.array_equal(got, want)
+
+
+def test_accept_errors_are_reported_not_launched(S):
+    lg = torch.zeros(1, 16, 100, dtype=torch.bfloat16, device="cuda")
+    d = torch.zeros(1, 15, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(S.SdError) as e:
+        S.sd_accept_greedy(d, lg, n, n, small)
+    assert e.value.status == S.SD_ERR_WORKSPACE
+    ws = S.workspace(S.sd_accept_sample_workspace_size(1, 16, 100))
+    with pytest.raises(S.SdError) as e:
+        S.sd_accept_sample(d, lg.float(), lg, 0.0, 1, 0, n, n, ws)
+    assert e.value.status == S.SD_ERR_INVALID_ARG
+    assert S.sd_fault_word() == 0
