@@ -163,45 +163,59 @@ attn_split_generic_kernel(const AttnParams p) {
 }
 
 // One warp per output row: out = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M).
+// Lane k computes the weight of split s0 + k; the weights are broadcast by
+// shuffles so the partial-output loads of consecutive splits are independent.
+template <int D>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict__ o_part,
                                                         const float *__restrict__ lse_part,
-                                                        float *__restrict__ out, long rows,
-                                                        int n_splits, int D) {
+                                                        float *__restrict__ out, long rows, int n_splits) {
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
+    constexpr int VW = D / 32;  // floats per lane
     const long row = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     float M = -INFINITY;
-    for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, lse_part[(long)s * rows + row]);
+    for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, __ldcg(lse_part + (long)s * rows + row));
     M = warp_max(M);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[VW];
+#pragma unroll
+    for (int e = 0; e < VW; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < n_splits; ++s) {
-            const float l = lse_part[(long)s * rows + row];
-            if (l == -INFINITY) continue;
-            const float w = __expf(l - M);
+        for (int s0 = 0; s0 < n_splits; s0 += 32) {
+            const int s = s0 + lane;
+            float w = 0.f;
+            if (s < n_splits) {
+                const float l = __ldcg(lse_part + (long)s * rows + row);
+                w = l == -INFINITY ? 0.f : __expf(l - M);
+            }
             wsum += w;
-            const float *src = o_part + ((long)s * rows + row) * D;
-            if (D == 128) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + lane * 4);
-                acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-                acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src + lane * 2);
-                acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+            const int nk = min(32, n_splits - s0);
+#pragma unroll 4
+            for (int k = 0; k < nk; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                if (wk == 0.f) continue;
+                const float *src = o_part + ((long)(s0 + k) * rows + row) * D + lane * VW;
+                if (VW == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                    acc[0] = fmaf(wk, v.x, acc[0]); acc[1] = fmaf(wk, v.y, acc[1]);
+                    acc[2] = fmaf(wk, v.z, acc[2]); acc[3] = fmaf(wk, v.w, acc[3]);
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                    acc[0] = fmaf(wk, v.x, acc[0]); acc[1] = fmaf(wk, v.y, acc[1]);
+                }
             }
         }
     }
+    wsum = warp_sum(wsum);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    float *dst = out + row * D;
-    if (D == 128) {
-        *reinterpret_cast<float4 *>(dst + lane * 4) =
-            make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    float *dst = out + row * D + lane * VW;
+    if (VW == 4) {
+        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
     } else {
-        *reinterpret_cast<float2 *>(dst + lane * 2) = make_float2(acc[0] * inv, acc[1] * inv);
+        *reinterpret_cast<float2 *>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
     }
 }
 
@@ -247,8 +261,11 @@ cudaError_t launch_lse_merge(const AttnParams &p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel, (const float *)p.o_part,
-                              (const float *)p.lse_part, p.out, rows, p.n_splits, p.D);
+    if (p.D == 128)
+        return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, (const float *)p.o_part, (const float *)p.lse_part,
+                                  p.out, rows, p.n_splits);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, (const float *)p.o_part, (const float *)p.lse_part,
+                              p.out, rows, p.n_splits);
 }
 
 }  // namespace sdv

@@ -27,6 +27,13 @@ def S():
     sd_verify.sd_set_attention_path(0)
 
 
+@pytest.fixture(autouse=True)
+def _automatic_path(S):
+    S.sd_set_attention_path(0)
+    yield
+    S.sd_set_attention_path(0)
+
+
 def tc_applies(dtype, D, G, T):
     return dtype == torch.bfloat16 and D == 128 and G * T <= 128
 
@@ -141,6 +148,25 @@ def test_verify_row_sees_exactly_ctx_plus_j(S):
         base, pert = base.reshape(T, Hq, D), pert.reshape(T, Hq, D)
         assert np.array_equal(base[:7], pert[:7])
         assert (np.abs(base[7:] - pert[7:]).max(axis=(1, 2)) > 1e-3).all()
+
+
+@pytest.mark.parametrize("direction", [1.0, -1.0])
+def test_verify_moving_running_max(S, direction):
+    # keys carry a component along q that grows (or shrinks) along the sequence,
+    # so the running max moves by many powers of two across tiles
+    B, T, Hq, Hkv, D, ctx = 1, 16, 28, 4, 128, 2000
+    inp = W.verify_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, ctx=ctx, seed=21)
+    u = torch.ones(D) / math.sqrt(D)
+    ramp = torch.linspace(0.0, 1.0, ctx + T - 1)
+    if direction < 0:
+        ramp = 1.0 - ramp
+    k = (0.2 * inp["k"].float() + 60.0 * ramp.view(1, -1, 1, 1) * u).to(torch.bfloat16)
+    q = (inp["q"].float() + u).to(torch.bfloat16)
+    inp2 = dict(inp, k=k, q=q)
+    want = oracle.attention_rows(q, k, inp["v"], inp["ctx"], 1.0)
+    for path in (1, 2):
+        got, _ = run_verify(S, inp2, path)
+        check_attention(got, want)
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 5])
