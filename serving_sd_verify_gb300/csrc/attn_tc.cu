@@ -12,11 +12,13 @@
 // that kv head form the M = 128 rows of the MMAs (zero-padded), so every K/V
 // tile is fetched from HBM once and serves every row:
 //   S_t = Q . K_t^T   (M 128, N 64 keys, K 128)   -> tensor memory, 2 buffers
-//   P_t = exp2(S_t * scale * log2e - m)  (bf16, written to shared memory)
-//   O  += P_t . V_t   (M 128, N 128,     K 64)    -> tensor memory
+//   P_t = exp2(S_t * scale * log2e - m), split as P_hi + P_lo, both bf16
+//   O  += P_hi . V_t + P_lo . V_t   (M 128, N 128, K 64)  -> tensor memory
+// (the two-term split keeps the weights to about 2^-17 relative, so the
+// product is as accurate as an fp32 P even when a few keys dominate)
 // Warp roles (192 threads): warps 0-3 own one query row per thread (tensor
 // memory lane = row) and run the softmax, warp 4 issues the TMA loads of a
-// 4-stage K/V ring, warp 5 allocates tensor memory and issues the MMAs from one
+// 3-stage K/V ring, warp 5 allocates tensor memory and issues the MMAs from one
 // elected thread.  The running max is only moved when it grows by more than
 // 2^8, so O is rescaled in tensor memory rarely (exact either way: the same
 // reference max is used for P and for l).  Every wait is bounded by the
@@ -35,17 +37,17 @@ namespace sdv {
 namespace {
 
 constexpr int kTcThreads = 192;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kBN = kTileKeys;             // keys per tile (64)
 constexpr int kQBytes = 2 * 128 * 128;      // two K-blocks of [128 rows x 128 B]
 constexpr int kKBytes = 2 * kBN * 128;      // two K-blocks of [64 keys x 128 B]
 constexpr int kVBytes = 2 * kBN * 128;      // two d-chunks of [64 keys x 128 B]
-constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16
+constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16 (one of the hi / lo halves)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kStages * kKBytes;
 constexpr int kOffP = kOffV + kStages * kVBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffP + 4 * kPBytes;  // 2 buffers x (hi, lo)
 constexpr int kNumBars = 2 * kStages + 9;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack for 1024-byte alignment
@@ -365,10 +367,13 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
                 tc_fence_after();
                 const int st = t % kStages;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sw128_desc(sP + (t & 1) * kPBytes + kk * 32, 16, 1024);
-                    const uint64_t bd = sw128_desc(sV + st * kVBytes + kk * 16 * 128, kBN * 128, 1024);
-                    umma_bf16(tmem, a, bd, idO, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sw128_desc(sP + ((t & 1) * 2 + half) * kPBytes + kk * 32, 16, 1024);
+                        const uint64_t bd = sw128_desc(sV + st * kVBytes + kk * 16 * 128, kBN * 128, 1024);
+                        umma_bf16(tmem, a, bd, idO, (t > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 umma_commit(pempty_bar(t & 1));
                 umma_commit(empty_bar(st));
@@ -444,24 +449,31 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
             m_used = m_new;
             l *= alpha;
             const bool live = m_used != -INFINITY;
-            uint32_t pk[32];
+            uint32_t pk[32], pl[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float p0 = live ? ex2(x[2 * c] - m_used) : 0.f;
                 const float p1 = live ? ex2(x[2 * c + 1] - m_used) : 0.f;
                 l += p0 + p1;
                 pk[c] = pack_bf16(p0, p1);
+                // residual after rounding to bf16 (exact in fp32), itself rounded to bf16
+                const float r0 = p0 - __uint_as_float(pk[c] << 16);
+                const float r1 = p1 - __uint_as_float(pk[c] & 0xffff0000u);
+                pl[c] = pack_bf16(r0, r1);
             }
             // P buffer (t & 1) is free once PV_{t-2} completed
             if (t >= 2) {
                 ok = __all_sync(0xffffffffu, mbar_wait(pempty_bar(t & 1), ((t - 2) >> 1) & 1, abort_flag, p.fault));
                 if (!ok) break;
             }
-            uint8_t *pb = sbase + kOffP + (t & 1) * kPBytes;
+            uint8_t *pb = sbase + kOffP + (t & 1) * 2 * kPBytes;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
+            for (int ch = 0; ch < 8; ++ch) {
                 *reinterpret_cast<uint4 *>(pb + sw128_off(r, ch)) =
                     make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                *reinterpret_cast<uint4 *>(pb + kPBytes + sw128_off(r, ch)) =
+                    make_uint4(pl[4 * ch], pl[4 * ch + 1], pl[4 * ch + 2], pl[4 * ch + 3]);
+            }
             // value rows past the last cache key of the split may hold anything: zero them
             if (!blk) {
                 const int v0 = max(0, min(kBN, cend - tile_key0(t)));
