@@ -195,12 +195,14 @@ sd_status sd_fault_word(uint32_t *out, int clear);
 
 /* Attention kernel selection, process-wide, for tests and measurement:
  * 0 = automatic (tensor-core kernel where it applies), 1 = force the
- * CUDA-core kernel, 2 = require the tensor-core kernel (calls it cannot
- * serve return SD_ERR_UNSUPPORTED).  Returns the previous setting. */
+ * CUDA-core kernel, 2 = require the tensor-core kernel, 3 = require its
+ * variant that stages the softmax weights through shared memory instead of
+ * tensor memory (calls the tensor-core kernel cannot serve return
+ * SD_ERR_UNSUPPORTED under 2 and 3).  Returns the previous setting. */
 int sd_set_attention_path(int path);
 
-/* Which kernel the last attention call on this thread launched:
- * 1 = CUDA-core split kernel, 2 = tensor-core split kernel; and its split count. */
+/* Which kernel the last attention call on this thread launched (1, 2 or 3 as
+ * above) and how many key splits it used. */
 int sd_last_attention_path(int *n_splits);
 
 #ifdef __cplusplus

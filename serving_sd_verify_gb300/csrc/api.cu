@@ -75,7 +75,7 @@ AttnPlan plan_attention(const AttnParams &p, int path) {
     AttnPlan pl;
     pl.path = path;
     int ctas_per_sm, min_keys, gran;
-    if (path == 2) { ctas_per_sm = 1; min_keys = 4 * kTileKeys; gran = kTileKeys; }
+    if (path >= 2) { ctas_per_sm = 1; min_keys = 4 * kTileKeys; gran = kTileKeys; }
     else { ctas_per_sm = 2; min_keys = 128; gran = 32; }
     const int target = std::max(1, sms * ctas_per_sm);
     int splits = (target + units - 1) / units;
@@ -122,8 +122,8 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     const int force = g_force_path.load();
     int path;
     if (force == 1) path = 1;
-    else if (attn_tc_supported(p)) path = 2;
-    else if (force == 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
+    else if (attn_tc_supported(p)) path = force == 3 ? 3 : 2;
+    else if (force >= 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
     else path = 1;
     AttnPlan pl = plan_attention(p, path);
     const size_t need = attn_workspace(p.B, p.T, p.Hq, p.D, pl.n_splits);
@@ -136,7 +136,8 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     p.lse_part = reinterpret_cast<float *>(w + align_up((size_t)pl.n_splits * rows * p.D * sizeof(float), 256));
     p.n_splits = pl.n_splits;
     p.keys_per_split = pl.keys_per_split;
-    cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
+    cudaError_t e = path == 2 ? launch_attn_tc(p, st) : path == 3 ? launch_attn_tc_smem_p(p, st)
+                                                                  : launch_attn_generic(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
     e = launch_lse_merge(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention merge kernel launch");
@@ -214,7 +215,7 @@ const char *sd_last_error(void) { return g_err; }
 int sd_version(void) { return 100; }
 
 int sd_set_attention_path(int path) {
-    if (path < 0 || path > 2) path = 0;
+    if (path < 0 || path > 3) path = 0;
     return g_force_path.exchange(path);
 }
 

@@ -10,20 +10,30 @@
 //
 // One CTA owns one (split, kv head, sequence).  All G*T query rows that read
 // that kv head form the M = 128 rows of the MMAs (zero-padded), so every K/V
-// tile is fetched from HBM once and serves every row:
-//   S_t = Q . K_t^T   (M 128, N 64 keys, K 128)   -> tensor memory, 2 buffers
-//   P_t = exp2(S_t * scale * log2e - m), split as P_hi + P_lo, both bf16
-//   O  += P_hi . V_t + P_lo . V_t   (M 128, N 128, K 64)  -> tensor memory
-// (the two-term split keeps the weights to about 2^-17 relative, so the
-// product is as accurate as an fp32 P even when a few keys dominate)
-// Warp roles (192 threads): warps 0-3 own one query row per thread (tensor
-// memory lane = row) and run the softmax, warp 4 issues the TMA loads of a
-// 3-stage K/V ring, warp 5 allocates tensor memory and issues the MMAs from one
-// elected thread.  The running max is only moved when it grows by more than
-// 2^8, so O is rescaled in tensor memory rarely (exact either way: the same
-// reference max is used for P and for l).  Every wait is bounded by the
-// global timer; a wait that gives up sets the fault word, and the CTA drains
-// its copies and MMAs and frees its tensor memory before it returns.
+// tile is fetched from HBM once and serves every row.  For key tile t:
+//   S_t = Q . K_t^T                       (M 128, N 64 keys, K 128)
+//   P_t = exp2(S_t * scale * log2e - m)   split as P_hi + P_lo, both bf16
+//   O_(t mod 2) += P_hi . V_t + P_lo . V_t  (M 128, N 128, K 64)
+// The two-term split keeps every weight to about 2^-17 relative, so the
+// product is as accurate as an fp32 P even when a few keys dominate.
+//
+// Warp roles (320 threads):
+//   warps 0-3 / 4-7  two softmax warpgroups; warpgroup w takes the tiles with
+//                    t mod 2 == w, has its own S/P buffer and O accumulator in
+//                    tensor memory and its own running max / sum; thread = row
+//                    (= tensor-memory lane).  The two halves are merged at the
+//                    end like two splits.
+//   warp 8           TMA producer of a K/V ring in shared memory
+//   warp 9           allocates tensor memory; one thread issues the MMAs,
+//                    serving whichever of "next S" / "next P.V" is ready.
+// P is written back into the tensor-memory columns that held S (variant
+// kPTmem) and read by the MMA as its A operand, which leaves shared memory to
+// a 5-stage K/V ring; the other variant stages P through shared memory.
+// The running max only moves when it grows by more than 2^8, so O is rescaled
+// in tensor memory rarely (exact either way: P and l use the same reference).
+// Every wait is bounded by the global timer; a wait that gives up sets the
+// fault word and the CTA drains its copies and MMAs before freeing tensor
+// memory and returning.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -36,26 +46,31 @@ namespace sdv {
 
 namespace {
 
-constexpr int kTcThreads = 192;
-constexpr int kStages = 3;
-constexpr int kBN = kTileKeys;             // keys per tile (64)
+constexpr int kTcThreads = 320;
+constexpr int kBN = kTileKeys;              // keys per tile (64)
 constexpr int kQBytes = 2 * 128 * 128;      // two K-blocks of [128 rows x 128 B]
 constexpr int kKBytes = 2 * kBN * 128;      // two K-blocks of [64 keys x 128 B]
 constexpr int kVBytes = 2 * kBN * 128;      // two d-chunks of [64 keys x 128 B]
-constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16 (one of the hi / lo halves)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + kStages * kKBytes;
-constexpr int kOffP = kOffV + kStages * kVBytes;
-constexpr int kOffBar = kOffP + 4 * kPBytes;  // 2 buffers x (hi, lo)
-constexpr int kNumBars = 2 * kStages + 9;
-constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack for 1024-byte alignment
-constexpr uint32_t kTmemCols = 256;         // O: cols [0,128), S0: [128,192), S1: [192,256)
+constexpr int kStageBytes = kKBytes + kVBytes;
+constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16, one half (hi or lo)
+constexpr uint32_t kTmemCols = 512;         // O0 [0,128) O1 [128,256) SP0 [256,320) SP1 [320,384)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+template <bool kPTmem> struct Layout {
+    static constexpr int kStages = kPTmem ? 5 : 3;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffStage = kQBytes;
+    static constexpr int kOffP = kOffStage + kStages * kStageBytes;          // smem P (variant 2 only)
+    static constexpr int kOffBar = kOffP + (kPTmem ? 0 : 4 * kPBytes);
+    // full[S], empty[S], sfull[2], pfull[2], pempty[2], qready, drain
+    static constexpr int kNumBars = 2 * kStages + 8;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                  // tmem base, abort flag
+    static constexpr int kOffXchg = kOffMisc + 16;                           // (m, l) exchange
+    static constexpr int kSmemBytes = kOffXchg + 2 * 128 * 8 + 1024;         // + alignment slack
+};
 
 struct TcParams {
     AttnParams a;
@@ -90,9 +105,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
 
 // Bounded wait for the phase of parity `parity` to complete.  Gives up when
-// another thread of the CTA gave up (abort flag) or after kWaitLimitNs.
+// another thread of the CTA gave up (abort flag, if given) or after kWaitLimitNs.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                        unsigned int *fault) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -100,9 +123,9 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
-            if (*abort_flag) return false;
+            if (abort_flag && *abort_flag) return false;
             if (global_timer() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
+                if (abort_flag) *abort_flag = 1;
                 set_fault(fault, FAULT_WAIT_TIMEOUT);
                 return false;
             }
@@ -124,6 +147,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // shared-memory matrix descriptor, 128-byte swizzle, sm_100 descriptor version 1
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -136,18 +162,28 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
-// instruction descriptor, kind::f16: bf16 A and B, fp32 D
+// instruction descriptor, kind::f16: bf16 A and B, fp32 D, A K-major
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+// D (tensor memory) (+)= A (shared memory, descriptor) . B (shared memory)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D (tensor memory) (+)= A (tensor memory) . B (shared memory)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -162,7 +198,7 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 #define SDV_S8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
                   "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 
-// 32 consecutive fp32 columns of this thread's lane; waits for completion
+// 32 consecutive 32-bit columns of this thread's lane; waits for completion
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13,"
@@ -173,14 +209,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     // tie the registers to the wait so no use is scheduled above it
     asm volatile("" : SDV_W8(0), SDV_W8(8), SDV_W8(16), SDV_W8(24));
 }
+// store without waiting (callers issue tmem_st_wait once after a batch)
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12,"
         " %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
         ::"r"(taddr), SDV_S8(0), SDV_S8(8), SDV_S8(16), SDV_S8(24)
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -199,9 +236,12 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+template <bool kPTmem>
 __global__ void __launch_bounds__(kTcThreads, 1)
 attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      const TcParams tp) {
+    using L = Layout<kPTmem>;
+    constexpr int NS = L::kStages;
     const AttnParams &p = tp.a;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -210,75 +250,33 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int T = p.T, G = p.Hq / p.Hkv, M = G * T;
-    const bool drafter = p.mode == 1;
 
-    int nb = p.nctx[b];
-    if (nb < 1 || nb > p.max_ctx) {
-        if (tid == 0) set_fault(p.fault, FAULT_BAD_CTX);
-        nb = max(1, min(nb, p.max_ctx));
-    }
-    const int k0 = s * p.keys_per_split;
-    const int k1 = k0 + p.keys_per_split;
-    // end of this split's keys taken from the cache (exclusive)
-    const int cend = drafter ? min(k1, nb) : min(k1, nb + T - 1);
-    const int n_cache_tiles = cend > k0 ? (cend - k0 + kBN - 1) / kBN : 0;
-    const bool has_block_tile = drafter && s == 0;
-    const int n_tiles = n_cache_tiles + (has_block_tile ? 1 : 0);
-    const long rows_total = (long)p.B * T * p.Hq;
-
-    if (n_tiles == 0) {  // nothing to read: mark the split empty for the merge
-        if (tid < M) {
-            const int j = tid / G, h = g * G + tid % G;
-            p.lse_part[(long)s * rows_total + ((long)b * T + j) * p.Hq + h] = -INFINITY;
-        }
-        return;
-    }
-
-    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
-    const uint32_t bar0 = base + kOffBar;
+    const uint32_t sQ = base + L::kOffQ, sStage = base + L::kOffStage, sP = base + L::kOffP;
+    const uint32_t bar0 = base + L::kOffBar;
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
-    auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
-    auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
-    auto sempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 + i); };
-    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 4 + i); };
-    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 6 + i); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 8);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + kOffMisc + 8);
+    auto empty_bar = [&](int i) { return bar0 + 8u * (NS + i); };
+    auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + i); };
+    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + 2 + i); };
+    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + 4 + i); };
+    const uint32_t qready_bar = bar0 + 8u * (2 * NS + 6);
+    const uint32_t drain_bar = bar0 + 8u * (2 * NS + 7);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 8);
+    float2 *xchg = reinterpret_cast<float2 *>(sbase + L::kOffXchg);  // [2][128] (m, l) per warpgroup
 
-    // tile t -> first key index (cache tiles) ; the drafter's block tile is t == 0 of split 0
-    auto tile_key0 = [&](int t) { return k0 + (t - (has_block_tile ? 1 : 0)) * kBN; };
-    auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
-
+    // ---- prologue that reads nothing produced upstream ----
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(sfull_bar(i), 1); mbar_init(sempty_bar(i), 128);
-            mbar_init(pfull_bar(i), 128); mbar_init(pempty_bar(i), 1);
-        }
+        for (int i = 0; i < NS; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 4); mbar_init(pempty_bar(i), 1); }
+        mbar_init(qready_bar, 8);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) {  // tensor memory for O and the two S buffers
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_holder)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    // Q rows r = j*G + hl of this kv head, zero-padded to 128 rows, 128-byte swizzled
-    if (warp < 4) {
-        const int r = tid;
-        const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-        for (int ch = 0; ch < 16; ++ch) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < M) {
-                const int j = r / G, h = g * G + r % G;
-                v = __ldg(reinterpret_cast<const uint4 *>(q + (((long)b * T + j) * p.Hq + h) * 128) + ch);
-            }
-            *reinterpret_cast<uint4 *>(sbase + kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7)) = v;
-        }
-        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -286,240 +284,344 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
     const uint32_t tmem = *tmem_holder;
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs of an upstream kernel are visible now
 #endif
 
-    if (warp == 4) {
+    const int T = p.T, G = p.Hq / p.Hkv, M = G * T;
+    const bool drafter = p.mode == 1;
+    int nb = p.nctx[b];
+    if (nb < 1 || nb > p.max_ctx) {
+        if (tid == 0) set_fault(p.fault, FAULT_BAD_CTX);
+        nb = max(1, min(nb, p.max_ctx));
+    }
+    const int k0 = s * p.keys_per_split;
+    const int k1 = k0 + p.keys_per_split;
+    const int cend = drafter ? min(k1, nb) : min(k1, nb + T - 1);  // end of this split's cache keys
+    const int n_cache_tiles = cend > k0 ? (cend - k0 + kBN - 1) / kBN : 0;
+    const bool has_block_tile = drafter && s == 0;
+    const int n_tiles = n_cache_tiles + (has_block_tile ? 1 : 0);
+    const long rows_total = (long)p.B * T * p.Hq;
+    auto tile_key0 = [&](int t) { return k0 + (t - (has_block_tile ? 1 : 0)) * kBN; };
+    auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
+
+    if (n_tiles == 0) {
+        // nothing to read: mark the split empty for the merge
+        if (tid < M) {
+            const int j = tid / G, h = g * G + tid % G;
+            p.lse_part[(long)s * rows_total + ((long)b * T + j) * p.Hq + h] = -INFINITY;
+        }
+    } else if (warp == 8) {
         // ------------------------------------------------------------------ producer
-        const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(p.kb);
-        const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(p.vb);
-        int issued = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % kStages;
-            if (t >= kStages && !mbar_wait(empty_bar(st), ((t / kStages) - 1) & 1, abort_flag, p.fault)) break;
-            const uint32_t dK = sK + st * kKBytes, dV = sV + st * kVBytes;
-            if (is_block_tile(t)) {
-                // the T block keys / values from [B, T, Hkv, D], rows >= T zero
-                for (int idx = lane; idx < kBN * 16; idx += 32) {
-                    const int row = idx >> 4, ch = idx & 15;
-                    uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
-                    if (row < T) {
-                        const long off = (((long)b * T + row) * p.Hkv + g) * 128;
-                        kv4 = __ldg(reinterpret_cast<const uint4 *>(kb + off) + ch);
-                        vv4 = __ldg(reinterpret_cast<const uint4 *>(vb + off) + ch);
-                    }
-                    const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
-                    *reinterpret_cast<uint4 *>(sbase + kOffK + st * kKBytes + o) = kv4;
-                    *reinterpret_cast<uint4 *>(sbase + kOffV + st * kVBytes + o) = vv4;
+        int t = 0;
+        if (has_block_tile) {
+            // the T block keys / values from [B, T, Hkv, D] into stage 0; rows >= T zero
+            const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(p.kb);
+            const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(p.vb);
+            uint8_t *stg = sbase + L::kOffStage;
+            for (int idx = lane; idx < kBN * 16; idx += 32) {
+                const int row = idx >> 4, ch = idx & 15;
+                uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
+                if (row < T) {
+                    const long off = (((long)b * T + row) * p.Hkv + g) * 128;
+                    kv4 = __ldg(reinterpret_cast<const uint4 *>(kb + off) + ch);
+                    vv4 = __ldg(reinterpret_cast<const uint4 *>(vb + off) + ch);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_bar(st));
-            } else if (lane == 0) {
-                const int key0 = tile_key0(t);
+                const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
+                *reinterpret_cast<uint4 *>(stg + o) = kv4;
+                *reinterpret_cast<uint4 *>(stg + kKBytes + o) = vv4;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(0));
+            t = 1;
+        }
+        int issued = t;
+        if (lane == 0) {
+            for (; t < n_tiles; ++t) {
+                const int st = t % NS;
+                if (t >= NS && !mbar_wait(empty_bar(st), ((t / NS) - 1) & 1, abort_flag, p.fault)) break;
+                const uint32_t dK = sStage + st * kStageBytes, dV = dK + kKBytes;
                 int c[4] = {0, 0, 0, b};
-                c[tp.dim_s] = key0;
+                c[tp.dim_s] = tile_key0(t);
                 c[tp.dim_h] = g;
-                mbar_arrive_expect_tx(full_bar(st), (uint32_t)(kKBytes + kVBytes));
+                mbar_arrive_expect_tx(full_bar(st), (uint32_t)kStageBytes);
                 tma_load_4d(dK, &tmap_k, full_bar(st), 0, c[1], c[2], c[3]);
                 tma_load_4d(dK + kBN * 128, &tmap_k, full_bar(st), 64, c[1], c[2], c[3]);
                 tma_load_4d(dV, &tmap_v, full_bar(st), 0, c[1], c[2], c[3]);
                 tma_load_4d(dV + kBN * 128, &tmap_v, full_bar(st), 64, c[1], c[2], c[3]);
+                issued = t + 1;
             }
-            __syncwarp();
-            issued = t + 1;
-        }
-        // on abort: let the copies already issued land before the CTA exits
-        if (*abort_flag && lane == 0) {
-            for (int t = max(0, issued - kStages); t < issued; ++t) {
-                volatile int never = 0;
-                mbar_wait(full_bar(t % kStages), (t / kStages) & 1, &never, p.fault);
+            // on abort: let the copies already issued land before the CTA exits
+            if (*abort_flag) {
+                for (int u = max(0, issued - NS); u < issued; ++u)
+                    mbar_wait(full_bar(u % NS), (u / NS) & 1, nullptr, p.fault);
             }
         }
-    } else if (warp == 5) {
+        __syncwarp();
+    } else if (warp == 9) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, kBN, false);
             const uint32_t idO = idesc_bf16(128, 128, true);
-            auto issue_S = [&](int t) {
-                const int st = t % kStages;
-                const uint32_t dcol = tmem + 128u + 64u * (t & 1);
+            bool ok = mbar_wait(qready_bar, 0, abort_flag, p.fault);
+            int nS = 0, nP = 0;
+            unsigned long long t0 = global_timer();
+            uint32_t spins = 0;
+            while (ok && nP < n_tiles) {
+                bool did = false;
+                // S_nS into buffer nS & 1 once K is loaded and P.V of tile nS-2 is done
+                if (nS < n_tiles && nS < nP + 2) {
+                    const int st = nS % NS;
+                    if (mbar_test(full_bar(st), (nS / NS) & 1) &&
+                        (nS < 2 || mbar_test(pempty_bar(nS & 1), ((nS - 2) >> 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t dcol = tmem + 256u + 64u * (nS & 1);
+                        const uint32_t kbase = sStage + st * kStageBytes;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = sw128_desc(sQ + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sw128_desc(sK + st * kKBytes + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(dcol, a, bd, idS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(sfull_bar(t & 1));
-            };
-            bool ok = mbar_wait(full_bar(0), 0, abort_flag, p.fault);
-            if (ok) { tc_fence_after(); issue_S(0); }
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                if (t + 1 < n_tiles) {
-                    const int t1 = t + 1;
-                    ok = mbar_wait(full_bar(t1 % kStages), (t1 / kStages) & 1, abort_flag, p.fault);
-                    if (ok && t1 >= 2) ok = mbar_wait(sempty_bar(t1 & 1), ((t1 - 2) >> 1) & 1, abort_flag, p.fault);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_S(t1);
-                }
-                ok = mbar_wait(pfull_bar(t & 1), (t >> 1) & 1, abort_flag, p.fault);
-                if (!ok) break;
-                tc_fence_after();
-                const int st = t % kStages;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sw128_desc(sP + ((t & 1) * 2 + half) * kPBytes + kk * 32, 16, 1024);
-                        const uint64_t bd = sw128_desc(sV + st * kVBytes + kk * 16 * 128, kBN * 128, 1024);
-                        umma_bf16(tmem, a, bd, idO, (t > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = sw128_desc(sQ + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
+                            umma_ss(dcol, a, bd, idS, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(sfull_bar(nS & 1));
+                        ++nS;
+                        did = true;
                     }
                 }
-                umma_commit(pempty_bar(t & 1));
-                umma_commit(empty_bar(st));
+                // P.V of tile nP once its softmax is done
+                if (nP < nS && mbar_test(pfull_bar(nP & 1), (nP >> 1) & 1)) {
+                    tc_fence_after();
+                    const int st = nP % NS;
+                    const int wb = nP & 1;
+                    const uint32_t vbase = sStage + st * kStageBytes + kKBytes;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, kBN * 128, 1024);
+                            const uint32_t acc = (nP >= 2 || half > 0 || kk > 0) ? 1u : 0u;
+                            if (kPTmem) {
+                                const uint32_t a_t = tmem + 256u + 64u * wb + 32u * half + 8u * kk;
+                                umma_ts(tmem + 128u * wb, a_t, bd, idO, acc);
+                            } else {
+                                const uint64_t a = sw128_desc(sP + (wb * 2 + half) * kPBytes + kk * 32, 16, 1024);
+                                umma_ss(tmem + 128u * wb, a, bd, idO, acc);
+                            }
+                        }
+                    }
+                    umma_commit(pempty_bar(wb));
+                    umma_commit(empty_bar(st));
+                    ++nP;
+                    did = true;
+                }
+                if (did) {
+                    t0 = global_timer();
+                    spins = 0;
+                } else if ((++spins & 63u) == 0) {
+                    if (*abort_flag) { ok = false; break; }
+                    if (global_timer() - t0 > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        set_fault(p.fault, FAULT_WAIT_TIMEOUT);
+                        ok = false;
+                    }
+                }
             }
             // every MMA issued above has completed before tensor memory is freed
             umma_commit(drain_bar);
-            volatile int never = 0;
-            mbar_wait(drain_bar, 0, &never, p.fault);
+            mbar_wait(drain_bar, 0, nullptr, p.fault);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------------ softmax (warps 0-3)
-        const int r = tid;                      // query row = tensor-memory lane
+        // ------------------------------------------------------------------ softmax (warps 0-7)
+        const int wg = warp >> 2;               // warpgroup: tiles t with t % 2 == wg
+        const int r = tid & 127;                // query row = tensor-memory lane
         const bool row_ok = r < M;
         const int j = row_ok ? r / G : 0;
         const float qk = p.scale * kLog2e;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t o_col = tmem + lane_off + 128u * wg;
+        const uint32_t sp_col = tmem + lane_off + 256u + 64u * wg;
+        if (wg == 0) {
+            // Q rows r = j*G + hl of this kv head, zero-padded to 128 rows, 128-byte swizzled
+            const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+            uint4 v[16];
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                v[ch] = make_uint4(0u, 0u, 0u, 0u);
+                if (row_ok) {
+                    const int h = g * G + r % G;
+                    v[ch] = __ldg(reinterpret_cast<const uint4 *>(q + (((long)b * T + j) * p.Hq + h) * 128) + ch);
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch)
+                *reinterpret_cast<uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7)) = v[ch];
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qready_bar);
+
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int t = 0; t < n_tiles && ok; ++t) {
-            ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(t & 1), (t >> 1) & 1, abort_flag, p.fault));
+        int last_t = -1;
+        for (int t = wg; t < n_tiles; t += 2) {
+            const int u = t >> 1;  // use index of this warpgroup's buffers
+            ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(wg), u & 1, abort_flag, p.fault));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[64];
             {
                 uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
                 uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
-                tmem_ld32(lane_base + 128u + 64u * (t & 1), lo);
-                tmem_ld32(lane_base + 128u + 64u * (t & 1) + 32u, hi);
+                tmem_ld32(sp_col, lo);
+                tmem_ld32(sp_col + 32u, hi);
             }
-            tc_fence_before();
-            mbar_arrive(sempty_bar(t & 1));
-
-            // mask: keys this row may see in this tile
+            // keys [0, nvalid) of the tile are visible to this row
             const bool blk = is_block_tile(t);
-            int nvalid;  // keys [0, nvalid) of the tile are visible to this row
+            int nvalid;
             if (blk) {
                 nvalid = T;
             } else {
-                const int key0 = tile_key0(t);
                 const int lim = drafter ? cend : min(cend, nb + j);
-                nvalid = max(0, min(kBN, lim - key0));
+                nvalid = max(0, min(kBN, lim - tile_key0(t)));
             }
             if (!row_ok) nvalid = 0;
             float x[64];
-            float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                x[c] = c < nvalid ? __uint_as_float(sr[c]) * qk : -INFINITY;
-                tmax = fmaxf(tmax, x[c]);
+            for (int c = 0; c < 64; ++c) x[c] = c < nvalid ? __uint_as_float(sr[c]) * qk : -INFINITY;
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mx[i] = fmaxf(fmaxf(fmaxf(x[8 * i], x[8 * i + 1]), fmaxf(x[8 * i + 2], x[8 * i + 3])),
+                              fmaxf(fmaxf(x[8 * i + 4], x[8 * i + 5]), fmaxf(x[8 * i + 6], x[8 * i + 7])));
             }
+            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             // move the reference max only when it grows by more than 2^8
-            const bool need = t > 0 && tmax > m_used + kRescaleThreshold;
+            const bool first = t == wg;
+            const bool need = !first && tmax > m_used + kRescaleThreshold;
             float alpha = 1.f;
-            float m_new = m_used;
-            if (t == 0) m_new = tmax;
-            else if (need) { m_new = tmax; alpha = ex2(m_used - m_new); }
-            if (__any_sync(0xffffffffu, need)) {
-                // O is read-modify-written in tensor memory once PV_{t-1} is complete
-                ok = mbar_wait(pempty_bar((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, p.fault);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            if (first) m_used = tmax;
+            else if (need) { alpha = ex2(m_used - tmax); m_used = tmax; }
+            // this warpgroup's previous P.V (tile t-2) must be done before O or
+            // (shared-memory variant) the P buffer is touched again
+            if (!first && (!kPTmem || __any_sync(0xffffffffu, need))) {
+                ok = __all_sync(0xffffffffu, mbar_wait(pempty_bar(wg), (u - 1) & 1, abort_flag, p.fault));
+                if (!ok) break;
                 tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + 32u * cc, o);
+                    tmem_ld32(o_col + 32u * cc, o);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(lane_base + 32u * cc, o);
+                    tmem_st32(o_col + 32u * cc, o);
                 }
-                tc_fence_before();
             }
-            m_used = m_new;
             l *= alpha;
             const bool live = m_used != -INFINITY;
             uint32_t pk[32], pl[32];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float p0 = live ? ex2(x[2 * c] - m_used) : 0.f;
                 const float p1 = live ? ex2(x[2 * c + 1] - m_used) : 0.f;
-                l += p0 + p1;
+                ls[c & 3] += p0 + p1;
                 pk[c] = pack_bf16(p0, p1);
                 // residual after rounding to bf16 (exact in fp32), itself rounded to bf16
                 const float r0 = p0 - __uint_as_float(pk[c] << 16);
                 const float r1 = p1 - __uint_as_float(pk[c] & 0xffff0000u);
                 pl[c] = pack_bf16(r0, r1);
             }
-            // P buffer (t & 1) is free once PV_{t-2} completed
-            if (t >= 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(pempty_bar(t & 1), ((t - 2) >> 1) & 1, abort_flag, p.fault));
-                if (!ok) break;
-            }
-            uint8_t *pb = sbase + kOffP + (t & 1) * 2 * kPBytes;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            if (kPTmem) {
+                // P over the S columns it came from: hi in [0,32), lo in [32,64)
+                tmem_st32(sp_col, pk);
+                tmem_st32(sp_col + 32u, pl);
+            } else {
+                uint8_t *pb = sbase + L::kOffP + wg * 2 * kPBytes;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                *reinterpret_cast<uint4 *>(pb + sw128_off(r, ch)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                *reinterpret_cast<uint4 *>(pb + kPBytes + sw128_off(r, ch)) =
-                    make_uint4(pl[4 * ch], pl[4 * ch + 1], pl[4 * ch + 2], pl[4 * ch + 3]);
+                for (int ch = 0; ch < 8; ++ch) {
+                    *reinterpret_cast<uint4 *>(pb + sw128_off(r, ch)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                    *reinterpret_cast<uint4 *>(pb + kPBytes + sw128_off(r, ch)) =
+                        make_uint4(pl[4 * ch], pl[4 * ch + 1], pl[4 * ch + 2], pl[4 * ch + 3]);
+                }
             }
-            // value rows past the last cache key of the split may hold anything: zero them
+            // value rows past the split's last cache key may hold anything: zero them
             if (!blk) {
                 const int v0 = max(0, min(kBN, cend - tile_key0(t)));
                 if (v0 < kBN) {
-                    uint8_t *vt = sbase + kOffV + (t % kStages) * kVBytes;
-                    for (int idx = tid; idx < (kBN - v0) * 16; idx += 128) {
+                    uint8_t *vt = sbase + L::kOffStage + (t % NS) * kStageBytes + kKBytes;
+                    for (int idx = r; idx < (kBN - v0) * 16; idx += 128) {
                         const int row = v0 + (idx >> 4), ch = idx & 15;
                         *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
             }
+            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(pfull_bar(t & 1));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull_bar(wg));
+            last_t = t;
         }
-        // epilogue: O / l and the log-sum-exp of this split
-        if (ok) ok = mbar_wait(pempty_bar((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag, p.fault);
+        // ---- epilogue: merge the two warpgroups' (m, l, O), write this split's partial ----
+        if (ok && last_t >= 0)
+            ok = mbar_wait(pempty_bar(wg), (last_t >> 1) & 1, abort_flag, p.fault);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        if (!ok || last_t < 0) { m_used = -INFINITY; l = 0.f; }
+        xchg[wg * 128 + r] = make_float2(m_used, l);
+        tc_fence_before();
+        named_sync(1, 256);  // both warpgroups' last P.V are complete past this point
+        const float2 mine = xchg[wg * 128 + r], other = xchg[(wg ^ 1) * 128 + r];
+        const float m0 = wg == 0 ? mine.x : other.x, l0 = wg == 0 ? mine.y : other.y;
+        const float m1 = wg == 0 ? other.x : mine.x, l1 = wg == 0 ? other.y : mine.y;
+        const float Mx = fmaxf(m0, m1);
+        const float f0 = l0 > 0.f ? ex2(m0 - Mx) : 0.f;
+        const float f1 = l1 > 0.f ? ex2(m1 - Mx) : 0.f;
+        const float Lsum = l0 * f0 + l1 * f1;
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const bool abort_seen = *abort_flag != 0;
+        if (!abort_seen) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
             const int h = g * G + (row_ok ? r % G : 0);
             const long frow = ((long)b * T + j) * p.Hq + h;
             float *dst = p.o_part + ((long)s * rows_total + frow) * 128;
+            // warpgroup wg writes output columns [64 wg, 64 wg + 64)
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + 32u * cc, o);
+            for (int cc = 0; cc < 2; ++cc) {
+                const uint32_t col = 64u * wg + 32u * cc;
+                uint32_t oa[32], ob[32];
+                tmem_ld32(tmem + lane_off + col, oa);
+                tmem_ld32(tmem + lane_off + 128u + col, ob);
                 if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(dst + 32 * cc + e) =
-                            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                                        __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                    for (int e = 0; e < 32; e += 4) {
+                        float4 v;
+                        float *pv = reinterpret_cast<float *>(&v);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float a0 = l0 > 0.f ? __uint_as_float(oa[e + q4]) * f0 : 0.f;
+                            const float a1 = l1 > 0.f ? __uint_as_float(ob[e + q4]) * f1 : 0.f;
+                            pv[q4] = (a0 + a1) * inv;
+                        }
+                        *reinterpret_cast<float4 *>(dst + col + e) = v;
+                    }
                 }
             }
-            if (row_ok)
-                p.lse_part[(long)s * rows_total + frow] = l > 0.f ? m_used * kLn2 + logf(l) : -INFINITY;
+            if (row_ok && wg == 0)
+                p.lse_part[(long)s * rows_total + frow] = Lsum > 0.f ? Mx * kLn2 + logf(Lsum) : -INFINITY;
         }
         tc_fence_before();
     }
 
-    // teardown: wait for every MMA of this CTA, then free tensor memory
+    // teardown: every MMA has completed (drain above); free tensor memory
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
@@ -573,6 +675,37 @@ bool make_map(CUtensorMap *m, const void *ptr, const sd_strides &kv, int S, int 
 
 int cache_slots(const AttnParams &p) { return p.mode == 0 ? p.max_ctx + p.T - 1 : p.max_ctx; }
 
+template <bool kPTmem>
+cudaError_t launch_tc_t(const AttnParams &p, cudaStream_t st) {
+    alignas(64) CUtensorMap mk, mv;
+    TcParams tp;
+    tp.a = p;
+    int ds2 = 0, dh2 = 0;
+    if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B, &tp.dim_s, &tp.dim_h)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B, &ds2, &dh2)) return cudaErrorInvalidValue;
+    constexpr int smem = Layout<kPTmem>::kSmemBytes;
+    static bool opted_in[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+        e = cudaFuncSetAttribute(attn_split_tc_kernel<kPTmem>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel<kPTmem>, mk, mv, tp);
+}
+
 }  // namespace
 
 bool attn_tc_supported(const AttnParams &p) {
@@ -583,34 +716,16 @@ bool attn_tc_supported(const AttnParams &p) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-    if (optin < kSmemBytes) return false;
+    if (optin < Layout<true>::kSmemBytes || optin < Layout<false>::kSmemBytes) return false;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     return major == 10 && minor == 3;
 }
 
-size_t attn_tc_smem_bytes(const AttnParams &) { return kSmemBytes; }
+size_t attn_tc_smem_bytes(const AttnParams &) { return Layout<true>::kSmemBytes; }
 
-cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
-    alignas(64) CUtensorMap mk, mv;
-    TcParams tp;
-    tp.a = p;
-    int ds2 = 0, dh2 = 0;
-    if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B, &tp.dim_s, &tp.dim_h)) return cudaErrorInvalidValue;
-    if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B, &ds2, &dh2)) return cudaErrorInvalidValue;
-    static bool opted_in[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
-        e = cudaFuncSetAttribute(attn_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) opted_in[dev] = true;
-    }
-    dim3 grid(p.n_splits, p.Hkv, p.B);
-    attn_split_tc_kernel<<<grid, kTcThreads, kSmemBytes, st>>>(mk, mv, tp);
-    return cudaGetLastError();
-}
+cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) { return launch_tc_t<true>(p, st); }
+cudaError_t launch_attn_tc_smem_p(const AttnParams &p, cudaStream_t st) { return launch_tc_t<false>(p, st); }
 
 }  // namespace sdv

@@ -49,7 +49,8 @@ struct AttnParams {
 
 // kernel launchers: return the launch error (cudaSuccess when enqueued)
 cudaError_t launch_attn_generic(const AttnParams &p, cudaStream_t st);
-cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
+cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);         // P kept in tensor memory
+cudaError_t launch_attn_tc_smem_p(const AttnParams &p, cudaStream_t st);  // P staged in shared memory
 cudaError_t launch_lse_merge(const AttnParams &p, cudaStream_t st);
 bool attn_tc_supported(const AttnParams &p);
 size_t attn_tc_smem_bytes(const AttnParams &p);
