@@ -7,12 +7,14 @@
 // the standard speculative accept/reject rule.  Philox: Salmon et al., SC'11,
 // section 3.2.
 //
-// Both reductions are vocabulary-wide over B*T rows: a grid of (chunk, row)
-// CTAs reads each row once with 16-byte loads, reduces within warps by
-// shuffles and across warps through shared memory, writes one partial per CTA,
-// and the last CTA to finish (a ticket counter in the workspace, returned to
-// zero by that CTA) combines the partials and runs the per-sequence scan.  No
-// CTA ever waits for another.
+// Both are vocabulary-wide reductions over B*T rows.  A grid of (chunk, row)
+// CTAs reads every row once: each thread pulls its share of the chunk into
+// registers with 16-byte loads issued together, reduces it, and the CTA
+// reduces across warps (shuffles, then shared memory) into one partial.  The
+// last CTA of a row to finish (a per-row ticket counter) combines that row's
+// partials; the last row to finish (a second counter) runs the per-sequence
+// scan.  Every counter is returned to zero by the CTA that read it last, so a
+// zero-filled workspace stays reusable.  No CTA ever waits for another.
 #include "common.cuh"
 
 #include <float.h>
@@ -24,6 +26,7 @@ namespace sdv {
 namespace {
 
 constexpr int kAccThreads = 256;
+constexpr int kMaxVec = 8;  // 16-byte vectors per thread and chunk
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10
@@ -55,27 +58,37 @@ __global__ void philox_kernel(const uint4 *__restrict__ ctr, uint64_t key, uint4
 }
 
 // ----------------------------------------------------------------------------
-// chunk traversal: calls f(index, value) for every element of [lo, hi) of a row,
-// in ascending index order per thread, 16-byte loads where aligned
+// a chunk [lo, hi) of one row, pulled into registers: vector v of this thread
+// holds elements a0 + (tid + v * kAccThreads) * PV + e; the unaligned head
+// [lo, a0) and tail [a1, hi) are read element by element
 // ----------------------------------------------------------------------------
-template <typename Tin, typename F>
-__device__ __forceinline__ void for_chunk(const Tin *row, int lo, int hi, F &&f) {
-    constexpr int PV = Elem<Tin>::kPerVec;
-    // first index >= lo whose address is 16-byte aligned
-    const uintptr_t base = reinterpret_cast<uintptr_t>(row);
-    int a0 = lo;
-    while (a0 < hi && ((base + (uintptr_t)a0 * sizeof(Tin)) & 15u)) ++a0;
-    const int nvec = (hi - a0) / PV;
-    const int a1 = a0 + nvec * PV;
-    for (int i = lo + (int)threadIdx.x; i < a0; i += kAccThreads) f(i, Elem<Tin>::load(row + i));
-    for (int v = threadIdx.x; v < nvec; v += kAccThreads) {
-        float x[PV];
-        Elem<Tin>::load_vec(row + a0 + v * PV, x);
+template <typename Tin>
+struct ChunkRegs {
+    static constexpr int PV = Elem<Tin>::kPerVec;
+    float x[kMaxVec][PV];
+    int a0, a1, nvec;
+
+    __device__ __forceinline__ void load(const Tin *row, int lo, int hi, float fill) {
+        const uintptr_t base = reinterpret_cast<uintptr_t>(row);
+        int s = lo;
+        while (s < hi && ((base + (uintptr_t)s * sizeof(Tin)) & 15u)) ++s;
+        a0 = s;
+        nvec = (hi - a0) / PV;
+        a1 = a0 + nvec * PV;
 #pragma unroll
-        for (int e = 0; e < PV; ++e) f(a0 + v * PV + e, x[e]);
+        for (int v = 0; v < kMaxVec; ++v) {
+            const int vi = threadIdx.x + v * kAccThreads;
+            if (vi < nvec) {
+                Elem<Tin>::load_vec(row + a0 + vi * PV, x[v]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < PV; ++e) x[v][e] = fill;
+            }
+        }
     }
-    for (int i = a1 + (int)threadIdx.x; i < hi; i += kAccThreads) f(i, Elem<Tin>::load(row + i));
-}
+    __device__ __forceinline__ int index(int v, int e) const { return a0 + ((int)threadIdx.x + v * kAccThreads) * PV + e; }
+    __device__ __forceinline__ bool valid(int v) const { return (int)threadIdx.x + v * kAccThreads < nvec; }
+};
 
 __device__ __forceinline__ void warp_argmax(float &v, int &i) {
 #pragma unroll
@@ -101,11 +114,17 @@ __device__ __forceinline__ void block_argmax(float &v, int &i) {
 }
 
 template <typename T>
+__device__ __forceinline__ T warp_sum(T x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <typename T>
 __device__ __forceinline__ T block_sum(T x) {
     __shared__ T sh[kAccThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    x = warp_sum(x);
     __syncthreads();
     if (lane == 0) sh[warp] = x;
     __syncthreads();
@@ -127,12 +146,18 @@ __device__ __forceinline__ float block_max(float x) {
     return t;
 }
 
-// last-CTA election: true in every thread of the CTA that finished last
-__device__ __forceinline__ bool last_cta_done(unsigned int *counter, unsigned int total) {
+// Last-CTA election on `counter` among `total` arrivals: true in every thread of
+// the CTA that arrived last, which also returns the counter to zero.  Writes
+// made before the call by any arriving CTA are visible to the elected one.
+__device__ __forceinline__ bool elect_last(unsigned int *counter, unsigned int total) {
     __shared__ bool is_last;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == total - 1;
+    if (threadIdx.x == 0) {
+        const unsigned int ticket = atomicAdd(counter, 1u);
+        is_last = ticket == total - 1;
+        if (is_last) *counter = 0u;
+    }
     __syncthreads();
     if (is_last) __threadfence();
     return is_last;
@@ -146,59 +171,77 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     const int c = blockIdx.x, row = blockIdx.y;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
     const Tin *lg = static_cast<const Tin *>(p.logits) + (long)row * p.V;
+    ChunkRegs<Tin> cr;
+    cr.load(lg, lo, hi, -INFINITY);
     float bv = -INFINITY;
     int bi = INT_MAX;
-    for_chunk<Tin>(lg, lo, hi, [&](int i, float x) {
+    // ascending index order within the thread keeps the lowest index on ties
+    for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) {
+        const float x = Elem<Tin>::load(lg + i);
         if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
-    });
+    }
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v) {
+        if (!cr.valid(v)) break;
+#pragma unroll
+        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) {
+            const int i = cr.index(v, e);
+            if (argmax_better(cr.x[v][e], i, bv, bi)) { bv = cr.x[v][e]; bi = i; }
+        }
+    }
+    for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) {
+        const float x = Elem<Tin>::load(lg + i);
+        if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
+    }
     block_argmax(bv, bi);
     if (threadIdx.x == 0) {
         p.pval[(long)row * p.n_chunks + c] = bv;
         p.pidx[(long)row * p.n_chunks + c] = bi;
     }
-    const unsigned int total = gridDim.x * gridDim.y;
-    if (!last_cta_done(p.counter, total)) return;
+    if (!elect_last(p.row_counter + row, gridDim.x)) return;
 
-    // finisher: per-row argmax over the chunk partials, then the prefix scan,
-    // over windows holding whole sequences (W rows, a multiple of T)
-    __shared__ int amax[kAccThreads];
-    const int R = p.B * p.T;
-    const int W = (kAccThreads / p.T) * p.T;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r0 = 0; r0 < R; r0 += W) {
-        for (int r = r0 + warp; r < min(R, r0 + W); r += kAccThreads / 32) {
-            float v = -INFINITY;
-            int i = INT_MAX;
-            for (int k = lane; k < p.n_chunks; k += 32) {
-                const float pv = __ldcg(p.pval + (long)r * p.n_chunks + k);
-                const int pi = __ldcg(p.pidx + (long)r * p.n_chunks + k);
-                if (argmax_better(pv, pi, v, i)) { v = pv; i = pi; }
-            }
-            warp_argmax(v, i);
-            if (lane == 0) {
-                if (i == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); i = 0; }
-                amax[r - r0] = i;
-            }
+    // last CTA of this row: the row's argmax from its chunk partials
+    if (threadIdx.x < 32) {
+        float v = -INFINITY;
+        int i = INT_MAX;
+        for (int k = threadIdx.x; k < p.n_chunks; k += 32) {
+            const float pv = __ldcg(p.pval + (long)row * p.n_chunks + k);
+            const int pi = __ldcg(p.pidx + (long)row * p.n_chunks + k);
+            if (argmax_better(pv, pi, v, i)) { v = pv; i = pi; }
         }
+        warp_argmax(v, i);
+        if (threadIdx.x == 0) {
+            if (i == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); i = 0; }
+            p.amax[row] = i;
+        }
+    }
+    if (!elect_last(p.counter, gridDim.y)) return;
+
+    // last row: the first-mismatch scan of every sequence
+    __shared__ int am[kAccThreads];
+    const int R = p.B * p.T;
+    const int W = (kAccThreads / p.T) * p.T;  // whole sequences per window
+    for (int r0 = 0; r0 < R; r0 += W) {
+        for (int r = r0 + (int)threadIdx.x; r < min(R, r0 + W); r += kAccThreads) am[r - r0] = __ldcg(p.amax + r);
         __syncthreads();
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
         for (int bl = threadIdx.x; bl < nbw; bl += kAccThreads) {
             const int b = b0 + bl, rb = bl * p.T;
             int n = p.T - 1;
             for (int j = 0; j < p.T - 1; ++j) {
-                if (p.draft[(long)b * (p.T - 1) + j] != amax[rb + j]) { n = j; break; }
+                if (p.draft[(long)b * (p.T - 1) + j] != am[rb + j]) { n = j; break; }
             }
             p.n_acc[b] = n;
-            p.corr[b] = amax[rb + n];
+            p.corr[b] = am[rb + n];
         }
         __syncthreads();
     }
-    if (threadIdx.x == 0) *p.counter = 0u;
 }
 
 // ----------------------------------------------------------------------------
-// sampled acceptance, pass 1: per-row max and sum of exp over chunks, then the
-// accept scan (last CTA)
+// sampled acceptance, pass 1: per-row max and normaliser of softmax(l / tau);
+// the last CTA of a row also tests that row's proposal, the last row finds
+// the first rejection of every sequence
 // ----------------------------------------------------------------------------
 template <typename Tin>
 __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleParams p) {
@@ -206,81 +249,102 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
     const Tin *lg = static_cast<const Tin *>(p.logits) + (long)row * p.V;
     const float it = p.inv_tau;
+    ChunkRegs<Tin> cr;
+    cr.load(lg, lo, hi, -INFINITY);
     float m = -INFINITY;
-    for_chunk<Tin>(lg, lo, hi, [&](int, float x) { m = fmaxf(m, x * it); });
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v)
+#pragma unroll
+        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) m = fmaxf(m, cr.x[v][e] * it);
+    for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) m = fmaxf(m, Elem<Tin>::load(lg + i) * it);
+    for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) m = fmaxf(m, Elem<Tin>::load(lg + i) * it);
     m = block_max(m);
-    float z = 0.f;
-    if (m != -INFINITY) for_chunk<Tin>(lg, lo, hi, [&](int, float x) { z += expf(x * it - m); });
-    const double zs = block_sum<double>((double)z);
+    double z = 0.0;
+    if (m != -INFINITY) {
+        float zf = 0.f;
+#pragma unroll
+        for (int v = 0; v < kMaxVec; ++v) {
+            float zv = 0.f;
+#pragma unroll
+            for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) zv += expf(cr.x[v][e] * it - m);  // fill -inf -> 0
+            zf += zv;
+        }
+        z = zf;
+        for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) z += expf(Elem<Tin>::load(lg + i) * it - m);
+        for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) z += expf(Elem<Tin>::load(lg + i) * it - m);
+    }
+    z = block_sum<double>(z);
     if (threadIdx.x == 0) {
         p.pm[(long)row * p.n_chunks + c] = m;
-        p.pz[(long)row * p.n_chunks + c] = (float)zs;
+        p.pz[(long)row * p.n_chunks + c] = (float)z;
     }
-    const unsigned int total = gridDim.x * gridDim.y;
-    if (!last_cta_done(p.counters, total)) return;
+    if (!elect_last(p.row_counter + row, gridDim.x)) return;
 
-    // finisher: per-row max / normaliser from the chunk partials (a warp per
-    // row), then one thread per sequence scans its rows in order; windows of
-    // W rows hold whole sequences
-    __shared__ float rowM[kAccThreads];
-    __shared__ float rowZ[kAccThreads];
+    // last CTA of this row: the row's max M and normaliser Z, then the test of
+    // its proposal (rows 0..T-2): accept iff u * q(d) < p(d)
+    if (threadIdx.x < 32) {
+        float M = -INFINITY;
+        for (int k = threadIdx.x; k < p.n_chunks; k += 32) M = fmaxf(M, __ldcg(p.pm + (long)row * p.n_chunks + k));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        double Z = 0.0;
+        for (int k = threadIdx.x; k < p.n_chunks; k += 32) {
+            const float mk = __ldcg(p.pm + (long)row * p.n_chunks + k);
+            if (mk != -INFINITY) Z += (double)__ldcg(p.pz + (long)row * p.n_chunks + k) * (double)expf(mk - M);
+        }
+        Z = warp_sum(Z);
+        if (threadIdx.x == 0) {
+            const int b = row / p.T, j = row % p.T;
+            p.row_stats[row] = make_float2(M, (float)Z);
+            int accept = 0;
+            if (j < p.T - 1) {
+                const int d = p.draft[(long)b * (p.T - 1) + j];
+                if (d >= 0 && d < p.V) {
+                    const float ld = Elem<Tin>::load(lg + d);
+                    const double pd = (double)expf(ld * it - M) / Z;
+                    const double qd = (double)__ldg(p.q + (long)row * p.V + d);
+                    const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
+                    accept = u * qd < pd ? 1 : 0;
+                } else {
+                    set_fault(p.fault, FAULT_BAD_DRAFT_ID);
+                }
+            }
+            p.accept[row] = accept;
+        }
+    }
+    if (!elect_last(p.counters, gridDim.y)) return;
+
+    // last row: first rejection of every sequence
+    __shared__ int acc_s[kAccThreads];
     const int R = p.B * p.T;
     const int W = (kAccThreads / p.T) * p.T;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int r0 = 0; r0 < R; r0 += W) {
-        for (int r = r0 + warp; r < min(R, r0 + W); r += kAccThreads / 32) {
-            float M = -INFINITY;
-            for (int k = lane; k < p.n_chunks; k += 32) M = fmaxf(M, __ldcg(p.pm + (long)r * p.n_chunks + k));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            double Z = 0.0;
-            for (int k = lane; k < p.n_chunks; k += 32) {
-                const float mk = __ldcg(p.pm + (long)r * p.n_chunks + k);
-                if (mk != -INFINITY)
-                    Z += (double)__ldcg(p.pz + (long)r * p.n_chunks + k) * (double)expf(mk - M);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-            if (lane == 0) { rowM[r - r0] = M; rowZ[r - r0] = (float)Z; }
-        }
+        for (int r = r0 + (int)threadIdx.x; r < min(R, r0 + W); r += kAccThreads) acc_s[r - r0] = __ldcg(p.accept + r);
         __syncthreads();
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
         for (int bl = threadIdx.x; bl < nbw; bl += kAccThreads) {
             const int b = b0 + bl;
             int n = p.T - 1;
-            for (int j = 0; j < p.T - 1; ++j) {
-                const long r = (long)b * p.T + j;
-                const float M = rowM[bl * p.T + j], Zr = rowZ[bl * p.T + j];
-                const int d = p.draft[(long)b * (p.T - 1) + j];
-                float pd = 0.f, qd = 0.f;
-                if (d >= 0 && d < p.V) {
-                    const Tin *lgr = static_cast<const Tin *>(p.logits) + r * p.V;
-                    pd = expf(Elem<Tin>::load(lgr + d) * it - M) / Zr;
-                    qd = __ldg(p.q + r * p.V + d);
-                } else {
-                    set_fault(p.fault, FAULT_BAD_DRAFT_ID);
-                }
-                const float u = philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
-                if (!(u * qd < pd)) { n = j; break; }
-            }
+            for (int j = 0; j < p.T - 1; ++j)
+                if (!acc_s[bl * p.T + j]) { n = j; break; }
+            const float2 st = __ldcg(p.row_stats + (long)b * p.T + n);
             p.n_acc[b] = n;
-            p.state[b] = make_float4(__int_as_float(n), rowM[bl * p.T + n], rowZ[bl * p.T + n], 0.f);
+            p.state[b] = make_float4(__int_as_float(n), st.x, st.y, 0.f);
         }
         __syncthreads();
     }
-    if (threadIdx.x == 0) *p.counters = 0u;
 }
 
 // ----------------------------------------------------------------------------
-// sampled acceptance, pass 2: chunk sums of the residual (and of p) on the
-// row that decides the next token, then the inverse-cdf draw (last CTA)
+// sampled acceptance, pass 2: on the row that decides the next token, chunk
+// sums of the residual r = max(p - q, 0) and of p; the last CTA of the
+// sequence picks the chunk where u' * S falls and searches inside it
 // ----------------------------------------------------------------------------
-template <typename Tin>
-__device__ __forceinline__ float draw_weight(const SampleParams &p, const Tin *lg, const float *qn,
-                                             bool residual, float M, float Z, int i, float x) {
-    const float pi = expf(x * p.inv_tau - M) / Z;
+// the weight of element i (the same fp32 arithmetic wherever it is used)
+__device__ __forceinline__ float residual_or_p(float x, float it, float M, float Z, float qi, bool residual) {
+    const float pi = expf(x * it - M) / Z;
     if (!residual) return pi;
-    const float r = pi - __ldg(qn + i);
+    const float r = pi - qi;
     return r > 0.f ? r : 0.f;
 }
 
@@ -291,108 +355,140 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     const int n = __float_as_int(st.x);
     const float M = st.y, Z = st.z;
     const bool rejected = n < p.T - 1;
-    const long r = (long)b * p.T + n;
-    const Tin *lg = static_cast<const Tin *>(p.logits) + r * p.V;
-    const float *qn = p.q + r * p.V;
+    const long row = (long)b * p.T + n;
+    const Tin *lg = static_cast<const Tin *>(p.logits) + row * p.V;
+    const float *qn = p.q + row * p.V;
+    const float it = p.inv_tau;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
+    ChunkRegs<Tin> cr;
+    cr.load(lg, lo, hi, -INFINITY);
     double sr = 0.0, sp = 0.0;
-    for_chunk<Tin>(lg, lo, hi, [&](int i, float x) {
-        const float pi = expf(x * p.inv_tau - M) / Z;
-        sp += pi;
-        if (rejected) {
-            const float rr = pi - __ldg(qn + i);
-            sr += rr > 0.f ? rr : 0.f;
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v) {
+        if (!cr.valid(v)) break;
+        float qv[ChunkRegs<Tin>::PV];
+#pragma unroll
+        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) qv[e] = rejected ? __ldg(qn + cr.index(v, e)) : 0.f;
+#pragma unroll
+        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) {
+            const float pi = expf(cr.x[v][e] * it - M) / Z;
+            sp += pi;
+            if (rejected) { const float r = pi - qv[e]; sr += r > 0.f ? r : 0.f; }
         }
-    });
+    }
+    auto scalar = [&](int i) {
+        const float pi = expf(Elem<Tin>::load(lg + i) * it - M) / Z;
+        sp += pi;
+        if (rejected) { const float r = pi - __ldg(qn + i); sr += r > 0.f ? r : 0.f; }
+    };
+    for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) scalar(i);
+    for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) scalar(i);
     sr = block_sum<double>(sr);
     sp = block_sum<double>(sp);
     if (threadIdx.x == 0) {
         p.rs[(long)b * p.n_chunks + c] = sr;
         p.ps[(long)b * p.n_chunks + c] = sp;
     }
-    const unsigned int total = gridDim.x * gridDim.y;
-    if (!last_cta_done(p.counters + 1, total)) return;
+    if (!elect_last(p.row_counter + b, gridDim.x)) return;
 
-    __shared__ double tsum[kAccThreads];
-    __shared__ int sel_chunk;
+    // last CTA of sequence b: which chunk holds u' * S
+    __shared__ int sel_chunk, sel_res;
     __shared__ double sel_base, sel_x;
-    __shared__ int sel_res;
-    for (int bb = 0; bb < p.B; ++bb) {
-        const float4 s2 = __ldcg(&p.state[bb]);
-        const int nb = __float_as_int(s2.x);
-        const float Mb = s2.y, Zb = s2.z;
-        const bool rej = nb < p.T - 1;
-        if (threadIdx.x == 0) {
-            double Sr = 0.0, Sp = 0.0;
-            for (int k = 0; k < p.n_chunks; ++k) {
-                Sr += __ldcg(p.rs + (long)bb * p.n_chunks + k);
-                Sp += __ldcg(p.ps + (long)bb * p.n_chunks + k);
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        double Sr = 0.0, Sp = 0.0;
+        for (int k = lane; k < p.n_chunks; k += 32) {
+            Sr += __ldcg(p.rs + (long)b * p.n_chunks + k);
+            Sp += __ldcg(p.ps + (long)b * p.n_chunks + k);
+        }
+        Sr = warp_sum(Sr);
+        Sp = warp_sum(Sp);
+        const bool use_r = rejected && Sr > 0.0;
+        const double *cs = (use_r ? p.rs : p.ps) + (long)b * p.n_chunks;
+        const double S = use_r ? Sr : Sp;
+        const double x = (double)philox_uniform(p.seed, (uint32_t)n, (uint32_t)b, 1u, p.offset) * S;
+        // inclusive prefix over the chunk sums, 32 chunks at a time
+        double carry = 0.0;
+        int found = -1, last_pos = -1;
+        double found_base = 0.0;
+        for (int k0 = 0; k0 < p.n_chunks && found < 0; k0 += 32) {
+            const int k = k0 + lane;
+            const double v = k < p.n_chunks ? __ldcg(cs + k) : 0.0;
+            double incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
-            const bool use_r = rej && Sr > 0.0;
-            const double* cs = use_r ? p.rs : p.ps;
-            const double S = use_r ? Sr : Sp;
-            const float u2 = philox_uniform(p.seed, (uint32_t)nb, (uint32_t)bb, 1u, p.offset);
-            const double x = (double)u2 * S;
+            const unsigned pos = __ballot_sync(0xffffffffu, k < p.n_chunks && v > 0.0);
+            if (pos) last_pos = k0 + 31 - __clz((int)pos);
+            const unsigned hit = __ballot_sync(0xffffffffu, k < p.n_chunks && carry + incl > x);
+            if (hit) {
+                const int l = __ffs((int)hit) - 1;
+                found = k0 + l;
+                found_base = carry + __shfl_sync(0xffffffffu, incl - v, l);
+            }
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (found < 0) {  // x reached the total through rounding: the last non-empty chunk
+            found = last_pos < 0 ? 0 : last_pos;
             double base = 0.0;
-            int ck = -1, last_pos = 0;
-            for (int k = 0; k < p.n_chunks; ++k) {
-                const double v = __ldcg(cs + (long)bb * p.n_chunks + k);
-                if (v > 0.0) last_pos = k;
-                if (ck < 0 && base + v > x) { ck = k; break; }
-                base += v;
-            }
-            if (ck < 0) {  // x reached the total through rounding: last non-empty chunk
-                ck = last_pos;
-                base = 0.0;
-                for (int k = 0; k < ck; ++k) base += __ldcg(cs + (long)bb * p.n_chunks + k);
-            }
-            sel_chunk = ck; sel_base = base; sel_x = x; sel_res = use_r ? 1 : 0;
+            for (int k = lane; k < found; k += 32) base += __ldcg(cs + k);
+            found_base = warp_sum(base);
         }
-        __syncthreads();
-        // inclusive scan of the selected chunk, in index order: each thread owns a
-        // contiguous run, runs are combined by an exclusive scan over threads
-        const long rr = (long)bb * p.T + nb;
-        const Tin *lgb = static_cast<const Tin *>(p.logits) + rr * p.V;
-        const float *qb = p.q + rr * p.V;
-        const int clo = sel_chunk * p.chunk, chi = min(p.V, clo + p.chunk);
-        const int per = (chi - clo + kAccThreads - 1) / kAccThreads;
-        const int tlo = min(chi, clo + (int)threadIdx.x * per), thi = min(chi, tlo + per);
-        double run = 0.0;
-        for (int i = tlo; i < thi; ++i)
-            run += draw_weight<Tin>(p, lgb, qb, sel_res != 0, Mb, Zb, i, Elem<Tin>::load(lgb + i));
-        tsum[threadIdx.x] = run;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            // find the thread whose run crosses x, then the element
-            double acc = sel_base;
-            int owner = -1;
-            for (int t = 0; t < kAccThreads; ++t) {
-                if (acc + tsum[t] > sel_x) { owner = t; break; }
-                acc += tsum[t];
-            }
-            int id = -1, last_pos = -1;
-            if (owner >= 0) {
-                const int olo = min(chi, clo + owner * per), ohi = min(chi, olo + per);
-                for (int i = olo; i < ohi; ++i) {
-                    const float w = draw_weight<Tin>(p, lgb, qb, sel_res != 0, Mb, Zb, i,
-                                                     Elem<Tin>::load(lgb + i));
-                    if (w > 0.f) last_pos = i;
-                    acc += w;
-                    if (acc > sel_x) { id = i; break; }
-                }
-            }
-            if (id < 0) {  // rounding: the last positive-weight index of the chunk
-                for (int i = chi - 1; i >= clo; --i) {
-                    if (draw_weight<Tin>(p, lgb, qb, sel_res != 0, Mb, Zb, i,
-                                         Elem<Tin>::load(lgb + i)) > 0.f) { last_pos = i; break; }
-                }
-                id = last_pos >= 0 ? last_pos : clo;
-            }
-            p.next_id[bb] = id;
+        if (lane == 0) { sel_chunk = found; sel_base = found_base; sel_x = x; sel_res = use_r ? 1 : 0; }
+    }
+    __syncthreads();
+
+    // inside the chunk: thread t owns a contiguous run of elements; runs are
+    // combined by an exclusive scan over the threads, the owner of the
+    // crossing then walks its run
+    constexpr int kRun = 16;
+    const int clo = sel_chunk * p.chunk, chi = min(p.V, clo + p.chunk);
+    const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (chunk <= 4096)
+    const int tlo = min(chi, clo + (int)threadIdx.x * per), thi = min(chi, tlo + per);
+    const bool res = sel_res != 0;
+    float w[kRun];
+    double run = 0.0;
+#pragma unroll
+    for (int e = 0; e < kRun; ++e) {
+        const int i = tlo + e;
+        w[e] = 0.f;
+        if (i < thi) {
+            const float qi = res ? __ldg(qn + i) : 0.f;
+            w[e] = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, qi, res);
         }
+        run += w[e];
+    }
+    __shared__ double tsum[kAccThreads];
+    __shared__ int s_id, s_lastpos;
+    tsum[threadIdx.x] = run;
+    if (threadIdx.x == 0) { s_id = INT_MAX; s_lastpos = -1; }
+    __syncthreads();
+    // inclusive scan over the threads (Hillis-Steele in shared memory)
+    for (int o = 1; o < kAccThreads; o <<= 1) {
+        const double y = threadIdx.x >= (unsigned)o ? tsum[threadIdx.x - o] : 0.0;
+        __syncthreads();
+        tsum[threadIdx.x] += y;
         __syncthreads();
     }
-    if (threadIdx.x == 0) p.counters[1] = 0u;
+    double acc = sel_base + (tsum[threadIdx.x] - run);
+    int last_here = -1;
+#pragma unroll
+    for (int e = 0; e < kRun; ++e) {
+        if (tlo + e >= thi) break;
+        if (w[e] > 0.f) last_here = tlo + e;
+        const double nxt = acc + (double)w[e];
+        if (nxt > sel_x && acc <= sel_x) { atomicMin(&s_id, tlo + e); break; }
+        acc = nxt;
+    }
+    if (last_here >= 0) atomicMax(&s_lastpos, last_here);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int id = s_id;
+        if (id == INT_MAX) id = s_lastpos >= 0 ? s_lastpos : clo;  // rounding: last positive weight
+        p.next_id[b] = id;
+    }
 }
 
 }  // namespace

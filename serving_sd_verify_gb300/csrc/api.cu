@@ -158,25 +158,49 @@ size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max
 // ----------------------------------------------------------------------------
 // acceptance planning
 // ----------------------------------------------------------------------------
-int accept_chunk(int rows, int V) {
+int accept_chunk(int rows, int V, int cap) {
     const int sms = device_sm_count();
     const long target = 4L * sms;  // CTAs
     long chunk = ((long)rows * V + target - 1) / target;
-    chunk = std::max(2048L, std::min(chunk, 16384L));
+    chunk = std::max(2048L, std::min(chunk, (long)cap));
     chunk = (chunk + 7) / 8 * 8;
     return (int)std::min<long>(chunk, (long)V);
 }
 
-size_t greedy_ws(int B, int T, int V, int chunk) {
-    const size_t parts = (size_t)B * T * ((V + chunk - 1) / chunk);
-    return kHeader + align_up(parts * sizeof(float), 256) + align_up(parts * sizeof(int), 256);
+int greedy_cap(sd_dtype dt) { return dt == SD_BF16 ? kGreedyChunkMaxBf16 : kGreedyChunkMaxF32; }
+
+// greedy workspace: [header: rows-finished counter][row counters][pval][pidx][amax]
+struct GreedyLayout {
+    size_t row_ctr, pval, pidx, amax, total;
+};
+GreedyLayout greedy_layout(int B, int T, int V, int chunk) {
+    const size_t R = (size_t)B * T, parts = R * ((V + chunk - 1) / chunk);
+    GreedyLayout l;
+    l.row_ctr = kHeader;
+    l.pval = l.row_ctr + align_up(R * 4, 256);
+    l.pidx = l.pval + align_up(parts * 4, 256);
+    l.amax = l.pidx + align_up(parts * 4, 256);
+    l.total = l.amax + align_up(R * 4, 256);
+    return l;
 }
 
-size_t sample_ws(int B, int T, int V, int chunk) {
-    const int nc = (V + chunk - 1) / chunk;
-    const size_t parts = (size_t)B * T * nc;
-    return kHeader + 2 * align_up(parts * sizeof(float), 256) + align_up((size_t)B * sizeof(float4), 256) +
-           2 * align_up((size_t)B * nc * sizeof(double), 256);
+// sample workspace: [header: counters][row counters][pm][pz][row_stats][accept][state][rs][ps]
+struct SampleLayout {
+    size_t row_ctr, pm, pz, row_stats, accept, state, rs, ps, total;
+};
+SampleLayout sample_layout(int B, int T, int V, int chunk) {
+    const size_t R = (size_t)B * T, nc = (V + chunk - 1) / chunk, parts = R * nc;
+    SampleLayout l;
+    l.row_ctr = kHeader;
+    l.pm = l.row_ctr + align_up(R * 4, 256);
+    l.pz = l.pm + align_up(parts * 4, 256);
+    l.row_stats = l.pz + align_up(parts * 4, 256);
+    l.accept = l.row_stats + align_up(R * 8, 256);
+    l.state = l.accept + align_up(R * 4, 256);
+    l.rs = l.state + align_up((size_t)B * 16, 256);
+    l.ps = l.rs + align_up((size_t)B * nc * 8, 256);
+    l.total = l.ps + align_up((size_t)B * nc * 8, 256);
+    return l;
 }
 
 }  // namespace
@@ -275,9 +299,8 @@ size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, in
 }
 
 size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
-    (void)dtype;
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
-    return greedy_ws(B, T, V, accept_chunk(B * T, V));
+    return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype))).total;
 }
 
 sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, int B, int T, int V,
@@ -292,17 +315,18 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
     GreedyParams p = {};
     p.draft = draft_ids; p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
     p.n_acc = n_accepted; p.corr = correction_id;
-    p.chunk = accept_chunk(B * T, V);
+    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype));
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
-    const size_t need = greedy_ws(B, T, V, p.chunk);
-    if (!workspace || workspace_bytes < need)
-        return fail(SD_ERR_WORKSPACE, "greedy workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    const GreedyLayout gl = greedy_layout(B, T, V, p.chunk);
+    if (!workspace || workspace_bytes < gl.total)
+        return fail(SD_ERR_WORKSPACE, "greedy workspace too small: need %zu bytes, got %zu", gl.total, workspace_bytes);
     if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     char *w = static_cast<char *>(workspace);
-    const size_t parts = (size_t)B * T * p.n_chunks;
     p.counter = reinterpret_cast<unsigned int *>(w);
-    p.pval = reinterpret_cast<float *>(w + kHeader);
-    p.pidx = reinterpret_cast<int *>(w + kHeader + align_up(parts * sizeof(float), 256));
+    p.row_counter = reinterpret_cast<unsigned int *>(w + gl.row_ctr);
+    p.pval = reinterpret_cast<float *>(w + gl.pval);
+    p.pidx = reinterpret_cast<int *>(w + gl.pidx);
+    p.amax = reinterpret_cast<int *>(w + gl.amax);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     cudaError_t e = launch_accept_greedy(p, static_cast<cudaStream_t>(stream));
@@ -313,7 +337,7 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
 size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype) {
     (void)dtype;
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
-    return sample_ws(B, T, V, accept_chunk(B * T, V));
+    return sample_layout(B, T, V, accept_chunk(B * T, V, kSampleChunkMax)).total;
 }
 
 sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, const void *target_logits,
@@ -333,21 +357,22 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.draft = draft_ids; p.q = draft_probs; p.logits = target_logits; p.B = B; p.T = T; p.V = V;
     p.dt = dtype; p.inv_tau = 1.0f / temperature; p.seed = philox_seed; p.offset = philox_offset;
     p.n_acc = n_accepted; p.next_id = next_id;
-    p.chunk = accept_chunk(B * T, V);
+    p.chunk = accept_chunk(B * T, V, kSampleChunkMax);
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
-    const size_t need = sample_ws(B, T, V, p.chunk);
-    if (!workspace || workspace_bytes < need)
-        return fail(SD_ERR_WORKSPACE, "sample workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    const SampleLayout sl = sample_layout(B, T, V, p.chunk);
+    if (!workspace || workspace_bytes < sl.total)
+        return fail(SD_ERR_WORKSPACE, "sample workspace too small: need %zu bytes, got %zu", sl.total, workspace_bytes);
     if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     char *w = static_cast<char *>(workspace);
-    const size_t parts = (size_t)B * T * p.n_chunks;
-    size_t off = kHeader;
     p.counters = reinterpret_cast<unsigned int *>(w);
-    p.pm = reinterpret_cast<float *>(w + off); off += align_up(parts * sizeof(float), 256);
-    p.pz = reinterpret_cast<float *>(w + off); off += align_up(parts * sizeof(float), 256);
-    p.state = reinterpret_cast<float4 *>(w + off); off += align_up((size_t)B * sizeof(float4), 256);
-    p.rs = reinterpret_cast<double *>(w + off); off += align_up((size_t)B * p.n_chunks * sizeof(double), 256);
-    p.ps = reinterpret_cast<double *>(w + off);
+    p.row_counter = reinterpret_cast<unsigned int *>(w + sl.row_ctr);
+    p.pm = reinterpret_cast<float *>(w + sl.pm);
+    p.pz = reinterpret_cast<float *>(w + sl.pz);
+    p.row_stats = reinterpret_cast<float2 *>(w + sl.row_stats);
+    p.accept = reinterpret_cast<int *>(w + sl.accept);
+    p.state = reinterpret_cast<float4 *>(w + sl.state);
+    p.rs = reinterpret_cast<double *>(w + sl.rs);
+    p.ps = reinterpret_cast<double *>(w + sl.ps);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     cudaError_t e = launch_accept_sample(p, static_cast<cudaStream_t>(stream));

@@ -162,9 +162,11 @@ attn_split_generic_kernel(const AttnParams p) {
     }
 }
 
-// One warp per output row: out = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M).
-// Lane k computes the weight of split s0 + k; the weights are broadcast by
-// shuffles so the partial-output loads of consecutive splits are independent.
+// Log-sum-exp merge of the split partials, one CTA of 4 warps per output row:
+//   out = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M),  M = max_s lse_s.
+// Warp w takes splits w, w+4, ...; each lane owns D/32 output columns.  Empty
+// splits carry lse = -inf and a zero partial, so the sums need no branch and
+// the loads of four splits are in flight together.
 template <int D>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict__ o_part,
                                                         const float *__restrict__ lse_part,
@@ -173,50 +175,63 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict_
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
     constexpr int VW = D / 32;  // floats per lane
-    const long row = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+    __shared__ float s_max[4];
+    __shared__ float s_wsum[4];
+    __shared__ float s_acc[4][D];
+    const long row = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float M = -INFINITY;
-    for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, __ldcg(lse_part + (long)s * rows + row));
+    for (int sp = threadIdx.x; sp < n_splits; sp += 128) M = fmaxf(M, __ldcg(lse_part + (long)sp * rows + row));
     M = warp_max(M);
+    if (lane == 0) s_max[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
     float acc[VW];
 #pragma unroll
     for (int e = 0; e < VW; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int s0 = 0; s0 < n_splits; s0 += 32) {
-            const int s = s0 + lane;
-            float w = 0.f;
-            if (s < n_splits) {
-                const float l = __ldcg(lse_part + (long)s * rows + row);
-                w = l == -INFINITY ? 0.f : __expf(l - M);
-            }
-            wsum += w;
-            const int nk = min(32, n_splits - s0);
-#pragma unroll 4
-            for (int k = 0; k < nk; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, w, k);
-                if (wk == 0.f) continue;
-                const float *src = o_part + ((long)(s0 + k) * rows + row) * D + lane * VW;
-                if (VW == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                    acc[0] = fmaf(wk, v.x, acc[0]); acc[1] = fmaf(wk, v.y, acc[1]);
-                    acc[2] = fmaf(wk, v.z, acc[2]); acc[3] = fmaf(wk, v.w, acc[3]);
+        int sp = warp;
+        for (; sp + 12 < n_splits; sp += 16) {
+            float w[4], v[4][VW];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const long ss = sp + 4 * u;
+                const float l = __ldcg(lse_part + ss * rows + row);
+                w[u] = __expf(l - M);  // 0 for an empty split (l = -inf)
+                const float *src = o_part + (ss * rows + row) * D + lane * VW;
+                if constexpr (VW == 4) {
+                    const float4 t4 = __ldcg(reinterpret_cast<const float4 *>(src));
+                    v[u][0] = t4.x; v[u][1] = t4.y; v[u][2] = t4.z; v[u][3] = t4.w;
                 } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                    acc[0] = fmaf(wk, v.x, acc[0]); acc[1] = fmaf(wk, v.y, acc[1]);
+                    const float2 t2 = __ldcg(reinterpret_cast<const float2 *>(src));
+                    v[u][0] = t2.x; v[u][1] = t2.y;
                 }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                wsum += w[u];
+#pragma unroll
+                for (int e = 0; e < VW; ++e) acc[e] = fmaf(w[u], v[u][e], acc[e]);
+            }
+        }
+        for (; sp < n_splits; sp += 4) {
+            const float l = __ldcg(lse_part + (long)sp * rows + row);
+            const float w = __expf(l - M);
+            const float *src = o_part + ((long)sp * rows + row) * D + lane * VW;
+            wsum += w;
+#pragma unroll
+            for (int e = 0; e < VW; ++e) acc[e] = fmaf(w, __ldcg(src + e), acc[e]);
         }
     }
-    wsum = warp_sum(wsum);
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    float *dst = out + row * D + lane * VW;
-    if (VW == 4) {
-        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    } else {
-        *reinterpret_cast<float2 *>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
-    }
+    if (lane == 0) s_wsum[warp] = wsum;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) s_acc[warp][lane * VW + e] = acc[e];
+    __syncthreads();
+    const float wt = (s_wsum[0] + s_wsum[1]) + (s_wsum[2] + s_wsum[3]);
+    const float inv = wt > 0.f ? 1.f / wt : 0.f;
+    for (int d = threadIdx.x; d < D; d += 128)
+        out[row * D + d] = ((s_acc[0][d] + s_acc[1][d]) + (s_acc[2][d] + s_acc[3][d])) * inv;
 }
 
 template <typename Tin, int D>
@@ -252,7 +267,7 @@ cudaError_t launch_attn_generic(const AttnParams &p, cudaStream_t st) {
 cudaError_t launch_lse_merge(const AttnParams &p, cudaStream_t st) {
     const long rows = (long)p.B * p.T * p.Hq;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
+    cfg.gridDim = dim3((unsigned)rows);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;

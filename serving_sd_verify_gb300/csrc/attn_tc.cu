@@ -19,16 +19,20 @@
 //
 // Warp roles (320 threads):
 //   warps 0-3 / 4-7  two softmax warpgroups; warpgroup w takes the tiles with
-//                    t mod 2 == w, has its own S/P buffer and O accumulator in
-//                    tensor memory and its own running max / sum; thread = row
-//                    (= tensor-memory lane).  The two halves are merged at the
-//                    end like two splits.
-//   warp 8           TMA producer of a K/V ring in shared memory
+//                    t mod 2 == w, has two S/P buffers and its own O
+//                    accumulator in tensor memory and its own running max /
+//                    sum; thread = row (= tensor-memory lane).  The two halves
+//                    are merged at the end like two splits.
+//   warp 8           TMA producer: Q first, then a K/V ring in shared memory
 //   warp 9           allocates tensor memory; one thread issues the MMAs,
 //                    serving whichever of "next S" / "next P.V" is ready.
-// P is written back into the tensor-memory columns that held S (variant
-// kPTmem) and read by the MMA as its A operand, which leaves shared memory to
-// a 5-stage K/V ring; the other variant stages P through shared memory.
+// Tensor memory: O0 [0,128), O1 [128,256), four S/P buffers of 64 columns;
+// tile t uses buffer t mod 4, so S of tile t+2 is computed while P.V of tile
+// t is still pending.  P is written back into the columns that held S
+// (variant kPTmem) and read by the MMA as its A operand, which leaves shared
+// memory to a 5-stage K/V ring; the other variant stages P through shared
+// memory.  The partial output leaves through shared memory so that the global
+// stores are coalesced.
 // The running max only moves when it grows by more than 2^8, so O is rescaled
 // in tensor memory rarely (exact either way: P and l use the same reference).
 // Every wait is bounded by the global timer; a wait that gives up sets the
@@ -53,7 +57,8 @@ constexpr int kKBytes = 2 * kBN * 128;      // two K-blocks of [64 keys x 128 B]
 constexpr int kVBytes = 2 * kBN * 128;      // two d-chunks of [64 keys x 128 B]
 constexpr int kStageBytes = kKBytes + kVBytes;
 constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16, one half (hi or lo)
-constexpr uint32_t kTmemCols = 512;         // O0 [0,128) O1 [128,256) SP0 [256,320) SP1 [320,384)
+constexpr uint32_t kTmemCols = 512;         // O0 [0,128) O1 [128,256) SP0..SP3 [256 + 64 i, +64)
+constexpr int kOStride = 132;               // floats per staged output row (bank-conflict padding)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -65,8 +70,8 @@ template <bool kPTmem> struct Layout {
     static constexpr int kOffStage = kQBytes;
     static constexpr int kOffP = kOffStage + kStages * kStageBytes;          // smem P (variant 2 only)
     static constexpr int kOffBar = kOffP + (kPTmem ? 0 : 4 * kPBytes);
-    // full[S], empty[S], sfull[2], pfull[2], pempty[2], qready, drain
-    static constexpr int kNumBars = 2 * kStages + 8;
+    // full[S], empty[S], sfull[4], pfull[4], pempty[4], qready, drain
+    static constexpr int kNumBars = 2 * kStages + 14;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                  // tmem base, abort flag
     static constexpr int kOffXchg = kOffMisc + 16;                           // (m, l) exchange
     static constexpr int kSmemBytes = kOffXchg + 2 * 128 * 8 + 1024;         // + alignment slack
@@ -76,6 +81,7 @@ struct TcParams {
     AttnParams a;
     int dim_s, dim_h;   // tensor-map dimension index of the slot and kv-head axes (1 or 2)
 };
+static_assert(128 * kOStride * 4 <= 5 * (2 * 64 * 128 * 2), "output staging fits in the K/V ring");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -198,16 +204,32 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 #define SDV_S8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
                   "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 
-// 32 consecutive 32-bit columns of this thread's lane; waits for completion
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 consecutive 32-bit columns of this thread's lane; completes at tmem_ld_wait
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13,"
         " %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : SDV_R8(0), SDV_R8(8), SDV_R8(16), SDV_R8(24)
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    // tie the registers to the wait so no use is scheduled above it
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// ties registers filled by tmem_ld32_async to the preceding wait
+__device__ __forceinline__ void tmem_ld_bind(uint32_t (&r)[32]) {
     asm volatile("" : SDV_W8(0), SDV_W8(8), SDV_W8(16), SDV_W8(24));
+}
+
+// 64 consecutive columns: both loads in flight before the single wait
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13,"
+        " %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31,"
+        " %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47,"
+        " %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+        : SDV_R8(0), SDV_R8(8), SDV_R8(16), SDV_R8(24), SDV_R8(32), SDV_R8(40), SDV_R8(48), SDV_R8(56)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile("" : SDV_W8(0), SDV_W8(8), SDV_W8(16), SDV_W8(24), SDV_W8(32), SDV_W8(40), SDV_W8(48),
+                 SDV_W8(56));
 }
 // store without waiting (callers issue tmem_st_wait once after a batch)
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -238,8 +260,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(
 // ---------------------------------------------------------------------------
 template <bool kPTmem>
 __global__ void __launch_bounds__(kTcThreads, 1)
-attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                     const TcParams tp) {
+attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const TcParams tp) {
     using L = Layout<kPTmem>;
     constexpr int NS = L::kStages;
     const AttnParams &p = tp.a;
@@ -256,10 +278,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (NS + i); };
     auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + i); };
-    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + 2 + i); };
-    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + 4 + i); };
-    const uint32_t qready_bar = bar0 + 8u * (2 * NS + 6);
-    const uint32_t drain_bar = bar0 + 8u * (2 * NS + 7);
+    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + 4 + i); };
+    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + 8 + i); };
+    const uint32_t qready_bar = bar0 + 8u * (2 * NS + 12);
+    const uint32_t drain_bar = bar0 + 8u * (2 * NS + 13);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 8);
     float2 *xchg = reinterpret_cast<float2 *>(sbase + L::kOffXchg);  // [2][128] (m, l) per warpgroup
@@ -267,8 +289,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
     // ---- prologue that reads nothing produced upstream ----
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 4); mbar_init(pempty_bar(i), 1); }
-        mbar_init(qready_bar, 8);
+        for (int i = 0; i < 4; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 4); mbar_init(pempty_bar(i), 1); }
+        mbar_init(qready_bar, 1 + 4);  // Q copy (with its bytes) + the four warps that zero the padding rows
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -305,13 +327,22 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
     auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
 
     if (n_tiles == 0) {
-        // nothing to read: mark the split empty for the merge
-        if (tid < M) {
-            const int j = tid / G, h = g * G + tid % G;
-            p.lse_part[(long)s * rows_total + ((long)b * T + j) * p.Hq + h] = -INFINITY;
+        // nothing to read: an empty split (lse = -inf, zero partial) for the merge
+        for (int idx = tid; idx < M * 32; idx += kTcThreads) {
+            const int rr = idx >> 5, c4 = idx & 31;
+            const long frow = ((long)b * T + rr / G) * p.Hq + g * G + rr % G;
+            reinterpret_cast<float4 *>(p.o_part + ((long)s * rows_total + frow) * 128)[c4] =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c4 == 0) p.lse_part[(long)s * rows_total + frow] = -INFINITY;
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            // Q first: rows r = j*G + hl of this kv head, two 64-column halves
+            mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * M));
+            tma_load_4d(sQ, &tmap_q, qready_bar, 0, g * G, 0, b);
+            tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, g * G, 0, b);
+        }
         int t = 0;
         if (has_block_tile) {
             // the T block keys / values from [B, T, Hkv, D] into stage 0; rows >= T zero
@@ -353,6 +384,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
             }
             // on abort: let the copies already issued land before the CTA exits
             if (*abort_flag) {
+                mbar_wait(qready_bar, 0, nullptr, p.fault);
                 for (int u = max(0, issued - NS); u < issued; ++u)
                     mbar_wait(full_bar(u % NS), (u / NS) & 1, nullptr, p.fault);
             }
@@ -369,13 +401,14 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
             uint32_t spins = 0;
             while (ok && nP < n_tiles) {
                 bool did = false;
-                // S_nS into buffer nS & 1 once K is loaded and P.V of tile nS-2 is done
-                if (nS < n_tiles && nS < nP + 2) {
+                // S of tile nS into buffer nS % 4 once K is loaded and the buffer's
+                // previous occupant (tile nS-4) has been consumed by its P.V
+                if (nS < n_tiles && nS < nP + 4) {
                     const int st = nS % NS;
                     if (mbar_test(full_bar(st), (nS / NS) & 1) &&
-                        (nS < 2 || mbar_test(pempty_bar(nS & 1), ((nS - 2) >> 1) & 1))) {
+                        (nS < 4 || mbar_test(pempty_bar(nS & 3), ((nS >> 2) - 1) & 1))) {
                         tc_fence_after();
-                        const uint32_t dcol = tmem + 256u + 64u * (nS & 1);
+                        const uint32_t dcol = tmem + 256u + 64u * (nS & 3);
                         const uint32_t kbase = sStage + st * kStageBytes;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
@@ -383,13 +416,13 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
                             const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
                             umma_ss(dcol, a, bd, idS, kk > 0 ? 1u : 0u);
                         }
-                        umma_commit(sfull_bar(nS & 1));
+                        umma_commit(sfull_bar(nS & 3));
                         ++nS;
                         did = true;
                     }
                 }
                 // P.V of tile nP once its softmax is done
-                if (nP < nS && mbar_test(pfull_bar(nP & 1), (nP >> 1) & 1)) {
+                if (nP < nS && mbar_test(pfull_bar(nP & 3), (nP >> 2) & 1)) {
                     tc_fence_after();
                     const int st = nP % NS;
                     const int wb = nP & 1;
@@ -401,7 +434,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
                             const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, kBN * 128, 1024);
                             const uint32_t acc = (nP >= 2 || half > 0 || kk > 0) ? 1u : 0u;
                             if (kPTmem) {
-                                const uint32_t a_t = tmem + 256u + 64u * wb + 32u * half + 8u * kk;
+                                const uint32_t a_t = tmem + 256u + 64u * (nP & 3) + 32u * half + 8u * kk;
                                 umma_ts(tmem + 128u * wb, a_t, bd, idO, acc);
                             } else {
                                 const uint64_t a = sw128_desc(sP + (wb * 2 + half) * kPBytes + kk * 32, 16, 1024);
@@ -409,7 +442,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
                             }
                         }
                     }
-                    umma_commit(pempty_bar(wb));
+                    umma_commit(pempty_bar(nP & 3));
                     umma_commit(empty_bar(st));
                     ++nP;
                     did = true;
@@ -440,42 +473,31 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
         const float qk = p.scale * kLog2e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t o_col = tmem + lane_off + 128u * wg;
-        const uint32_t sp_col = tmem + lane_off + 256u + 64u * wg;
         if (wg == 0) {
-            // Q rows r = j*G + hl of this kv head, zero-padded to 128 rows, 128-byte swizzled
-            const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-            uint4 v[16];
+            // Q rows past the M real rows are zero (the copy fills rows [0, M))
+            if (!row_ok) {
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                v[ch] = make_uint4(0u, 0u, 0u, 0u);
-                if (row_ok) {
-                    const int h = g * G + r % G;
-                    v[ch] = __ldg(reinterpret_cast<const uint4 *>(q + (((long)b * T + j) * p.Hq + h) * 128) + ch);
-                }
+                for (int ch = 0; ch < 16; ++ch)
+                    *reinterpret_cast<uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
             }
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch)
-                *reinterpret_cast<uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7)) = v[ch];
-            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qready_bar);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qready_bar);
 
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         int last_t = -1;
         for (int t = wg; t < n_tiles; t += 2) {
-            const int u = t >> 1;  // use index of this warpgroup's buffers
-            ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(wg), u & 1, abort_flag, p.fault));
+            const int bi = t & 3;   // S/P buffer
+            const int u = t >> 2;   // use index of that buffer
+            const uint32_t sp_col = tmem + lane_off + 256u + 64u * bi;
+            ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(bi), u & 1, abort_flag, p.fault));
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[64];
-            {
-                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
-                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
-                tmem_ld32(sp_col, lo);
-                tmem_ld32(sp_col + 32u, hi);
-            }
+            tmem_ld64(sp_col, sr);
             // keys [0, nvalid) of the tile are visible to this row
             const bool blk = is_block_tile(t);
             int nvalid;
@@ -486,17 +508,21 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
                 nvalid = max(0, min(kBN, lim - tile_key0(t)));
             }
             if (!row_ok) nvalid = 0;
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = c < nvalid ? __uint_as_float(sr[c]) * qk : -INFINITY;
+            // tile max of the raw scores (qk > 0 keeps the order)
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                mx[i] = fmaxf(fmaxf(fmaxf(x[8 * i], x[8 * i + 1]), fmaxf(x[8 * i + 2], x[8 * i + 3])),
-                              fmaxf(fmaxf(x[8 * i + 4], x[8 * i + 5]), fmaxf(x[8 * i + 6], x[8 * i + 7])));
+                float m8 = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = 8 * i + e;
+                    m8 = fmaxf(m8, c < nvalid ? __uint_as_float(sr[c]) : -INFINITY);
+                }
+                mx[i] = m8;
             }
-            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+            const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float tmax = smax * qk;
             // move the reference max only when it grows by more than 2^8
             const bool first = t == wg;
             const bool need = !first && tmax > m_used + kRescaleThreshold;
@@ -506,28 +532,40 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
             // this warpgroup's previous P.V (tile t-2) must be done before O or
             // (shared-memory variant) the P buffer is touched again
             if (!first && (!kPTmem || __any_sync(0xffffffffu, need))) {
-                ok = __all_sync(0xffffffffu, mbar_wait(pempty_bar(wg), (u - 1) & 1, abort_flag, p.fault));
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(pempty_bar((t - 2) & 3), ((t - 2) >> 2) & 1, abort_flag, p.fault));
                 if (!ok) break;
                 tc_fence_after();
             }
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(o_col + 32u * cc, o);
+                for (int cc = 0; cc < 4; cc += 2) {
+                    uint32_t oa[32], ob[32];
+                    tmem_ld32_async(o_col + 32u * cc, oa);
+                    tmem_ld32_async(o_col + 32u * (cc + 1), ob);
+                    tmem_ld_wait();
+                    tmem_ld_bind(oa);
+                    tmem_ld_bind(ob);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(o_col + 32u * cc, o);
+                    for (int e = 0; e < 32; ++e) {
+                        oa[e] = __float_as_uint(__uint_as_float(oa[e]) * alpha);
+                        ob[e] = __float_as_uint(__uint_as_float(ob[e]) * alpha);
+                    }
+                    tmem_st32(o_col + 32u * cc, oa);
+                    tmem_st32(o_col + 32u * (cc + 1), ob);
                 }
             }
             l *= alpha;
             const bool live = m_used != -INFINITY;
+            const float neg_m = live ? -m_used : 0.f;
             uint32_t pk[32], pl[32];
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = live ? ex2(x[2 * c] - m_used) : 0.f;
-                const float p1 = live ? ex2(x[2 * c + 1] - m_used) : 0.f;
+                const float e0 = ex2(fmaf(__uint_as_float(sr[2 * c]), qk, neg_m));
+                const float e1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), qk, neg_m));
+                const float p0 = (live && 2 * c < nvalid) ? e0 : 0.f;
+                const float p1 = (live && 2 * c + 1 < nvalid) ? e1 : 0.f;
                 ls[c & 3] += p0 + p1;
                 pk[c] = pack_bf16(p0, p1);
                 // residual after rounding to bf16 (exact in fp32), itself rounded to bf16
@@ -566,12 +604,12 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pfull_bar(wg));
+            if (lane == 0) mbar_arrive(pfull_bar(bi));
             last_t = t;
         }
         // ---- epilogue: merge the two warpgroups' (m, l, O), write this split's partial ----
         if (ok && last_t >= 0)
-            ok = mbar_wait(pempty_bar(wg), (last_t >> 1) & 1, abort_flag, p.fault);
+            ok = mbar_wait(pempty_bar(last_t & 3), (last_t >> 2) & 1, abort_flag, p.fault);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok || last_t < 0) { m_used = -INFINITY; l = 0.f; }
         xchg[wg * 128 + r] = make_float2(m_used, l);
@@ -586,37 +624,52 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_co
         const float Lsum = l0 * f0 + l1 * f1;
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         const bool abort_seen = *abort_flag != 0;
+        // stage the normalised rows in shared memory (the K/V ring is idle now);
+        // warpgroup wg fills output columns [64 wg, 64 wg + 64)
+        float *ostage = reinterpret_cast<float *>(sbase + L::kOffStage);
         if (!abort_seen) {
             tc_fence_after();
-            const int h = g * G + (row_ok ? r % G : 0);
-            const long frow = ((long)b * T + j) * p.Hq + h;
-            float *dst = p.o_part + ((long)s * rows_total + frow) * 128;
-            // warpgroup wg writes output columns [64 wg, 64 wg + 64)
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const uint32_t col = 64u * wg + 32u * cc;
                 uint32_t oa[32], ob[32];
-                tmem_ld32(tmem + lane_off + col, oa);
-                tmem_ld32(tmem + lane_off + 128u + col, ob);
-                if (row_ok) {
+                tmem_ld32_async(tmem + lane_off + col, oa);
+                tmem_ld32_async(tmem + lane_off + 128u + col, ob);
+                tmem_ld_wait();
+                tmem_ld_bind(oa);
+                tmem_ld_bind(ob);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        float4 v;
-                        float *pv = reinterpret_cast<float *>(&v);
+                for (int e = 0; e < 32; e += 4) {
+                    float v[4];
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float a0 = l0 > 0.f ? __uint_as_float(oa[e + q4]) * f0 : 0.f;
-                            const float a1 = l1 > 0.f ? __uint_as_float(ob[e + q4]) * f1 : 0.f;
-                            pv[q4] = (a0 + a1) * inv;
-                        }
-                        *reinterpret_cast<float4 *>(dst + col + e) = v;
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float a0 = l0 > 0.f ? __uint_as_float(oa[e + q4]) * f0 : 0.f;
+                        const float a1 = l1 > 0.f ? __uint_as_float(ob[e + q4]) * f1 : 0.f;
+                        v[q4] = (a0 + a1) * inv;
                     }
+                    *reinterpret_cast<float4 *>(ostage + r * kOStride + col + e) = make_float4(v[0], v[1], v[2], v[3]);
                 }
             }
-            if (row_ok && wg == 0)
-                p.lse_part[(long)s * rows_total + frow] = Lsum > 0.f ? Mx * kLn2 + logf(Lsum) : -INFINITY;
+            if (row_ok && wg == 0) {
+                const int h = g * G + r % G;
+                p.lse_part[(long)s * rows_total + ((long)b * T + j) * p.Hq + h] =
+                    Lsum > 0.f ? Mx * kLn2 + logf(Lsum) : -INFINITY;
+            }
         }
         tc_fence_before();
+        named_sync(1, 256);
+        if (!abort_seen) {
+            // rows (j, hl) of one j are G consecutive rows of the partial output:
+            // copy them out as contiguous float4 runs
+            const int per_j = G * 32;  // float4s
+            for (int idx = tid; idx < M * 32; idx += 256) {
+                const int jj = idx / per_j, rem = idx % per_j, hl = rem >> 5, c4 = rem & 31;
+                const int rr = jj * G + hl;
+                const float4 v = *reinterpret_cast<const float4 *>(ostage + rr * kOStride + c4 * 4);
+                float *dst = p.o_part + ((long)s * rows_total + ((long)b * T + jj) * p.Hq + g * G + hl) * 128;
+                *reinterpret_cast<float4 *>(dst + c4 * 4) = v;
+            }
+        }
     }
 
     // teardown: every MMA has completed (drain above); free tensor memory
@@ -675,12 +728,28 @@ bool make_map(CUtensorMap *m, const void *ptr, const sd_strides &kv, int S, int 
 
 int cache_slots(const AttnParams &p) { return p.mode == 0 ? p.max_ctx + p.T - 1 : p.max_ctx; }
 
+// 4-D map over the contiguous queries [B, T, Hq, D]; box: 64 d x G heads x T rows x 1,
+// which lands in shared memory as rows j*G + hl of 128 bytes
+bool make_q_map(CUtensorMap *m, const AttnParams &p) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const int G = p.Hq / p.Hkv;
+    cuuint64_t dims[4] = {128, (cuuint64_t)p.Hq, (cuuint64_t)p.T, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {256, (cuuint64_t)p.Hq * 256, (cuuint64_t)p.T * p.Hq * 256};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)p.T, 1}, estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.q), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <bool kPTmem>
 cudaError_t launch_tc_t(const AttnParams &p, cudaStream_t st) {
-    alignas(64) CUtensorMap mk, mv;
+    alignas(64) CUtensorMap mq, mk, mv;
     TcParams tp;
     tp.a = p;
     int ds2 = 0, dh2 = 0;
+    if (!make_q_map(&mq, p)) return cudaErrorInvalidValue;
     if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B, &tp.dim_s, &tp.dim_h)) return cudaErrorInvalidValue;
     if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B, &ds2, &dh2)) return cudaErrorInvalidValue;
     constexpr int smem = Layout<kPTmem>::kSmemBytes;
@@ -703,7 +772,7 @@ cudaError_t launch_tc_t(const AttnParams &p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel<kPTmem>, mk, mv, tp);
+    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel<kPTmem>, mq, mk, mv, tp);
 }
 
 }  // namespace

@@ -55,6 +55,8 @@ cudaError_t launch_lse_merge(const AttnParams &p, cudaStream_t st);
 bool attn_tc_supported(const AttnParams &p);
 size_t attn_tc_smem_bytes(const AttnParams &p);
 
+// Acceptance workspaces hold ticket counters that must be zero before the
+// first call and are returned to zero by every completed call.
 struct GreedyParams {
     const int32_t *draft;
     const void *logits;
@@ -62,9 +64,11 @@ struct GreedyParams {
     sd_dtype dt;
     int32_t *n_acc, *corr;
     int chunk, n_chunks;
-    unsigned int *counter;
-    float *pval;
-    int *pidx;
+    unsigned int *counter;          // rows finished
+    unsigned int *row_counter;      // [B*T] chunks finished per row
+    float *pval;                    // [B*T, n_chunks] chunk max
+    int *pidx;                      // [B*T, n_chunks] its index
+    int *amax;                      // [B*T] row argmax
     unsigned int *fault;
 };
 cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st);
@@ -79,13 +83,19 @@ struct SampleParams {
     uint64_t seed;
     uint32_t offset;
     int32_t *n_acc, *next_id;
-    int chunk, n_chunks;
-    unsigned int *counters;         // [2]
+    int chunk, n_chunks;            // chunk <= kSampleChunkMax
+    unsigned int *counters;         // [0]: rows finished (pass 1)
+    unsigned int *row_counter;      // [B*T] chunks finished per row (pass 1) / per sequence (pass 2)
     float *pm, *pz;                 // [B*T, n_chunks] chunk max and sum of exp
-    float4 *state;                  // [B]: (n as int bits, M, Z, unused)
+    float2 *row_stats;              // [B*T] (M, Z) of softmax(l / tau)
+    int *accept;                    // [B*T] proposal of row accepted
+    float4 *state;                  // [B]: (n as int bits, M, Z, unused) of the deciding row
     double *rs, *ps;                // [B, n_chunks] residual / p chunk sums
     unsigned int *fault;
 };
+constexpr int kSampleChunkMax = 4096;
+constexpr int kGreedyChunkMaxBf16 = 16384;
+constexpr int kGreedyChunkMaxF32 = 8192;
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);
 
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int64_t n,
