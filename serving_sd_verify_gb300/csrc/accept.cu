@@ -26,7 +26,6 @@ namespace sdv {
 namespace {
 
 constexpr int kAccThreads = 256;
-constexpr int kMaxVec = 8;  // 16-byte vectors per thread and chunk
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10
@@ -58,14 +57,14 @@ __global__ void philox_kernel(const uint4 *__restrict__ ctr, uint64_t key, uint4
 }
 
 // ----------------------------------------------------------------------------
-// a chunk [lo, hi) of one row, pulled into registers: vector v of this thread
-// holds elements a0 + (tid + v * kAccThreads) * PV + e; the unaligned head
-// [lo, a0) and tail [a1, hi) are read element by element
+// a chunk [lo, hi) of one row, pulled into registers: vector v (< NV) of this
+// thread holds elements a0 + (tid + v * kAccThreads) * PV + e; the unaligned
+// head [lo, a0) and tail [a1, hi) are read element by element
 // ----------------------------------------------------------------------------
-template <typename Tin>
+template <typename Tin, int NV>
 struct ChunkRegs {
     static constexpr int PV = Elem<Tin>::kPerVec;
-    float x[kMaxVec][PV];
+    float x[NV][PV];
     int a0, a1, nvec;
 
     __device__ __forceinline__ void load(const Tin *row, int lo, int hi, float fill) {
@@ -76,7 +75,7 @@ struct ChunkRegs {
         nvec = (hi - a0) / PV;
         a1 = a0 + nvec * PV;
 #pragma unroll
-        for (int v = 0; v < kMaxVec; ++v) {
+        for (int v = 0; v < NV; ++v) {
             const int vi = threadIdx.x + v * kAccThreads;
             if (vi < nvec) {
                 Elem<Tin>::load_vec(row + a0 + vi * PV, x[v]);
@@ -146,6 +145,14 @@ __device__ __forceinline__ float block_max(float x) {
     return t;
 }
 
+// Programmatic dependent launch: the kernel may start while the previous one in
+// the stream drains; wait here until its results are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+#if __CUDA_ARCH__ >= 900
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
 // Last-CTA election on `counter` among `total` arrivals: true in every thread of
 // the CTA that arrived last, which also returns the counter to zero.  Writes
 // made before the call by any arriving CTA are visible to the elected one.
@@ -166,12 +173,13 @@ __device__ __forceinline__ bool elect_last(unsigned int *counter, unsigned int t
 // ----------------------------------------------------------------------------
 // greedy acceptance
 // ----------------------------------------------------------------------------
-template <typename Tin>
+template <typename Tin, int NV>
 __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams p) {
+    grid_dependency_wait();
     const int c = blockIdx.x, row = blockIdx.y;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
     const Tin *lg = static_cast<const Tin *>(p.logits) + (long)row * p.V;
-    ChunkRegs<Tin> cr;
+    ChunkRegs<Tin, NV> cr;
     cr.load(lg, lo, hi, -INFINITY);
     float bv = -INFINITY;
     int bi = INT_MAX;
@@ -181,10 +189,10 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
         if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
     }
 #pragma unroll
-    for (int v = 0; v < kMaxVec; ++v) {
+    for (int v = 0; v < NV; ++v) {
         if (!cr.valid(v)) break;
 #pragma unroll
-        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) {
+        for (int e = 0; e < ChunkRegs<Tin, NV>::PV; ++e) {
             const int i = cr.index(v, e);
             if (argmax_better(cr.x[v][e], i, bv, bi)) { bv = cr.x[v][e]; bi = i; }
         }
@@ -243,19 +251,20 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
 // the last CTA of a row also tests that row's proposal, the last row finds
 // the first rejection of every sequence
 // ----------------------------------------------------------------------------
-template <typename Tin>
+template <typename Tin, int NV>
 __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleParams p) {
+    grid_dependency_wait();
     const int c = blockIdx.x, row = blockIdx.y;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
     const Tin *lg = static_cast<const Tin *>(p.logits) + (long)row * p.V;
     const float it = p.inv_tau;
-    ChunkRegs<Tin> cr;
+    ChunkRegs<Tin, NV> cr;
     cr.load(lg, lo, hi, -INFINITY);
     float m = -INFINITY;
 #pragma unroll
-    for (int v = 0; v < kMaxVec; ++v)
+    for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) m = fmaxf(m, cr.x[v][e] * it);
+        for (int e = 0; e < ChunkRegs<Tin, NV>::PV; ++e) m = fmaxf(m, cr.x[v][e] * it);
     for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) m = fmaxf(m, Elem<Tin>::load(lg + i) * it);
     for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) m = fmaxf(m, Elem<Tin>::load(lg + i) * it);
     m = block_max(m);
@@ -263,10 +272,10 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     if (m != -INFINITY) {
         float zf = 0.f;
 #pragma unroll
-        for (int v = 0; v < kMaxVec; ++v) {
+        for (int v = 0; v < NV; ++v) {
             float zv = 0.f;
 #pragma unroll
-            for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) zv += expf(cr.x[v][e] * it - m);  // fill -inf -> 0
+            for (int e = 0; e < ChunkRegs<Tin, NV>::PV; ++e) zv += expf(cr.x[v][e] * it - m);  // fill -inf -> 0
             zf += zv;
         }
         z = zf;
@@ -348,8 +357,9 @@ __device__ __forceinline__ float residual_or_p(float x, float it, float M, float
     return r > 0.f ? r : 0.f;
 }
 
-template <typename Tin>
+template <typename Tin, int NV>
 __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SampleParams p) {
+    grid_dependency_wait();
     const int c = blockIdx.x, b = blockIdx.y;
     const float4 st = p.state[b];
     const int n = __float_as_int(st.x);
@@ -360,31 +370,39 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     const float *qn = p.q + row * p.V;
     const float it = p.inv_tau;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
-    ChunkRegs<Tin> cr;
+    ChunkRegs<Tin, NV> cr;
     cr.load(lg, lo, hi, -INFINITY);
-    double sr = 0.0, sp = 0.0;
+    // per-thread sums in fp32 (at most a few dozen terms), the CTA total in fp64
+    float srf = 0.f, spf = 0.f;
+    constexpr int PV = ChunkRegs<Tin, NV>::PV;
+    float qv[NV][PV];
 #pragma unroll
-    for (int v = 0; v < kMaxVec; ++v) {
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int e = 0; e < PV; ++e) qv[v][e] = (rejected && cr.valid(v)) ? __ldg(qn + cr.index(v, e)) : 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
         if (!cr.valid(v)) break;
-        float qv[ChunkRegs<Tin>::PV];
+        float sv = 0.f, rv = 0.f;
 #pragma unroll
-        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) qv[e] = rejected ? __ldg(qn + cr.index(v, e)) : 0.f;
-#pragma unroll
-        for (int e = 0; e < ChunkRegs<Tin>::PV; ++e) {
+        for (int e = 0; e < PV; ++e) {
             const float pi = expf(cr.x[v][e] * it - M) / Z;
-            sp += pi;
-            if (rejected) { const float r = pi - qv[e]; sr += r > 0.f ? r : 0.f; }
+            sv += pi;
+            const float r = pi - qv[v][e];
+            rv += r > 0.f ? r : 0.f;
         }
+        spf += sv;
+        srf += rv;
     }
     auto scalar = [&](int i) {
         const float pi = expf(Elem<Tin>::load(lg + i) * it - M) / Z;
-        sp += pi;
-        if (rejected) { const float r = pi - __ldg(qn + i); sr += r > 0.f ? r : 0.f; }
+        spf += pi;
+        if (rejected) { const float r = pi - __ldg(qn + i); srf += r > 0.f ? r : 0.f; }
     };
     for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) scalar(i);
     for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) scalar(i);
-    sr = block_sum<double>(sr);
-    sp = block_sum<double>(sp);
+    const double sr = block_sum<double>(rejected ? (double)srf : 0.0);
+    const double sp = block_sum<double>((double)spf);
     if (threadIdx.x == 0) {
         p.rs[(long)b * p.n_chunks + c] = sr;
         p.ps[(long)b * p.n_chunks + c] = sp;
@@ -448,31 +466,36 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (chunk <= 4096)
     const int tlo = min(chi, clo + (int)threadIdx.x * per), thi = min(chi, tlo + per);
     const bool res = sel_res != 0;
-    float w[kRun];
-    double run = 0.0;
+    float w[kRun], xin[kRun], qin[kRun];
 #pragma unroll
     for (int e = 0; e < kRun; ++e) {
         const int i = tlo + e;
-        w[e] = 0.f;
-        if (i < thi) {
-            const float qi = res ? __ldg(qn + i) : 0.f;
-            w[e] = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, qi, res);
-        }
-        run += w[e];
+        xin[e] = i < thi ? Elem<Tin>::load(lg + i) : 0.f;
+        qin[e] = (i < thi && res) ? __ldg(qn + i) : 0.f;
     }
-    __shared__ double tsum[kAccThreads];
+    float runf = 0.f;
+#pragma unroll
+    for (int e = 0; e < kRun; ++e) {
+        w[e] = tlo + e < thi ? residual_or_p(xin[e], it, M, Z, qin[e], res) : 0.f;
+        runf += w[e];
+    }
+    // exclusive prefix of the runs over the threads: warp scans, then warp totals
+    const double run = (double)runf;
+    __shared__ double wtot[kAccThreads / 32];
     __shared__ int s_id, s_lastpos;
-    tsum[threadIdx.x] = run;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    double incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wtot[wid] = incl;
     if (threadIdx.x == 0) { s_id = INT_MAX; s_lastpos = -1; }
     __syncthreads();
-    // inclusive scan over the threads (Hillis-Steele in shared memory)
-    for (int o = 1; o < kAccThreads; o <<= 1) {
-        const double y = threadIdx.x >= (unsigned)o ? tsum[threadIdx.x - o] : 0.0;
-        __syncthreads();
-        tsum[threadIdx.x] += y;
-        __syncthreads();
-    }
-    double acc = sel_base + (tsum[threadIdx.x] - run);
+    double before = 0.0;
+    for (int k = 0; k < wid; ++k) before += wtot[k];
+    double acc = sel_base + before + (incl - run);
     int last_here = -1;
 #pragma unroll
     for (int e = 0; e < kRun; ++e) {
@@ -493,23 +516,61 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
 
 }  // namespace
 
+// vectors per thread needed to hold one chunk in registers
+template <typename Tin> int vec_per_thread(int chunk) {
+    const int v = (chunk + Elem<Tin>::kPerVec * kAccThreads - 1) / (Elem<Tin>::kPerVec * kAccThreads);
+    return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : 8;
+}
+
+// launch with programmatic stream serialization (overlaps the previous kernel's tail)
+template <typename P>
+cudaError_t launch_pdl(void (*kern)(const P), dim3 grid, cudaStream_t st, const P &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAccThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+#define SDV_DISPATCH_NV(KERNEL, TIN, NVV, GRID, ST, P, ERR)                     \
+    do {                                                                       \
+        switch (NVV) {                                                         \
+            case 1: ERR = launch_pdl(KERNEL<TIN, 1>, GRID, ST, P); break;      \
+            case 2: ERR = launch_pdl(KERNEL<TIN, 2>, GRID, ST, P); break;      \
+            case 4: ERR = launch_pdl(KERNEL<TIN, 4>, GRID, ST, P); break;      \
+            default: ERR = launch_pdl(KERNEL<TIN, 8>, GRID, ST, P); break;     \
+        }                                                                      \
+    } while (0)
+
 cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st) {
     dim3 grid(p.n_chunks, p.B * p.T);
-    if (p.dt == SD_BF16) greedy_kernel<__nv_bfloat16><<<grid, kAccThreads, 0, st>>>(p);
-    else greedy_kernel<float><<<grid, kAccThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaError_t e;
+    if (p.dt == SD_BF16) SDV_DISPATCH_NV(greedy_kernel, __nv_bfloat16, vec_per_thread<__nv_bfloat16>(p.chunk), grid, st, p, e);
+    else SDV_DISPATCH_NV(greedy_kernel, float, vec_per_thread<float>(p.chunk), grid, st, p, e);
+    return e;
 }
 
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st) {
     dim3 g1(p.n_chunks, p.B * p.T), g2(p.n_chunks, p.B);
+    cudaError_t e;
     if (p.dt == SD_BF16) {
-        sample_stats_kernel<__nv_bfloat16><<<g1, kAccThreads, 0, st>>>(p);
-        sample_draw_kernel<__nv_bfloat16><<<g2, kAccThreads, 0, st>>>(p);
+        const int nv = vec_per_thread<__nv_bfloat16>(p.chunk);
+        SDV_DISPATCH_NV(sample_stats_kernel, __nv_bfloat16, nv, g1, st, p, e);
+        if (e != cudaSuccess) return e;
+        SDV_DISPATCH_NV(sample_draw_kernel, __nv_bfloat16, nv, g2, st, p, e);
     } else {
-        sample_stats_kernel<float><<<g1, kAccThreads, 0, st>>>(p);
-        sample_draw_kernel<float><<<g2, kAccThreads, 0, st>>>(p);
+        const int nv = vec_per_thread<float>(p.chunk);
+        SDV_DISPATCH_NV(sample_stats_kernel, float, nv, g1, st, p, e);
+        if (e != cudaSuccess) return e;
+        SDV_DISPATCH_NV(sample_draw_kernel, float, nv, g2, st, p, e);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int64_t n,
