@@ -220,25 +220,31 @@ def hbm_peak(sustained: bool):
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement; MEASURED_PEAKS.json absent)"
 
 
-def csrc_digest():
+# sources that define each measured kernel (a capture is valid while they are unchanged)
+KERNEL_SOURCES = {
+    "verify_attention": ["attn_tc.cu", "common.cuh", "internal.h"],
+}
+
+
+def csrc_digest(files):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "serving_sd_verify_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in files:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_key):
-    """Per-launch DRAM bytes of `kernel_key` from profiles/traffic.txt, if it was
-    captured from the current kernel sources; else None."""
+    """Per-launch DRAM bytes (read + write) of `kernel_key` from
+    profiles/traffic.txt, if that capture was taken from the current kernel
+    sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    dig = csrc_digest()
+    dig = csrc_digest(KERNEL_SOURCES[kernel_key])
     for line in lines:
         f = line.split()
         if len(f) >= 3 and not line.startswith("#") and f[0] == kernel_key and f[2] == dig:
@@ -480,7 +486,8 @@ def main():
         k = kernels["verify_attention"]
         achieved = k["GBps"]
         traffic = ncu_traffic("verify_attention")
-        roofline = {"kernel": "verify attention split kernel + LSE merge (one sd_verify_attention call)",
+        roofline = {"kernel": "verify attention split kernel + LSE merge (one sd_verify_attention call); "
+                              "traffic is the split kernel's DRAM bytes per launch",
                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_source": peak_src,
                     "traffic": traffic,
