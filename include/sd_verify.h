@@ -174,6 +174,27 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs,
 size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype);
 
 /* ------------------------------------------------------------------------
+ * Greedy acceptance without a caller workspace
+ *
+ * No counterpart in the method's pages: this is a convenience of the library.
+ * For hosts that cannot hand the library device memory -- their own pool
+ * allocator owns all of it and extensions may not call cudaMalloc, or only the
+ * input and output buffers are at hand when the call is made.  Computes
+ * exactly what sd_accept_greedy computes, with the same arguments minus the
+ * workspace.  Scratch is a 1 MiB device array owned by the library (held on
+ * every GPU that loads it until the process exits); shapes whose workspace
+ * (sd_accept_greedy_workspace_size) exceeds 1 MiB return SD_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call clears and then uses the same array, so calls must not overlap
+ * on the GPU: issue them on one stream (calls on different streams or from
+ * different threads without ordering race).  Nothing on this path allocates.
+ * ------------------------------------------------------------------------ */
+sd_status sd_accept_greedy_noalloc(const int32_t *draft_ids, const void *target_logits,
+                                   int B, int T, int V, sd_dtype dtype,
+                                   int32_t *n_accepted, int32_t *correction_id, void *stream);
+
+/* ------------------------------------------------------------------------
  * Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
  * 3", SC'11), the generator behind sd_accept_sample, exposed so callers can
  * check it: counters device uint32 [n, 4], out device uint32 [n, 4],

@@ -217,6 +217,8 @@ int device_sm_count() {
     return cache[dev];
 }
 
+sd_status report_error(sd_status s, const char *msg) { return fail(s, "%s", msg); }
+
 }  // namespace sdv
 
 using namespace sdv;

@@ -103,4 +103,7 @@ cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int6
 
 int device_sm_count();              // SMs of the current device (cached)
 
+// records `msg` as this thread's sd_last_error() and returns `s`
+sd_status report_error(sd_status s, const char *msg);
+
 }  // namespace sdv

@@ -24,7 +24,7 @@ SYMBOLS = [
     "sd_verify_attention", "sd_verify_attention_workspace_size",
     "sd_draft_block_attention", "sd_draft_block_attention_workspace_size",
     "sd_accept_greedy", "sd_accept_greedy_workspace_size",
-    "sd_accept_sample", "sd_accept_sample_workspace_size",
+    "sd_accept_sample", "sd_accept_sample_workspace_size", "sd_accept_greedy_noalloc",
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path",
 ]
@@ -72,6 +72,8 @@ def load():
     lib.sd_accept_sample.restype = _i
     lib.sd_accept_sample_workspace_size.argtypes = [_i] * 4
     lib.sd_accept_sample_workspace_size.restype = _sz
+    lib.sd_accept_greedy_noalloc.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]
+    lib.sd_accept_greedy_noalloc.restype = _i
     lib.sd_philox4x32_10.argtypes = [_vp, ctypes.c_uint64, _vp, ctypes.c_int64, _vp]
     lib.sd_philox4x32_10.restype = _i
     lib.sd_status_string.argtypes = [_i]
