@@ -131,8 +131,8 @@ size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, in
  *   correction_id device int32 [B]: argmax of row n_accepted (the target's
  *                 token at the first mismatch, or the bonus token)
  *   argmax ties go to the lowest index; values compare exactly in fp32
- *   workspace: its first 256 bytes must be zero before the first call on it;
- *   each completed call leaves them zero again.
+ *   workspace: zero-filled before the first call on it; each completed call
+ *   leaves its counters zero again, so it stays reusable.
  * ------------------------------------------------------------------------ */
 sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits,
                            int B, int T, int V, sd_dtype dtype,
@@ -163,7 +163,8 @@ size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype);
  *                normalised distributions)
  *   temperature  > 0 (temperature 0 is sd_accept_greedy)
  *   n_accepted, next_id  device int32 [B]
- *   workspace: first 256 bytes zero before the first call; left zero.
+ *   workspace: zero-filled before the first call on it; each completed call
+ *   leaves its counters zero again.
  * ------------------------------------------------------------------------ */
 sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs,
                            const void *target_logits, int B, int T, int V, sd_dtype dtype,

@@ -154,19 +154,22 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 
 // Last-CTA election on `counter` among `total` arrivals: true in every thread of
-// the CTA that arrived last, which also returns the counter to zero.  Writes
-// made before the call by any arriving CTA are visible to the elected one.
+// the CTA that arrived last, which also returns the counter to zero.  Only
+// thread 0 of a CTA writes that CTA's partial results; its fence before the
+// ticket makes them visible to the elected CTA, which reads them from L2.
 __device__ __forceinline__ bool elect_last(unsigned int *counter, unsigned int total) {
     __shared__ bool is_last;
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
+        __threadfence();
         const unsigned int ticket = atomicAdd(counter, 1u);
         is_last = ticket == total - 1;
-        if (is_last) *counter = 0u;
+        if (is_last) {
+            *counter = 0u;
+            __threadfence();
+        }
     }
     __syncthreads();
-    if (is_last) __threadfence();
     return is_last;
 }
 
@@ -206,31 +209,30 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
         p.pval[(long)row * p.n_chunks + c] = bv;
         p.pidx[(long)row * p.n_chunks + c] = bi;
     }
-    if (!elect_last(p.row_counter + row, gridDim.x)) return;
+    if (!elect_last(p.counter, gridDim.x * gridDim.y)) return;
 
-    // last CTA of this row: the row's argmax from its chunk partials
-    if (threadIdx.x < 32) {
-        float v = -INFINITY;
-        int i = INT_MAX;
-        for (int k = threadIdx.x; k < p.n_chunks; k += 32) {
-            const float pv = __ldcg(p.pval + (long)row * p.n_chunks + k);
-            const int pi = __ldcg(p.pidx + (long)row * p.n_chunks + k);
-            if (argmax_better(pv, pi, v, i)) { v = pv; i = pi; }
-        }
-        warp_argmax(v, i);
-        if (threadIdx.x == 0) {
-            if (i == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); i = 0; }
-            p.amax[row] = i;
-        }
-    }
-    if (!elect_last(p.counter, gridDim.y)) return;
-
-    // last row: the first-mismatch scan of every sequence
+    // last CTA: every row's argmax from its chunk partials (a warp per row,
+    // lanes over chunks), then the first-mismatch scan of every sequence, over
+    // windows of W rows that hold whole sequences
     __shared__ int am[kAccThreads];
     const int R = p.B * p.T;
-    const int W = (kAccThreads / p.T) * p.T;  // whole sequences per window
+    const int W = (kAccThreads / p.T) * p.T;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int r0 = 0; r0 < R; r0 += W) {
-        for (int r = r0 + (int)threadIdx.x; r < min(R, r0 + W); r += kAccThreads) am[r - r0] = __ldcg(p.amax + r);
+        for (int r = r0 + warp; r < min(R, r0 + W); r += kAccThreads / 32) {
+            float v = -INFINITY;
+            int i = INT_MAX;
+            for (int k = lane; k < p.n_chunks; k += 32) {
+                const float pv = __ldcg(p.pval + (long)r * p.n_chunks + k);
+                const int pi = __ldcg(p.pidx + (long)r * p.n_chunks + k);
+                if (argmax_better(pv, pi, v, i)) { v = pv; i = pi; }
+            }
+            warp_argmax(v, i);
+            if (lane == 0) {
+                if (i == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); i = 0; }
+                am[r - r0] = i;
+            }
+        }
         __syncthreads();
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
         for (int bl = threadIdx.x; bl < nbw; bl += kAccThreads) {
@@ -286,49 +288,55 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     if (threadIdx.x == 0) {
         p.pm[(long)row * p.n_chunks + c] = m;
         p.pz[(long)row * p.n_chunks + c] = (float)z;
-    }
-    if (!elect_last(p.row_counter + row, gridDim.x)) return;
-
-    // last CTA of this row: the row's max M and normaliser Z, then the test of
-    // its proposal (rows 0..T-2): accept iff u * q(d) < p(d)
-    if (threadIdx.x < 32) {
-        float M = -INFINITY;
-        for (int k = threadIdx.x; k < p.n_chunks; k += 32) M = fmaxf(M, __ldcg(p.pm + (long)row * p.n_chunks + k));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        double Z = 0.0;
-        for (int k = threadIdx.x; k < p.n_chunks; k += 32) {
-            const float mk = __ldcg(p.pm + (long)row * p.n_chunks + k);
-            if (mk != -INFINITY) Z += (double)__ldcg(p.pz + (long)row * p.n_chunks + k) * (double)expf(mk - M);
-        }
-        Z = warp_sum(Z);
-        if (threadIdx.x == 0) {
-            const int b = row / p.T, j = row % p.T;
-            p.row_stats[row] = make_float2(M, (float)Z);
-            int accept = 0;
-            if (j < p.T - 1) {
-                const int d = p.draft[(long)b * (p.T - 1) + j];
-                if (d >= 0 && d < p.V) {
-                    const float ld = Elem<Tin>::load(lg + d);
-                    const double pd = (double)expf(ld * it - M) / Z;
-                    const double qd = (double)__ldg(p.q + (long)row * p.V + d);
-                    const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
-                    accept = u * qd < pd ? 1 : 0;
-                } else {
-                    set_fault(p.fault, FAULT_BAD_DRAFT_ID);
-                }
-            }
-            p.accept[row] = accept;
+        // the CTA whose chunk holds this row's proposal records its logit and q
+        const int b = row / p.T, j = row % p.T;
+        if (j < p.T - 1) {
+            const int d = p.draft[(long)b * (p.T - 1) + j];
+            if (d >= lo && d < hi)
+                p.row_stats[row] = make_float2(Elem<Tin>::load(lg + d), __ldg(p.q + (long)row * p.V + d));
         }
     }
-    if (!elect_last(p.counters, gridDim.y)) return;
+    if (!elect_last(p.counters, gridDim.x * gridDim.y)) return;
 
-    // last row: first rejection of every sequence
+    // last CTA: every row's max M and normaliser Z (a warp per row, lanes over
+    // chunks) and the test of its proposal (rows 0..T-2): accept iff
+    // u * q(d) < p(d); then the first rejection of every sequence, over windows
+    // of W rows that hold whole sequences
     __shared__ int acc_s[kAccThreads];
+    __shared__ float2 mz_s[kAccThreads];
     const int R = p.B * p.T;
     const int W = (kAccThreads / p.T) * p.T;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int r0 = 0; r0 < R; r0 += W) {
-        for (int r = r0 + (int)threadIdx.x; r < min(R, r0 + W); r += kAccThreads) acc_s[r - r0] = __ldcg(p.accept + r);
+        for (int r = r0 + warp; r < min(R, r0 + W); r += kAccThreads / 32) {
+            float M = -INFINITY;
+            for (int k = lane; k < p.n_chunks; k += 32) M = fmaxf(M, __ldcg(p.pm + (long)r * p.n_chunks + k));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            double Z = 0.0;
+            for (int k = lane; k < p.n_chunks; k += 32) {
+                const float mk = __ldcg(p.pm + (long)r * p.n_chunks + k);
+                if (mk != -INFINITY) Z += (double)__ldcg(p.pz + (long)r * p.n_chunks + k) * (double)expf(mk - M);
+            }
+            Z = warp_sum(Z);
+            if (lane == 0) {
+                const int b = r / p.T, j = r % p.T;
+                int accept = 0;
+                if (j < p.T - 1) {
+                    const int d = p.draft[(long)b * (p.T - 1) + j];
+                    if (d >= 0 && d < p.V) {
+                        const float2 lq = __ldcg(p.row_stats + r);
+                        const double pd = (double)expf(lq.x * it - M) / Z;
+                        const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
+                        accept = u * (double)lq.y < pd ? 1 : 0;
+                    } else {
+                        set_fault(p.fault, FAULT_BAD_DRAFT_ID);
+                    }
+                }
+                acc_s[r - r0] = accept;
+                mz_s[r - r0] = make_float2(M, (float)Z);
+            }
+        }
         __syncthreads();
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
         for (int bl = threadIdx.x; bl < nbw; bl += kAccThreads) {
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
             int n = p.T - 1;
             for (int j = 0; j < p.T - 1; ++j)
                 if (!acc_s[bl * p.T + j]) { n = j; break; }
-            const float2 st = __ldcg(p.row_stats + (long)b * p.T + n);
+            const float2 st = mz_s[bl * p.T + n];
             p.n_acc[b] = n;
             p.state[b] = make_float4(__int_as_float(n), st.x, st.y, 0.f);
         }
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     const Tin *lg = static_cast<const Tin *>(p.logits) + row * p.V;
     const float *qn = p.q + row * p.V;
     const float it = p.inv_tau;
-    const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
+    const int lo = c * p.draw_chunk, hi = min(p.V, lo + p.draw_chunk);
     ChunkRegs<Tin, NV> cr;
     cr.load(lg, lo, hi, -INFINITY);
     // per-thread sums in fp32 (at most a few dozen terms), the CTA total in fp64
@@ -404,8 +412,8 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     const double sr = block_sum<double>(rejected ? (double)srf : 0.0);
     const double sp = block_sum<double>((double)spf);
     if (threadIdx.x == 0) {
-        p.rs[(long)b * p.n_chunks + c] = sr;
-        p.ps[(long)b * p.n_chunks + c] = sp;
+        p.rs[(long)b * p.n_draw_chunks + c] = sr;
+        p.ps[(long)b * p.n_draw_chunks + c] = sp;
     }
     if (!elect_last(p.row_counter + b, gridDim.x)) return;
 
@@ -415,32 +423,32 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         double Sr = 0.0, Sp = 0.0;
-        for (int k = lane; k < p.n_chunks; k += 32) {
-            Sr += __ldcg(p.rs + (long)b * p.n_chunks + k);
-            Sp += __ldcg(p.ps + (long)b * p.n_chunks + k);
+        for (int k = lane; k < p.n_draw_chunks; k += 32) {
+            Sr += __ldcg(p.rs + (long)b * p.n_draw_chunks + k);
+            Sp += __ldcg(p.ps + (long)b * p.n_draw_chunks + k);
         }
         Sr = warp_sum(Sr);
         Sp = warp_sum(Sp);
         const bool use_r = rejected && Sr > 0.0;
-        const double *cs = (use_r ? p.rs : p.ps) + (long)b * p.n_chunks;
+        const double *cs = (use_r ? p.rs : p.ps) + (long)b * p.n_draw_chunks;
         const double S = use_r ? Sr : Sp;
         const double x = (double)philox_uniform(p.seed, (uint32_t)n, (uint32_t)b, 1u, p.offset) * S;
         // inclusive prefix over the chunk sums, 32 chunks at a time
         double carry = 0.0;
         int found = -1, last_pos = -1;
         double found_base = 0.0;
-        for (int k0 = 0; k0 < p.n_chunks && found < 0; k0 += 32) {
+        for (int k0 = 0; k0 < p.n_draw_chunks && found < 0; k0 += 32) {
             const int k = k0 + lane;
-            const double v = k < p.n_chunks ? __ldcg(cs + k) : 0.0;
+            const double v = k < p.n_draw_chunks ? __ldcg(cs + k) : 0.0;
             double incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const double y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            const unsigned pos = __ballot_sync(0xffffffffu, k < p.n_chunks && v > 0.0);
+            const unsigned pos = __ballot_sync(0xffffffffu, k < p.n_draw_chunks && v > 0.0);
             if (pos) last_pos = k0 + 31 - __clz((int)pos);
-            const unsigned hit = __ballot_sync(0xffffffffu, k < p.n_chunks && carry + incl > x);
+            const unsigned hit = __ballot_sync(0xffffffffu, k < p.n_draw_chunks && carry + incl > x);
             if (hit) {
                 const int l = __ffs((int)hit) - 1;
                 found = k0 + l;
@@ -462,8 +470,8 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     // combined by an exclusive scan over the threads, the owner of the
     // crossing then walks its run
     constexpr int kRun = 16;
-    const int clo = sel_chunk * p.chunk, chi = min(p.V, clo + p.chunk);
-    const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (chunk <= 4096)
+    const int clo = sel_chunk * p.draw_chunk, chi = min(p.V, clo + p.draw_chunk);
+    const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (draw chunk <= 4096)
     const int tlo = min(chi, clo + (int)threadIdx.x * per), thi = min(chi, tlo + per);
     const bool res = sel_res != 0;
     float w[kRun], xin[kRun], qin[kRun];
@@ -557,18 +565,16 @@ cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st) {
-    dim3 g1(p.n_chunks, p.B * p.T), g2(p.n_chunks, p.B);
+    dim3 g1(p.n_chunks, p.B * p.T), g2(p.n_draw_chunks, p.B);
     cudaError_t e;
     if (p.dt == SD_BF16) {
-        const int nv = vec_per_thread<__nv_bfloat16>(p.chunk);
-        SDV_DISPATCH_NV(sample_stats_kernel, __nv_bfloat16, nv, g1, st, p, e);
+        SDV_DISPATCH_NV(sample_stats_kernel, __nv_bfloat16, vec_per_thread<__nv_bfloat16>(p.chunk), g1, st, p, e);
         if (e != cudaSuccess) return e;
-        SDV_DISPATCH_NV(sample_draw_kernel, __nv_bfloat16, nv, g2, st, p, e);
+        SDV_DISPATCH_NV(sample_draw_kernel, __nv_bfloat16, vec_per_thread<__nv_bfloat16>(p.draw_chunk), g2, st, p, e);
     } else {
-        const int nv = vec_per_thread<float>(p.chunk);
-        SDV_DISPATCH_NV(sample_stats_kernel, float, nv, g1, st, p, e);
+        SDV_DISPATCH_NV(sample_stats_kernel, float, vec_per_thread<float>(p.chunk), g1, st, p, e);
         if (e != cudaSuccess) return e;
-        SDV_DISPATCH_NV(sample_draw_kernel, float, nv, g2, st, p, e);
+        SDV_DISPATCH_NV(sample_draw_kernel, float, vec_per_thread<float>(p.draw_chunk), g2, st, p, e);
     }
     return e;
 }

@@ -169,37 +169,45 @@ int accept_chunk(int rows, int V, int cap) {
 
 int greedy_cap(sd_dtype dt) { return dt == SD_BF16 ? kGreedyChunkMaxBf16 : kGreedyChunkMaxF32; }
 
-// greedy workspace: [header: rows-finished counter][row counters][pval][pidx][amax]
+// greedy workspace: [header: CTAs-finished counter][pval][pidx]
 struct GreedyLayout {
-    size_t row_ctr, pval, pidx, amax, total;
+    size_t pval, pidx, total;
 };
 GreedyLayout greedy_layout(int B, int T, int V, int chunk) {
     const size_t R = (size_t)B * T, parts = R * ((V + chunk - 1) / chunk);
     GreedyLayout l;
-    l.row_ctr = kHeader;
-    l.pval = l.row_ctr + align_up(R * 4, 256);
+    l.pval = kHeader;
     l.pidx = l.pval + align_up(parts * 4, 256);
-    l.amax = l.pidx + align_up(parts * 4, 256);
-    l.total = l.amax + align_up(R * 4, 256);
+    l.total = l.pidx + align_up(parts * 4, 256);
     return l;
 }
 
-// sample workspace: [header: counters][row counters][pm][pz][row_stats][accept][state][rs][ps]
+// chunk of the sampled rule's second pass (one row per sequence): about two
+// CTAs per SM over the B rows
+int draw_chunk_for(int B, int V) {
+    const int sms = device_sm_count();
+    long c = ((long)B * V + 2L * sms - 1) / (2L * sms);
+    c = std::max(512L, std::min(c, (long)kSampleChunkMax));
+    c = (c + 7) / 8 * 8;
+    return (int)std::min<long>(c, (long)V);
+}
+
+// sample workspace: [header: pass-1 counter][per-sequence counters][pm][pz][row_stats][state][rs][ps]
 struct SampleLayout {
-    size_t row_ctr, pm, pz, row_stats, accept, state, rs, ps, total;
+    size_t row_ctr, pm, pz, row_stats, state, rs, ps, total;
 };
-SampleLayout sample_layout(int B, int T, int V, int chunk) {
+SampleLayout sample_layout(int B, int T, int V, int chunk, int draw_chunk) {
     const size_t R = (size_t)B * T, nc = (V + chunk - 1) / chunk, parts = R * nc;
+    const size_t nd = (V + draw_chunk - 1) / draw_chunk;
     SampleLayout l;
     l.row_ctr = kHeader;
-    l.pm = l.row_ctr + align_up(R * 4, 256);
+    l.pm = l.row_ctr + align_up((size_t)B * 4, 256);
     l.pz = l.pm + align_up(parts * 4, 256);
     l.row_stats = l.pz + align_up(parts * 4, 256);
-    l.accept = l.row_stats + align_up(R * 8, 256);
-    l.state = l.accept + align_up(R * 4, 256);
+    l.state = l.row_stats + align_up(R * 8, 256);
     l.rs = l.state + align_up((size_t)B * 16, 256);
-    l.ps = l.rs + align_up((size_t)B * nc * 8, 256);
-    l.total = l.ps + align_up((size_t)B * nc * 8, 256);
+    l.ps = l.rs + align_up((size_t)B * nd * 8, 256);
+    l.total = l.ps + align_up((size_t)B * nd * 8, 256);
     return l;
 }
 
@@ -325,10 +333,8 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
     if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     char *w = static_cast<char *>(workspace);
     p.counter = reinterpret_cast<unsigned int *>(w);
-    p.row_counter = reinterpret_cast<unsigned int *>(w + gl.row_ctr);
     p.pval = reinterpret_cast<float *>(w + gl.pval);
     p.pidx = reinterpret_cast<int *>(w + gl.pidx);
-    p.amax = reinterpret_cast<int *>(w + gl.amax);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     cudaError_t e = launch_accept_greedy(p, static_cast<cudaStream_t>(stream));
@@ -339,7 +345,7 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
 size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype) {
     (void)dtype;
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
-    return sample_layout(B, T, V, accept_chunk(B * T, V, kSampleChunkMax)).total;
+    return sample_layout(B, T, V, accept_chunk(B * T, V, kSampleChunkMax), draw_chunk_for(B, V)).total;
 }
 
 sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, const void *target_logits,
@@ -361,7 +367,9 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.n_acc = n_accepted; p.next_id = next_id;
     p.chunk = accept_chunk(B * T, V, kSampleChunkMax);
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
-    const SampleLayout sl = sample_layout(B, T, V, p.chunk);
+    p.draw_chunk = draw_chunk_for(B, V);
+    p.n_draw_chunks = (V + p.draw_chunk - 1) / p.draw_chunk;
+    const SampleLayout sl = sample_layout(B, T, V, p.chunk, p.draw_chunk);
     if (!workspace || workspace_bytes < sl.total)
         return fail(SD_ERR_WORKSPACE, "sample workspace too small: need %zu bytes, got %zu", sl.total, workspace_bytes);
     if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -371,7 +379,6 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.pm = reinterpret_cast<float *>(w + sl.pm);
     p.pz = reinterpret_cast<float *>(w + sl.pz);
     p.row_stats = reinterpret_cast<float2 *>(w + sl.row_stats);
-    p.accept = reinterpret_cast<int *>(w + sl.accept);
     p.state = reinterpret_cast<float4 *>(w + sl.state);
     p.rs = reinterpret_cast<double *>(w + sl.rs);
     p.ps = reinterpret_cast<double *>(w + sl.ps);

@@ -14,23 +14,26 @@
 //   S_t = Q . K_t^T                       (M 128, N 64 keys, K 128)
 //   P_t = exp2(S_t * scale * log2e - m)   split as P_hi + P_lo, both bf16
 //   O_(t mod 2) += P_hi . V_t + P_lo . V_t  (M 128, N 128, K 64)
-// The two-term split keeps every weight to about 2^-17 relative, so the
+// The two-term split keeps every weight to within 2^-14 relative, so the
 // product is as accurate as an fp32 P even when a few keys dominate.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3 / 4-7  two softmax warpgroups; warpgroup w takes the tiles with
 //                    t mod 2 == w, has two S/P buffers and its own O
 //                    accumulator in tensor memory and its own running max /
 //                    sum; thread = row (= tensor-memory lane).  The two halves
 //                    are merged at the end like two splits.
 //   warp 8           TMA producer: Q first, then a K/V ring in shared memory
-//   warp 9           allocates tensor memory; one thread issues the MMAs,
-//                    serving whichever of "next S" / "next P.V" is ready.
-// Tensor memory: O0 [0,128), O1 [128,256), four S/P buffers of 64 columns;
-// tile t uses buffer t mod 4, so S of tile t+2 is computed while P.V of tile
-// t is still pending.  P is written back into the columns that held S
+//   warp 9           allocates tensor memory; one thread issues the S MMAs
+//   warp 10          one thread issues the P.V MMAs
+// The two issuers each wait only on their own barriers, so a finished softmax
+// never waits behind the issue of the next S (or the other way round).
+// Tensor memory: O0 [0,128), O1 [128,256), three S/P buffers of 64 columns
+// and Q (64 columns, the A operand of every S, so S reads only K from shared
+// memory); tile t uses buffer t mod 3, so S of the next tiles is computed
+// while P.V of tile t is still pending.  P is written back into the columns that held S
 // (variant kPTmem) and read by the MMA as its A operand, which leaves shared
-// memory to a 5-stage K/V ring; the other variant stages P through shared
+// memory to a 6-stage K/V ring; the other variant stages P through shared
 // memory.  The partial output leaves through shared memory so that the global
 // stores are coalesced.
 // The running max only moves when it grows by more than 2^8, so O is rescaled
@@ -50,14 +53,16 @@ namespace sdv {
 
 namespace {
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 352;
 constexpr int kBN = kTileKeys;              // keys per tile (64)
 constexpr int kQBytes = 2 * 128 * 128;      // two K-blocks of [128 rows x 128 B]
 constexpr int kKBytes = 2 * kBN * 128;      // two K-blocks of [64 keys x 128 B]
 constexpr int kVBytes = 2 * kBN * 128;      // two d-chunks of [64 keys x 128 B]
 constexpr int kStageBytes = kKBytes + kVBytes;
 constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16, one half (hi or lo)
-constexpr uint32_t kTmemCols = 512;         // O0 [0,128) O1 [128,256) SP0..SP3 [256 + 64 i, +64)
+constexpr uint32_t kTmemCols = 512;         // O0 [0,128) O1 [128,256) SP0..SP2 [256 + 64 i, +64) Q [448,512)
+constexpr int kSP = 3;                      // S/P buffers in tensor memory
+constexpr uint32_t kQCol = 448;             // Q as the A operand of S: bf16 pairs, 64 columns
 constexpr int kOStride = 132;               // floats per staged output row (bank-conflict padding)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -65,16 +70,16 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 template <bool kPTmem> struct Layout {
-    static constexpr int kStages = kPTmem ? 5 : 3;
+    static constexpr int kStages = kPTmem ? 6 : 3;
     static constexpr int kOffQ = 0;
     static constexpr int kOffStage = kQBytes;
     static constexpr int kOffP = kOffStage + kStages * kStageBytes;          // smem P (variant 2 only)
     static constexpr int kOffBar = kOffP + (kPTmem ? 0 : 4 * kPBytes);
-    // full[S], empty[S], sfull[4], pfull[4], pempty[4], qready, drain
-    static constexpr int kNumBars = 2 * kStages + 14;
+    // full[S], empty[S], sfull[3], pfull[3], pempty[3], qready, qtmem, drain x2
+    static constexpr int kNumBars = 2 * kStages + 3 * kSP + 4;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                  // tmem base, abort flag
-    static constexpr int kOffXchg = kOffMisc + 16;                           // (m, l) exchange
-    static constexpr int kSmemBytes = kOffXchg + 2 * 128 * 8 + 1024;         // + alignment slack
+    static constexpr int kOffXchg = kOffQ;  // (m, l) exchange, in the Q tile once every MMA is done
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;                  // + alignment slack
 };
 
 struct TcParams {
@@ -111,15 +116,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-
 // Bounded wait for the phase of parity `parity` to complete.  Gives up when
 // another thread of the CTA gave up (abort flag, if given) or after kWaitLimitNs.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
@@ -247,11 +243,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
 // byte offset of 16-byte chunk c (0..7) of row r in a [rows x 128 B] tile with 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -278,10 +269,12 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (NS + i); };
     auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + i); };
-    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + 4 + i); };
-    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + 8 + i); };
-    const uint32_t qready_bar = bar0 + 8u * (2 * NS + 12);
-    const uint32_t drain_bar = bar0 + 8u * (2 * NS + 13);
+    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + kSP + i); };
+    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + 2 * kSP + i); };
+    const uint32_t qready_bar = bar0 + 8u * (2 * NS + 3 * kSP);
+    const uint32_t qtmem_bar = bar0 + 8u * (2 * NS + 3 * kSP + 1);
+    const uint32_t drain_bar = bar0 + 8u * (2 * NS + 3 * kSP + 2);
+    const uint32_t drain2_bar = bar0 + 8u * (2 * NS + 3 * kSP + 3);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 8);
     float2 *xchg = reinterpret_cast<float2 *>(sbase + L::kOffXchg);  // [2][128] (m, l) per warpgroup
@@ -289,9 +282,11 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     // ---- prologue that reads nothing produced upstream ----
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
-        for (int i = 0; i < 4; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 4); mbar_init(pempty_bar(i), 1); }
-        mbar_init(qready_bar, 1 + 4);  // Q copy (with its bytes) + the four warps that zero the padding rows
+        for (int i = 0; i < kSP; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 4); mbar_init(pempty_bar(i), 1); }
+        mbar_init(qready_bar, 1);  // the Q copy, with its bytes
+        mbar_init(qtmem_bar, 4);   // the four warps that move Q into tensor memory
         mbar_init(drain_bar, 1);
+        mbar_init(drain2_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -391,77 +386,63 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
         __syncwarp();
     } else if (warp == 9) {
-        // ------------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------------ S issuer
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, kBN, false);
-            const uint32_t idO = idesc_bf16(128, 128, true);
-            bool ok = mbar_wait(qready_bar, 0, abort_flag, p.fault);
-            int nS = 0, nP = 0;
-            unsigned long long t0 = global_timer();
-            uint32_t spins = 0;
-            while (ok && nP < n_tiles) {
-                bool did = false;
-                // S of tile nS into buffer nS % 4 once K is loaded and the buffer's
-                // previous occupant (tile nS-4) has been consumed by its P.V
-                if (nS < n_tiles && nS < nP + 4) {
-                    const int st = nS % NS;
-                    if (mbar_test(full_bar(st), (nS / NS) & 1) &&
-                        (nS < 4 || mbar_test(pempty_bar(nS & 3), ((nS >> 2) - 1) & 1))) {
-                        tc_fence_after();
-                        const uint32_t dcol = tmem + 256u + 64u * (nS & 3);
-                        const uint32_t kbase = sStage + st * kStageBytes;
+            bool ok = mbar_wait(qtmem_bar, 0, abort_flag, p.fault);
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                // K of tile t loaded, and buffer t % 3 consumed by the P.V of tile t-3
+                const int bi = t % kSP;
+                ok = mbar_wait(full_bar(t % NS), (t / NS) & 1, abort_flag, p.fault);
+                if (ok && t >= kSP) ok = mbar_wait(pempty_bar(bi), ((t / kSP) - 1) & 1, abort_flag, p.fault);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t dcol = tmem + 256u + 64u * bi;
+                const uint32_t kbase = sStage + (t % NS) * kStageBytes;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t a = sw128_desc(sQ + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-                            umma_ss(dcol, a, bd, idS, kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(sfull_bar(nS & 3));
-                        ++nS;
-                        did = true;
-                    }
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
+                    umma_ts(dcol, tmem + kQCol + 8u * kk, bd, idS, kk > 0 ? 1u : 0u);
                 }
-                // P.V of tile nP once its softmax is done
-                if (nP < nS && mbar_test(pfull_bar(nP & 3), (nP >> 2) & 1)) {
-                    tc_fence_after();
-                    const int st = nP % NS;
-                    const int wb = nP & 1;
-                    const uint32_t vbase = sStage + st * kStageBytes + kKBytes;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, kBN * 128, 1024);
-                            const uint32_t acc = (nP >= 2 || half > 0 || kk > 0) ? 1u : 0u;
-                            if (kPTmem) {
-                                const uint32_t a_t = tmem + 256u + 64u * (nP & 3) + 32u * half + 8u * kk;
-                                umma_ts(tmem + 128u * wb, a_t, bd, idO, acc);
-                            } else {
-                                const uint64_t a = sw128_desc(sP + (wb * 2 + half) * kPBytes + kk * 32, 16, 1024);
-                                umma_ss(tmem + 128u * wb, a, bd, idO, acc);
-                            }
-                        }
-                    }
-                    umma_commit(pempty_bar(nP & 3));
-                    umma_commit(empty_bar(st));
-                    ++nP;
-                    did = true;
-                }
-                if (did) {
-                    t0 = global_timer();
-                    spins = 0;
-                } else if ((++spins & 63u) == 0) {
-                    if (*abort_flag) { ok = false; break; }
-                    if (global_timer() - t0 > kWaitLimitNs) {
-                        *abort_flag = 1;
-                        set_fault(p.fault, FAULT_WAIT_TIMEOUT);
-                        ok = false;
-                    }
-                }
+                umma_commit(sfull_bar(bi));
             }
-            // every MMA issued above has completed before tensor memory is freed
+            // every MMA this thread issued has completed before tensor memory is freed
             umma_commit(drain_bar);
             mbar_wait(drain_bar, 0, nullptr, p.fault);
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            const uint32_t idO = idesc_bf16(128, 128, true);
+            bool ok = true;
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                ok = mbar_wait(pfull_bar(t % kSP), (t / kSP) & 1, abort_flag, p.fault);
+                if (!ok) break;
+                tc_fence_after();
+                const int st = t % NS;
+                const int wb = t & 1;
+                const uint32_t vbase = sStage + st * kStageBytes + kKBytes;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, kBN * 128, 1024);
+                        const uint32_t acc = (t >= 2 || half > 0 || kk > 0) ? 1u : 0u;
+                        if (kPTmem) {
+                            const uint32_t a_t = tmem + 256u + 64u * (t % kSP) + 32u * half + 8u * kk;
+                            umma_ts(tmem + 128u * wb, a_t, bd, idO, acc);
+                        } else {
+                            const uint64_t a = sw128_desc(sP + (wb * 2 + half) * kPBytes + kk * 32, 16, 1024);
+                            umma_ss(tmem + 128u * wb, a, bd, idO, acc);
+                        }
+                    }
+                }
+                umma_commit(pempty_bar(t % kSP));
+                umma_commit(empty_bar(st));
+            }
+            umma_commit(drain2_bar);
+            mbar_wait(drain2_bar, 0, nullptr, p.fault);
         }
         __syncwarp();
     } else {
@@ -474,24 +455,32 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t o_col = tmem + lane_off + 128u * wg;
         if (wg == 0) {
-            // Q rows past the M real rows are zero (the copy fills rows [0, M))
-            if (!row_ok) {
+            // Q into tensor memory (the A operand of S): row r = lane r, bf16
+            // pairs along K; rows past the M real ones are zero
+            const bool qok = __all_sync(0xffffffffu, mbar_wait(qready_bar, 0, abort_flag, p.fault));
+            uint32_t qa[32], qb[32];
 #pragma unroll
-                for (int ch = 0; ch < 16; ++ch)
-                    *reinterpret_cast<uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
+            for (int ch = 0; ch < 16; ++ch) {
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (row_ok && qok)
+                    v = *reinterpret_cast<const uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7));
+                uint32_t *dst = ch < 8 ? &qa[4 * ch] : &qb[4 * (ch - 8)];
+                dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
             }
+            tmem_st32(tmem + lane_off + kQCol, qa);
+            tmem_st32(tmem + lane_off + kQCol + 32u, qb);
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(qready_bar);
+            if (lane == 0) mbar_arrive(qtmem_bar);
         }
 
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         int last_t = -1;
         for (int t = wg; t < n_tiles; t += 2) {
-            const int bi = t & 3;   // S/P buffer
-            const int u = t >> 2;   // use index of that buffer
+            const int bi = t % kSP;  // S/P buffer
+            const int u = t / kSP;   // use index of that buffer
             const uint32_t sp_col = tmem + lane_off + 256u + 64u * bi;
             ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(bi), u & 1, abort_flag, p.fault));
             if (!ok) break;
@@ -533,7 +522,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // (shared-memory variant) the P buffer is touched again
             if (!first && (!kPTmem || __any_sync(0xffffffffu, need))) {
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(pempty_bar((t - 2) & 3), ((t - 2) >> 2) & 1, abort_flag, p.fault));
+                                mbar_wait(pempty_bar((t - 2) % kSP), ((t - 2) / kSP) & 1, abort_flag, p.fault));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -567,11 +556,14 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 const float p0 = (live && 2 * c < nvalid) ? e0 : 0.f;
                 const float p1 = (live && 2 * c + 1 < nvalid) ? e1 : 0.f;
                 ls[c & 3] += p0 + p1;
-                pk[c] = pack_bf16(p0, p1);
-                // residual after rounding to bf16 (exact in fp32), itself rounded to bf16
-                const float r0 = p0 - __uint_as_float(pk[c] << 16);
-                const float r1 = p1 - __uint_as_float(pk[c] & 0xffff0000u);
-                pl[c] = pack_bf16(r0, r1);
+                // hi = p truncated to bf16; lo = the exact fp32 remainder truncated
+                // to bf16: |p - hi - lo| < 2^-14 p.  Byte permutes instead of
+                // conversion instructions.
+                const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                pk[c] = __byte_perm(b0, b1, 0x7632);
+                const uint32_t q0 = __float_as_uint(p0 - __uint_as_float(b0 & 0xffff0000u));
+                const uint32_t q1 = __float_as_uint(p1 - __uint_as_float(b1 & 0xffff0000u));
+                pl[c] = __byte_perm(q0, q1, 0x7632);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             if (kPTmem) {
@@ -609,12 +601,15 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
         // ---- epilogue: merge the two warpgroups' (m, l, O), write this split's partial ----
         if (ok && last_t >= 0)
-            ok = mbar_wait(pempty_bar(last_t & 3), (last_t >> 2) & 1, abort_flag, p.fault);
+            ok = mbar_wait(pempty_bar(last_t % kSP), (last_t / kSP) & 1, abort_flag, p.fault);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok || last_t < 0) { m_used = -INFINITY; l = 0.f; }
-        xchg[wg * 128 + r] = make_float2(m_used, l);
         tc_fence_before();
-        named_sync(1, 256);  // both warpgroups' last P.V are complete past this point
+        // both warpgroups' last P.V, hence every MMA of the CTA, are complete past
+        // this point: the Q tile is free for the (m, l) exchange
+        named_sync(1, 256);
+        xchg[wg * 128 + r] = make_float2(m_used, l);
+        named_sync(1, 256);
         const float2 mine = xchg[wg * 128 + r], other = xchg[(wg ^ 1) * 128 + r];
         const float m0 = wg == 0 ? mine.x : other.x, l0 = wg == 0 ? mine.y : other.y;
         const float m1 = wg == 0 ? other.x : mine.x, l1 = wg == 0 ? other.y : mine.y;

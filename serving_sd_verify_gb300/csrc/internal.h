@@ -64,11 +64,9 @@ struct GreedyParams {
     sd_dtype dt;
     int32_t *n_acc, *corr;
     int chunk, n_chunks;
-    unsigned int *counter;          // rows finished
-    unsigned int *row_counter;      // [B*T] chunks finished per row
+    unsigned int *counter;          // CTAs finished
     float *pval;                    // [B*T, n_chunks] chunk max
     int *pidx;                      // [B*T, n_chunks] its index
-    int *amax;                      // [B*T] row argmax
     unsigned int *fault;
 };
 cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st);
@@ -83,14 +81,14 @@ struct SampleParams {
     uint64_t seed;
     uint32_t offset;
     int32_t *n_acc, *next_id;
-    int chunk, n_chunks;            // chunk <= kSampleChunkMax
-    unsigned int *counters;         // [0]: rows finished (pass 1)
-    unsigned int *row_counter;      // [B*T] chunks finished per row (pass 1) / per sequence (pass 2)
+    int chunk, n_chunks;            // pass 1 chunks, chunk <= kSampleChunkMax
+    int draw_chunk, n_draw_chunks;  // pass 2 chunks, draw_chunk <= kSampleChunkMax
+    unsigned int *counters;         // [0]: CTAs of pass 1 finished
+    unsigned int *row_counter;      // [B] CTAs of pass 2 finished per sequence
     float *pm, *pz;                 // [B*T, n_chunks] chunk max and sum of exp
-    float2 *row_stats;              // [B*T] (M, Z) of softmax(l / tau)
-    int *accept;                    // [B*T] proposal of row accepted
+    float2 *row_stats;              // [B*T] (logit, q) of the row's proposal
     float4 *state;                  // [B]: (n as int bits, M, Z, unused) of the deciding row
-    double *rs, *ps;                // [B, n_chunks] residual / p chunk sums
+    double *rs, *ps;                // [B, n_draw_chunks] residual / p chunk sums
     unsigned int *fault;
 };
 constexpr int kSampleChunkMax = 4096;
