@@ -79,6 +79,9 @@ typedef struct {
  *   query head h reads kv head h / (Hq / Hkv)
  *   logits are scale * q.k; softmax and accumulation in fp32
  *   T in [1, 16]; D in {64, 128}; Hq % Hkv == 0; (Hq / Hkv) * T <= 256
+ *
+ * workspace: zero-filled before the first call on it (it holds per-(sequence,
+ * kv head) counters of the splits that every completed call returns to zero).
  * ------------------------------------------------------------------------ */
 sd_status sd_verify_attention(const void *q, const void *k_cache, const void *v_cache,
                               sd_strides kv, const int32_t *ctx_len, int max_ctx,
@@ -105,6 +108,7 @@ size_t sd_verify_attention_workspace_size(int B, int T, int Hq, int Hkv, int D,
  *   out          fp32 [B, T, Hq, D]
  *   every row attends to context keys [0, n_ctx[b]) followed by the T block keys
  *   limits as for sd_verify_attention
+ *   workspace as for sd_verify_attention (zero-filled before its first call)
  * ------------------------------------------------------------------------ */
 sd_status sd_draft_block_attention(const void *q, const void *k_ctx, const void *v_ctx,
                                    sd_strides ctx, const int32_t *n_ctx, int max_ctx,
@@ -217,13 +221,12 @@ sd_status sd_fault_word(uint32_t *out, int clear);
 
 /* Attention kernel selection, process-wide, for tests and measurement:
  * 0 = automatic (tensor-core kernel where it applies), 1 = force the
- * CUDA-core kernel, 2 = require the tensor-core kernel, 3 = require its
- * variant that stages the softmax weights through shared memory instead of
- * tensor memory (calls the tensor-core kernel cannot serve return
- * SD_ERR_UNSUPPORTED under 2 and 3).  Returns the previous setting. */
+ * CUDA-core kernel, 2 = require the tensor-core kernel (calls it cannot
+ * serve return SD_ERR_UNSUPPORTED).  Other values select 0.  Returns the
+ * previous setting. */
 int sd_set_attention_path(int path);
 
-/* Which kernel the last attention call on this thread launched (1, 2 or 3 as
+/* Which kernel the last attention call on this thread launched (1 or 2 as
  * above) and how many key splits it used. */
 int sd_last_attention_path(int *n_splits);
 

@@ -75,10 +75,12 @@ AttnPlan plan_attention(const AttnParams &p, int path) {
     AttnPlan pl;
     pl.path = path;
     int ctas_per_sm, min_keys, gran;
-    if (path >= 2) { ctas_per_sm = 1; min_keys = 4 * kTileKeys; gran = kTileKeys; }
+    if (path >= 2) { ctas_per_sm = 1; min_keys = 2 * kTcTileKeys; gran = kTcTileKeys; }
     else { ctas_per_sm = 2; min_keys = 128; gran = 32; }
     const int target = std::max(1, sms * ctas_per_sm);
-    int splits = (target + units - 1) / units;
+    // the tensor-core grid stays within one CTA per SM, so that the splits of
+    // a (sequence, kv head) can merge inside the kernel
+    int splits = path >= 2 ? std::max(1, target / units) : (target + units - 1) / units;
     splits = std::max(1, std::min(splits, (N + min_keys - 1) / min_keys));
     int kps = (N + splits - 1) / splits;
     kps = (kps + gran - 1) / gran * gran;
@@ -87,9 +89,11 @@ AttnPlan plan_attention(const AttnParams &p, int path) {
     return pl;
 }
 
-size_t attn_workspace(int B, int T, int Hq, int D, int n_splits) {
+// attention workspace: [header][merge counters, B * Hkv][o_part][lse_part]
+size_t attn_counters_bytes(int B, int Hkv) { return align_up((size_t)B * Hkv * sizeof(unsigned int), 256); }
+size_t attn_workspace(int B, int T, int Hq, int Hkv, int D, int n_splits) {
     const size_t rows = (size_t)B * T * Hq;
-    return kHeader + align_up((size_t)n_splits * rows * D * sizeof(float), 256) +
+    return kHeader + attn_counters_bytes(B, Hkv) + align_up((size_t)n_splits * rows * D * sizeof(float), 256) +
            align_up((size_t)n_splits * rows * sizeof(float), 256);
 }
 
@@ -122,25 +126,35 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     const int force = g_force_path.load();
     int path;
     if (force == 1) path = 1;
-    else if (attn_tc_supported(p)) path = force == 3 ? 3 : 2;
+    else if (attn_tc_supported(p)) path = 2;
     else if (force >= 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
     else path = 1;
     AttnPlan pl = plan_attention(p, path);
-    const size_t need = attn_workspace(p.B, p.T, p.Hq, p.D, pl.n_splits);
+    const size_t need = attn_workspace(p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits);
     if (!ws || ws_bytes < need)
         return fail(SD_ERR_WORKSPACE, "attention workspace too small: need %zu bytes, got %zu", need, ws_bytes);
     if (!aligned16(ws)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     const size_t rows = (size_t)p.B * p.T * p.Hq;
-    char *w = static_cast<char *>(ws) + kHeader;
+    p.merge_ctr = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + kHeader);
+    char *w = static_cast<char *>(ws) + kHeader + attn_counters_bytes(p.B, p.Hkv);
     p.o_part = reinterpret_cast<float *>(w);
     p.lse_part = reinterpret_cast<float *>(w + align_up((size_t)pl.n_splits * rows * p.D * sizeof(float), 256));
     p.n_splits = pl.n_splits;
     p.keys_per_split = pl.keys_per_split;
-    cudaError_t e = path == 2 ? launch_attn_tc(p, st) : path == 3 ? launch_attn_tc_smem_p(p, st)
-                                                                  : launch_attn_generic(p, st);
+    // tensor-core path: one split writes the output itself; several merge
+    // inside the kernel when the whole grid is resident at once (at most one
+    // CTA per SM), else in the merge kernel
+    p.merge = 0;
+    if (path == 2) {
+        if (pl.n_splits == 1) p.merge = 2;
+        else if ((long)pl.n_splits * p.Hkv * p.B <= device_sm_count()) p.merge = 1;
+    }
+    cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
-    e = launch_lse_merge(p, st);
-    if (e != cudaSuccess) return cuda_fail(e, "attention merge kernel launch");
+    if (p.merge == 0) {
+        e = launch_lse_merge(p, st);
+        if (e != cudaSuccess) return cuda_fail(e, "attention merge kernel launch");
+    }
     g_last_path = path;
     g_last_splits = pl.n_splits;
     return SD_OK;
@@ -150,8 +164,8 @@ size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max
     if (B < 1 || T < 1 || T > kMaxT || Hq < 1 || Hkv < 1 || max_ctx < 1 || (D != 64 && D != 128)) return 0;
     AttnParams p = {};
     p.mode = mode; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dt; p.max_ctx = max_ctx;
-    size_t need = attn_workspace(B, T, Hq, D, plan_attention(p, 1).n_splits);
-    need = std::max(need, attn_workspace(B, T, Hq, D, plan_attention(p, 2).n_splits));
+    size_t need = attn_workspace(B, T, Hq, Hkv, D, plan_attention(p, 1).n_splits);
+    need = std::max(need, attn_workspace(B, T, Hq, Hkv, D, plan_attention(p, 2).n_splits));
     return need;
 }
 
@@ -249,7 +263,7 @@ const char *sd_last_error(void) { return g_err; }
 int sd_version(void) { return 100; }
 
 int sd_set_attention_path(int path) {
-    if (path < 0 || path > 3) path = 0;
+    if (path < 0 || path > 2) path = 0;
     return g_force_path.exchange(path);
 }
 

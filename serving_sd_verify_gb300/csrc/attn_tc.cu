@@ -10,34 +10,37 @@
 //
 // One CTA owns one (split, kv head, sequence).  All G*T query rows that read
 // that kv head form the M = 128 rows of the MMAs (zero-padded), so every K/V
-// tile is fetched from HBM once and serves every row.  For key tile t:
-//   S_t = Q . K_t^T                       (M 128, N 64 keys, K 128)
+// tile is fetched from HBM once and serves every row.  For key tile t
+// (128 keys):
+//   S_t = Q . K_t^T                       (M 128, N 128 keys, K 128)
 //   P_t = exp2(S_t * scale * log2e - m)   split as P_hi + P_lo, both bf16
-//   O_(t mod 2) += P_hi . V_t + P_lo . V_t  (M 128, N 128, K 64)
+//   O  += P_hi . V_t + P_lo . V_t         (M 128, N 128, K 128)
 // The two-term split keeps every weight to within 2^-14 relative, so the
 // product is as accurate as an fp32 P even when a few keys dominate.
 //
-// Warp roles (352 threads):
-//   warps 0-3 / 4-7  two softmax warpgroups; warpgroup w takes the tiles with
-//                    t mod 2 == w, has two S/P buffers and its own O
-//                    accumulator in tensor memory and its own running max /
-//                    sum; thread = row (= tensor-memory lane).  The two halves
-//                    are merged at the end like two splits.
-//   warp 8           TMA producer: Q first, then a K/V ring in shared memory
-//   warp 9           allocates tensor memory; one thread issues the S MMAs
-//   warp 10          one thread issues the P.V MMAs
-// The two issuers each wait only on their own barriers, so a finished softmax
-// never waits behind the issue of the next S (or the other way round).
-// Tensor memory: O0 [0,128), O1 [128,256), three S/P buffers of 64 columns
-// and Q (64 columns, the A operand of every S, so S reads only K from shared
-// memory); tile t uses buffer t mod 3, so S of the next tiles is computed
-// while P.V of tile t is still pending.  P is written back into the columns that held S
-// (variant kPTmem) and read by the MMA as its A operand, which leaves shared
-// memory to a 6-stage K/V ring; the other variant stages P through shared
-// memory.  The partial output leaves through shared memory so that the global
-// stores are coalesced.
+// Warp roles (384 threads):
+//   warp 0           TMA producer: Q, then K tiles and V tiles into rings of
+//                    three 32 KB slots each
+//   warp 1           allocates tensor memory; one thread issues every MMA: S
+//                    up to three tiles ahead, and P.V as soon as its P is written
+//   warps 4-7, 8-11  two softmax warpgroups, both on every tile: warpgroup w
+//                    takes keys [64 w, 64 w + 64) of it; thread = row (=
+//                    tensor-memory lane).  They exchange the row max through
+//                    shared memory, so both hold the same reference max and O
+//                    is a single accumulator.
+// A K slot is refilled as soon as the S that read it has completed, a V slot
+// once its P.V has.  The producer sets up the barriers and issues Q and the
+// first K/V tiles before the CTA-wide sync, so the copies overlap the tensor
+// memory allocation.
+// Tensor memory: O [0,128) and three S/P buffers [128 + 128 i, +128).  P is
+// written back over the S columns it came from (hi and lo halves of each
+// 64-key half) and read by the P.V MMAs as their A operand.  The partial
+// output leaves through shared memory so that the global stores are
+// coalesced.  With several splits the kernel also merges them (see
+// merge_group); with one it writes the output itself.
 // The running max only moves when it grows by more than 2^8, so O is rescaled
 // in tensor memory rarely (exact either way: P and l use the same reference).
+// Tiles that every row sees in full skip the per-key masks.
 // Every wait is bounded by the global timer; a wait that gives up sets the
 // fault word and the CTA drains its copies and MMAs before freeing tensor
 // memory and returning.
@@ -53,40 +56,38 @@ namespace sdv {
 
 namespace {
 
-constexpr int kTcThreads = 352;
-constexpr int kBN = kTileKeys;              // keys per tile (64)
-constexpr int kQBytes = 2 * 128 * 128;      // two K-blocks of [128 rows x 128 B]
-constexpr int kKBytes = 2 * kBN * 128;      // two K-blocks of [64 keys x 128 B]
-constexpr int kVBytes = 2 * kBN * 128;      // two d-chunks of [64 keys x 128 B]
-constexpr int kStageBytes = kKBytes + kVBytes;
-constexpr int kPBytes = 128 * 128;          // [128 rows x 64 keys] bf16, one half (hi or lo)
-constexpr uint32_t kTmemCols = 512;         // O0 [0,128) O1 [128,256) SP0..SP2 [256 + 64 i, +64) Q [448,512)
+constexpr int kTcThreads = 384;
+constexpr int kProducerWarp = 0;            // TMA producer
+constexpr int kMmaWarp = 1;                 // tensor-memory allocation, MMA issue
+constexpr int kSoftmaxWarp0 = 4;            // warps 4-7 and 8-11: the two softmax warpgroups
+constexpr int kBN = kTcTileKeys;            // keys per tile (128)
+constexpr int kTileBytes = 2 * kBN * 128;   // K or V tile: two 64-column blocks of [128 keys x 128 B]
+constexpr int kQBytes = 2 * 128 * 128;      // Q: two 64-column blocks of [128 rows x 128 B]
+constexpr int kKSlots = 3, kVSlots = 3;
 constexpr int kSP = 3;                      // S/P buffers in tensor memory
-constexpr uint32_t kQCol = 448;             // Q as the A operand of S: bf16 pairs, 64 columns
+constexpr uint32_t kTmemCols = 512;         // O [0,128), S/P buffer i at [128 + 128 i, +128)
 constexpr int kOStride = 132;               // floats per staged output row (bank-conflict padding)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-template <bool kPTmem> struct Layout {
-    static constexpr int kStages = kPTmem ? 6 : 3;
+struct Layout {
     static constexpr int kOffQ = 0;
-    static constexpr int kOffStage = kQBytes;
-    static constexpr int kOffP = kOffStage + kStages * kStageBytes;          // smem P (variant 2 only)
-    static constexpr int kOffBar = kOffP + (kPTmem ? 0 : 4 * kPBytes);
-    // full[S], empty[S], sfull[3], pfull[3], pempty[3], qready, qtmem, drain x2
-    static constexpr int kNumBars = 2 * kStages + 3 * kSP + 4;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                  // tmem base, abort flag
-    static constexpr int kOffXchg = kOffQ;  // (m, l) exchange, in the Q tile once every MMA is done
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;                  // + alignment slack
+    static constexpr int kOffK = kQBytes;
+    static constexpr int kOffV = kOffK + kKSlots * kTileBytes;
+    static constexpr int kOffBar = kOffV + kVSlots * kTileBytes;
+    // kfull[3] kempty[3] vfull[3] vempty[3] sfull[3] pfull[3] pempty[3] qready drain
+    static constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 3 * kSP + 2;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                 // tmem base, abort flag, merge flag
+    static constexpr int kOffX = kOffMisc + 16;                             // [2][128] per-row exchange
+    // epilogue, once every copy and MMA is done: the staged output rows, in the
+    // (then idle) K ring
+    static constexpr int kOffOStage = kOffK;
+    static constexpr int kSmemBytes = kOffX + 2 * 128 * 4 + 1024;           // + alignment slack
+    static_assert(128 * kOStride * 4 <= kKSlots * kTileBytes, "staging fits in the K ring");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
-
-struct TcParams {
-    AttnParams a;
-    int dim_s, dim_h;   // tensor-map dimension index of the slot and kv-head axes (1 or 2)
-};
-static_assert(128 * kOStride * 4 <= 5 * (2 * 64 * 128 * 2), "output staging fits in the K/V ring");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -116,6 +117,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase of parity `parity` to complete.  Gives up when
 // another thread of the CTA gave up (abort flag, if given) or after kWaitLimitNs.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
@@ -141,6 +150,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
 
@@ -235,6 +253,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         ::"r"(taddr), SDV_S8(0), SDV_S8(8), SDV_S8(16), SDV_S8(24)
         : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12,"
+        " %13, %14, %15, %16};" ::"r"(taddr), SDV_S8(0), SDV_S8(8)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -247,15 +271,117 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
 // ---------------------------------------------------------------------------
+// merge of the splits inside the kernel
+// ---------------------------------------------------------------------------
+// Bounded wait until the counter reaches `target`.
+__device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int target) {
+    const unsigned long long t0 = global_timer();
+    for (uint32_t it = 0;; ++it) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((it & 15u) == 15u && global_timer() - t0 > kWaitLimitNs) return false;
+        __nanosleep(32);
+    }
+}
+
+// Every split of sequence b, kv head g has written its partial (rows
+// normalised by their own sum, plus their log-sum-exp); once all of them have
+// arrived, split s combines rows s, s + n, s + 2n, ... of the group's M rows
+// (n = splits): out = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max).
+// The whole grid is resident (at most one CTA per SM), so the wait ends.  The
+// counter is returned to zero by the last split to finish merging.  `scratch`
+// is idle shared memory (the K/V rings).
+constexpr int kMergeChunk = 8;  // splits summed by one work unit, loads all in flight
+__device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int G, long rows_total,
+                            volatile int *go, uint8_t *scratch) {
+    unsigned int *ctr = p.merge_ctr + ((long)b * p.Hkv + g);
+    const int n = (int)gridDim.x;
+    const int tid = threadIdx.x;
+    __threadfence();  // this thread's partial stores are visible device-wide
+    __syncthreads();
+    if (tid == 0) {
+        atomicAdd(ctr, 1u);
+        const bool ok = wait_count(ctr, (unsigned int)n);
+        if (!ok) set_fault(p.fault, FAULT_WAIT_TIMEOUT);
+        *go = ok ? 1 : 0;
+    }
+    __syncthreads();
+    const int R = s < M ? (M - s + n - 1) / n : 0;   // rows of this split
+    const int K = (n + kMergeChunk - 1) / kMergeChunk;
+    float *wgt = reinterpret_cast<float *>(scratch);                     // [R][n] lse, then weights
+    float *inv = wgt + R * n;                                            // [R] 1 / sum of weights
+    float4 *part = reinterpret_cast<float4 *>(scratch + ((R * n + R) * 4 + 15) / 16 * 16);  // [K][R][32]
+    auto frow_of = [&](int ri) {
+        const int rr = s + ri * n;
+        return ((long)b * p.T + rr / G) * p.Hq + g * G + rr % G;
+    };
+    if (*go && R > 0) {
+        for (int i = tid; i < R * n; i += kTcThreads)
+            wgt[i] = __ldcg(p.lse_part + (long)(i % n) * rows_total + frow_of(i / n));
+        __syncthreads();
+        for (int ri = tid; ri < R; ri += kTcThreads) {
+            float m = -INFINITY;
+            for (int sp = 0; sp < n; ++sp) m = fmaxf(m, wgt[ri * n + sp]);
+            float sum = 0.f;
+            for (int sp = 0; sp < n; ++sp) {
+                const float l = wgt[ri * n + sp];
+                const float w = l == -INFINITY ? 0.f : __expf(l - m);  // an empty split weighs 0
+                wgt[ri * n + sp] = w;
+                sum += w;
+            }
+            inv[ri] = sum > 0.f ? 1.f / sum : 0.f;
+        }
+        __syncthreads();
+        for (int u = tid; u < K * R * 32; u += kTcThreads) {
+            const int k = u / (R * 32), ri = (u / 32) % R, c4 = u & 31;
+            const long frow = frow_of(ri);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            // branch-free, so that the chunk's loads are all in flight at once:
+            // past the last split, re-read the last one with weight 0
+            float4 v[kMergeChunk];
+            float w[kMergeChunk];
+#pragma unroll
+            for (int e = 0; e < kMergeChunk; ++e) {
+                const int sp = min(k * kMergeChunk + e, n - 1);
+                v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ((long)sp * rows_total + frow) * 128) + c4);
+                w[e] = k * kMergeChunk + e < n ? wgt[ri * n + sp] : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < kMergeChunk; ++e) {
+                acc.x = fmaf(w[e], v[e].x, acc.x); acc.y = fmaf(w[e], v[e].y, acc.y);
+                acc.z = fmaf(w[e], v[e].z, acc.z); acc.w = fmaf(w[e], v[e].w, acc.w);
+            }
+            part[u] = acc;
+        }
+        __syncthreads();
+        for (int i = tid; i < R * 32; i += kTcThreads) {
+            const int ri = i / 32, c4 = i & 31;
+            float4 acc = part[i];
+            for (int k = 1; k < K; ++k) {
+                const float4 v = part[k * R * 32 + i];
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            const float f = inv[ri];
+            reinterpret_cast<float4 *>(p.out + frow_of(ri) * 128)[c4] =
+                make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+        }
+    }
+    // back to zero once every split of the group has merged
+    __syncthreads();
+    if (tid == 0 && *go) {
+        const unsigned int ticket = atomicAdd(ctr, 1u);
+        if (ticket == 2u * (unsigned int)n - 1u) atomicExch(ctr, 0u);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool kPTmem>
 __global__ void __launch_bounds__(kTcThreads, 1)
 attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const TcParams tp) {
-    using L = Layout<kPTmem>;
-    constexpr int NS = L::kStages;
-    const AttnParams &p = tp.a;
+                     const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+    using L = Layout;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -264,47 +390,52 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const uint32_t sQ = base + L::kOffQ, sStage = base + L::kOffStage, sP = base + L::kOffP;
+    const uint32_t sQ = base + L::kOffQ, sK = base + L::kOffK, sV = base + L::kOffV;
     const uint32_t bar0 = base + L::kOffBar;
-    auto full_bar = [&](int i) { return bar0 + 8u * i; };
-    auto empty_bar = [&](int i) { return bar0 + 8u * (NS + i); };
-    auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + i); };
-    auto pfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + kSP + i); };
-    auto pempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + 2 * kSP + i); };
-    const uint32_t qready_bar = bar0 + 8u * (2 * NS + 3 * kSP);
-    const uint32_t qtmem_bar = bar0 + 8u * (2 * NS + 3 * kSP + 1);
-    const uint32_t drain_bar = bar0 + 8u * (2 * NS + 3 * kSP + 2);
-    const uint32_t drain2_bar = bar0 + 8u * (2 * NS + 3 * kSP + 3);
+    auto kfull_bar = [&](int i) { return bar0 + 8u * i; };
+    auto kempty_bar = [&](int i) { return bar0 + 8u * (kKSlots + i); };
+    auto vfull_bar = [&](int i) { return bar0 + 8u * (2 * kKSlots + i); };
+    auto vempty_bar = [&](int i) { return bar0 + 8u * (2 * kKSlots + kVSlots + i); };
+    const uint32_t bar1 = bar0 + 8u * (2 * kKSlots + 2 * kVSlots);
+    auto sfull_bar = [&](int i) { return bar1 + 8u * i; };               // S in buffer i computed
+    auto pfull_bar = [&](int i) { return bar1 + 8u * (kSP + i); };       // P in buffer i written (8 warps)
+    auto pempty_bar = [&](int i) { return bar1 + 8u * (2 * kSP + i); };  // P.V of buffer i completed
+    const uint32_t qready_bar = bar1 + 8u * (3 * kSP);
+    const uint32_t drain_bar = bar1 + 8u * (3 * kSP + 1);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 8);
-    float2 *xchg = reinterpret_cast<float2 *>(sbase + L::kOffXchg);  // [2][128] (m, l) per warpgroup
+    float *xrow = reinterpret_cast<float *>(sbase + L::kOffX);  // [2][128]: one value per row and warpgroup
 
-    // ---- prologue that reads nothing produced upstream ----
-    if (tid == 0) {
-        for (int i = 0; i < NS; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
-        for (int i = 0; i < kSP; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 4); mbar_init(pempty_bar(i), 1); }
+    const bool producer = warp == kProducerWarp && lane == 0;
+    if (producer) {
+        for (int i = 0; i < kKSlots; ++i) { mbar_init(kfull_bar(i), 1); mbar_init(kempty_bar(i), 1); }
+        for (int i = 0; i < kVSlots; ++i) { mbar_init(vfull_bar(i), 1); mbar_init(vempty_bar(i), 1); }
+        for (int i = 0; i < kSP; ++i) { mbar_init(sfull_bar(i), 1); mbar_init(pfull_bar(i), 8); mbar_init(pempty_bar(i), 1); }
         mbar_init(qready_bar, 1);  // the Q copy, with its bytes
-        mbar_init(qtmem_bar, 4);   // the four warps that move Q into tensor memory
         mbar_init(drain_bar, 1);
-        mbar_init(drain2_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
     }
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_holder)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_holder;
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs of an upstream kernel are visible now
 #endif
 
     const int T = p.T, G = p.Hq / p.Hkv, M = G * T;
+    if (producer) {
+        // Q first: rows r = j*G + hl of this kv head, two 64-column halves
+        mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * M));
+        tma_load_4d(sQ, &tmap_q, qready_bar, 0, g * G, 0, b);
+        tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, g * G, 0, b);
+    }
     const bool drafter = p.mode == 1;
     int nb = p.nctx[b];
     if (nb < 1 || nb > p.max_ctx) {
@@ -317,33 +448,57 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const int n_cache_tiles = cend > k0 ? (cend - k0 + kBN - 1) / kBN : 0;
     const bool has_block_tile = drafter && s == 0;
     const int n_tiles = n_cache_tiles + (has_block_tile ? 1 : 0);
+    const int first_tma = has_block_tile ? 1 : 0;  // tile 0 of the drafter's split 0 is the block
     const long rows_total = (long)p.B * T * p.Hq;
-    auto tile_key0 = [&](int t) { return k0 + (t - (has_block_tile ? 1 : 0)) * kBN; };
+    auto tile_key0 = [&](int t) { return k0 + (t - first_tma) * kBN; };
     auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
+    // keys every row of the block sees: the drafter's context, the target's
+    // cache before the block
+    const int all_see = min(cend, nb);
+
+    // one copy per tile: map coordinates (d within a half, key, half, kv head, sequence)
+    auto issue_k = [&](int t) {
+        const int slot = t % kKSlots;
+        mbar_arrive_expect_tx(kfull_bar(slot), (uint32_t)kTileBytes);
+        tma_load_5d(sK + slot * kTileBytes, &tmap_k, kfull_bar(slot), 0, tile_key0(t), 0, g, b);
+    };
+    auto issue_v = [&](int t) {
+        const int slot = t % kVSlots;
+        mbar_arrive_expect_tx(vfull_bar(slot), (uint32_t)kTileBytes);
+        tma_load_5d(sV + slot * kTileBytes, &tmap_v, vfull_bar(slot), 0, tile_key0(t), 0, g, b);
+    };
+    // first wave, before the CTA-wide sync: every slot of both rings
+    int next_k = first_tma, next_v = first_tma;
+    if (producer) {
+        for (; next_k < min(n_tiles, kKSlots); ++next_k) {
+            issue_k(next_k);
+            if (next_v < min(n_tiles, kVSlots)) issue_v(next_v++);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
 
     if (n_tiles == 0) {
-        // nothing to read: an empty split (lse = -inf, zero partial) for the merge
+        // nothing to read: an empty split (lse = -inf, zero partial) for the merge;
+        // the Q copy issued above lands before the CTA exits
+        if (producer) mbar_wait(qready_bar, 0, nullptr, p.fault);
         for (int idx = tid; idx < M * 32; idx += kTcThreads) {
             const int rr = idx >> 5, c4 = idx & 31;
             const long frow = ((long)b * T + rr / G) * p.Hq + g * G + rr % G;
-            reinterpret_cast<float4 *>(p.o_part + ((long)s * rows_total + frow) * 128)[c4] =
-                make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c4 == 0) p.lse_part[(long)s * rows_total + frow] = -INFINITY;
+            float *dst = p.merge == 2 ? p.out + frow * 128 : p.o_part + ((long)s * rows_total + frow) * 128;
+            reinterpret_cast<float4 *>(dst)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c4 == 0 && p.merge != 2) p.lse_part[(long)s * rows_total + frow] = -INFINITY;
         }
-    } else if (warp == 8) {
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ producer
-        if (lane == 0) {
-            // Q first: rows r = j*G + hl of this kv head, two 64-column halves
-            mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * M));
-            tma_load_4d(sQ, &tmap_q, qready_bar, 0, g * G, 0, b);
-            tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, g * G, 0, b);
-        }
-        int t = 0;
         if (has_block_tile) {
-            // the T block keys / values from [B, T, Hkv, D] into stage 0; rows >= T zero
+            // the T block keys / values from [B, T, Hkv, D] into slot 0 of each ring; rows >= T zero
             const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(p.kb);
             const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(p.vb);
-            uint8_t *stg = sbase + L::kOffStage;
+            uint8_t *ks = sbase + L::kOffK, *vs = sbase + L::kOffV;
             for (int idx = lane; idx < kBN * 16; idx += 32) {
                 const int row = idx >> 4, ch = idx & 15;
                 uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
@@ -353,302 +508,295 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     vv4 = __ldg(reinterpret_cast<const uint4 *>(vb + off) + ch);
                 }
                 const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
-                *reinterpret_cast<uint4 *>(stg + o) = kv4;
-                *reinterpret_cast<uint4 *>(stg + kKBytes + o) = vv4;
+                *reinterpret_cast<uint4 *>(ks + o) = kv4;
+                *reinterpret_cast<uint4 *>(vs + o) = vv4;
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(full_bar(0));
-            t = 1;
+            if (lane == 0) { mbar_arrive(kfull_bar(0)); mbar_arrive(vfull_bar(0)); }
         }
-        int issued = t;
         if (lane == 0) {
-            for (; t < n_tiles; ++t) {
-                const int st = t % NS;
-                if (t >= NS && !mbar_wait(empty_bar(st), ((t / NS) - 1) & 1, abort_flag, p.fault)) break;
-                const uint32_t dK = sStage + st * kStageBytes, dV = dK + kKBytes;
-                int c[4] = {0, 0, 0, b};
-                c[tp.dim_s] = tile_key0(t);
-                c[tp.dim_h] = g;
-                mbar_arrive_expect_tx(full_bar(st), (uint32_t)kStageBytes);
-                tma_load_4d(dK, &tmap_k, full_bar(st), 0, c[1], c[2], c[3]);
-                tma_load_4d(dK + kBN * 128, &tmap_k, full_bar(st), 64, c[1], c[2], c[3]);
-                tma_load_4d(dV, &tmap_v, full_bar(st), 0, c[1], c[2], c[3]);
-                tma_load_4d(dV + kBN * 128, &tmap_v, full_bar(st), 64, c[1], c[2], c[3]);
-                issued = t + 1;
+            // the older of the two pending loads first (K on a tie)
+            while (next_k < n_tiles || next_v < n_tiles) {
+                if (next_k < n_tiles && next_k <= next_v) {
+                    const int t = next_k;
+                    if (t >= kKSlots &&
+                        !mbar_wait(kempty_bar(t % kKSlots), ((t / kKSlots) - 1) & 1, abort_flag, p.fault))
+                        break;
+                    issue_k(t);
+                    ++next_k;
+                } else {
+                    const int t = next_v;
+                    if (t >= kVSlots &&
+                        !mbar_wait(vempty_bar(t % kVSlots), ((t / kVSlots) - 1) & 1, abort_flag, p.fault))
+                        break;
+                    issue_v(t);
+                    ++next_v;
+                }
             }
             // on abort: let the copies already issued land before the CTA exits
             if (*abort_flag) {
                 mbar_wait(qready_bar, 0, nullptr, p.fault);
-                for (int u = max(0, issued - NS); u < issued; ++u)
-                    mbar_wait(full_bar(u % NS), (u / NS) & 1, nullptr, p.fault);
+                for (int u = max(first_tma, next_k - kKSlots); u < next_k; ++u)
+                    mbar_wait(kfull_bar(u % kKSlots), (u / kKSlots) & 1, nullptr, p.fault);
+                for (int u = max(first_tma, next_v - kVSlots); u < next_v; ++u)
+                    mbar_wait(vfull_bar(u % kVSlots), (u / kVSlots) & 1, nullptr, p.fault);
             }
         }
         __syncwarp();
-    } else if (warp == 9) {
-        // ------------------------------------------------------------------ S issuer
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------------ MMA issuer
+        // Q rows past the M real ones are zero, so the padding rows of S are
+        // finite (the copy writes rows [0, M) only)
+        for (int idx = lane; idx < (128 - M) * 16; idx += 32) {
+            const int row = M + (idx >> 4), ch = idx & 15;
+            *reinterpret_cast<uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(row, ch & 7)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, kBN, false);
-            bool ok = mbar_wait(qtmem_bar, 0, abort_flag, p.fault);
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                // K of tile t loaded, and buffer t % 3 consumed by the P.V of tile t-3
-                const int bi = t % kSP;
-                ok = mbar_wait(full_bar(t % NS), (t / NS) & 1, abort_flag, p.fault);
-                if (ok && t >= kSP) ok = mbar_wait(pempty_bar(bi), ((t / kSP) - 1) & 1, abort_flag, p.fault);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t dcol = tmem + 256u + 64u * bi;
-                const uint32_t kbase = sStage + (t % NS) * kStageBytes;
+            const uint32_t idO = idesc_bf16(128, 128, true);
+            bool ok = mbar_wait(qready_bar, 0, abort_flag, p.fault);
+            // S runs up to kSP tiles ahead of P.V; whichever of the next S and
+            // the next P.V can go is issued, P.V first
+            int ns = 0, npv = 0;
+            unsigned long long t_last = global_timer();
+            for (uint32_t spin = 0; ok && npv < n_tiles;) {
+                if (npv < ns && mbar_test(pfull_bar(npv % kSP), (npv / kSP) & 1) &&
+                    mbar_test(vfull_bar(npv % kVSlots), (npv / kVSlots) & 1)) {
+                    // P.V(npv): O += P_hi . V + P_lo . V over the 128 keys
+                    tc_fence_after();
+                    const uint32_t vb = sV + (npv % kVSlots) * kTileBytes;
+                    const uint32_t pb = tmem + 128u + 128u * (npv % kSP);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-                    umma_ts(dcol, tmem + kQCol + 8u * kk, bd, idS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // 16 keys: V rows 16 kk.., P columns of the 64-key half kk / 4
+                        const uint64_t bd = sw128_desc(vb + kk * 16 * 128, kBN * 128, 1024);
+                        const uint32_t a = pb + 64u * (kk >> 2) + 8u * (kk & 3);
+                        umma_ts(tmem, a, bd, idO, (npv > 0 || kk > 0) ? 1u : 0u);
+                        umma_ts(tmem, a + 32u, bd, idO, 1u);
+                    }
+                    umma_commit(pempty_bar(npv % kSP));
+                    umma_commit(vempty_bar(npv % kVSlots));
+                    ++npv;
+                    t_last = global_timer();
+                    continue;
                 }
-                umma_commit(sfull_bar(bi));
+                if (ns < n_tiles && ns < npv + kSP && mbar_test(kfull_bar(ns % kKSlots), (ns / kKSlots) & 1) &&
+                    (ns < kSP || mbar_test(pempty_bar(ns % kSP), ((ns / kSP) - 1) & 1))) {
+                    // S(ns) into buffer ns % 3, free once P.V(ns - 3) has read it
+                    tc_fence_after();
+                    const uint32_t kb = sK + (ns % kKSlots) * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                        umma_ss(tmem + 128u + 128u * (ns % kSP), sw128_desc(sQ + off, 16, 1024),
+                                sw128_desc(kb + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024), idS,
+                                kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(sfull_bar(ns % kSP));
+                    umma_commit(kempty_bar(ns % kKSlots));
+                    ++ns;
+                    t_last = global_timer();
+                    continue;
+                }
+                // nothing ready yet: bounded
+                if ((++spin & 63u) == 0) {
+                    if (*abort_flag) ok = false;
+                    else if (global_timer() - t_last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        set_fault(p.fault, FAULT_WAIT_TIMEOUT);
+                        ok = false;
+                    }
+                }
             }
-            // every MMA this thread issued has completed before tensor memory is freed
+            // every MMA has completed before tensor memory is freed
             umma_commit(drain_bar);
             mbar_wait(drain_bar, 0, nullptr, p.fault);
         }
         __syncwarp();
-    } else if (warp == 10) {
-        // ------------------------------------------------------------------ P.V issuer
-        if (lane == 0) {
-            const uint32_t idO = idesc_bf16(128, 128, true);
-            bool ok = true;
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                ok = mbar_wait(pfull_bar(t % kSP), (t / kSP) & 1, abort_flag, p.fault);
-                if (!ok) break;
-                tc_fence_after();
-                const int st = t % NS;
-                const int wb = t & 1;
-                const uint32_t vbase = sStage + st * kStageBytes + kKBytes;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, kBN * 128, 1024);
-                        const uint32_t acc = (t >= 2 || half > 0 || kk > 0) ? 1u : 0u;
-                        if (kPTmem) {
-                            const uint32_t a_t = tmem + 256u + 64u * (t % kSP) + 32u * half + 8u * kk;
-                            umma_ts(tmem + 128u * wb, a_t, bd, idO, acc);
-                        } else {
-                            const uint64_t a = sw128_desc(sP + (wb * 2 + half) * kPBytes + kk * 32, 16, 1024);
-                            umma_ss(tmem + 128u * wb, a, bd, idO, acc);
-                        }
-                    }
-                }
-                umma_commit(pempty_bar(t % kSP));
-                umma_commit(empty_bar(st));
-            }
-            umma_commit(drain2_bar);
-            mbar_wait(drain2_bar, 0, nullptr, p.fault);
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------------ softmax (warps 0-7)
-        const int wg = warp >> 2;               // warpgroup: tiles t with t % 2 == wg
-        const int r = tid & 127;                // query row = tensor-memory lane
+    } else if (warp >= kSoftmaxWarp0) {
+        // ------------------------------------------------------------------ softmax (warps 4-11)
+        // both warpgroups take every tile: warpgroup wg the keys [64 wg, 64 wg + 64);
+        // they share the row max through shared memory, so O is one accumulator
+        const int sidx = tid - 32 * kSoftmaxWarp0;  // thread index among the softmax warps
+        const int wg = sidx >> 7;                   // key half of every tile
+        const int r = sidx & 127;                   // query row = tensor-memory lane (warp % 4 picks the lanes)
         const bool row_ok = r < M;
         const int j = row_ok ? r / G : 0;
         const float qk = p.scale * kLog2e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t o_col = tmem + lane_off + 128u * wg;
-        if (wg == 0) {
-            // Q into tensor memory (the A operand of S): row r = lane r, bf16
-            // pairs along K; rows past the M real ones are zero
-            const bool qok = __all_sync(0xffffffffu, mbar_wait(qready_bar, 0, abort_flag, p.fault));
-            uint32_t qa[32], qb[32];
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (row_ok && qok)
-                    v = *reinterpret_cast<const uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(r, ch & 7));
-                uint32_t *dst = ch < 8 ? &qa[4 * ch] : &qb[4 * (ch - 8)];
-                dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
-            }
-            tmem_st32(tmem + lane_off + kQCol, qa);
-            tmem_st32(tmem + lane_off + kQCol + 32u, qb);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qtmem_bar);
-        }
+        const uint32_t o_col = tmem + lane_off + 64u * wg;   // this warpgroup's half of O (rescale, epilogue)
 
+        // Every softmax warp runs every iteration, whatever happens: the two
+        // warpgroups meet at named barriers each tile.  After a failed wait the
+        // warp keeps going on meaningless values (the fault word is set and
+        // every later wait returns at once) so that no barrier is left short.
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        int last_t = -1;
-        for (int t = wg; t < n_tiles; t += 2) {
-            const int bi = t % kSP;  // S/P buffer
-            const int u = t / kSP;   // use index of that buffer
-            const uint32_t sp_col = tmem + lane_off + 256u + 64u * bi;
-            ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(bi), u & 1, abort_flag, p.fault));
-            if (!ok) break;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int bi = t % kSP;
+            const uint32_t sp_col = tmem + lane_off + 128u + 128u * bi + 64u * wg;
+            ok = __all_sync(0xffffffffu, mbar_wait(sfull_bar(bi), (t / kSP) & 1, abort_flag, p.fault)) && ok;
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld64(sp_col, sr);
-            // keys [0, nvalid) of the tile are visible to this row
+            // keys [0, nvalid) of the tile are visible to this row; a tile below
+            // every row's limit needs no mask (the padding rows past M compute
+            // finite values that are never stored)
             const bool blk = is_block_tile(t);
+            const bool whole = !blk && tile_key0(t) + kBN <= all_see;
             int nvalid;
-            if (blk) {
-                nvalid = T;
+            if (whole) {
+                nvalid = kBN;
+            } else if (blk) {
+                nvalid = row_ok ? T : 0;
             } else {
                 const int lim = drafter ? cend : min(cend, nb + j);
-                nvalid = max(0, min(kBN, lim - tile_key0(t)));
+                nvalid = row_ok ? max(0, min(kBN, lim - tile_key0(t))) : 0;
             }
-            if (!row_ok) nvalid = 0;
-            // tile max of the raw scores (qk > 0 keeps the order)
+            const int nv_half = min(64, max(0, nvalid - 64 * wg));  // visible keys of this half
+            uint32_t sa[32], sb[32];
+            tmem_ld32_async(sp_col, sa);
+            tmem_ld32_async(sp_col + 32u, sb);
+            tmem_ld_wait();
+            tmem_ld_bind(sa);
+            tmem_ld_bind(sb);
+            // row max of the raw scores (qk > 0 keeps the order), shared with the
+            // other warpgroup: both then take the same decisions below
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
+                const uint32_t *src = i < 4 ? sa : sb;
+                const int o = 8 * (i & 3);
                 float m8 = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int c = 8 * i + e;
-                    m8 = fmaxf(m8, c < nvalid ? __uint_as_float(sr[c]) : -INFINITY);
-                }
+                for (int e = 0; e < 8; ++e)
+                    m8 = fmaxf(m8, (whole || 8 * i + e < nv_half) ? __uint_as_float(src[o + e]) : -INFINITY);
                 mx[i] = m8;
             }
-            const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+            const float hmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float tmax = smax * qk;
+            xrow[wg * 128 + r] = hmax;
+            named_sync(1, 256);
+            const float omax = xrow[(wg ^ 1) * 128 + r];
+            named_sync(1, 256);  // both read before the next tile writes
+            const float tmax = fmaxf(hmax, omax) * qk;
             // move the reference max only when it grows by more than 2^8
-            const bool first = t == wg;
+            const bool first = t == 0;
             const bool need = !first && tmax > m_used + kRescaleThreshold;
             float alpha = 1.f;
             if (first) m_used = tmax;
             else if (need) { alpha = ex2(m_used - tmax); m_used = tmax; }
-            // this warpgroup's previous P.V (tile t-2) must be done before O or
-            // (shared-memory variant) the P buffer is touched again
-            if (!first && (!kPTmem || __any_sync(0xffffffffu, need))) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(pempty_bar((t - 2) % kSP), ((t - 2) / kSP) & 1, abort_flag, p.fault));
-                if (!ok) break;
-                tc_fence_after();
-            }
             if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-                for (int cc = 0; cc < 4; cc += 2) {
-                    uint32_t oa[32], ob[32];
+                // the previous P.V must be done before O is rescaled (this
+                // warpgroup's 64 columns of it)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(pempty_bar((t - 1) % kSP), ((t - 1) / kSP) & 1, abort_flag, p.fault)) && ok;
+                tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t oa[32];
                     tmem_ld32_async(o_col + 32u * cc, oa);
-                    tmem_ld32_async(o_col + 32u * (cc + 1), ob);
                     tmem_ld_wait();
                     tmem_ld_bind(oa);
-                    tmem_ld_bind(ob);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        oa[e] = __float_as_uint(__uint_as_float(oa[e]) * alpha);
-                        ob[e] = __float_as_uint(__uint_as_float(ob[e]) * alpha);
-                    }
+                    for (int e = 0; e < 32; ++e) oa[e] = __float_as_uint(__uint_as_float(oa[e]) * alpha);
                     tmem_st32(o_col + 32u * cc, oa);
-                    tmem_st32(o_col + 32u * (cc + 1), ob);
                 }
             }
             l *= alpha;
             const bool live = m_used != -INFINITY;
             const float neg_m = live ? -m_used : 0.f;
-            uint32_t pk[32], pl[32];
+            const int nv = live ? nv_half : 0;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            // P of this 64-key half over the S columns it came from: hi in [0,32),
+            // lo in [32,64).  hi = p truncated to bf16; lo = the exact fp32
+            // remainder truncated to bf16: |p - hi - lo| < 2^-14 p.  Byte
+            // permutes instead of conversion instructions.
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float e0 = ex2(fmaf(__uint_as_float(sr[2 * c]), qk, neg_m));
-                const float e1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), qk, neg_m));
-                const float p0 = (live && 2 * c < nvalid) ? e0 : 0.f;
-                const float p1 = (live && 2 * c + 1 < nvalid) ? e1 : 0.f;
-                ls[c & 3] += p0 + p1;
-                // hi = p truncated to bf16; lo = the exact fp32 remainder truncated
-                // to bf16: |p - hi - lo| < 2^-14 p.  Byte permutes instead of
-                // conversion instructions.
-                const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-                pk[c] = __byte_perm(b0, b1, 0x7632);
-                const uint32_t q0 = __float_as_uint(p0 - __uint_as_float(b0 & 0xffff0000u));
-                const uint32_t q1 = __float_as_uint(p1 - __uint_as_float(b1 & 0xffff0000u));
-                pl[c] = __byte_perm(q0, q1, 0x7632);
+            for (int q = 0; q < 2; ++q) {   // 32 keys at a time
+                const uint32_t *sq = q == 0 ? sa : sb;
+                uint32_t pk[16], pl[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int k0c = 32 * q + 2 * c;
+                    float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
+                    float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
+                    if (!whole) {
+                        p0 = k0c < nv ? p0 : 0.f;
+                        p1 = k0c + 1 < nv ? p1 : 0.f;
+                    }
+                    ls[c & 3] += p0 + p1;
+                    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                    pk[c] = __byte_perm(b0, b1, 0x7632);
+                    const uint32_t q0 = __float_as_uint(p0 - __uint_as_float(b0 & 0xffff0000u));
+                    const uint32_t q1 = __float_as_uint(p1 - __uint_as_float(b1 & 0xffff0000u));
+                    pl[c] = __byte_perm(q0, q1, 0x7632);
+                }
+                tmem_st16(sp_col + 16u * q, pk);
+                tmem_st16(sp_col + 32u + 16u * q, pl);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (kPTmem) {
-                // P over the S columns it came from: hi in [0,32), lo in [32,64)
-                tmem_st32(sp_col, pk);
-                tmem_st32(sp_col + 32u, pl);
-            } else {
-                uint8_t *pb = sbase + L::kOffP + wg * 2 * kPBytes;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    *reinterpret_cast<uint4 *>(pb + sw128_off(r, ch)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                    *reinterpret_cast<uint4 *>(pb + kPBytes + sw128_off(r, ch)) =
-                        make_uint4(pl[4 * ch], pl[4 * ch + 1], pl[4 * ch + 2], pl[4 * ch + 3]);
-                }
-            }
-            // value rows past the split's last cache key may hold anything: zero them
-            if (!blk) {
-                const int v0 = max(0, min(kBN, cend - tile_key0(t)));
-                if (v0 < kBN) {
-                    uint8_t *vt = sbase + L::kOffStage + (t % NS) * kStageBytes + kKBytes;
-                    for (int idx = r; idx < (kBN - v0) * 16; idx += 128) {
-                        const int row = v0 + (idx >> 4), ch = idx & 15;
-                        *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7)) =
-                            make_uint4(0u, 0u, 0u, 0u);
+            // value rows past the split's last cache key may hold anything (P is
+            // zero there, but 0 * NaN is not): each warpgroup zeroes those of
+            // its key half once V(t) has landed
+            if (!blk && !whole) {
+                const int v0 = max(64 * wg, min(64 * wg + 64, cend - tile_key0(t)));
+                if (ok && v0 < 64 * wg + 64) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(vfull_bar(t % kVSlots), (t / kVSlots) & 1, abort_flag,
+                                                           p.fault));
+                    if (ok) {
+                        uint8_t *vt = sbase + L::kOffV + (t % kVSlots) * kTileBytes;
+                        for (int idx = r; idx < (64 * wg + 64 - v0) * 16; idx += 128) {
+                            const int row = v0 + (idx >> 4), ch = idx & 15;
+                            *reinterpret_cast<uint4 *>(vt + (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
                     }
                 }
             }
             tmem_st_wait();
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull_bar(bi));
-            last_t = t;
         }
-        // ---- epilogue: merge the two warpgroups' (m, l, O), write this split's partial ----
-        if (ok && last_t >= 0)
-            ok = mbar_wait(pempty_bar(last_t % kSP), (last_t / kSP) & 1, abort_flag, p.fault);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok || last_t < 0) { m_used = -INFINITY; l = 0.f; }
+        // ---- epilogue: normalise O, write this split's partial (or the output) ----
+        const int last_t = n_tiles - 1;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(pempty_bar(last_t % kSP), (last_t / kSP) & 1, abort_flag, p.fault)) && ok;
+        if (!ok) { m_used = -INFINITY; l = 0.f; }
         tc_fence_before();
-        // both warpgroups' last P.V, hence every MMA of the CTA, are complete past
-        // this point: the Q tile is free for the (m, l) exchange
+        // the last P.V, hence every MMA (and every copy they read), is complete
+        // past this point: the rings are free for the staging
         named_sync(1, 256);
-        xchg[wg * 128 + r] = make_float2(m_used, l);
+        xrow[wg * 128 + r] = l;
         named_sync(1, 256);
-        const float2 mine = xchg[wg * 128 + r], other = xchg[(wg ^ 1) * 128 + r];
-        const float m0 = wg == 0 ? mine.x : other.x, l0 = wg == 0 ? mine.y : other.y;
-        const float m1 = wg == 0 ? other.x : mine.x, l1 = wg == 0 ? other.y : mine.y;
-        const float Mx = fmaxf(m0, m1);
-        const float f0 = l0 > 0.f ? ex2(m0 - Mx) : 0.f;
-        const float f1 = l1 > 0.f ? ex2(m1 - Mx) : 0.f;
-        const float Lsum = l0 * f0 + l1 * f1;
+        const float Lsum = wg == 0 ? l + xrow[128 + r] : xrow[r] + l;  // same order in both
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         const bool abort_seen = *abort_flag != 0;
-        // stage the normalised rows in shared memory (the K/V ring is idle now);
-        // warpgroup wg fills output columns [64 wg, 64 wg + 64)
-        float *ostage = reinterpret_cast<float *>(sbase + L::kOffStage);
+        // stage the normalised rows in shared memory; warpgroup wg fills output
+        // columns [64 wg, 64 wg + 64)
+        float *ostage = reinterpret_cast<float *>(sbase + L::kOffOStage);
         if (!abort_seen) {
             tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
-                const uint32_t col = 64u * wg + 32u * cc;
-                uint32_t oa[32], ob[32];
-                tmem_ld32_async(tmem + lane_off + col, oa);
-                tmem_ld32_async(tmem + lane_off + 128u + col, ob);
+                uint32_t oa[32];
+                tmem_ld32_async(o_col + 32u * cc, oa);
                 tmem_ld_wait();
                 tmem_ld_bind(oa);
-                tmem_ld_bind(ob);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float v[4];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const float a0 = l0 > 0.f ? __uint_as_float(oa[e + q4]) * f0 : 0.f;
-                        const float a1 = l1 > 0.f ? __uint_as_float(ob[e + q4]) * f1 : 0.f;
-                        v[q4] = (a0 + a1) * inv;
-                    }
-                    *reinterpret_cast<float4 *>(ostage + r * kOStride + col + e) = make_float4(v[0], v[1], v[2], v[3]);
-                }
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(ostage + r * kOStride + 64 * wg + 32 * cc + e) =
+                        make_float4(__uint_as_float(oa[e]) * inv, __uint_as_float(oa[e + 1]) * inv,
+                                    __uint_as_float(oa[e + 2]) * inv, __uint_as_float(oa[e + 3]) * inv);
             }
-            if (row_ok && wg == 0) {
+            if (row_ok && wg == 0 && p.merge != 2) {
                 const int h = g * G + r % G;
                 p.lse_part[(long)s * rows_total + ((long)b * T + j) * p.Hq + h] =
-                    Lsum > 0.f ? Mx * kLn2 + logf(Lsum) : -INFINITY;
+                    Lsum > 0.f ? m_used * kLn2 + logf(Lsum) : -INFINITY;
             }
         }
         tc_fence_before();
@@ -657,11 +805,12 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // rows (j, hl) of one j are G consecutive rows of the partial output:
             // copy them out as contiguous float4 runs
             const int per_j = G * 32;  // float4s
-            for (int idx = tid; idx < M * 32; idx += 256) {
+            for (int idx = sidx; idx < M * 32; idx += 256) {
                 const int jj = idx / per_j, rem = idx % per_j, hl = rem >> 5, c4 = rem & 31;
                 const int rr = jj * G + hl;
                 const float4 v = *reinterpret_cast<const float4 *>(ostage + rr * kOStride + c4 * 4);
-                float *dst = p.o_part + ((long)s * rows_total + ((long)b * T + jj) * p.Hq + g * G + hl) * 128;
+                const long frow = ((long)b * T + jj) * p.Hq + g * G + hl;
+                float *dst = p.merge == 2 ? p.out + frow * 128 : p.o_part + ((long)s * rows_total + frow) * 128;
                 *reinterpret_cast<float4 *>(dst + c4 * 4) = v;
             }
         }
@@ -669,11 +818,14 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 
     // teardown: every MMA has completed (drain above); free tensor memory
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
+    if (p.merge == 1)
+        merge_group(p, s, g, b, M, G, rows_total, reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 12),
+                    sbase + L::kOffK);
 }
 
 // ---------------------------------------------------------------------------
@@ -693,35 +845,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map over a [B, S, Hkv, D] bf16 tensor with element strides kv; the slot
-// and head axes are ordered by stride.  Box: 64 d x 64 slots x 1 head x 1 seq.
-bool make_map(CUtensorMap *m, const void *ptr, const sd_strides &kv, int S, int Hkv, int B, int *dim_s,
-              int *dim_h) {
+// 5-D map over a [B, S, Hkv, D] bf16 cache with element strides kv, the D axis
+// seen as (64 columns, 2 halves) and the halves placed outside the slots:
+// dims (d % 64, slot, d / 64, kv head, sequence).  One box of 64 x 128 slots x 2
+// lands as two [128 slots x 128 B] blocks, the layout the MMAs read.
+bool make_map(CUtensorMap *m, const void *ptr, const sd_strides &kv, int S, int Hkv, int B) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
-    const bool s_inner = kv.s <= kv.h;
-    *dim_s = s_inner ? 1 : 2;
-    *dim_h = s_inner ? 2 : 1;
-    cuuint64_t dims[4], strides[3];
-    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
-    dims[0] = 128;
-    dims[*dim_s] = (cuuint64_t)S;
-    dims[*dim_h] = (cuuint64_t)Hkv;
-    dims[3] = (cuuint64_t)B;
-    strides[*dim_s - 1] = (cuuint64_t)kv.s * 2;
-    strides[*dim_h - 1] = (cuuint64_t)kv.h * 2;
-    strides[2] = (cuuint64_t)kv.b * 2;
-    box[0] = 64;
-    box[*dim_s] = kBN;
-    box[*dim_h] = 1;
-    box[3] = 1;
-    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+    cuuint64_t dims[5] = {64, (cuuint64_t)S, 2, (cuuint64_t)Hkv, (cuuint64_t)B};
+    cuuint64_t strides[4] = {(cuuint64_t)kv.s * 2, 128, (cuuint64_t)kv.h * 2, (cuuint64_t)kv.b * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)kBN, 2, 1, 1}, estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-int cache_slots(const AttnParams &p) { return p.mode == 0 ? p.max_ctx + p.T - 1 : p.max_ctx; }
 
 // 4-D map over the contiguous queries [B, T, Hq, D]; box: 64 d x G heads x T rows x 1,
 // which lands in shared memory as rows j*G + hl of 128 bytes
@@ -738,22 +876,20 @@ bool make_q_map(CUtensorMap *m, const AttnParams &p) {
     return r == CUDA_SUCCESS;
 }
 
-template <bool kPTmem>
-cudaError_t launch_tc_t(const AttnParams &p, cudaStream_t st) {
+int cache_slots(const AttnParams &p) { return p.mode == 0 ? p.max_ctx + p.T - 1 : p.max_ctx; }
+
+cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     alignas(64) CUtensorMap mq, mk, mv;
-    TcParams tp;
-    tp.a = p;
-    int ds2 = 0, dh2 = 0;
     if (!make_q_map(&mq, p)) return cudaErrorInvalidValue;
-    if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B, &tp.dim_s, &tp.dim_h)) return cudaErrorInvalidValue;
-    if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B, &ds2, &dh2)) return cudaErrorInvalidValue;
-    constexpr int smem = Layout<kPTmem>::kSmemBytes;
+    if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B)) return cudaErrorInvalidValue;
+    if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B)) return cudaErrorInvalidValue;
+    constexpr int smem = Layout::kSmemBytes;
     static bool opted_in[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !opted_in[dev]) {
-        e = cudaFuncSetAttribute(attn_split_tc_kernel<kPTmem>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(attn_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev] = true;
     }
@@ -767,7 +903,7 @@ cudaError_t launch_tc_t(const AttnParams &p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel<kPTmem>, mq, mk, mv, tp);
+    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
 }
 
 }  // namespace
@@ -780,16 +916,15 @@ bool attn_tc_supported(const AttnParams &p) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-    if (optin < Layout<true>::kSmemBytes || optin < Layout<false>::kSmemBytes) return false;
+    if (optin < Layout::kSmemBytes) return false;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     return major == 10 && minor == 3;
 }
 
-size_t attn_tc_smem_bytes(const AttnParams &) { return Layout<true>::kSmemBytes; }
+size_t attn_tc_smem_bytes(const AttnParams &) { return Layout::kSmemBytes; }
 
-cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) { return launch_tc_t<true>(p, st); }
-cudaError_t launch_attn_tc_smem_p(const AttnParams &p, cudaStream_t st) { return launch_tc_t<false>(p, st); }
+cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) { return launch_tc(p, st); }
 
 }  // namespace sdv

@@ -20,7 +20,8 @@ enum FaultBits : unsigned int {
 };
 
 constexpr int kMaxT = 16;           // block rows (anchor + 15 proposals)
-constexpr int kTileKeys = 64;       // keys per tile, shared by both attention kernels
+constexpr int kTileKeys = 64;       // keys per tile of the CUDA-core attention kernel
+constexpr int kTcTileKeys = 128;    // keys per tile of the tensor-core attention kernel
 
 // Attention launch description (both the target verify and the drafter).
 //  key index space of sequence b:
@@ -44,13 +45,18 @@ struct AttnParams {
     int n_splits, keys_per_split;
     float *o_part;                  // [n_splits, B*T*Hq, D]
     float *lse_part;                // [n_splits, B*T*Hq]
+    // how the splits are combined: 0 a separate merge kernel, 1 merged inside
+    // the split kernel once every split of a (sequence, kv head) has arrived
+    // (counters merge_ctr[B * Hkv], zero between calls), 2 a single split that
+    // writes the output itself
+    int merge;
+    unsigned int *merge_ctr;
     unsigned int *fault;
 };
 
 // kernel launchers: return the launch error (cudaSuccess when enqueued)
 cudaError_t launch_attn_generic(const AttnParams &p, cudaStream_t st);
-cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);         // P kept in tensor memory
-cudaError_t launch_attn_tc_smem_p(const AttnParams &p, cudaStream_t st);  // P staged in shared memory
+cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
 cudaError_t launch_lse_merge(const AttnParams &p, cudaStream_t st);
 bool attn_tc_supported(const AttnParams &p);
 size_t attn_tc_smem_bytes(const AttnParams &p);

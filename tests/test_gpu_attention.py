@@ -50,7 +50,7 @@ def run_verify(S, inp, path, max_ctx=None, out_rows=None):
     used = S.sd_last_attention_path()
     torch.cuda.synchronize()
     assert S.sd_fault_word() == 0
-    if path in (1, 2, 3):
+    if path in (1, 2):
         assert used[0] == path
     return out.cpu().numpy().reshape(B * T * Hq, D), used
 
@@ -69,13 +69,13 @@ def run_draft(S, d, layer, path, max_ctx=None):
     used = S.sd_last_attention_path()
     torch.cuda.synchronize()
     assert S.sd_fault_word() == 0
-    if path in (1, 2, 3):
+    if path in (1, 2):
         assert used[0] == path
     return out.cpu().numpy().reshape(B * T * Hq, D)
 
 
 def paths_for(dtype, D, G, T):
-    return [1, 2, 3] if tc_applies(dtype, D, G, T) else [1]
+    return [1, 2] if tc_applies(dtype, D, G, T) else [1]
 
 
 VERIFY_CASES = [
@@ -110,7 +110,7 @@ def test_verify_max_ctx_larger_than_ctx(S):
     k[1, 900 + T - 1:] = float("nan"); v[1, 900 + T - 1:] = float("nan")
     inp2 = dict(inp, k=k, v=v)
     want = oracle_verify_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], 1.0, np.arange(B * T * Hq))
-    for path in (1, 2, 3):
+    for path in (1, 2):
         got, _ = run_verify(S, inp2, path, max_ctx=1100)
         check_attention(got, want)
 
@@ -126,7 +126,7 @@ def test_verify_strided_cache(S):
     kd = inp["k"].permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
     vd = inp["v"].permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
     assert kd.stride(1) == D and kh.stride(1) == D
-    for path in (1, 2, 3):
+    for path in (1, 2):
         out = torch.zeros(B, T, Hq, D, device="cuda")
         ws = S.workspace(S.sd_verify_attention_workspace_size(B, T, Hq, Hkv, D, 333, S.SD_BF16))
         S.sd_set_attention_path(path)
@@ -139,7 +139,7 @@ def test_verify_row_sees_exactly_ctx_plus_j(S):
     # perturbing slot ctx+j changes rows > j only (GPU, both paths)
     B, T, Hq, Hkv, D, ctx = 1, 16, 28, 4, 128, 500
     inp = W.verify_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, ctx=ctx, seed=8)
-    for path in (1, 2, 3):
+    for path in (1, 2):
         base, _ = run_verify(S, inp, path)
         k2, v2 = inp["k"].clone(), inp["v"].clone()
         k2[0, ctx + 6] += 2.0
@@ -164,7 +164,7 @@ def test_verify_moving_running_max(S, direction):
     q = (inp["q"].float() + u).to(torch.bfloat16)
     inp2 = dict(inp, k=k, q=q)
     want = oracle.attention_rows(q, k, inp["v"], inp["ctx"], 1.0)
-    for path in (1, 2, 3):
+    for path in (1, 2):
         got, _ = run_verify(S, inp2, path)
         check_attention(got, want)
 
@@ -239,7 +239,7 @@ def test_bad_ctx_len_sets_fault_word_without_faulting(S):
     ctx = torch.tensor([5000], dtype=torch.int32, device="cuda")
     out = torch.zeros(1, 16, 28, 128, device="cuda")
     ws = S.workspace(S.sd_verify_attention_workspace_size(1, 16, 28, 4, 128, 300, S.SD_BF16))
-    for path in (1, 2, 3):
+    for path in (1, 2):
         S.sd_set_attention_path(path)
         S.sd_verify_attention(q, k, v, ctx, 300, out, 1.0, ws)
         assert S.sd_fault_word() & 1
