@@ -292,7 +292,7 @@ __device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int ta
 // The whole grid is resident (at most one CTA per SM), so the wait ends.  The
 // counter is returned to zero by the last split to finish merging.  `scratch`
 // is idle shared memory (the K/V rings).
-constexpr int kMergeChunk = 8;  // splits summed by one work unit, loads all in flight
+constexpr int kMergeBatch = 12;  // loads one merge thread keeps in flight
 __device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int G, long rows_total,
                             volatile int *go, uint8_t *scratch) {
     unsigned int *ctr = p.merge_ctr + ((long)b * p.Hkv + g);
@@ -308,7 +308,10 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int
     }
     __syncthreads();
     const int R = s < M ? (M - s + n - 1) / n : 0;   // rows of this split
-    const int K = (n + kMergeChunk - 1) / kMergeChunk;
+    // the splits of a row are cut into K chunks, so that about one (row, 4
+    // columns, chunk) unit falls to each thread
+    const int K = max(1, min(n, kTcThreads / max(1, R * 32)));
+    const int chunk = (n + K - 1) / K;
     float *wgt = reinterpret_cast<float *>(scratch);                     // [R][n] lse, then weights
     float *inv = wgt + R * n;                                            // [R] 1 / sum of weights
     float4 *part = reinterpret_cast<float4 *>(scratch + ((R * n + R) * 4 + 15) / 16 * 16);  // [K][R][32]
@@ -336,21 +339,24 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int
         for (int u = tid; u < K * R * 32; u += kTcThreads) {
             const int k = u / (R * 32), ri = (u / 32) % R, c4 = u & 31;
             const long frow = frow_of(ri);
+            const int sp0 = k * chunk, sp1 = min(n, sp0 + chunk);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            // branch-free, so that the chunk's loads are all in flight at once:
-            // past the last split, re-read the last one with weight 0
-            float4 v[kMergeChunk];
-            float w[kMergeChunk];
+            for (int sb = sp0; sb < sp1; sb += kMergeBatch) {
+                // branch-free, so that the batch's loads are all in flight at
+                // once: past the chunk's end, re-read its last split with weight 0
+                float4 v[kMergeBatch];
+                float w[kMergeBatch];
 #pragma unroll
-            for (int e = 0; e < kMergeChunk; ++e) {
-                const int sp = min(k * kMergeChunk + e, n - 1);
-                v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ((long)sp * rows_total + frow) * 128) + c4);
-                w[e] = k * kMergeChunk + e < n ? wgt[ri * n + sp] : 0.f;
-            }
+                for (int e = 0; e < kMergeBatch; ++e) {
+                    const int sp = min(sb + e, sp1 - 1);
+                    v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ((long)sp * rows_total + frow) * 128) + c4);
+                    w[e] = sb + e < sp1 ? wgt[ri * n + sp] : 0.f;
+                }
 #pragma unroll
-            for (int e = 0; e < kMergeChunk; ++e) {
-                acc.x = fmaf(w[e], v[e].x, acc.x); acc.y = fmaf(w[e], v[e].y, acc.y);
-                acc.z = fmaf(w[e], v[e].z, acc.z); acc.w = fmaf(w[e], v[e].w, acc.w);
+                for (int e = 0; e < kMergeBatch; ++e) {
+                    acc.x = fmaf(w[e], v[e].x, acc.x); acc.y = fmaf(w[e], v[e].y, acc.y);
+                    acc.z = fmaf(w[e], v[e].z, acc.z); acc.w = fmaf(w[e], v[e].w, acc.w);
+                }
             }
             part[u] = acc;
         }
