@@ -126,15 +126,22 @@ class DeviceSet:
         return sum(t.numel() * t.element_size() for t in ts)
 
 
-KERNELS_PER_STEP = LAYERS * 2 + 2 + 1 + 2  # (split + merge) x 5 attention calls, greedy, sample x2
+# kernels of one step: 5 attention calls (1 launch each when the splits merge
+# inside the split kernel, else 2; set from the library after a warm-up
+# step), greedy 1, sampled 2
+ATTN_LAUNCHES = {"draft": 2, "verify": 2}
+def kernels_per_step():
+    return LAYERS * ATTN_LAUNCHES["draft"] + ATTN_LAUNCHES["verify"] + 1 + 2
 
 
 def run_step(S, ds, stream=None, parts=("draft", "verify", "greedy", "sample")):
     if "draft" in parts:
         for li, (q, kb, vb) in enumerate(ds.layers):
             S.sd_draft_block_attention(q, ds.kc, ds.vc, ds.nctx, CTX, kb, vb, ds.dout[li], 1.0, ds.ws_d, stream)
+        ATTN_LAUNCHES["draft"] = S.sd_last_attention_launches()
     if "verify" in parts:
         S.sd_verify_attention(ds.q, ds.k, ds.v, ds.ctx, CTX, ds.out, 1.0, ds.ws_v, stream)
+        ATTN_LAUNCHES["verify"] = S.sd_last_attention_launches()
     if "greedy" in parts:
         S.sd_accept_greedy(ds.draft, ds.logits, ds.n, ds.c, ds.ws_g, stream)
     if "sample" in parts:
@@ -475,7 +482,8 @@ def main():
         kernels["draft_attention"]["note"] = ("average over the 4 layers of one step; they share one projected "
                                               "context, so layers 2-4 read it from L2 and only the first call "
                                               "is HBM-bound")
-        for name, nl in (("draft_attention", 2), ("verify_attention", 2), ("accept_greedy", 1),
+        for name, nl in (("draft_attention", ATTN_LAUNCHES["draft"]), ("verify_attention", ATTN_LAUNCHES["verify"]),
+                         ("accept_greedy", 1),
                          ("accept_sample", 2)):
             kernels[name]["kernel_launches_per_call"] = nl
 
@@ -486,8 +494,9 @@ def main():
         k = kernels["verify_attention"]
         achieved = k["GBps"]
         traffic = ncu_traffic("verify_attention")
-        roofline = {"kernel": "verify attention split kernel + LSE merge (one sd_verify_attention call); "
-                              "traffic is the split kernel's DRAM bytes per launch",
+        roofline = {"kernel": "verify attention (one sd_verify_attention call: split pass with the "
+                              "log-sum-exp merge inside the same kernel); traffic is that kernel's DRAM "
+                              "bytes per launch",
                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_source": peak_src,
                     "traffic": traffic,
@@ -530,7 +539,7 @@ def main():
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": steps_done * KERNELS_PER_STEP,
+            "gpu_launches": steps_done * kernels_per_step(),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -230,6 +230,12 @@ int sd_set_attention_path(int path);
  * above) and how many key splits it used. */
 int sd_last_attention_path(int *n_splits);
 
+/* How many kernels the last attention call on this thread launched: 1 when the
+ * splits were merged inside the split kernel (or there was one split), 2 when
+ * a separate merge kernel followed.  No counterpart on the pages: a count for
+ * measurement. */
+int sd_last_attention_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,6 +22,7 @@ namespace {
 thread_local char g_err[512] = "";
 thread_local int g_last_path = 0;
 thread_local int g_last_splits = 0;
+thread_local int g_last_launches = 0;
 std::atomic<int> g_force_path{0};
 
 constexpr size_t kHeader = 256;  // counters; zero between calls
@@ -157,6 +158,7 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     }
     g_last_path = path;
     g_last_splits = pl.n_splits;
+    g_last_launches = p.merge == 0 ? 2 : 1;
     return SD_OK;
 }
 
@@ -270,6 +272,10 @@ int sd_set_attention_path(int path) {
 int sd_last_attention_path(int *n_splits) {
     if (n_splits) *n_splits = g_last_splits;
     return g_last_path;
+}
+
+int sd_last_attention_launches(void) {
+    return g_last_launches;
 }
 
 sd_status sd_fault_word(uint32_t *out, int clear) {

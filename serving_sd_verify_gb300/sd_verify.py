@@ -26,7 +26,7 @@ SYMBOLS = [
     "sd_accept_greedy", "sd_accept_greedy_workspace_size",
     "sd_accept_sample", "sd_accept_sample_workspace_size", "sd_accept_greedy_noalloc",
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
-    "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path",
+    "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
 ]
 
 
@@ -88,6 +88,8 @@ def load():
     lib.sd_set_attention_path.restype = _i
     lib.sd_last_attention_path.argtypes = [ctypes.POINTER(_i)]
     lib.sd_last_attention_path.restype = _i
+    lib.sd_last_attention_launches.argtypes = []
+    lib.sd_last_attention_launches.restype = _i
     _lib = lib
     return lib
 
@@ -240,6 +242,11 @@ def sd_fault_word(clear: bool = True) -> int:
 
 def sd_set_attention_path(path: int) -> int:
     return load().sd_set_attention_path(int(path))
+
+
+def sd_last_attention_launches() -> int:
+    """Kernels the last attention call on this thread launched (1 or 2)."""
+    return int(load().sd_last_attention_launches())
 
 
 def sd_last_attention_path():
