@@ -522,22 +522,29 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             if (lane == 0) { mbar_arrive(kfull_bar(0)); mbar_arrive(vfull_bar(0)); }
         }
         if (lane == 0) {
-            // the older of the two pending loads first (K on a tie)
-            while (next_k < n_tiles || next_v < n_tiles) {
-                if (next_k < n_tiles && next_k <= next_v) {
-                    const int t = next_k;
-                    if (t >= kKSlots &&
-                        !mbar_wait(kempty_bar(t % kKSlots), ((t / kKSlots) - 1) & 1, abort_flag, p.fault))
+            // whichever ring has a free slot first: a K slot frees when its S has
+            // completed, a V slot when its P.V has, so neither waits behind the other
+            unsigned long long t_last = global_timer();
+            for (uint32_t spin = 0; next_k < n_tiles || next_v < n_tiles;) {
+                if (next_k < n_tiles &&
+                    (next_k < kKSlots || mbar_test(kempty_bar(next_k % kKSlots), ((next_k / kKSlots) - 1) & 1))) {
+                    issue_k(next_k++);
+                    t_last = global_timer();
+                    continue;
+                }
+                if (next_v < n_tiles &&
+                    (next_v < kVSlots || mbar_test(vempty_bar(next_v % kVSlots), ((next_v / kVSlots) - 1) & 1))) {
+                    issue_v(next_v++);
+                    t_last = global_timer();
+                    continue;
+                }
+                if ((++spin & 63u) == 0) {
+                    if (*abort_flag) break;
+                    if (global_timer() - t_last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        set_fault(p.fault, FAULT_WAIT_TIMEOUT);
                         break;
-                    issue_k(t);
-                    ++next_k;
-                } else {
-                    const int t = next_v;
-                    if (t >= kVSlots &&
-                        !mbar_wait(vempty_bar(t % kVSlots), ((t / kVSlots) - 1) & 1, abort_flag, p.fault))
-                        break;
-                    issue_v(t);
-                    ++next_v;
+                    }
                 }
             }
             // on abort: let the copies already issued land before the CTA exits
