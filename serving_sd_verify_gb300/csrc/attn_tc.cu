@@ -538,7 +538,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     t_last = global_timer();
                     continue;
                 }
-                if ((++spin & 63u) == 0) {
+                // nothing free yet: back off, so the poll does not take issue
+                // slots and shared-memory bandwidth from the softmax warps
+                __nanosleep(64);
+                if ((++spin & 15u) == 0) {
                     if (*abort_flag) break;
                     if (global_timer() - t_last > kWaitLimitNs) {
                         *abort_flag = 1;
@@ -615,8 +618,9 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     t_last = global_timer();
                     continue;
                 }
-                // nothing ready yet: bounded
-                if ((++spin & 63u) == 0) {
+                // nothing ready yet: back off (see the producer), bounded
+                __nanosleep(32);
+                if ((++spin & 15u) == 0) {
                     if (*abort_flag) ok = false;
                     else if (global_timer() - t_last > kWaitLimitNs) {
                         *abort_flag = 1;
@@ -677,16 +681,29 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tmem_ld_bind(sb);
             // row max of the raw scores (qk > 0 keeps the order), shared with the
             // other warpgroup: both then take the same decisions below
+            // (separate loops: a select folded into the unmasked one costs ~6x)
             float mx[8];
+            if (whole) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t *src = i < 4 ? sa : sb;
-                const int o = 8 * (i & 3);
-                float m8 = -INFINITY;
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t *src = i < 4 ? sa : sb;
+                    const int o = 8 * (i & 3);
+                    float m8 = __uint_as_float(src[o]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    m8 = fmaxf(m8, (whole || 8 * i + e < nv_half) ? __uint_as_float(src[o + e]) : -INFINITY);
-                mx[i] = m8;
+                    for (int e = 1; e < 8; ++e) m8 = fmaxf(m8, __uint_as_float(src[o + e]));
+                    mx[i] = m8;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t *src = i < 4 ? sa : sb;
+                    const int o = 8 * (i & 3);
+                    float m8 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        m8 = fmaxf(m8, 8 * i + e < nv_half ? __uint_as_float(src[o + e]) : -INFINITY);
+                    mx[i] = m8;
+                }
             }
             const float hmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -727,19 +744,23 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // lo in [32,64).  hi = p truncated to bf16; lo = the exact fp32
             // remainder truncated to bf16: |p - hi - lo| < 2^-14 p.  Byte
             // permutes instead of conversion instructions.
+            // the masked keys of an edge tile are cleared in the scores first
+            // (-inf gives a weight of 0), so the exponential loop has no selects
+            if (!whole) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    if (c >= nv) sa[c] = 0xff800000u;
+                    if (32 + c >= nv) sb[c] = 0xff800000u;
+                }
+            }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {   // 32 keys at a time
                 const uint32_t *sq = q == 0 ? sa : sb;
                 uint32_t pk[16], pl[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const int k0c = 32 * q + 2 * c;
-                    float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
-                    float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
-                    if (!whole) {
-                        p0 = k0c < nv ? p0 : 0.f;
-                        p1 = k0c + 1 < nv ? p1 : 0.f;
-                    }
+                    const float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
+                    const float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
                     ls[c & 3] += p0 + p1;
                     const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
                     pk[c] = __byte_perm(b0, b1, 0x7632);
