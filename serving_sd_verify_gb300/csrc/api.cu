@@ -176,7 +176,7 @@ size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max
 // ----------------------------------------------------------------------------
 int accept_chunk(int rows, int V, int cap) {
     const int sms = device_sm_count();
-    const long target = 4L * sms;  // CTAs
+    const long target = 2L * sms;  // CTAs: about two per SM (fewer finisher tickets, one wave)
     long chunk = ((long)rows * V + target - 1) / target;
     chunk = std::max(2048L, std::min(chunk, (long)cap));
     chunk = (chunk + 7) / 8 * 8;
@@ -199,11 +199,11 @@ GreedyLayout greedy_layout(int B, int T, int V, int chunk) {
 }
 
 // chunk of the sampled rule's second pass (one row per sequence): about two
-// CTAs per SM over the B rows
+// CTAs per SM over the B rows, at least 1024 elements
 int draw_chunk_for(int B, int V) {
     const int sms = device_sm_count();
     long c = ((long)B * V + 2L * sms - 1) / (2L * sms);
-    c = std::max(512L, std::min(c, (long)kSampleChunkMax));
+    c = std::max(1024L, std::min(c, (long)kSampleChunkMax));
     c = (c + 7) / 8 * 8;
     return (int)std::min<long>(c, (long)V);
 }

@@ -97,7 +97,7 @@ struct SampleParams {
     double *rs, *ps;                // [B, n_draw_chunks] residual / p chunk sums
     unsigned int *fault;
 };
-constexpr int kSampleChunkMax = 4096;
+constexpr int kSampleChunkMax = 8192;
 constexpr int kGreedyChunkMaxBf16 = 16384;
 constexpr int kGreedyChunkMaxF32 = 8192;
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);

@@ -245,3 +245,39 @@ def test_bad_ctx_len_sets_fault_word_without_faulting(S):
         assert S.sd_fault_word() & 1
         want = oracle.attention_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], 1.0)
         check_attention(out.cpu().numpy().reshape(-1, 128), want)
+
+
+def test_verify_in_kernel_merge_reuses_its_workspace(S):
+    """The tensor-core kernel merges its splits inside the kernel through one
+    counter per (sequence, kv head) kept in the workspace: every completed call
+    leaves the counters at zero, so a second call on the same workspace gives
+    the same bits; a single split writes the output directly (one launch)."""
+    cfg = W.config(2)
+    inp, dims = cfg["attn"], cfg["dims"]
+    B, T, Hq, Hkv, D = dims["B"], dims["T"], dims["Hq"], dims["Hkv"], dims["D"]
+    q, k, v, ctx = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda(), inp["ctx"].cuda()
+    mc = inp["max_ctx"]
+    ws = S.workspace(S.sd_verify_attention_workspace_size(B, T, Hq, Hkv, D, mc, S._dt(q)))
+    outs = []
+    S.sd_set_attention_path(2)
+    for _ in range(2):
+        out = torch.full((B, T, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        S.sd_verify_attention(q, k, v, ctx, mc, out, inp["scale"], ws)
+        path, n_splits = S.sd_last_attention_path()
+        launches = S.sd_last_attention_launches()
+        torch.cuda.synchronize()
+        assert S.sd_fault_word() == 0
+        assert path == 2 and n_splits > 1 and launches == 1
+        assert int(ws[256:256 + 4 * B * Hkv].abs().sum()) == 0, "merge counters not returned to zero"
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    rows = sample_rows(B, T, Hq, 16, seed=22)
+    want = oracle_verify_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], inp["scale"], rows)
+    check_attention(outs[1].numpy().reshape(B * T * Hq, D)[rows], want)
+    # a context short enough for one split: the kernel writes the output itself
+    small = W.verify_inputs(B=1, T=16, Hq=28, Hkv=4, D=128, ctx=[130], dtype=torch.bfloat16, seed=23)
+    got, used = run_verify(S, small, 2)
+    assert used == (2, 1) and S.sd_last_attention_launches() == 1
+    check_attention(got, oracle_verify_rows(small["q"], small["k"], small["v"], small["ctx"], small["scale"],
+                                            list(range(16 * 28))))
+    S.sd_set_attention_path(0)
