@@ -470,8 +470,9 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     // combined by an exclusive scan over the threads, the owner of the
     // crossing then walks its run
     constexpr int kRun = 16;
+    static_assert(kRun * kAccThreads >= kDrawChunkMax, "the search covers a whole draw chunk");
     const int clo = sel_chunk * p.draw_chunk, chi = min(p.V, clo + p.draw_chunk);
-    const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (draw chunk <= 4096)
+    const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (draw chunk <= kDrawChunkMax)
     const int tlo = min(chi, clo + (int)threadIdx.x * per), thi = min(chi, tlo + per);
     const bool res = sel_res != 0;
     float w[kRun], xin[kRun], qin[kRun];

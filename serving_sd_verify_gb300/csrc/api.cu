@@ -203,7 +203,7 @@ GreedyLayout greedy_layout(int B, int T, int V, int chunk) {
 int draw_chunk_for(int B, int V) {
     const int sms = device_sm_count();
     long c = ((long)B * V + 2L * sms - 1) / (2L * sms);
-    c = std::max(1024L, std::min(c, (long)kSampleChunkMax));
+    c = std::max(1024L, std::min(c, (long)kDrawChunkMax));
     c = (c + 7) / 8 * 8;
     return (int)std::min<long>(c, (long)V);
 }

@@ -88,7 +88,7 @@ struct SampleParams {
     uint32_t offset;
     int32_t *n_acc, *next_id;
     int chunk, n_chunks;            // pass 1 chunks, chunk <= kSampleChunkMax
-    int draw_chunk, n_draw_chunks;  // pass 2 chunks, draw_chunk <= kSampleChunkMax
+    int draw_chunk, n_draw_chunks;  // pass 2 chunks, draw_chunk <= kDrawChunkMax
     unsigned int *counters;         // [0]: CTAs of pass 1 finished
     unsigned int *row_counter;      // [B] CTAs of pass 2 finished per sequence
     float *pm, *pz;                 // [B*T, n_chunks] chunk max and sum of exp
@@ -98,6 +98,7 @@ struct SampleParams {
     unsigned int *fault;
 };
 constexpr int kSampleChunkMax = 8192;
+constexpr int kDrawChunkMax = 4096;  // pass 2 chunk bound: 16 elements per thread of the in-chunk search
 constexpr int kGreedyChunkMaxBf16 = 16384;
 constexpr int kGreedyChunkMaxF32 = 8192;
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);

@@ -160,6 +160,7 @@ def assert_sample_parity(inp, n, nx, tau, seed, offset=0):
     (3, 5, 5_003, 1.3, torch.float32),
     (64, 4, 2_000, 1.0, torch.bfloat16),
     (2, 1, 3_000, 1.0, torch.bfloat16),
+    (12, 4, 152_064, 1.0, torch.bfloat16),   # the largest draw chunk (4096 elements)
 ])
 def test_sample_matches_oracle(S, B, T, V, tau, dtype):
     inp = W.sample_inputs(B=B, T=T, V=V, seed=B + V, dtype=dtype)
