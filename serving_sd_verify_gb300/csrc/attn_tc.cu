@@ -232,19 +232,6 @@ __device__ __forceinline__ void tmem_ld_bind(uint32_t (&r)[32]) {
     asm volatile("" : SDV_W8(0), SDV_W8(8), SDV_W8(16), SDV_W8(24));
 }
 
-// 64 consecutive columns: both loads in flight before the single wait
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13,"
-        " %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31,"
-        " %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47,"
-        " %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-        : SDV_R8(0), SDV_R8(8), SDV_R8(16), SDV_R8(24), SDV_R8(32), SDV_R8(40), SDV_R8(48), SDV_R8(56)
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    asm volatile("" : SDV_W8(0), SDV_W8(8), SDV_W8(16), SDV_W8(24), SDV_W8(32), SDV_W8(40), SDV_W8(48),
-                 SDV_W8(56));
-}
 // store without waiting (callers issue tmem_st_wait once after a batch)
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
