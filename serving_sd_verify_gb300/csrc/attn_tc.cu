@@ -824,15 +824,14 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         named_sync(1, 256);
         if (!abort_seen) {
             // rows (j, hl) of one j are G consecutive rows of the partial output:
-            // copy them out as contiguous float4 runs
-            const int per_j = G * 32;  // float4s
-            for (int idx = sidx; idx < M * 32; idx += 256) {
-                const int jj = idx / per_j, rem = idx % per_j, hl = rem >> 5, c4 = rem & 31;
-                const int rr = jj * G + hl;
-                const float4 v = *reinterpret_cast<const float4 *>(ostage + rr * kOStride + c4 * 4);
-                const long frow = ((long)b * T + jj) * p.Hq + g * G + hl;
-                float *dst = p.merge == 2 ? p.out + frow * 128 : p.o_part + ((long)s * rows_total + frow) * 128;
-                *reinterpret_cast<float4 *>(dst + c4 * 4) = v;
+            // copy them out as contiguous float4 runs, block row by block row
+            // (no divisions in the loop)
+            float *obase = p.merge == 2 ? p.out : p.o_part + (long)s * rows_total * 128;
+            for (int jj = 0; jj < T; ++jj) {
+                float4 *dst = reinterpret_cast<float4 *>(obase + (((long)b * T + jj) * p.Hq + g * G) * 128);
+                const float *src = ostage + jj * G * kOStride;
+                for (int rem = sidx; rem < G * 32; rem += 256)
+                    dst[rem] = *reinterpret_cast<const float4 *>(src + (rem >> 5) * kOStride + (rem & 31) * 4);
             }
         }
     }
