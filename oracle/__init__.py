@@ -76,6 +76,14 @@ def _load():
                                          ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32,
                                          _ip, _ip, ctypes.c_void_p]
     lib.oracle_accept_sample.restype = ctypes.c_int
+    _up32 = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+    lib.oracle_tree_attention_rows.argtypes = [
+        _dp, _dp, _dp, _ip, _up32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_long, _dp]
+    lib.oracle_tree_attention_rows.restype = ctypes.c_int
+    lib.oracle_accept_tree_greedy.argtypes = [_ip, _ip, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              _ip, _ip, _ip, _ip]
+    lib.oracle_accept_tree_greedy.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -145,6 +153,28 @@ def attention_rows(q, k, v, nctx, scale, *, mode=0, kb=None, vb=None, rows=None,
     return (out, lse) if return_lse else out
 
 
+def tree_attention_rows(q, k, v, nctx, tree_mask, scale, *, rows=None):
+    """Exact fp64 tree-verify attention for the selected flat rows (b*T + j)*Hq + h.
+
+    Node j of sequence b attends to cache keys [0, nctx-1) and to the block
+    slots k (cache slot nctx-1+k) whose bit is set in tree_mask[b, j].
+    q [B,T,Hq,D]; k, v [B,Sc,Hkv,D]; tree_mask [B,T] (uint32).  Returns out [n_rows, D].
+    """
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    B, T, Hq, D = qd.shape
+    _, Sc, Hkv, _ = kd.shape
+    n = _i32(nctx).reshape(B)
+    m = np.ascontiguousarray(np.asarray(tree_mask, dtype=np.uint32).reshape(B * T))
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+    n_rows = B * T * Hq if rows_a is None else rows_a.size
+    out = np.zeros((n_rows, D), dtype=np.float64)
+    rc = _load().oracle_tree_attention_rows(qd, kd, vd, n, m, B, T, Hq, Hkv, D, Sc, float(scale),
+                                            _ptr(rows_a), n_rows, out)
+    if rc != 0:
+        raise ValueError("oracle_tree_attention_rows rejected its arguments")
+    return out
+
+
 def lse_merge(o_parts, lse_parts):
     """o_parts [S, D], lse_parts [S] -> (out [D], merged lse)."""
     o = _f64(o_parts)
@@ -172,6 +202,24 @@ def accept_greedy(draft_ids, logits, return_argmax=False):
     if rc != 0:
         raise ValueError("oracle_accept_greedy rejected its arguments")
     return (n, c, am) if return_argmax else (n, c)
+
+
+def accept_tree_greedy(tokens, parents, logits):
+    """Greedy acceptance over a draft tree: tokens, parents [B,T] (parents[:,0] = -1,
+    parents[:,j] < j), logits [B,T,V] -> (n_accepted [B], correction [B], best node [B],
+    path [B,T] (accepted nodes at depth 1..n, then -1))."""
+    lg = _f64(logits)
+    B, T, V = lg.shape
+    tk = np.ascontiguousarray(_i32(tokens).reshape(B, T))
+    pa = np.ascontiguousarray(_i32(parents).reshape(B, T))
+    n = np.zeros(B, dtype=np.int32)
+    c = np.zeros(B, dtype=np.int32)
+    best = np.zeros(B, dtype=np.int32)
+    path = np.zeros((B, T), dtype=np.int32)
+    rc = _load().oracle_accept_tree_greedy(tk, pa, lg, B, T, V, n, c, best, path)
+    if rc != 0:
+        raise ValueError("oracle_accept_tree_greedy rejected its arguments")
+    return n, c, best, path
 
 
 def accept_sample(draft_ids, draft_probs, logits, temperature, seed, offset=0,

@@ -186,6 +186,65 @@ int oracle_attention_rows(const double *q, const double *kc, const double *vc,
 }
 
 /*
+ * Tree verification (the "Tree-60" variant in the VFlash-FM speedup table):
+ * the block's T slots are the nodes of a draft tree in topological order,
+ * node 0 the anchor; their K/V sit at cache slots ctx-1 .. ctx-2+T as in the
+ * chain case.  Node j attends to the context before the anchor, cache keys
+ * [0, ctx-1), and to the block slots k whose bit is set in mask[b*T + j]
+ * (its ancestors and itself), in increasing k.  A chain mask (bits 0..j)
+ * gives exactly the keys [0, ctx+j) of oracle_attention_rows, in the same
+ * order.  Arguments as there; mask is [B*T].
+ */
+int oracle_tree_attention_rows(const double *q, const double *kc, const double *vc, const int *nctx,
+                               const unsigned int *mask, int B, int T, int Hq, int Hkv, int D, int Sc,
+                               double scale, const long *rows, long n_rows, double *out) {
+    if (B < 1 || T < 1 || T > 32 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return -1;
+    const int G = Hq / Hkv;
+    long total_rows = (long)B * T * Hq;
+    if (rows == NULL) n_rows = total_rows;
+    long max_keys = (long)Sc;
+    double *s = (double *)malloc(sizeof(double) * (size_t)max_keys);
+    long *ki = (long *)malloc(sizeof(long) * (size_t)max_keys);
+    if (!s || !ki) { free(s); free(ki); return -1; }
+    for (long r = 0; r < n_rows; ++r) {
+        long flat = rows ? rows[r] : r;
+        if (flat < 0 || flat >= total_rows) { free(s); free(ki); return -1; }
+        int h = (int)(flat % Hq);
+        int j = (int)((flat / Hq) % T);
+        int b = (int)(flat / ((long)Hq * T));
+        int g = h / G;
+        const double *qr = q + flat * D;
+        long c = nctx[b];
+        if (c < 1 || c - 1 + T > Sc) { free(s); free(ki); return -1; }
+        long n = 0;
+        for (long i = 0; i < c - 1; ++i) ki[n++] = i;
+        for (int k = 0; k < T; ++k)
+            if ((mask[(long)b * T + j] >> k) & 1u) ki[n++] = c - 1 + k;
+        double *o = out + r * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (n == 0) continue;
+        double m = -INFINITY;
+        for (long i = 0; i < n; ++i) {
+            const double *kr = kc + (((long)b * Sc + ki[i]) * Hkv + g) * D;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qr[d] * kr[d];
+            s[i] = scale * acc;
+            if (s[i] > m) m = s[i];
+        }
+        double denom = 0.0;
+        for (long i = 0; i < n; ++i) {
+            const double *vr = vc + (((long)b * Sc + ki[i]) * Hkv + g) * D;
+            double w = exp(s[i] - m);
+            denom += w;
+            for (int d = 0; d < D; ++d) o[d] += w * vr[d];
+        }
+        for (int d = 0; d < D; ++d) o[d] /= denom;
+    }
+    free(s); free(ki);
+    return 0;
+}
+
+/*
  * Log-sum-exp merge of attention over disjoint key ranges:
  * out = sum_s exp(lse_s - M) o_s / sum_s exp(lse_s - M), M = max_s lse_s;
  * ranges with lse = -inf hold no key and are skipped.
@@ -242,6 +301,47 @@ int oracle_accept_greedy(const int *draft, const double *logits, int B, int T, i
         }
         n_acc[b] = n;
         corr[b] = a[n];
+    }
+    return 0;
+}
+
+/*
+ * Greedy acceptance over a draft tree (nodes in topological order, node 0 the
+ * anchor; parent[b][j] < j, parent[b][0] = -1; token[b][j] is node j's
+ * proposal, token[b][0] unused).  a_j = argmax of logits row j (ties: lowest
+ * index).  The anchor is accepted; node j >= 1 is accepted when its parent
+ * is and token[j] == a_parent(j) (the target's greedy pick after the
+ * parent).  The committed path ends at the accepted node of greatest depth,
+ * the lowest index among equals:
+ *   n_acc[b]  its depth (proposals accepted), best[b] the node,
+ *   corr[b]   a_best (the target's own next token),
+ *   path[b]   the accepted nodes from depth 1 to n_acc, then -1.
+ * A chain tree (parent j-1, token[j] = draft[j-1]) gives oracle_accept_greedy.
+ */
+int oracle_accept_tree_greedy(const int *token, const int *parent, const double *logits, int B, int T,
+                              int V, int *n_acc, int *corr, int *best, int *path) {
+    if (B < 1 || T < 1 || T > 64 || V < 1) return -1;
+    for (int b = 0; b < B; ++b) {
+        int a[64], acc[64], depth[64];
+        for (int j = 0; j < T; ++j) a[j] = argmax_lowest(logits + ((long)b * T + j) * V, V);
+        int bj = 0;
+        for (int j = 0; j < T; ++j) {
+            const int pj = parent[(long)b * T + j];
+            if (j == 0) {
+                if (pj != -1) return -1;
+                acc[0] = 1; depth[0] = 0;
+                continue;
+            }
+            if (pj < 0 || pj >= j) return -1;
+            acc[j] = acc[pj] && token[(long)b * T + j] == a[pj];
+            depth[j] = depth[pj] + 1;
+            if (acc[j] && depth[j] > depth[bj]) bj = j;
+        }
+        n_acc[b] = depth[bj];
+        corr[b] = a[bj];
+        best[b] = bj;
+        for (int k = 0; k < T; ++k) path[(long)b * T + k] = -1;
+        for (int v = bj; v != 0; v = parent[(long)b * T + v]) path[(long)b * T + depth[v] - 1] = v;
     }
     return 0;
 }
