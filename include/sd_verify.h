@@ -121,6 +121,31 @@ size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, in
                                                int max_ctx, sd_dtype dtype);
 
 /* ------------------------------------------------------------------------
+ * Tree verify attention
+ *
+ * Source: "VFlash-FM" project page, speedup table: its fastest variant
+ * verifies a draft tree ("Tree-60") rather than a chain.  The page gives no
+ * layout; the one taken here: the block's T slots are the tree's nodes in
+ * topological order, node 0 the anchor, their K/V at cache slots
+ * ctx_len-1 .. ctx_len-2+T exactly as for sd_verify_attention.  Node j
+ * attends to the cache keys [0, ctx_len-1) (the context before the anchor)
+ * and to the slots ctx_len-1+k of every bit k set in tree_mask[b][j] (its
+ * ancestors and itself).  A chain mask (bits 0..j) gives sd_verify_attention.
+ *
+ *   tree_mask  device uint32 [B, T]; bit k < T (T <= 16 here: the tensor-core
+ *              kernel holds all G*T rows of a kv head in one 128-row tile)
+ *   everything else as for sd_verify_attention (same workspace size)
+ * ------------------------------------------------------------------------ */
+sd_status sd_verify_tree_attention(const void *q, const void *k_cache, const void *v_cache,
+                                   sd_strides kv, const int32_t *ctx_len, int max_ctx,
+                                   const uint32_t *tree_mask, float *out, int B, int T, int Hq,
+                                   int Hkv, int D, sd_dtype dtype, float scale,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+size_t sd_verify_tree_attention_workspace_size(int B, int T, int Hq, int Hkv, int D,
+                                               int max_ctx, sd_dtype dtype);
+
+/* ------------------------------------------------------------------------
  * Greedy acceptance
  *
  * Source: "VFlash-FM" project page, worked cycle: the target keeps the
@@ -177,6 +202,34 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs,
                            void *workspace, size_t workspace_bytes, void *stream);
 
 size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype);
+
+/* ------------------------------------------------------------------------
+ * Greedy acceptance over a draft tree
+ *
+ * Source: "VFlash-FM" project page (speedup table, tree verification; the
+ * greedy rule of the worked cycle).  With a_j the argmax of logits row j
+ * (ties: lowest index), the anchor is accepted and node j >= 1 is accepted
+ * when its parent is and tokens[b][j] == a_parent: the target's own greedy
+ * pick after the parent.  The committed path ends at the accepted node of
+ * greatest depth (the lowest index among equals), so a chain tree gives
+ * sd_accept_greedy.
+ *
+ *   tokens         device int32 [B, T]: tokens[b][j] is node j's proposal
+ *                  (tokens[b][0], the anchor, is not read)
+ *   parents        device int32 [B, T]: parents[b][0] = -1, parents[b][j] in
+ *                  [0, j); anything else sets the fault word
+ *   target_logits  [B, T, V] as for sd_accept_greedy
+ *   n_accepted     device int32 [B]: depth of that node (proposals kept)
+ *   correction_id  device int32 [B]: a_node (the target's next token)
+ *   path           device int32 [B, T]: the kept nodes at depth 1..n, then -1
+ *   workspace      as for sd_accept_greedy (same size)
+ * ------------------------------------------------------------------------ */
+sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, const void *target_logits,
+                                int B, int T, int V, sd_dtype dtype, int32_t *n_accepted,
+                                int32_t *correction_id, int32_t *path, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+size_t sd_accept_tree_greedy_workspace_size(int B, int T, int V, sd_dtype dtype);
 
 /* ------------------------------------------------------------------------
  * Greedy acceptance without a caller workspace

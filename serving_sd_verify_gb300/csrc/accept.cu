@@ -237,12 +237,37 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
         for (int bl = threadIdx.x; bl < nbw; bl += kAccThreads) {
             const int b = b0 + bl, rb = bl * p.T;
-            int n = p.T - 1;
-            for (int j = 0; j < p.T - 1; ++j) {
-                if (p.draft[(long)b * (p.T - 1) + j] != am[rb + j]) { n = j; break; }
+            if (p.parents) {
+                // draft tree: node j is accepted when its parent is and its token
+                // equals the target's pick after the parent; the deepest accepted
+                // node (lowest index among equals) ends the committed path
+                const int32_t *par = p.parents + (long)b * p.T, *tok = p.draft + (long)b * p.T;
+                uint32_t acc = 1u;  // bit j: node j accepted (the anchor always)
+                int depth[kMaxT];
+                depth[0] = 0;
+                int best = 0;
+                for (int j = 1; j < p.T; ++j) {
+                    const int pj = par[j];
+                    if (pj < 0 || pj >= j) { set_fault(p.fault, FAULT_BAD_TREE); depth[j] = 0; continue; }
+                    depth[j] = depth[pj] + 1;
+                    if (((acc >> pj) & 1u) && tok[j] == am[rb + pj]) {
+                        acc |= 1u << j;
+                        if (depth[j] > depth[best]) best = j;
+                    }
+                }
+                p.n_acc[b] = depth[best];
+                p.corr[b] = am[rb + best];
+                int32_t *path = p.path + (long)b * p.T;
+                for (int k = depth[best]; k < p.T; ++k) path[k] = -1;
+                for (int v = best; v != 0; v = par[v]) path[depth[v] - 1] = v;
+            } else {
+                int n = p.T - 1;
+                for (int j = 0; j < p.T - 1; ++j) {
+                    if (p.draft[(long)b * (p.T - 1) + j] != am[rb + j]) { n = j; break; }
+                }
+                p.n_acc[b] = n;
+                p.corr[b] = am[rb + n];
             }
-            p.n_acc[b] = n;
-            p.corr[b] = am[rb + n];
         }
         __syncthreads();
     }

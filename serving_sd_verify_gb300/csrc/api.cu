@@ -67,7 +67,7 @@ struct AttnPlan {
 };
 
 // keys of the longest sequence's key space
-int max_keys(int mode, int max_ctx, int T) { return mode == 0 ? max_ctx + T - 1 : max_ctx + T; }
+int max_keys(int mode, int max_ctx, int T) { return mode == 1 ? max_ctx + T : max_ctx + T - 1; }
 
 AttnPlan plan_attention(const AttnParams &p, int path) {
     const int sms = device_sm_count();
@@ -102,6 +102,7 @@ sd_status validate_attention(const AttnParams &p) {
     if (!p.q || !p.kc || !p.vc || !p.nctx || !p.out)
         return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
     if (p.mode == 1 && (!p.kb || !p.vb)) return fail(SD_ERR_INVALID_ARG, "null block key/value pointer");
+    if (p.mode == 2 && !p.tree_mask) return fail(SD_ERR_INVALID_ARG, "null tree mask");
     if (p.B < 1 || p.T < 1 || p.T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
     if (p.Hq < 1 || p.Hkv < 1 || p.Hq % p.Hkv) return fail(SD_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
     if (p.D != 64 && p.D != 128) return fail(SD_ERR_UNSUPPORTED, "D must be 64 or 128");
@@ -328,6 +329,24 @@ size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, in
     return attention_ws_size(1, B, T, Hq, Hkv, D, max_ctx, dtype);
 }
 
+sd_status sd_verify_tree_attention(const void *q, const void *k_cache, const void *v_cache, sd_strides kv,
+                                   const int32_t *ctx_len, int max_ctx, const uint32_t *tree_mask, float *out,
+                                   int B, int T, int Hq, int Hkv, int D, sd_dtype dtype, float scale,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    AttnParams p = {};
+    p.q = q; p.kc = k_cache; p.vc = v_cache; p.kv = kv; p.nctx = ctx_len; p.mode = 2;
+    p.tree_mask = tree_mask;
+    p.out = out; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dtype; p.scale = scale;
+    p.max_ctx = max_ctx;
+    p.fault = fault_ptr();
+    return run_attention(p, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t sd_verify_tree_attention_workspace_size(int B, int T, int Hq, int Hkv, int D, int max_ctx,
+                                               sd_dtype dtype) {
+    return attention_ws_size(2, B, T, Hq, Hkv, D, max_ctx, dtype);
+}
+
 size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
     return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype))).total;
@@ -359,6 +378,41 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     cudaError_t e = launch_accept_greedy(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "greedy accept launch");
+    return SD_OK;
+}
+
+size_t sd_accept_tree_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
+    return sd_accept_greedy_workspace_size(B, T, V, dtype);
+}
+
+sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, const void *target_logits, int B,
+                                int T, int V, sd_dtype dtype, int32_t *n_accepted, int32_t *correction_id,
+                                int32_t *path, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 1 || T < 1 || T > kMaxT || V < 1) return fail(SD_ERR_INVALID_ARG, "need B >= 1, T in [1, 16], V >= 1");
+    if (!target_logits || !n_accepted || !correction_id || !tokens || !parents || !path)
+        return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (dtype != SD_BF16 && dtype != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if ((reinterpret_cast<uintptr_t>(target_logits) % esize(dtype)) != 0)
+        return fail(SD_ERR_INVALID_ARG, "logits pointer not aligned to its element size");
+    GreedyParams p = {};
+    p.draft = tokens; p.parents = parents; p.path = path;
+    p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
+    p.n_acc = n_accepted; p.corr = correction_id;
+    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype));
+    p.n_chunks = (V + p.chunk - 1) / p.chunk;
+    const GreedyLayout gl = greedy_layout(B, T, V, p.chunk);
+    if (!workspace || workspace_bytes < gl.total)
+        return fail(SD_ERR_WORKSPACE, "tree greedy workspace too small: need %zu bytes, got %zu", gl.total,
+                    workspace_bytes);
+    if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    char *w = static_cast<char *>(workspace);
+    p.counter = reinterpret_cast<unsigned int *>(w);
+    p.pval = reinterpret_cast<float *>(w + gl.pval);
+    p.pidx = reinterpret_cast<int *>(w + gl.pidx);
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_accept_greedy(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree greedy accept launch");
     return SD_OK;
 }
 

@@ -63,7 +63,7 @@ attn_split_generic_kernel(const AttnParams p) {
         if (tid == 0) set_fault(p.fault, FAULT_BAD_CTX);
         nb = max(1, min(nb, p.max_ctx));
     }
-    const int N_b = p.mode == 0 ? nb + T - 1 : nb + T;
+    const int N_b = p.mode == 1 ? nb + T : nb + T - 1;
     const int k0 = s * p.keys_per_split;
     const int k1 = min(N_b, k0 + p.keys_per_split);
     const float qscale = p.scale * kLog2e;
@@ -115,9 +115,15 @@ attn_split_generic_kernel(const AttnParams p) {
             __syncthreads();
             for (int r = warp; r < nr; r += kGenThreads / 32) {
                 const int row = rc0 + r, j = row / G;
-                const int limit = min(k1, p.mode == 0 ? nb + j : N_b);
                 const int key = kt + lane;
-                const bool valid = key < limit;
+                bool valid;
+                if (p.mode == 2) {
+                    // tree: the context before the anchor, then the slots of the node's mask
+                    const int slot = key - (nb - 1);
+                    valid = key < k1 && (slot < 0 || (slot < T && ((p.tree_mask[(long)b * T + j] >> slot) & 1u)));
+                } else {
+                    valid = key < min(k1, p.mode == 0 ? nb + j : N_b);
+                }
                 float sc = 0.f;
                 const float *qr = Qs + r * D;
                 const float *kr = Ks + lane * KS;

@@ -446,8 +446,9 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     auto tile_key0 = [&](int t) { return k0 + (t - first_tma) * kBN; };
     auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
     // keys every row of the block sees: the drafter's context, the target's
-    // cache before the block
-    const int all_see = min(cend, nb);
+    // cache before the block (before the anchor for a tree)
+    const bool tree = p.mode == 2;
+    const int all_see = min(cend, tree ? nb - 1 : nb);
 
     // one copy per tile: map coordinates (d within a half, key, half, kv head, sequence)
     auto issue_k = [&](int t) {
@@ -650,16 +651,26 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // finite values that are never stored)
             const bool blk = is_block_tile(t);
             const bool whole = !blk && tile_key0(t) + kBN <= all_see;
-            int nvalid;
-            if (whole) {
-                nvalid = kBN;
-            } else if (blk) {
-                nvalid = row_ok ? T : 0;
-            } else {
-                const int lim = drafter ? cend : min(cend, nb + j);
-                nvalid = row_ok ? max(0, min(kBN, lim - tile_key0(t))) : 0;
+            // bit c: key c of this warpgroup's half of the tile is visible to the row
+            uint64_t vis = ~0ull;
+            if (!whole) {
+                auto prefix = [](int n) { return n <= 0 ? 0ull : n >= 64 ? ~0ull : (1ull << n) - 1ull; };
+                const int key0h = tile_key0(t) + 64 * wg;
+                if (!row_ok) {
+                    vis = 0ull;
+                } else if (blk) {
+                    vis = prefix(T - 64 * wg);
+                } else if (tree) {
+                    vis = prefix(min(cend, nb - 1) - key0h);
+                    const uint32_t tm = p.tree_mask[(long)b * T + j];
+                    for (int k = 0; k < T; ++k) {
+                        const int pos = nb - 1 + k - key0h;
+                        if (pos >= 0 && pos < 64 && key0h + pos < cend && ((tm >> k) & 1u)) vis |= 1ull << pos;
+                    }
+                } else {
+                    vis = prefix((drafter ? cend : min(cend, nb + j)) - key0h);
+                }
             }
-            const int nv_half = min(64, max(0, nvalid - 64 * wg));  // visible keys of this half
             uint32_t sa[32], sb[32];
             tmem_ld32_async(sp_col, sa);
             tmem_ld32_async(sp_col + 32u, sb);
@@ -688,7 +699,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     float m8 = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        m8 = fmaxf(m8, 8 * i + e < nv_half ? __uint_as_float(src[o + e]) : -INFINITY);
+                        m8 = fmaxf(m8, ((vis >> (8 * i + e)) & 1ull) ? __uint_as_float(src[o + e]) : -INFINITY);
                     mx[i] = m8;
                 }
             }
@@ -725,7 +736,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             l *= alpha;
             const bool live = m_used != -INFINITY;
             const float neg_m = live ? -m_used : 0.f;
-            const int nv = live ? nv_half : 0;
+            if (!live) vis = 0ull;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
             // P of this 64-key half over the S columns it came from: hi in [0,32),
             // lo in [32,64).  hi = p truncated to bf16; lo = the exact fp32
@@ -733,11 +744,11 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // permutes instead of conversion instructions.
             // the masked keys of an edge tile are cleared in the scores first
             // (-inf gives a weight of 0), so the exponential loop has no selects
-            if (!whole) {
+            if (!whole || !live) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    if (c >= nv) sa[c] = 0xff800000u;
-                    if (32 + c >= nv) sb[c] = 0xff800000u;
+                    if (!((vis >> c) & 1ull)) sa[c] = 0xff800000u;
+                    if (!((vis >> (32 + c)) & 1ull)) sb[c] = 0xff800000u;
                 }
             }
 #pragma unroll
@@ -896,7 +907,7 @@ bool make_q_map(CUtensorMap *m, const AttnParams &p) {
     return r == CUDA_SUCCESS;
 }
 
-int cache_slots(const AttnParams &p) { return p.mode == 0 ? p.max_ctx + p.T - 1 : p.max_ctx; }
+int cache_slots(const AttnParams &p) { return p.mode == 1 ? p.max_ctx : p.max_ctx + p.T - 1; }
 
 cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     alignas(64) CUtensorMap mq, mk, mv;

@@ -17,6 +17,7 @@ enum FaultBits : unsigned int {
     FAULT_NAN_ROW = 1u << 2,        // argmax row without any ordered value (NaN)
     FAULT_WAIT_TIMEOUT = 1u << 3,   // a bounded mbarrier wait gave up
     FAULT_TMEM_ALLOC = 1u << 4,     // tensor-memory allocation returned out of range
+    FAULT_BAD_TREE = 1u << 5,       // a tree node's parent outside [0, node)
 };
 
 constexpr int kMaxT = 16;           // block rows (anchor + 15 proposals)
@@ -28,6 +29,9 @@ constexpr int kTcTileKeys = 128;    // keys per tile of the tensor-core attentio
 //   mode 0 (verify):  N_b = nctx[b] + T - 1 cache keys; row j sees [0, nctx[b] + j)
 //   mode 1 (drafter): N_b = nctx[b] + T; keys [0, nctx[b]) from the cache,
 //                     [nctx[b], N_b) from the block tensors; every row sees all
+//   mode 2 (tree):    N_b = nctx[b] + T - 1 cache keys; row j sees
+//                     [0, nctx[b] - 1) and block slot nctx[b] - 1 + k for every
+//                     bit k set in tree_mask[b * T + j]
 //  split s covers keys [s * keys_per_split, (s + 1) * keys_per_split) of that space.
 struct AttnParams {
     const void *q;                  // [B, T, Hq, D]
@@ -36,6 +40,7 @@ struct AttnParams {
     const int32_t *nctx;            // [B]
     int mode;
     const void *kb, *vb;            // [B, T, Hkv, D] (mode 1)
+    const uint32_t *tree_mask;      // [B, T] (mode 2)
     float *out;                     // [B, T, Hq, D]
     int B, T, Hq, Hkv, D;
     sd_dtype dt;
@@ -64,7 +69,9 @@ size_t attn_tc_smem_bytes(const AttnParams &p);
 // Acceptance workspaces hold ticket counters that must be zero before the
 // first call and are returned to zero by every completed call.
 struct GreedyParams {
-    const int32_t *draft;
+    const int32_t *draft;           // chain: [B, T-1] proposals; tree: [B, T] node tokens
+    const int32_t *parents;         // tree only: [B, T], parents[b][0] = -1, parents[b][j] < j
+    int32_t *path;                  // tree only: [B, T] accepted nodes at depth 1..n, then -1
     const void *logits;
     int B, T, V;
     sd_dtype dt;

@@ -24,6 +24,8 @@ SYMBOLS = [
     "sd_verify_attention", "sd_verify_attention_workspace_size",
     "sd_draft_block_attention", "sd_draft_block_attention_workspace_size",
     "sd_accept_greedy", "sd_accept_greedy_workspace_size",
+    "sd_verify_tree_attention", "sd_verify_tree_attention_workspace_size",
+    "sd_accept_tree_greedy", "sd_accept_tree_greedy_workspace_size",
     "sd_accept_sample", "sd_accept_sample_workspace_size", "sd_accept_greedy_noalloc",
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
@@ -65,6 +67,15 @@ def load():
     lib.sd_draft_block_attention_workspace_size.restype = _sz
     lib.sd_accept_greedy.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]
     lib.sd_accept_greedy.restype = _i
+    lib.sd_verify_tree_attention.argtypes = [_vp, _vp, _vp, Strides, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                             ctypes.c_float, _vp, _sz, _vp]
+    lib.sd_verify_tree_attention.restype = _i
+    lib.sd_verify_tree_attention_workspace_size.argtypes = [_i] * 7
+    lib.sd_verify_tree_attention_workspace_size.restype = _sz
+    lib.sd_accept_tree_greedy.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.sd_accept_tree_greedy.restype = _i
+    lib.sd_accept_tree_greedy_workspace_size.argtypes = [_i] * 4
+    lib.sd_accept_tree_greedy_workspace_size.restype = _sz
     lib.sd_accept_greedy_workspace_size.argtypes = [_i] * 4
     lib.sd_accept_greedy_workspace_size.restype = _sz
     lib.sd_accept_sample.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, ctypes.c_uint64,
@@ -197,6 +208,49 @@ def sd_draft_block_attention(q, k_ctx, v_ctx, n_ctx, max_ctx, k_blk, v_blk, out,
                                            int(max_ctx), _p(k_blk), _p(v_blk), _p(out), B, T, Hq, Hkv,
                                            D, _dt(q), float(scale), _p(ws), ws.numel() * ws.element_size(),
                                            _stream(stream)))
+
+
+def sd_verify_tree_attention_workspace_size(B, T, Hq, Hkv, D, max_ctx, dtype=SD_BF16) -> int:
+    return load().sd_verify_tree_attention_workspace_size(B, T, Hq, Hkv, D, max_ctx, dtype)
+
+
+def sd_accept_tree_greedy_workspace_size(B, T, V, dtype=SD_BF16) -> int:
+    return load().sd_accept_tree_greedy_workspace_size(B, T, V, dtype)
+
+
+def sd_verify_tree_attention(q, k_cache, v_cache, ctx_len, max_ctx, tree_mask, out, scale, ws, stream=None):
+    """As sd_verify_attention, plus tree_mask int32/uint32 [B,T] (bit k: node sees block slot k)."""
+    _need_cuda(q, k_cache, v_cache, ctx_len, tree_mask, out, ws)
+    B, T, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    if not q.is_contiguous() or not out.is_contiguous() or out.dtype != torch.float32:
+        raise ValueError("q and out must be contiguous; out fp32")
+    if ctx_len.dtype != torch.int32 or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("ctx_len int32; q, k_cache, v_cache of one dtype")
+    if tree_mask.dtype not in (torch.int32, torch.uint32) or tree_mask.numel() != B * T or not tree_mask.is_contiguous():
+        raise ValueError("tree_mask: contiguous 32-bit [B, T]")
+    if k_cache.stride() != v_cache.stride():
+        raise ValueError("k_cache and v_cache must share strides")
+    _check(load().sd_verify_tree_attention(_p(q), _p(k_cache), _p(v_cache), _kv_strides(k_cache), _p(ctx_len),
+                                           int(max_ctx), _p(tree_mask), _p(out), B, T, Hq, Hkv, D, _dt(q),
+                                           float(scale), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sd_accept_tree_greedy(tokens, parents, target_logits, n_accepted, correction_id, path, ws, stream=None):
+    """tokens, parents int32 [B,T]; target_logits [B,T,V]; n_accepted, correction_id int32 [B];
+    path int32 [B,T]."""
+    _need_cuda(tokens, parents, target_logits, n_accepted, correction_id, path, ws)
+    B, T, V = target_logits.shape
+    for t in (tokens, parents, path):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() != B * T:
+            raise ValueError("tokens, parents and path are contiguous int32 [B, T]")
+    if not target_logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    if n_accepted.dtype != torch.int32 or correction_id.dtype != torch.int32:
+        raise ValueError("ids are int32")
+    _check(load().sd_accept_tree_greedy(_p(tokens), _p(parents), _p(target_logits), B, T, V, _dt(target_logits),
+                                        _p(n_accepted), _p(correction_id), _p(path), _p(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def sd_accept_greedy(draft_ids, target_logits, n_accepted, correction_id, ws, stream=None):
