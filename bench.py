@@ -66,6 +66,9 @@ BYTES = {
     "accept_greedy": T * V * 2 + (T - 1) * 4 + 8,
     # logits read twice (stats, then the deciding row), q gathered + one q row
     "accept_sample": T * V * 2 + V * 2 + V * 4 + (T - 1) * 8 + 8,
+    # the tree rows (not part of the timed step): the same reads plus the tree
+    "verify_tree_attention": attn_bytes(CTX + T - 1) + T * 4,
+    "accept_tree_greedy": T * V * 2 + T * 8 + T * 4 + 8,
 }
 
 
@@ -94,8 +97,25 @@ def make_inputs(device):
                        for j in range(T - 1)]], dtype=np.int32)
     smp["q"] = torch.from_numpy(q.astype(np.float32))
     smp["draft"] = torch.from_numpy(draft)
+    # a seeded 16-node draft tree (each node's parent among the 3 before it);
+    # node tokens mostly equal the target's pick after the parent
+    trng = np.random.default_rng(60)
+    parents = np.full(T, -1, dtype=np.int32)
+    for j in range(1, T):
+        parents[j] = trng.integers(max(0, j - 3), j)
+    mask = np.zeros(T, dtype=np.int64)
+    for j in range(T):
+        v = j
+        while v != -1:
+            mask[j] |= 1 << v
+            v = parents[v]
+    am = cfg2["greedy"]["logits"].float().numpy().argmax(-1)[0]
+    tokens = np.array([0] + [int(am[parents[j]]) if trng.random() < 0.7 else int(trng.integers(0, V))
+                             for j in range(1, T)], dtype=np.int32)
+    tree = {"mask": torch.from_numpy(mask.astype(np.int32)).reshape(1, T),
+            "parents": torch.from_numpy(parents).reshape(1, T), "tokens": torch.from_numpy(tokens).reshape(1, T)}
     log(f"[bench] inputs generated in {time.time() - t0:.1f}s")
-    return {"attn": cfg2["attn"], "greedy": cfg2["greedy"], "drafter": dr, "sample": smp}
+    return {"attn": cfg2["attn"], "greedy": cfg2["greedy"], "drafter": dr, "sample": smp, "tree": tree}
 
 
 class DeviceSet:
@@ -120,6 +140,13 @@ class DeviceSet:
         self.ws_d = S.workspace(S.sd_draft_block_attention_workspace_size(1, T, HQ, HKV, D, CTX), device)
         self.ws_g = S.workspace(S.sd_accept_greedy_workspace_size(1, T, V), device)
         self.ws_s = S.workspace(S.sd_accept_sample_workspace_size(1, T, V), device)
+        tr = host["tree"]
+        self.tmask, self.tparents, self.ttokens = dv(tr["mask"]), dv(tr["parents"]), dv(tr["tokens"])
+        self.tpath = torch.zeros(1, T, dtype=torch.int32, device=device)
+        self.tn = torch.zeros(1, dtype=torch.int32, device=device)
+        self.tc = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws_tv = S.workspace(S.sd_verify_tree_attention_workspace_size(1, T, HQ, HKV, D, CTX), device)
+        self.ws_tg = S.workspace(S.sd_accept_tree_greedy_workspace_size(1, T, V), device)
 
     def nbytes(self):
         ts = [self.q, self.k, self.v, self.kc, self.vc, self.logits, self.sq]
@@ -146,6 +173,10 @@ def run_step(S, ds, stream=None, parts=("draft", "verify", "greedy", "sample")):
         S.sd_accept_greedy(ds.draft, ds.logits, ds.n, ds.c, ds.ws_g, stream)
     if "sample" in parts:
         S.sd_accept_sample(ds.sdraft, ds.sq, ds.logits, 1.0, 1234, 0, ds.sn, ds.snx, ds.ws_s, stream)
+    if "tree_verify" in parts:
+        S.sd_verify_tree_attention(ds.q, ds.k, ds.v, ds.ctx, CTX, ds.tmask, ds.out, 1.0, ds.ws_tv, stream)
+    if "tree_greedy" in parts:
+        S.sd_accept_tree_greedy(ds.ttokens, ds.tparents, ds.logits, ds.tn, ds.tc, ds.tpath, ds.ws_tg, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -463,7 +494,9 @@ def main():
         flush = torch.empty(320 * 1024 * 1024, dtype=torch.uint8, device=device)
         n_rep = 30
         for name, part, launches in (("draft_attention", "draft", LAYERS), ("verify_attention", "verify", 1),
-                                     ("accept_greedy", "greedy", 1), ("accept_sample", "sample", 1)):
+                                     ("accept_greedy", "greedy", 1), ("accept_sample", "sample", 1),
+                                     ("verify_tree_attention", "tree_verify", 1),
+                                     ("accept_tree_greedy", "tree_greedy", 1)):
             evs = []
             with torch.cuda.stream(stream):
                 for i in range(n_rep):
@@ -482,9 +515,13 @@ def main():
         kernels["draft_attention"]["note"] = ("average over the 4 layers of one step; they share one projected "
                                               "context, so layers 2-4 read it from L2 and only the first call "
                                               "is HBM-bound")
+        for name in ("verify_tree_attention", "accept_tree_greedy"):
+            kernels[name]["note"] = ("tree verification (a seeded 16-node draft tree), timed alone; not part of "
+                                     "the step, which uses the chain calls")
         for name, nl in (("draft_attention", ATTN_LAUNCHES["draft"]), ("verify_attention", ATTN_LAUNCHES["verify"]),
                          ("accept_greedy", 1),
-                         ("accept_sample", 2)):
+                         ("accept_sample", 2), ("verify_tree_attention", ATTN_LAUNCHES["verify"]),
+                         ("accept_tree_greedy", 1)):
             kernels[name]["kernel_launches_per_call"] = nl
 
     # ---- roofline: the verify attention (the spec kernel), timed cold ----
