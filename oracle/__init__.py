@@ -84,6 +84,9 @@ def _load():
     lib.oracle_accept_tree_greedy.argtypes = [_ip, _ip, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               _ip, _ip, _ip, _ip]
     lib.oracle_accept_tree_greedy.restype = ctypes.c_int
+    lib.oracle_project_rows.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_long, _dp]
+    lib.oracle_project_rows.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -172,6 +175,22 @@ def tree_attention_rows(q, k, v, nctx, tree_mask, scale, *, rows=None):
                                             _ptr(rows_a), n_rows, out)
     if rc != 0:
         raise ValueError("oracle_tree_attention_rows rejected its arguments")
+    return out
+
+
+def project_rows(hidden, weight, rows=None):
+    """Exact fp64 linear map of the selected rows: hidden [N, Hd], weight [Dout, Hd]
+    -> out [n_rows, Dout] = hidden[rows] @ weight^T."""
+    h = _f64(hidden)
+    w = _f64(weight)
+    N, Hd = h.shape
+    Dout = w.shape[0]
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+    n_rows = N if rows_a is None else rows_a.size
+    out = np.zeros((n_rows, Dout), dtype=np.float64)
+    rc = _load().oracle_project_rows(h, w, N, Hd, Dout, _ptr(rows_a), n_rows, out)
+    if rc != 0:
+        raise ValueError("oracle_project_rows rejected its arguments")
     return out
 
 

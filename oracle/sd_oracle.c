@@ -245,6 +245,29 @@ int oracle_tree_attention_rows(const double *q, const double *kc, const double *
 }
 
 /*
+ * Drafter K/V projector ("VFlash-FM" project page, "How VFlash-FM works":
+ * the drafter's keys and values are a linear map of the hidden states the
+ * target has cached).  For the selected rows r: out[i][c] = sum_k h[r][k] *
+ * w[c][k], exact in fp64 (w is [Dout, Hd], the out-features x in-features
+ * layout of a linear layer's weight).
+ */
+int oracle_project_rows(const double *h, const double *w, int N, int Hd, int Dout, const long *rows, long n_rows,
+                        double *out) {
+    if (N < 1 || Hd < 1 || Dout < 1) return -1;
+    if (rows == NULL) n_rows = N;
+    for (long i = 0; i < n_rows; ++i) {
+        const long r = rows ? rows[i] : i;
+        if (r < 0 || r >= N) return -1;
+        for (int c = 0; c < Dout; ++c) {
+            double acc = 0.0;
+            for (int k = 0; k < Hd; ++k) acc += h[r * Hd + k] * w[(long)c * Hd + k];
+            out[i * Dout + c] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
  * Log-sum-exp merge of attention over disjoint key ranges:
  * out = sum_s exp(lse_s - M) o_s / sum_s exp(lse_s - M), M = max_s lse_s;
  * ranges with lse = -inf hold no key and are skipped.
