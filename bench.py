@@ -39,7 +39,10 @@ sys.path.insert(0, ROOT)
 METRIC = "verified 16-token blocks/sec and HBM GB/s (% of peak) at 25,119-token ctx"
 WORKLOAD = "llava-ov-7b-verify-ctx25119-h28kv4-d128-bf16 + 4-layer drafter + greedy & sampled accept (V=152064)"
 CTX, T, HQ, HKV, D, V, LAYERS = 25_119, 16, 28, 4, 128, 152_064, 4
+HD = 3584           # target hidden size (Qwen2-7B), the projector's input width
+APPEND = 8          # rows one cycle appends to the drafter's context (accepted + correction)
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -69,7 +72,10 @@ BYTES = {
     # the tree rows (not part of the timed step): the same reads plus the tree
     "verify_tree_attention": attn_bytes(CTX + T - 1) + T * 4,
     "accept_tree_greedy": T * V * 2 + T * 8 + T * 4 + 8,
+    # projector append: both weights read once, the new rows in and out
+    "project_append": 2 * HKV * D * HD * 2 + APPEND * HD * 2 + 2 * APPEND * HKV * D * 2,
 }
+PROJ_PREFILL_FLOPS = 2 * CTX * HD * 2 * HKV * D
 
 
 # ---------------------------------------------------------------------------
@@ -114,8 +120,11 @@ def make_inputs(device):
                              for j in range(1, T)], dtype=np.int32)
     tree = {"mask": torch.from_numpy(mask.astype(np.int32)).reshape(1, T),
             "parents": torch.from_numpy(parents).reshape(1, T), "tokens": torch.from_numpy(tokens).reshape(1, T)}
+    # the drafter K/V projector in a linear layer's [out, in] layout, bf16
+    proj = {"h": h, "wk": wk.t().contiguous().to(torch.bfloat16), "wv": wv.t().contiguous().to(torch.bfloat16)}
     log(f"[bench] inputs generated in {time.time() - t0:.1f}s")
-    return {"attn": cfg2["attn"], "greedy": cfg2["greedy"], "drafter": dr, "sample": smp, "tree": tree}
+    return {"attn": cfg2["attn"], "greedy": cfg2["greedy"], "drafter": dr, "sample": smp, "tree": tree,
+            "proj": proj}
 
 
 class DeviceSet:
@@ -151,6 +160,22 @@ class DeviceSet:
     def nbytes(self):
         ts = [self.q, self.k, self.v, self.kc, self.vc, self.logits, self.sq]
         return sum(t.numel() * t.element_size() for t in ts)
+
+
+class ProjSet:
+    """The drafter K/V projector's operands in HBM: the context's target hidden
+    states [CTX, HD], W_k / W_v [HKV*D, HD], and the projected context."""
+
+    def __init__(self, hp, device):
+        import torch
+        self.h = hp["h"].to(device).contiguous()
+        self.wk, self.wv = hp["wk"].to(device), hp["wv"].to(device)
+        self.k = torch.empty(CTX, HKV * D, dtype=torch.bfloat16, device=device)
+        self.v = torch.empty_like(self.k)
+
+    def run(self, S, stream, n_rows):
+        r0 = CTX - n_rows
+        S.sd_project_kv(self.h[r0:], self.wk, self.wv, self.k[r0:], self.v[r0:], stream)
 
 
 # kernels of one step: 5 attention calls (1 launch each when the splits merge
@@ -258,9 +283,24 @@ def hbm_peak(sustained: bool):
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement; MEASURED_PEAKS.json absent)"
 
 
+def bf16_peak(sustained: bool):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        for key in (["bf16_tflops_sustained", "bf16_tflops"] if sustained else ["bf16_tflops"]):
+            if key in mp and mp[key]:
+                v = mp[key]
+                v = v.get("value", v) if isinstance(v, dict) else v
+                return float(v), f"measured ({key}, MEASURED_PEAKS.json)"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement; MEASURED_PEAKS.json absent)"
+
+
 # sources that define each measured kernel (a capture is valid while they are unchanged)
 KERNEL_SOURCES = {
-    "verify_attention": ["attn_tc.cu", "common.cuh", "internal.h"],
+    "verify_attention": ["attn_tc.cu", "tcgen05.cuh", "common.cuh", "internal.h"],
 }
 
 
@@ -511,6 +551,33 @@ def main():
             kernels[name] = {"us_per_call": per_launch * 1e6, "calls_per_step": launches,
                              "algorithmic_bytes_per_call": BYTES[name],
                              "GBps": BYTES[name] / per_launch / 1e9}
+        proj = ProjSet(host["proj"], device)
+        for name, n_rows in (("project_prefill", CTX), ("project_append", APPEND)):
+            evs = []
+            with torch.cuda.stream(stream):
+                for i in range(n_rep):
+                    flush.zero_()
+                    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e_a.record(stream)
+                    proj.run(S, stream, n_rows)
+                    e_b.record(stream)
+                    evs.append((e_a, e_b))
+            torch.cuda.synchronize()
+            per = sum(a.elapsed_time(b) for a, b in evs[3:]) / 1e3 / (n_rep - 3)
+            kernels[name] = {"us_per_call": per * 1e6, "calls_per_step": 0, "kernel_launches_per_call": 1,
+                             "rows": n_rows, "path": S.sd_last_projector_path()}
+        del proj
+        tpk, tsrc = bf16_peak(sustained=False)
+        kp = kernels["project_prefill"]
+        kp["TFLOPs"] = PROJ_PREFILL_FLOPS / (kp["us_per_call"] * 1e-6) / 1e12
+        kp["frac_of_bf16_peak"] = kp["TFLOPs"] / tpk
+        kp["peak_source"] = tsrc
+        kp["note"] = (f"drafter K/V projector over the whole {CTX}-row context ({HD} -> 2 x {HKV * D}), "
+                      "tensor cores; a prefill-time call, not part of the step")
+        ka = kernels["project_append"]
+        ka["algorithmic_bytes_per_call"] = BYTES["project_append"]
+        ka["GBps"] = BYTES["project_append"] / (ka["us_per_call"] * 1e-6) / 1e9
+        ka["note"] = f"the {APPEND} rows one cycle commits, appended to the drafter's context; not part of the step"
         del flush
         kernels["draft_attention"]["note"] = ("average over the 4 layers of one step; they share one projected "
                                               "context, so layers 2-4 read it from L2 and only the first call "
@@ -540,7 +607,8 @@ def main():
                     "algorithmic_bytes_per_launch": BYTES["verify_attention"],
                     "units_per_launch": f"{CTX + T - 1} keys x {HKV} kv heads (K and V bf16, D {D}) + Q + out"}
         for name, kk in kernels.items():
-            kk["frac_of_peak"] = kk["GBps"] / peak
+            if "GBps" in kk:
+                kk["frac_of_peak"] = kk["GBps"] / peak
 
     # ---- end to end: host buffers, copies inside the timed region ----
     e2e = None

@@ -232,6 +232,34 @@ sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, c
 size_t sd_accept_tree_greedy_workspace_size(int B, int T, int V, sd_dtype dtype);
 
 /* ------------------------------------------------------------------------
+ * Drafter K/V projector
+ *
+ * Source: "VFlash-FM" project page, "How VFlash-FM works": the drafter reads
+ * no pixels; the keys and values its block attends to are a learned linear
+ * map of the hidden states the target already keeps for every context
+ * position.  For rows n in [0, N):
+ *   k_out[n][c] = sum_f hidden[n][f] * w_k[c][f]
+ *   v_out[n][c] = sum_f hidden[n][f] * w_v[c][f]      (c < Dout, f < Hd)
+ * fp32 accumulation, rounded once to bf16 (round to nearest even).  Run once
+ * over the whole context (prefill) and then over the rows each cycle commits
+ * (the incremental append), so the drafter's cache grows with the target's.
+ *
+ *   hidden      device bf16 [N, Hd], row stride ld_hidden elements
+ *   w_k, w_v    device bf16 [Dout, Hd] contiguous (a linear layer's weight)
+ *   k_out/v_out device bf16 [N, Dout], row stride ld_out elements: with a
+ *               [B, S, Hkv, D] cache, Dout = Hkv * D and k_out points at the
+ *               first row to write; rows outside [0, N) are not touched
+ *   dtype       SD_BF16 (SD_FP32 returns SD_ERR_UNSUPPORTED)
+ * Requires Hd % 8 == 0, Dout % 32 == 0, ld_hidden >= Hd and ld_out >= Dout,
+ * both multiples of 8, every pointer 16-byte aligned, 0 <= N <= 2^21 (N = 0
+ * launches nothing).  Up to 32 rows run on CUDA cores (the weights are
+ * read once); more rows run as a tensor-core GEMM.  No workspace.
+ * ------------------------------------------------------------------------ */
+sd_status sd_project_kv(const void *hidden, int64_t ld_hidden, const void *w_k, const void *w_v,
+                        int N, int Hd, int Dout, void *k_out, void *v_out, int64_t ld_out,
+                        sd_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------------------
  * Greedy acceptance without a caller workspace
  *
  * No counterpart in the method's pages: this is a convenience of the library.
@@ -288,6 +316,16 @@ int sd_last_attention_path(int *n_splits);
  * a separate merge kernel followed.  No counterpart on the pages: a count for
  * measurement. */
 int sd_last_attention_launches(void);
+
+/* Projector kernel selection, process-wide, for tests and measurement:
+ * 0 = automatic (above), 1 = CUDA cores for every N, 2 = tensor cores for
+ * every N >= 1 (calls it cannot serve return SD_ERR_UNSUPPORTED).  Other
+ * values select 0.  Returns the previous setting. */
+int sd_set_projector_path(int path);
+
+/* Which projector kernel the last sd_project_kv on this thread launched:
+ * 1 or 2 as above, 0 if none. */
+int sd_last_projector_path(void);
 
 #ifdef __cplusplus
 }

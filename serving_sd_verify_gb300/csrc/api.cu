@@ -24,6 +24,8 @@ thread_local int g_last_path = 0;
 thread_local int g_last_splits = 0;
 thread_local int g_last_launches = 0;
 std::atomic<int> g_force_path{0};
+std::atomic<int> g_force_proj_path{0};
+thread_local int g_last_proj_path = 0;
 
 constexpr size_t kHeader = 256;  // counters; zero between calls
 constexpr int kMaxDevices = 64;
@@ -462,6 +464,52 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     if (e != cudaSuccess) return cuda_fail(e, "sampled accept launch");
     return SD_OK;
 }
+
+sd_status sd_project_kv(const void *hidden, int64_t ld_hidden, const void *w_k, const void *w_v, int N, int Hd,
+                        int Dout, void *k_out, void *v_out, int64_t ld_out, sd_dtype dtype, void *stream) {
+    g_last_proj_path = 0;
+    if (dtype == SD_FP32) return fail(SD_ERR_UNSUPPORTED, "the projector takes bf16 tensors only");
+    if (dtype != SD_BF16) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if (N < 0 || N > (1 << 21)) return fail(SD_ERR_INVALID_ARG, "need 0 <= N <= 2^21");
+    if (Hd < 8 || Hd % 8 != 0 || Hd > (1 << 20)) return fail(SD_ERR_INVALID_ARG, "need Hd a positive multiple of 8");
+    if (Dout < 32 || Dout % 32 != 0 || Dout > (1 << 20))
+        return fail(SD_ERR_INVALID_ARG, "need Dout a positive multiple of 32");
+    if (ld_hidden < Hd || ld_hidden % 8 != 0 || ld_out < Dout || ld_out % 8 != 0)
+        return fail(SD_ERR_INVALID_ARG, "row strides must cover a row and be multiples of 8 elements");
+    if (N == 0) return SD_OK;
+    if (!hidden || !w_k || !w_v || !k_out || !v_out) return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(hidden) || !aligned16(w_k) || !aligned16(w_v) || !aligned16(k_out) || !aligned16(v_out))
+        return fail(SD_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+    ProjParams p = {};
+    p.h = static_cast<const __nv_bfloat16 *>(hidden);
+    p.wk = static_cast<const __nv_bfloat16 *>(w_k);
+    p.wv = static_cast<const __nv_bfloat16 *>(w_v);
+    p.k_out = static_cast<__nv_bfloat16 *>(k_out);
+    p.v_out = static_cast<__nv_bfloat16 *>(v_out);
+    p.ld_h = (long)ld_hidden; p.ld_out = (long)ld_out;
+    p.N = N; p.Hd = Hd; p.Dout = Dout;
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    const int force = g_force_proj_path.load();
+    int path = N <= kProjSmallRows ? 1 : 2;
+    if (force == 1) path = 1;
+    if (force == 2) path = 2;
+    if (path == 2 && !project_tc_supported()) {
+        if (force == 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core projector needs sm_103 and 200 KB shared memory");
+        path = 1;
+    }
+    cudaError_t e = launch_project(p, path, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "projector launch");
+    g_last_proj_path = path;
+    return SD_OK;
+}
+
+int sd_set_projector_path(int path) {
+    if (path < 0 || path > 2) path = 0;
+    return g_force_proj_path.exchange(path);
+}
+
+int sd_last_projector_path(void) { return g_last_proj_path; }
 
 sd_status sd_philox4x32_10(const uint32_t *counters, uint64_t key, uint32_t *out, int64_t n, void *stream) {
     if (n < 0) return fail(SD_ERR_INVALID_ARG, "n must be >= 0");

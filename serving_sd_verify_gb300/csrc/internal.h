@@ -2,6 +2,7 @@
 // Not installed; callers use include/sd_verify.h.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -109,6 +110,22 @@ constexpr int kDrawChunkMax = 4096;  // pass 2 chunk bound: 16 elements per thre
 constexpr int kGreedyChunkMaxBf16 = 16384;
 constexpr int kGreedyChunkMaxF32 = 8192;
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);
+
+// Drafter K/V projector: k_out[n] = h[n] . wk^T, v_out[n] = h[n] . wv^T for
+// rows n < N; h [N, Hd] row stride ld_h, wk / wv [Dout, Hd] contiguous,
+// outputs row stride ld_out (elements).
+struct ProjParams {
+    const __nv_bfloat16 *h;
+    const __nv_bfloat16 *wk, *wv;
+    __nv_bfloat16 *k_out, *v_out;
+    long ld_h, ld_out;
+    int N, Hd, Dout;
+    unsigned int *fault;
+};
+constexpr int kProjSmallRows = 32;  // rows per CTA of the CUDA-core projector
+// path: 1 CUDA cores, 2 tensor cores (requires project_tc_supported())
+cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st);
+bool project_tc_supported();
 
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int64_t n,
                           cudaStream_t st);

@@ -1,0 +1,301 @@
+// Drafter K/V projector: K = H . W_k^T and V = H . W_v^T, bf16 in, fp32
+// accumulation, bf16 out, written row by row into the drafter's context cache.
+//
+// Source: "VFlash-FM" project page, "How VFlash-FM works": the drafter never
+// reads the video; its keys and values are a linear map of the hidden states
+// the target has already cached for every context position.  It runs once over
+// the whole context (prefill) and then, every cycle, over the few positions
+// just committed (the incremental append).
+//
+// Prefill (many rows): a tcgen05 GEMM.  One CTA per (128-row tile, 256-column
+// tile of [K | V]); the hidden-state and weight tiles (64 features deep,
+// 128-byte swizzle) stream through a 4-stage TMA ring; one thread issues
+// M128 N256 K16 MMAs into a 256-column fp32 accumulator in tensor memory; four
+// warps convert it to bf16 and store it.
+// Append (a few rows): bound by reading the weights once, so CUDA cores: a
+// warp per output column, lanes over the features, kProjSmallRows rows per CTA.
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace sdv {
+
+namespace {
+
+constexpr int kPjThreads = 256;   // warp 0 TMA, warp 1 MMA + tensor memory, warps 4-7 epilogue
+constexpr int kPjM = 128, kPjN = 256, kPjK = 64;
+constexpr int kPjStages = 4;
+constexpr int kPjABytes = kPjM * 128;   // [128 rows x 64 features] bf16
+constexpr int kPjBBytes = kPjN * 128;   // [256 out-columns x 64 features] bf16
+constexpr int kPjStageBytes = kPjABytes + kPjBBytes;
+constexpr int kPjOffBar = kPjStages * kPjStageBytes;
+constexpr int kPjNumBars = 2 * kPjStages + 1;
+constexpr int kPjOffMisc = kPjOffBar + 8 * kPjNumBars;
+constexpr int kPjSmem = kPjOffMisc + 16 + 1024;
+static_assert(kPjSmem <= 227 * 1024, "shared memory per CTA");
+
+constexpr int kSmallWarps = 8;
+
+__global__ void __launch_bounds__(kPjThreads, 1)
+project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wk,
+                  const __grid_constant__ CUtensorMap tm_wv, const ProjParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *sbase = smem_raw + (base - raw_u32);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int mt = blockIdx.x, nt = blockIdx.y;
+    const int n_per = (p.Dout + kPjN - 1) / kPjN;   // column tiles per matrix
+    const bool is_v = nt >= n_per;
+    const int col0 = (is_v ? nt - n_per : nt) * kPjN;
+    const CUtensorMap *tw = is_v ? &tm_wv : &tm_wk;
+    const int nk = (p.Hd + kPjK - 1) / kPjK;
+
+    const uint32_t bar0 = base + kPjOffBar;
+    auto full_bar = [&](int i) { return bar0 + 8u * i; };
+    auto empty_bar = [&](int i) { return bar0 + 8u * (kPjStages + i); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kPjStages);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + kPjOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + kPjOffMisc + 8);
+
+    if (tid == 0) {
+        for (int i = 0; i < kPjStages; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_h)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tw)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)), "r"(256) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+#if __CUDA_ARCH__ >= 900
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kt = 0; kt < nk; ++kt) {
+                const int st = kt % kPjStages;
+                if (kt >= kPjStages &&
+                    !mbar_wait(empty_bar(st), ((kt / kPjStages) - 1) & 1, abort_flag, p.fault))
+                    break;
+                const uint32_t a = base + st * kPjStageBytes;
+                mbar_arrive_expect_tx(full_bar(st), (uint32_t)kPjStageBytes);
+                tma_load_2d(a, &tm_h, full_bar(st), kt * kPjK, mt * kPjM);
+                tma_load_2d(a + kPjABytes, tw, full_bar(st), kt * kPjK, col0);
+                issued = kt + 1;
+            }
+            if (*abort_flag)  // let the copies already issued land before the CTA exits
+                for (int u = max(0, issued - kPjStages); u < issued; ++u)
+                    mbar_wait(full_bar(u % kPjStages), (u / kPjStages) & 1, nullptr, p.fault);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kPjM, kPjN, false);
+            for (int kt = 0; kt < nk; ++kt) {
+                const int st = kt % kPjStages;
+                if (!mbar_wait(full_bar(st), (kt / kPjStages) & 1, abort_flag, p.fault)) break;
+                tc_fence_after();
+                const uint32_t a = base + st * kPjStageBytes, bm = a + kPjABytes;
+#pragma unroll
+                for (int kk = 0; kk < kPjK / 16; ++kk)
+                    umma_ss(tmem, sw128_desc(a + kk * 32, 16, 1024), sw128_desc(bm + kk * 32, 16, 1024), idesc,
+                            (kt > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(empty_bar(st));
+            }
+            umma_commit(done_bar);  // every MMA issued, complete or not, before the epilogue and teardown
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, p.fault));
+        tc_fence_after();
+        const int r = (warp - 4) * 32 + lane;   // tensor-memory lane = tile row
+        const long grow = (long)mt * kPjM + r;
+        const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        __nv_bfloat16 *out = (is_v ? p.v_out : p.k_out) + grow * p.ld_out + col0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kPjN; c0 += 32) {
+            uint32_t acc[32];
+            tmem_ld32_async(taddr + (uint32_t)c0, acc);   // warp-wide: before any divergence
+            tmem_ld_wait();
+            tmem_ld_bind(acc);
+            if (ok && !*abort_flag && grow < p.N && col0 + c0 < p.Dout) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const __nv_bfloat162 h2 =
+                        __floats2bfloat162_rn(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
+                    pk[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(out + c0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        // the epilogue waited on done_bar: every MMA has completed
+        if (*abort_flag && lane == 0) mbar_wait(done_bar, 0, nullptr, p.fault);
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+    }
+}
+
+// Few rows: out[n][c] = sum_k h[n][k] w[c][k], a warp per output column c of
+// [K | V], lanes over 8-feature vectors; CTA (x, y) takes columns
+// [8x, 8x + 8) and rows [NR y, NR y + NR).  The weight row is read from memory
+// once per row group; the hidden rows are shared by the CTA's warps through L1.
+template <int NR>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+project_small_kernel(const ProjParams p) {
+#if __CUDA_ARCH__ >= 900
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+    const int lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kSmallWarps + (threadIdx.x >> 5);
+    if (c >= 2 * p.Dout) return;
+    const bool is_v = c >= p.Dout;
+    const int cc = is_v ? c - p.Dout : c;
+    const int n0 = blockIdx.y * NR;
+    const int nr = min(NR, p.N - n0);
+    const __nv_bfloat16 *w = (is_v ? p.wv : p.wk) + (long)cc * p.Hd;
+    const __nv_bfloat16 *h = p.h + (long)n0 * p.ld_h;
+    float acc[NR];
+#pragma unroll
+    for (int n = 0; n < NR; ++n) acc[n] = 0.f;
+    for (int k = lane * 8; k < p.Hd; k += 256) {
+        float wf[8];
+        unpack_bf16x8(ld_stream_u4(w + k), wf);
+#pragma unroll
+        for (int n = 0; n < NR; ++n) {
+            if (n < nr) {
+                float hf[8];
+                Elem<__nv_bfloat16>::load_vec(h + (long)n * p.ld_h + k, hf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[n] = fmaf(hf[e], wf[e], acc[n]);
+            }
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NR; ++n) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], o);
+    }
+    if (lane < nr) {
+        float v = acc[0];
+#pragma unroll
+        for (int n = 1; n < NR; ++n) v = lane == n ? acc[n] : v;
+        (is_v ? p.v_out : p.k_out)[(long)(n0 + lane) * p.ld_out + cc] = __float2bfloat16_rn(v);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_pj() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D map over a row-major bf16 matrix [rows, cols] with row stride ld (elements);
+// box: 64 columns x box_rows rows, 128-byte swizzle
+bool make_map_2d(CUtensorMap *m, const void *ptr, long rows, long cols, long ld, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn_pj();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows}, estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K, typename P>
+cudaError_t launch_pdl_pj(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const P &args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+}  // namespace
+
+bool project_tc_supported() {
+    if (!encode_fn_pj()) return false;
+    int dev = 0, optin = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    return optin >= kPjSmem && major == 10 && minor == 3;
+}
+
+cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st) {
+    if (p.N <= 0) return cudaSuccess;
+    if (path == 1) {
+        const int nr = p.N <= 8 ? 8 : p.N <= 16 ? 16 : kProjSmallRows;
+        const dim3 grid((unsigned)((2 * p.Dout + kSmallWarps - 1) / kSmallWarps), (unsigned)((p.N + nr - 1) / nr));
+        const dim3 block(kSmallWarps * 32);
+        if (nr == 8) return launch_pdl_pj(project_small_kernel<8>, grid, block, 0, st, p);
+        if (nr == 16) return launch_pdl_pj(project_small_kernel<16>, grid, block, 0, st, p);
+        return launch_pdl_pj(project_small_kernel<kProjSmallRows>, grid, block, 0, st, p);
+    }
+    alignas(64) CUtensorMap mh, mk, mv;
+    if (!make_map_2d(&mh, p.h, p.N, p.Hd, p.ld_h, kPjM)) return cudaErrorInvalidValue;
+    if (!make_map_2d(&mk, p.wk, p.Dout, p.Hd, p.Hd, kPjN)) return cudaErrorInvalidValue;
+    if (!make_map_2d(&mv, p.wv, p.Dout, p.Hd, p.Hd, kPjN)) return cudaErrorInvalidValue;
+    static bool opted_in[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+        e = cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPjSmem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+    }
+    const dim3 grid((unsigned)((p.N + kPjM - 1) / kPjM), (unsigned)(2 * ((p.Dout + kPjN - 1) / kPjN)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kPjThreads);
+    cfg.dynamicSmemBytes = kPjSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, project_tc_kernel, mh, mk, mv, p);
+}
+
+}  // namespace sdv

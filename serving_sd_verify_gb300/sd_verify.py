@@ -29,6 +29,7 @@ SYMBOLS = [
     "sd_accept_sample", "sd_accept_sample_workspace_size", "sd_accept_greedy_noalloc",
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
+    "sd_project_kv", "sd_set_projector_path", "sd_last_projector_path",
 ]
 
 
@@ -101,6 +102,12 @@ def load():
     lib.sd_last_attention_path.restype = _i
     lib.sd_last_attention_launches.argtypes = []
     lib.sd_last_attention_launches.restype = _i
+    lib.sd_project_kv.argtypes = [_vp, ctypes.c_int64, _vp, _vp, _i, _i, _i, _vp, _vp, ctypes.c_int64, _i, _vp]
+    lib.sd_project_kv.restype = _i
+    lib.sd_set_projector_path.argtypes = [_i]
+    lib.sd_set_projector_path.restype = _i
+    lib.sd_last_projector_path.argtypes = []
+    lib.sd_last_projector_path.restype = _i
     _lib = lib
     return lib
 
@@ -279,6 +286,32 @@ def sd_accept_sample(draft_ids, draft_probs, target_logits, temperature, philox_
                                    _dt(target_logits), float(temperature), int(philox_seed),
                                    int(philox_offset), _p(n_accepted), _p(next_id), _p(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sd_project_kv(hidden, w_k, w_v, k_out, v_out, stream=None):
+    """hidden bf16 [N, Hd] (rows may be strided); w_k, w_v bf16 [Dout, Hd]
+    contiguous; k_out, v_out bf16 [N, Dout] (rows may be strided, e.g. a slice
+    of a [S, Hkv * D] cache view)."""
+    _need_cuda(hidden, w_k, w_v, k_out, v_out)
+    N, Hd = hidden.shape
+    Dout = w_k.shape[0]
+    if w_k.shape != (Dout, Hd) or w_v.shape != (Dout, Hd) or not (w_k.is_contiguous() and w_v.is_contiguous()):
+        raise ValueError("w_k and w_v are contiguous [Dout, Hd]")
+    if k_out.shape != (N, Dout) or v_out.shape != (N, Dout) or k_out.stride() != v_out.stride():
+        raise ValueError("k_out and v_out are [N, Dout] with equal strides")
+    if hidden.stride(1) != 1 or k_out.stride(1) != 1:
+        raise ValueError("the last axis must be contiguous")
+    dt = _dt(hidden)
+    _check(load().sd_project_kv(_p(hidden), hidden.stride(0), _p(w_k), _p(w_v), N, Hd, Dout, _p(k_out), _p(v_out),
+                                k_out.stride(0), dt, _stream(stream)))
+
+
+def sd_set_projector_path(path: int) -> int:
+    return load().sd_set_projector_path(int(path))
+
+
+def sd_last_projector_path() -> int:
+    return int(load().sd_last_projector_path())
 
 
 def sd_philox4x32_10(counters, key, out, stream=None):
