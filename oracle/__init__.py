@@ -87,6 +87,14 @@ def _load():
     lib.oracle_project_rows.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                         ctypes.c_long, _dp]
     lib.oracle_project_rows.restype = ctypes.c_int
+    lib.oracle_commit_tokens.argtypes = [_ip, ctypes.c_int, ctypes.c_void_p, _ip, _ip, ctypes.c_int, ctypes.c_int,
+                                         _ip, ctypes.c_int, ctypes.c_void_p, _ip, _ip, ctypes.c_int, _ip, _ip]
+    lib.oracle_commit_tokens.restype = ctypes.c_int
+    _u8 = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+    lib.oracle_compact_tree_kv.argtypes = [_u8, _u8, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+                                           _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, _ip]
+    lib.oracle_compact_tree_kv.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -192,6 +200,60 @@ def project_rows(hidden, weight, rows=None):
     if rc != 0:
         raise ValueError("oracle_project_rows rejected its arguments")
     return out
+
+
+def commit_tokens(proposals, n_accepted, next_token, ctx_len, out_tokens, out_len, ctx_cap, path=None):
+    """Commit of a verified block on copies of the state.  proposals [B, P]
+    (chain: the T-1 drafts; tree: the T node tokens, with path [B, T] the kept
+    nodes by depth); n_accepted, next_token, ctx_len, out_len [B];
+    out_tokens [B, out_cap].  Returns a dict with the new ctx_len, draft_ctx
+    (= ctx_len - 1), out_tokens, out_len, anchor and status (1 = rejected, left
+    unchanged)."""
+    prop = np.ascontiguousarray(_i32(proposals))
+    B = prop.shape[0]
+    ps = prop.shape[1] if prop.ndim == 2 else 0
+    prop = prop.reshape(-1) if prop.size else np.zeros(1, dtype=np.int32)
+    n = np.ascontiguousarray(_i32(n_accepted).reshape(B))
+    nx = np.ascontiguousarray(_i32(next_token).reshape(B))
+    ctx = np.array(_i32(ctx_len).reshape(B), dtype=np.int32)
+    toks = np.array(_i32(out_tokens), dtype=np.int32)
+    out_cap = toks.shape[1]
+    olen = np.array(_i32(out_len).reshape(B), dtype=np.int32)
+    dctx = np.array(ctx - 1, dtype=np.int32)
+    anchor = np.full(B, -1, dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    if path is not None:
+        pa = np.ascontiguousarray(_i32(path))
+        T = pa.shape[1]
+        pth = _ptr(pa.reshape(-1))
+    else:
+        pa, T, pth = None, ps + 1, None
+    rc = _load().oracle_commit_tokens(prop, ps, pth, n, nx, B, T, ctx, int(ctx_cap), _ptr(dctx), toks, olen,
+                                      out_cap, anchor, status)
+    if rc != 0:
+        raise ValueError("oracle_commit_tokens rejected its arguments")
+    return {"ctx_len": ctx, "draft_ctx": dctx, "out_tokens": toks, "out_len": olen, "anchor": anchor,
+            "status": status}
+
+
+def compact_tree_kv(k_cache, v_cache, ctx_len, path, n_accepted):
+    """Tree commit of the target's K/V cache on copies: k_cache, v_cache
+    [B, S, Hkv, D] numpy arrays of any element type (moved as raw bytes);
+    ctx_len (before the commit), n_accepted [B]; path [B, T].  Returns
+    (k, v, status)."""
+    k = np.array(k_cache, copy=True, order="C")
+    v = np.array(v_cache, copy=True, order="C")
+    B, S, Hkv, D = k.shape
+    pa = np.ascontiguousarray(_i32(path))
+    T = pa.shape[1]
+    status = np.zeros(B, dtype=np.int32)
+    kb, vb = k.view(np.uint8).reshape(-1), v.view(np.uint8).reshape(-1)
+    rc = _load().oracle_compact_tree_kv(kb, vb, S * Hkv * D, Hkv * D, D, k.itemsize,
+                                        np.ascontiguousarray(_i32(ctx_len).reshape(B)), pa.reshape(-1),
+                                        np.ascontiguousarray(_i32(n_accepted).reshape(B)), B, T, S, Hkv, D, status)
+    if rc != 0:
+        raise ValueError("oracle_compact_tree_kv rejected its arguments")
+    return k, v, status
 
 
 def lse_merge(o_parts, lse_parts):

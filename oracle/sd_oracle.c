@@ -461,3 +461,93 @@ int oracle_accept_sample(const int *draft, const double *q, const double *logits
     free(p); free(r);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Commit / rollback                                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Commit of a verified block ("VFlash-FM" project page, "How VFlash-FM
+ * works", the worked cycle: the accepted prefix and the target's own token at
+ * the first disagreement are committed, everything after them is dropped,
+ * and the next cycle starts from that token as its anchor).  Sequence b with
+ * n = n_acc[b] kept proposals:
+ *   kept proposal i (i < n): chain (path NULL) prop[b*ps + i]; tree
+ *     prop[b*ps + path[b*T + i]] (path lists the kept nodes by depth)
+ *   out_tokens[b*out_cap + out_len[b] + i] = kept proposal i, then
+ *   out_tokens[b*out_cap + out_len[b] + n] = next_tok[b]; out_len[b] += n + 1
+ *   ctx_len[b] += n + 1: ctx counts the anchor, so the new anchor (next_tok)
+ *     sits at position ctx_len[b] - 1
+ *   draft_ctx[b] = ctx_len[b] - 1 when given: the drafter's context is every
+ *     position before the anchor
+ *   anchor[b] = next_tok[b]
+ * A sequence with n outside [0, T-1], a kept node outside [1, T), or a commit
+ * that would pass ctx_cap or out_cap is left as it was and gets status[b] = 1;
+ * the others get 0.
+ */
+int oracle_commit_tokens(const int *prop, int ps, const int *path, const int *n_acc, const int *next_tok,
+                         int B, int T, int *ctx_len, int ctx_cap, int *draft_ctx, int *out_tokens, int *out_len,
+                         int out_cap, int *anchor, int *status) {
+    if (B < 1 || T < 1 || ps < 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int n = n_acc[b];
+        int ok = n >= 0 && n <= T - 1;
+        if (ok && path)
+            for (int i = 0; i < n; ++i)
+                if (path[b * T + i] < 1 || path[b * T + i] >= T) ok = 0;
+        if (ok && ((long)ctx_len[b] + n + 1 > ctx_cap || (long)out_len[b] + n + 1 > out_cap)) ok = 0;
+        status[b] = ok ? 0 : 1;
+        if (!ok) continue;
+        int *dst = out_tokens + (long)b * out_cap + out_len[b];
+        for (int i = 0; i < n; ++i) dst[i] = path ? prop[(long)b * ps + path[b * T + i]] : prop[(long)b * ps + i];
+        dst[n] = next_tok[b];
+        out_len[b] += n + 1;
+        ctx_len[b] += n + 1;
+        if (draft_ctx) draft_ctx[b] = ctx_len[b] - 1;
+        anchor[b] = next_tok[b];
+    }
+    return 0;
+}
+
+/*
+ * Tree commit in the target's KV cache (same passage: only the accepted path
+ * survives and the next block follows it).  Block slot k of sequence b sits
+ * at cache position ctx_len[b] - 1 + k (the anchor at k = 0), ctx_len taken
+ * before the commit.  For depth d = 1..n_acc[b], position ctx-1+d receives
+ * the row that was at position ctx-1+path[b*T + d-1] (every kv head, K and
+ * V); every other position keeps its row.  Rows move as raw bytes: es bytes
+ * per element, strides sb, ss, sh in elements, D contiguous.  A sequence whose
+ * block does not fit the S positions, whose n is outside [0, T-1] or whose
+ * kept node is outside [1, T) is left alone with status[b] = 1.
+ */
+int oracle_compact_tree_kv(uint8_t *kc, uint8_t *vc, long sb, long ss, long sh, int es, const int *ctx_len,
+                           const int *path, const int *n_acc, int B, int T, int S, int Hkv, int D, int *status) {
+    if (B < 1 || T < 1 || Hkv < 1 || D < 1 || es < 1) return -1;
+    const long row = (long)D * es;
+    uint8_t *tmp = (uint8_t *)malloc((size_t)T * Hkv * row + 1);
+    if (!tmp) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int n = n_acc[b], c = ctx_len[b];
+        int ok = n >= 0 && n <= T - 1 && c >= 1 && (long)c - 1 + T <= S;
+        for (int i = 0; ok && i < n; ++i)
+            if (path[b * T + i] < 1 || path[b * T + i] >= T) ok = 0;
+        status[b] = ok ? 0 : 1;
+        if (!ok) continue;
+        for (int pass = 0; pass < 2; ++pass) {
+            uint8_t *cache = pass == 0 ? kc : vc;
+            /* read every kept row first, then write them in depth order */
+            for (int d = 1; d <= n; ++d)
+                for (int h = 0; h < Hkv; ++h) {
+                    const long src = ((long)b * sb + (long)(c - 1 + path[b * T + d - 1]) * ss + (long)h * sh) * es;
+                    memcpy(tmp + ((long)(d - 1) * Hkv + h) * row, cache + src, (size_t)row);
+                }
+            for (int d = 1; d <= n; ++d)
+                for (int h = 0; h < Hkv; ++h) {
+                    const long dst = ((long)b * sb + (long)(c - 1 + d) * ss + (long)h * sh) * es;
+                    memcpy(cache + dst, tmp + ((long)(d - 1) * Hkv + h) * row, (size_t)row);
+                }
+        }
+    }
+    free(tmp);
+    return 0;
+}
