@@ -481,9 +481,9 @@ int oracle_accept_sample(const int *draft, const double *q, const double *logits
  *   draft_ctx[b] = ctx_len[b] - 1 when given: the drafter's context is every
  *     position before the anchor
  *   anchor[b] = next_tok[b]
- * A sequence with n outside [0, T-1], a kept node outside [1, T), or a commit
- * that would pass ctx_cap or out_cap is left as it was and gets status[b] = 1;
- * the others get 0.
+ * A sequence with n outside [0, T-1], a kept node outside [1, T), ctx_len < 1
+ * (it counts the anchor), out_len < 0, or a commit that would pass ctx_cap or
+ * out_cap is left as it was and gets status[b] = 1; the others get 0.
  */
 int oracle_commit_tokens(const int *prop, int ps, const int *path, const int *n_acc, const int *next_tok,
                          int B, int T, int *ctx_len, int ctx_cap, int *draft_ctx, int *out_tokens, int *out_len,
@@ -495,6 +495,7 @@ int oracle_commit_tokens(const int *prop, int ps, const int *path, const int *n_
         if (ok && path)
             for (int i = 0; i < n; ++i)
                 if (path[b * T + i] < 1 || path[b * T + i] >= T) ok = 0;
+        if (ok && (ctx_len[b] < 1 || out_len[b] < 0)) ok = 0; /* ctx counts the anchor: at least 1 */
         if (ok && ((long)ctx_len[b] + n + 1 > ctx_cap || (long)out_len[b] + n + 1 > out_cap)) ok = 0;
         status[b] = ok ? 0 : 1;
         if (!ok) continue;
