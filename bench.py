@@ -178,6 +178,61 @@ class ProjSet:
         S.sd_project_kv(self.h[r0:], self.wk, self.wv, self.k[r0:], self.v[r0:], stream)
 
 
+ROOM = 1024         # spare cache positions of the cycle measurement (the context grows each replay)
+
+
+class CycleSet:
+    """A whole speculative cycle on resident state, captured in one CUDA
+    graph: the drafter's 4 layers, the target verify, greedy acceptance, the
+    drafter-context append of the committed rows and the commit (ctx_len,
+    tokens, anchor) -- nothing returns to the host between cycles.  The caches
+    hold ROOM spare positions, so every replay really extends the context."""
+
+    def __init__(self, ds, proj, device, S):
+        import torch
+        bf = torch.bfloat16
+        self.ds, self.proj = ds, proj
+        self.k = torch.zeros(1, CTX + ROOM + T - 1, HKV, D, dtype=bf, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.k[:, :CTX + T - 1] = ds.k
+        self.v[:, :CTX + T - 1] = ds.v
+        self.kc = torch.zeros(1, CTX + ROOM, HKV, D, dtype=bf, device=device)
+        self.vc = torch.zeros_like(self.kc)
+        self.kc[:, :CTX] = ds.kc
+        self.vc[:, :CTX] = ds.vc
+        self.ctx, self.dctx = ds.ctx.clone(), ds.nctx.clone()
+        g = torch.Generator(device="cpu").manual_seed(77)
+        self.hid = torch.randn(1, T, HD, generator=g).to(bf).to(device)
+        self.n = torch.zeros(1, dtype=torch.int32, device=device)
+        self.c = torch.zeros(1, dtype=torch.int32, device=device)
+        self.toks = torch.full((1, 64 * T), -1, dtype=torch.int32, device=device)
+        self.olen = torch.zeros(1, dtype=torch.int32, device=device)
+        self.anchor = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws_v = S.workspace(S.sd_verify_attention_workspace_size(1, T, HQ, HKV, D, CTX + ROOM), device)
+        self.ws_d = S.workspace(S.sd_draft_block_attention_workspace_size(1, T, HQ, HKV, D, CTX + ROOM), device)
+        self.launches = 0
+
+    def commit(self, S, stream):
+        kcv = self.kc.view(1, CTX + ROOM, HKV * D)
+        vcv = self.vc.view(1, CTX + ROOM, HKV * D)
+        S.sd_project_kv_commit(self.hid, self.proj.wk, self.proj.wv, self.n, self.dctx, kcv, vcv, stream=stream)
+        S.sd_commit_tokens(self.ds.draft, self.n, self.c, self.ctx, self.toks, self.olen, self.anchor, CTX + ROOM,
+                           draft_ctx=self.dctx, stream=stream)
+
+    def cycle(self, S, stream):
+        ds = self.ds
+        launches = 0
+        for li, (q, kb, vb) in enumerate(ds.layers):
+            S.sd_draft_block_attention(q, self.kc, self.vc, self.dctx, CTX + ROOM, kb, vb, ds.dout[li], 1.0,
+                                       self.ws_d, stream)
+            launches += S.sd_last_attention_launches()
+        S.sd_verify_attention(ds.q, self.k, self.v, self.ctx, CTX + ROOM, ds.out, 1.0, self.ws_v, stream)
+        launches += S.sd_last_attention_launches()
+        S.sd_accept_greedy(ds.draft, ds.logits, self.n, self.c, ds.ws_g, stream)
+        self.commit(S, stream)
+        self.launches = launches + 3
+
+
 # kernels of one step: 5 attention calls (1 launch each when the splits merge
 # inside the split kernel, else 2; set from the library after a warm-up
 # step), greedy 1, sampled 2
@@ -553,20 +608,64 @@ def main():
                              "GBps": BYTES[name] / per_launch / 1e9}
         proj = ProjSet(host["proj"], device)
         for name, n_rows in (("project_prefill", CTX), ("project_append", APPEND)):
+            # one call captured in a graph, so the binding's host time stays
+            # out of the event window
+            with torch.cuda.stream(stream):
+                proj.run(S, stream, n_rows)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                proj.run(S, stream, n_rows)
             evs = []
             with torch.cuda.stream(stream):
                 for i in range(n_rep):
                     flush.zero_()
                     e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e_a.record(stream)
-                    proj.run(S, stream, n_rows)
+                    g.replay()
                     e_b.record(stream)
                     evs.append((e_a, e_b))
             torch.cuda.synchronize()
+            del g
             per = sum(a.elapsed_time(b) for a, b in evs[3:]) / 1e3 / (n_rep - 3)
             kernels[name] = {"us_per_call": per * 1e6, "calls_per_step": 0, "kernel_launches_per_call": 1,
                              "rows": n_rows, "path": S.sd_last_projector_path()}
-        del proj
+        # a whole cycle (draft x4, verify, accept, append, commit) and the
+        # commit alone (append + commit), each one graph replay after an L2 flush
+        cyc = CycleSet(sets[0], proj, device, S)
+        for name, fn in (("spec_cycle", cyc.cycle), ("commit", cyc.commit)):
+            with torch.cuda.stream(stream):
+                fn(S, stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(S, stream)
+            ctx_a = int(cyc.ctx.item())
+            evs = []
+            with torch.cuda.stream(stream):
+                for i in range(n_rep):
+                    flush.zero_()
+                    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e_a.record(stream)
+                    g.replay()
+                    e_b.record(stream)
+                    evs.append((e_a, e_b))
+            torch.cuda.synchronize()
+            del g
+            per = sum(a.elapsed_time(b) for a, b in evs[3:]) / 1e3 / (n_rep - 3)
+            grown = int(cyc.ctx.item()) - ctx_a
+            kernels[name] = {"us_per_call": per * 1e6, "calls_per_step": 0,
+                             "kernel_launches_per_call": cyc.launches if name == "spec_cycle" else 2,
+                             "tokens_committed_per_call": grown / n_rep}
+        assert S.sd_fault_word() == 0, "device guard fired in the cycle measurement"
+        kc_ = kernels["spec_cycle"]
+        kc_["committed_tokens_per_s"] = kc_["tokens_committed_per_call"] / (kc_["us_per_call"] * 1e-6)
+        kc_["note"] = ("one speculative cycle in one CUDA graph: 4 drafter layers, target verify, greedy "
+                       "acceptance, drafter-context append of the committed rows, commit (ctx_len, tokens, "
+                       "anchor); no host round trip; the context grows by the committed tokens every replay")
+        kernels["commit"]["note"] = ("the device-side commit alone: projector append of the committed rows "
+                                     "(weights read once) + token / length update")
+        del cyc, proj
         tpk, tsrc = bf16_peak(sustained=False)
         kp = kernels["project_prefill"]
         kp["TFLOPs"] = PROJ_PREFILL_FLOPS / (kp["us_per_call"] * 1e-6) / 1e12

@@ -252,12 +252,89 @@ size_t sd_accept_tree_greedy_workspace_size(int B, int T, int V, sd_dtype dtype)
  *   dtype       SD_BF16 (SD_FP32 returns SD_ERR_UNSUPPORTED)
  * Requires Hd % 8 == 0, Dout % 32 == 0, ld_hidden >= Hd and ld_out >= Dout,
  * both multiples of 8, every pointer 16-byte aligned, 0 <= N <= 2^21 (N = 0
- * launches nothing).  Up to 32 rows run on CUDA cores (the weights are
- * read once); more rows run as a tensor-core GEMM.  No workspace.
+ * launches nothing).  Up to 16 rows run on CUDA cores (the weights are read
+ * once, the rows staged in shared memory: 16 * Hd * 2 bytes <= 200 KB, else
+ * 8 rows per CTA); more rows run as a tensor-core GEMM.  No workspace.
  * ------------------------------------------------------------------------ */
 sd_status sd_project_kv(const void *hidden, int64_t ld_hidden, const void *w_k, const void *w_v,
                         int N, int Hd, int Dout, void *k_out, void *v_out, int64_t ld_out,
                         sd_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Commit of a verified block, on the device
+ *
+ * Source: "VFlash-FM" project page, "How VFlash-FM works" and its worked
+ * cycle: the accepted prefix and the target's own token at the first
+ * disagreement are committed, the rest of the block is discarded, and the
+ * next cycle starts from that token as its anchor.  These three calls read
+ * the acceptance results from device memory, so a whole cycle -- draft,
+ * verify, accept, append, commit -- can be enqueued (or captured in one CUDA
+ * graph) and repeated with no host round trip.  Per cycle, in stream order:
+ * sd_compact_tree_kv (trees only), sd_project_kv_commit, then
+ * sd_commit_tokens (the first two read ctx_len / draft_ctx before the third
+ * advances them).  Guards never trap: a sequence whose n_accepted, path or
+ * lengths are out of range is skipped and bit 6 of the fault word is set.
+ *
+ * Conventions (those of the attention calls): ctx_len counts the anchor;
+ * block slot k of sequence b is cache position ctx_len[b] - 1 + k; the
+ * drafter's context is every position before the anchor (ctx_len - 1 rows).
+ * ------------------------------------------------------------------------ */
+
+/* Tokens and lengths.  With n = n_accepted[b]:
+ *   kept proposal i < n: chain (path NULL) proposals[b * proposal_stride + i];
+ *     tree proposals[b * proposal_stride + path[b * T + i]] (path as written
+ *     by sd_accept_tree_greedy: the kept nodes by depth)
+ *   out_tokens[b * out_cap + out_len[b] + i] = kept proposal i, then
+ *   out_tokens[b * out_cap + out_len[b] + n] = next_token[b];
+ *   out_len[b] += n + 1; ctx_len[b] += n + 1; draft_ctx[b] = ctx_len[b] - 1
+ *   (if draft_ctx is not NULL); anchor[b] = next_token[b]; status[b] = 0.
+ * A commit with n outside [0, T-1], a kept node outside [1, T), ctx_len + n + 1
+ * > ctx_cap or out_len + n + 1 > out_cap leaves sequence b unchanged and sets
+ * status[b] = 1 (if status is not NULL) and the fault word.
+ *   proposals    device int32: chain [B, >= T-1] drafts, tree [B, >= T] node tokens
+ *   n_accepted, next_token  device int32 [B] (sd_accept_* outputs; next_token
+ *                is the correction or the sampled next id)
+ *   ctx_len, draft_ctx, out_len, anchor, status  device int32 [B], updated in place
+ *   out_tokens   device int32 [B, out_cap]
+ *   ctx_cap      the largest ctx_len the caches can take (for a cache of S
+ *                positions verified in T-slot blocks: S - T + 1) */
+sd_status sd_commit_tokens(const int32_t *proposals, int proposal_stride, const int32_t *path,
+                           const int32_t *n_accepted, const int32_t *next_token, int B, int T,
+                           int32_t *ctx_len, int ctx_cap, int32_t *draft_ctx, int32_t *out_tokens,
+                           int32_t *out_len, int out_cap, int32_t *anchor, int32_t *status, void *stream);
+
+/* Tree rollback in the target's K/V cache: for depth d = 1..n_accepted[b],
+ * position ctx_len[b]-1+d takes the row at position ctx_len[b]-1+path[b*T+d-1]
+ * (every kv head, K and V, moved bit for bit); all other positions keep their
+ * rows.  After it the cache holds the committed sequence in order and the
+ * next block overwrites what follows.  ctx_len is read, not changed.
+ *   k_cache, v_cache  [B, max_slots, Hkv, D] with element strides kv, D
+ *                contiguous; D * element size a multiple of 16 bytes, <= 512
+ *   path         device int32 [B, T] (sd_accept_tree_greedy's)
+ * A sequence whose block passes max_slots is skipped (fault word). */
+sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const int32_t *ctx_len,
+                             const int32_t *path, const int32_t *n_accepted, int B, int T,
+                             int max_slots, int Hkv, int D, sd_dtype dtype, void *stream);
+
+/* The drafter's context append for the committed rows (the incremental
+ * append of sd_project_kv with the row count on the device): for r = 0..n
+ * (n = n_accepted[b]), hidden row src = 0 (the anchor) or r (chain) or
+ * path[b*T + r-1] (tree) of sequence b's block is projected (as in
+ * sd_project_kv) into drafter context row draft_ctx[b] + r.
+ *   hidden_block device bf16: row src of sequence b at
+ *                hidden_block + b * hidden_bstride + src * ld_hidden
+ *   k_ctx, v_ctx device bf16: row i of sequence b at + b * ctx_bstride +
+ *                i * ld_out; rows past max_rows are never written (a commit
+ *                that would pass it is skipped and sets the fault word)
+ *   draft_ctx    device int32 [B]: the drafter's context length before the
+ *                commit (sd_commit_tokens advances it afterwards)
+ * Requirements as for sd_project_kv, and Hd <= 6400 (the block's 16 hidden
+ * rows are staged in 200 KB of shared memory; else SD_ERR_UNSUPPORTED). */
+sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int64_t hidden_bstride,
+                               const void *w_k, const void *w_v, int Hd, int Dout,
+                               const int32_t *n_accepted, const int32_t *path, const int32_t *draft_ctx,
+                               int B, int T, void *k_ctx, void *v_ctx, int64_t ctx_bstride, int64_t ld_out,
+                               int max_rows, sd_dtype dtype, void *stream);
 
 /* ------------------------------------------------------------------------
  * Greedy acceptance without a caller workspace
@@ -297,7 +374,10 @@ const char *sd_last_error(void);        /* reason for the last non-OK status on 
 int sd_version(void);                   /* 100 * major + minor */
 
 /* Device fault word: 0 while no kernel guard fired.  Reading synchronises the
- * current device; `clear` resets it to 0. */
+ * current device; `clear` resets it to 0.  Bits: 0 ctx_len outside
+ * [1, max_ctx]; 1 a draft id outside [0, V); 2 a logits row with no ordered
+ * value (NaN); 3 a bounded wait gave up; 4 tensor-memory allocation failed;
+ * 5 a tree parent outside [0, node); 6 a commit out of range (skipped). */
 sd_status sd_fault_word(uint32_t *out, int clear);
 
 /* Attention kernel selection, process-wide, for tests and measurement:

@@ -491,16 +491,107 @@ sd_status sd_project_kv(const void *hidden, int64_t ld_hidden, const void *w_k, 
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     const int force = g_force_proj_path.load();
-    int path = N <= kProjSmallRows ? 1 : 2;
+    const bool small_ok = project_small_supported(8, Hd);   // 16 rows per CTA where they fit, else 8
+    int path = N <= kProjSmallRows && small_ok ? 1 : 2;
     if (force == 1) path = 1;
     if (force == 2) path = 2;
     if (path == 2 && !project_tc_supported()) {
         if (force == 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core projector needs sm_103 and 200 KB shared memory");
         path = 1;
     }
+    if (path == 1 && !small_ok)
+        return fail(SD_ERR_UNSUPPORTED, "CUDA-core projector stages 8 rows of Hd in 200 KB: Hd too large");
     cudaError_t e = launch_project(p, path, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "projector launch");
     g_last_proj_path = path;
+    return SD_OK;
+}
+
+sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int64_t hidden_bstride, const void *w_k,
+                               const void *w_v, int Hd, int Dout, const int32_t *n_accepted, const int32_t *path,
+                               const int32_t *draft_ctx, int B, int T, void *k_ctx, void *v_ctx,
+                               int64_t ctx_bstride, int64_t ld_out, int max_rows, sd_dtype dtype, void *stream) {
+    if (dtype == SD_FP32) return fail(SD_ERR_UNSUPPORTED, "the projector takes bf16 tensors only");
+    if (dtype != SD_BF16) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if (B < 1 || T < 1 || T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    if (Hd < 8 || Hd % 8 != 0 || Hd > (1 << 20)) return fail(SD_ERR_INVALID_ARG, "need Hd a positive multiple of 8");
+    if (Dout < 32 || Dout % 32 != 0 || Dout > (1 << 20))
+        return fail(SD_ERR_INVALID_ARG, "need Dout a positive multiple of 32");
+    if (ld_hidden < Hd || ld_hidden % 8 != 0 || hidden_bstride < (int64_t)T * ld_hidden || hidden_bstride % 8 != 0)
+        return fail(SD_ERR_INVALID_ARG, "hidden strides must cover a block and be multiples of 8 elements");
+    if (max_rows < 1 || ld_out < Dout || ctx_bstride < (int64_t)max_rows * ld_out)
+        return fail(SD_ERR_INVALID_ARG, "output strides must cover max_rows rows of Dout elements");
+    if (!hidden_block || !w_k || !w_v || !k_ctx || !v_ctx || !n_accepted || !draft_ctx)
+        return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(hidden_block) || !aligned16(w_k) || !aligned16(w_v))
+        return fail(SD_ERR_INVALID_ARG, "hidden states and weights must be 16-byte aligned");
+    if (!project_small_supported(kMaxT, Hd))
+        return fail(SD_ERR_UNSUPPORTED, "the append stages 16 rows of Hd in 200 KB of shared memory: Hd <= 6400");
+    if ((reinterpret_cast<uintptr_t>(k_ctx) | reinterpret_cast<uintptr_t>(v_ctx)) % 2 != 0)
+        return fail(SD_ERR_INVALID_ARG, "outputs must be 2-byte aligned");
+    ProjParams p = {};
+    p.h = static_cast<const __nv_bfloat16 *>(hidden_block);
+    p.wk = static_cast<const __nv_bfloat16 *>(w_k);
+    p.wv = static_cast<const __nv_bfloat16 *>(w_v);
+    p.k_out = static_cast<__nv_bfloat16 *>(k_ctx);
+    p.v_out = static_cast<__nv_bfloat16 *>(v_ctx);
+    p.ld_h = (long)ld_hidden; p.ld_out = (long)ld_out;
+    p.h_bstride = (long)hidden_bstride; p.out_bstride = (long)ctx_bstride;
+    p.N = T; p.Hd = Hd; p.Dout = Dout;
+    p.n_acc = n_accepted; p.path = path; p.dst_row0 = draft_ctx;
+    p.B = B; p.T = T; p.max_rows = max_rows;
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_project_commit(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "projector append launch");
+    return SD_OK;
+}
+
+sd_status sd_commit_tokens(const int32_t *proposals, int proposal_stride, const int32_t *path,
+                           const int32_t *n_accepted, const int32_t *next_token, int B, int T, int32_t *ctx_len,
+                           int ctx_cap, int32_t *draft_ctx, int32_t *out_tokens, int32_t *out_len, int out_cap,
+                           int32_t *anchor, int32_t *status, void *stream) {
+    if (B < 1 || T < 1 || T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    if (proposal_stride < (path ? T : T - 1)) return fail(SD_ERR_INVALID_ARG, "proposal_stride too small");
+    if (ctx_cap < 1 || out_cap < 1) return fail(SD_ERR_INVALID_ARG, "need ctx_cap >= 1 and out_cap >= 1");
+    if ((T > 1 && !proposals) || !n_accepted || !next_token || !ctx_len || !out_tokens || !out_len || !anchor)
+        return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    CommitParams p = {};
+    p.prop = proposals; p.ps = proposal_stride; p.path = path;
+    p.n_acc = n_accepted; p.next_tok = next_token; p.B = B; p.T = T;
+    p.ctx_len = ctx_len; p.ctx_cap = ctx_cap; p.draft_ctx = draft_ctx;
+    p.out_tokens = out_tokens; p.out_len = out_len; p.out_cap = out_cap;
+    p.anchor = anchor; p.status = status;
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_commit_tokens(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    return SD_OK;
+}
+
+sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const int32_t *ctx_len,
+                             const int32_t *path, const int32_t *n_accepted, int B, int T, int max_slots, int Hkv,
+                             int D, sd_dtype dtype, void *stream) {
+    if (B < 1 || T < 1 || T > kMaxT || Hkv < 1 || D < 1 || max_slots < T)
+        return fail(SD_ERR_INVALID_ARG, "need B, Hkv, D >= 1, T in [1, 16] and max_slots >= T");
+    if (dtype != SD_BF16 && dtype != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    const int es = (int)esize(dtype);
+    if ((D * es) % 16 != 0 || D * es > kMaxHeadBytes)
+        return fail(SD_ERR_UNSUPPORTED, "a (position, head) row must be a multiple of 16 bytes, at most 512");
+    if (kv.s < (int64_t)Hkv * D && kv.h < (int64_t)D)
+        return fail(SD_ERR_INVALID_ARG, "cache strides overlap");
+    if ((kv.b * es) % 16 != 0 || (kv.s * es) % 16 != 0 || (kv.h * es) % 16 != 0)
+        return fail(SD_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+    if (!k_cache || !v_cache || !ctx_len || !path || !n_accepted) return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return fail(SD_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+    CompactParams p = {};
+    p.kc = k_cache; p.vc = v_cache; p.kv = kv; p.es = es;
+    p.ctx_len = ctx_len; p.path = path; p.n_acc = n_accepted;
+    p.B = B; p.T = T; p.S = max_slots; p.Hkv = Hkv; p.D = D;
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_compact_tree_kv(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree compaction launch");
     return SD_OK;
 }
 

@@ -19,11 +19,13 @@ enum FaultBits : unsigned int {
     FAULT_WAIT_TIMEOUT = 1u << 3,   // a bounded mbarrier wait gave up
     FAULT_TMEM_ALLOC = 1u << 4,     // tensor-memory allocation returned out of range
     FAULT_BAD_TREE = 1u << 5,       // a tree node's parent outside [0, node)
+    FAULT_BAD_COMMIT = 1u << 6,     // a commit with n_acc / path / lengths out of range (skipped)
 };
 
 constexpr int kMaxT = 16;           // block rows (anchor + 15 proposals)
 constexpr int kTileKeys = 64;       // keys per tile of the CUDA-core attention kernel
 constexpr int kTcTileKeys = 128;    // keys per tile of the tensor-core attention kernel
+constexpr int kMaxHeadBytes = 512;  // bytes of one (position, kv head) row the tree compaction moves
 
 // Attention launch description (both the target verify and the drafter).
 //  key index space of sequence b:
@@ -120,12 +122,52 @@ struct ProjParams {
     __nv_bfloat16 *k_out, *v_out;
     long ld_h, ld_out;
     int N, Hd, Dout;
+    // commit-time append (launch_project_commit): sequence b's rows are
+    // 0..n_acc[b] of its block (row r >= 1 is node path[b * T + r - 1] when
+    // path is given), read at h + b * h_bstride, written to output rows
+    // dst_row0[b] + r at k_out / v_out + b * out_bstride; max_rows bounds them
+    const int32_t *n_acc, *path, *dst_row0;
+    long h_bstride, out_bstride;
+    int B, T, max_rows;
     unsigned int *fault;
 };
-constexpr int kProjSmallRows = 32;  // rows per CTA of the CUDA-core projector
+constexpr int kProjSmallRows = 16;  // rows per CTA of the CUDA-core projector
+constexpr size_t kProjSmallSmemMax = 200 * 1024;  // its hidden rows staged in shared memory
 // path: 1 CUDA cores, 2 tensor cores (requires project_tc_supported())
 cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st);
 bool project_tc_supported();
+bool project_small_supported(int rows_per_cta, int Hd);  // those rows of Hd fit its shared memory
+cudaError_t launch_project_commit(const ProjParams &p, cudaStream_t st);
+
+// Commit of a verified block: tokens and lengths (one warp per sequence) and,
+// for trees, the move of the kept nodes' K/V rows to consecutive positions.
+struct CommitParams {
+    const int32_t *prop;            // [B, ps] proposals (chain drafts or tree node tokens)
+    int ps;
+    const int32_t *path;            // tree: [B, T] kept nodes by depth; chain: null
+    const int32_t *n_acc, *next_tok;
+    int B, T;
+    int32_t *ctx_len;
+    int ctx_cap;
+    int32_t *draft_ctx;             // nullable
+    int32_t *out_tokens;            // [B, out_cap]
+    int32_t *out_len;
+    int out_cap;
+    int32_t *anchor;
+    int32_t *status;                // nullable
+    unsigned int *fault;
+};
+cudaError_t launch_commit_tokens(const CommitParams &p, cudaStream_t st);
+
+struct CompactParams {
+    void *kc, *vc;                  // [B, S, Hkv, D] with strides kv (elements)
+    sd_strides kv;
+    int es;                         // bytes per element
+    const int32_t *ctx_len, *path, *n_acc;
+    int B, T, S, Hkv, D;
+    unsigned int *fault;
+};
+cudaError_t launch_compact_tree_kv(const CompactParams &p, cudaStream_t st);
 
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int64_t n,
                           cudaStream_t st);

@@ -37,6 +37,7 @@ constexpr int kPjSmem = kPjOffMisc + 16 + 1024;
 static_assert(kPjSmem <= 227 * 1024, "shared memory per CTA");
 
 constexpr int kSmallWarps = 8;
+constexpr int kSmallInFlight = 8;        // weight vectors per lane per batch
 
 __global__ void __launch_bounds__(kPjThreads, 1)
 project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wk,
@@ -159,51 +160,118 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
     }
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+}
+
 // Few rows: out[n][c] = sum_k h[n][k] w[c][k], a warp per output column c of
 // [K | V], lanes over 8-feature vectors; CTA (x, y) takes columns
-// [8x, 8x + 8) and rows [NR y, NR y + NR).  The weight row is read from memory
-// once per row group; the hidden rows are shared by the CTA's warps through L1.
-template <int NR>
+// [8x, 8x + 8) and rows [NR y, NR y + NR).  The CTA's hidden rows are copied
+// once into shared memory (cp.async, all in flight together) while the first
+// batch of weight vectors is already on its way; the weights stream from
+// memory once per row group, double-buffered in registers.
+// kGather (the commit-time append): CTA row y is sequence b, its rows are
+// 0..n_acc[b] of that sequence's block (row r >= 1 is tree node
+// path[b][r-1] when a path is given) and they land at output rows
+// dst_row0[b] + r; all three come from device memory.
+template <int NR, bool kGather>
 __global__ void __launch_bounds__(kSmallWarps * 32)
 project_small_kernel(const ProjParams p) {
+    extern __shared__ uint4 hs[];                 // [nr][Hd / 8]: the hidden rows, bf16
+    __shared__ long s_off[NR];                    // element offset of row r in p.h
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
-    const int lane = threadIdx.x & 31;
-    const int c = blockIdx.x * kSmallWarps + (threadIdx.x >> 5);
-    if (c >= 2 * p.Dout) return;
+    const int tid = threadIdx.x, lane = tid & 31;
+    int nr;
+    long out_row0;                                // element offset of output row 0
+    if (kGather) {
+        const int b = blockIdx.y;
+        const int n = p.n_acc[b];
+        const int d0 = p.dst_row0[b];
+        bool ok = n >= 0 && n < p.T && n < NR && d0 >= 0 && (long)d0 + n + 1 <= p.max_rows;
+        for (int r = 1; ok && r <= n; ++r) {
+            const int src = p.path ? p.path[(long)b * p.T + r - 1] : r;
+            ok = src >= 1 && src < p.T;
+        }
+        if (!ok) {                                // uniform over the CTA
+            if (blockIdx.x == 0 && tid == 0) set_fault(p.fault, FAULT_BAD_COMMIT);
+            return;
+        }
+        nr = n + 1;
+        if (tid < nr) {
+            const int src = tid == 0 ? 0 : p.path ? p.path[(long)b * p.T + tid - 1] : tid;
+            s_off[tid] = (long)b * p.h_bstride + (long)src * p.ld_h;
+        }
+        out_row0 = (long)b * p.out_bstride + (long)d0 * p.ld_out;
+    } else {
+        const int n0 = blockIdx.y * NR;
+        nr = min(NR, p.N - n0);
+        if (tid < nr) s_off[tid] = (long)(n0 + tid) * p.ld_h;
+        out_row0 = (long)n0 * p.ld_out;
+    }
+    __syncthreads();
+    const int hv = p.Hd / 8;                      // 16-byte vectors per hidden row
+    for (int i = tid; i < nr * hv; i += kSmallWarps * 32) {
+        const int r = i / hv, x = i - r * hv;
+        cp_async16(smem_u32(hs + i), p.h + s_off[r] + 8 * x);
+    }
+
+    const int c = min(blockIdx.x * kSmallWarps + (tid >> 5), 2 * p.Dout - 1);
     const bool is_v = c >= p.Dout;
     const int cc = is_v ? c - p.Dout : c;
-    const int n0 = blockIdx.y * NR;
-    const int nr = min(NR, p.N - n0);
     const __nv_bfloat16 *w = (is_v ? p.wv : p.wk) + (long)cc * p.Hd;
-    const __nv_bfloat16 *h = p.h + (long)n0 * p.ld_h;
+    constexpr int kU = kSmallInFlight;
+    uint4 cur[kU], nxt[kU];
+    auto load = [&](uint4 (&dst)[kU], int k0) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int k = k0 + u * 256;
+            dst[u] = k < p.Hd ? ld_stream_u4(w + k) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    load(cur, lane * 8);
+    cp_async_wait_all();
+    __syncthreads();
+
     float acc[NR];
 #pragma unroll
     for (int n = 0; n < NR; ++n) acc[n] = 0.f;
-    for (int k = lane * 8; k < p.Hd; k += 256) {
-        float wf[8];
-        unpack_bf16x8(ld_stream_u4(w + k), wf);
+    for (int k0 = lane * 8; k0 < p.Hd; k0 += 256 * kU) {
+        if (k0 + 256 * kU < p.Hd) load(nxt, k0 + 256 * kU);
 #pragma unroll
-        for (int n = 0; n < NR; ++n) {
-            if (n < nr) {
-                float hf[8];
-                Elem<__nv_bfloat16>::load_vec(h + (long)n * p.ld_h + k, hf);
+        for (int u = 0; u < kU; ++u) {
+            const int k = k0 + u * 256;
+            if (k < p.Hd) {
+                float wf[8];
+                unpack_bf16x8(cur[u], wf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[n] = fmaf(hf[e], wf[e], acc[n]);
+                for (int n = 0; n < NR; ++n) {
+                    if (n < nr) {
+                        float hf[8];
+                        unpack_bf16x8(hs[n * hv + (k >> 3)], hf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[n] = fmaf(hf[e], wf[e], acc[n]);
+                    }
+                }
             }
         }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
     }
 #pragma unroll
     for (int n = 0; n < NR; ++n) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], o);
     }
-    if (lane < nr) {
+    if (lane < nr && blockIdx.x * kSmallWarps + (tid >> 5) < 2 * p.Dout) {
         float v = acc[0];
 #pragma unroll
         for (int n = 1; n < NR; ++n) v = lane == n ? acc[n] : v;
-        (is_v ? p.v_out : p.k_out)[(long)(n0 + lane) * p.ld_out + cc] = __float2bfloat16_rn(v);
+        (is_v ? p.v_out : p.k_out)[out_row0 + (long)lane * p.ld_out + cc] = __float2bfloat16_rn(v);
     }
 }
 
@@ -249,6 +317,25 @@ cudaError_t launch_pdl_pj(K kern, dim3 grid, dim3 block, size_t smem, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
+// dynamic shared memory of the CUDA-core kernel: NR hidden rows
+size_t small_smem(int NR, int Hd) { return (size_t)NR * Hd * 2; }
+
+template <int NR, bool kGather>
+cudaError_t launch_small(const ProjParams &p, dim3 grid, cudaStream_t st) {
+    static bool opted_in[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+        e = cudaFuncSetAttribute(project_small_kernel<NR, kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kProjSmallSmemMax);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+    }
+    return launch_pdl_pj(project_small_kernel<NR, kGather>, grid, dim3(kSmallWarps * 32), small_smem(NR, p.Hd), st,
+                         p);
+}
+
 }  // namespace
 
 bool project_tc_supported() {
@@ -261,15 +348,22 @@ bool project_tc_supported() {
     return optin >= kPjSmem && major == 10 && minor == 3;
 }
 
+bool project_small_supported(int rows_per_cta, int Hd) {
+    return small_smem(rows_per_cta, Hd) <= kProjSmallSmemMax;
+}
+
+cudaError_t launch_project_commit(const ProjParams &p, cudaStream_t st) {
+    const dim3 grid((unsigned)((2 * p.Dout + kSmallWarps - 1) / kSmallWarps), (unsigned)p.B);
+    return launch_small<kMaxT, true>(p, grid, st);
+}
+
 cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st) {
     if (p.N <= 0) return cudaSuccess;
     if (path == 1) {
-        const int nr = p.N <= 8 ? 8 : p.N <= 16 ? 16 : kProjSmallRows;
+        const int nr = (p.N <= 8 || small_smem(kProjSmallRows, p.Hd) > kProjSmallSmemMax) ? 8 : kProjSmallRows;
         const dim3 grid((unsigned)((2 * p.Dout + kSmallWarps - 1) / kSmallWarps), (unsigned)((p.N + nr - 1) / nr));
-        const dim3 block(kSmallWarps * 32);
-        if (nr == 8) return launch_pdl_pj(project_small_kernel<8>, grid, block, 0, st, p);
-        if (nr == 16) return launch_pdl_pj(project_small_kernel<16>, grid, block, 0, st, p);
-        return launch_pdl_pj(project_small_kernel<kProjSmallRows>, grid, block, 0, st, p);
+        if (nr == 8) return launch_small<8, false>(p, grid, st);
+        return launch_small<kProjSmallRows, false>(p, grid, st);
     }
     alignas(64) CUtensorMap mh, mk, mv;
     if (!make_map_2d(&mh, p.h, p.N, p.Hd, p.ld_h, kPjM)) return cudaErrorInvalidValue;

@@ -30,6 +30,7 @@ SYMBOLS = [
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
     "sd_project_kv", "sd_set_projector_path", "sd_last_projector_path",
+    "sd_commit_tokens", "sd_compact_tree_kv", "sd_project_kv_commit",
 ]
 
 
@@ -104,6 +105,14 @@ def load():
     lib.sd_last_attention_launches.restype = _i
     lib.sd_project_kv.argtypes = [_vp, ctypes.c_int64, _vp, _vp, _i, _i, _i, _vp, _vp, ctypes.c_int64, _i, _vp]
     lib.sd_project_kv.restype = _i
+    lib.sd_commit_tokens.argtypes = [_vp, _i, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp]
+    lib.sd_commit_tokens.restype = _i
+    lib.sd_compact_tree_kv.argtypes = [_vp, _vp, Strides, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
+    lib.sd_compact_tree_kv.restype = _i
+    _i64 = ctypes.c_int64
+    lib.sd_project_kv_commit.argtypes = [_vp, _i64, _i64, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp,
+                                         _i64, _i64, _i, _i, _vp]
+    lib.sd_project_kv_commit.restype = _i
     lib.sd_set_projector_path.argtypes = [_i]
     lib.sd_set_projector_path.restype = _i
     lib.sd_last_projector_path.argtypes = []
@@ -304,6 +313,58 @@ def sd_project_kv(hidden, w_k, w_v, k_out, v_out, stream=None):
     dt = _dt(hidden)
     _check(load().sd_project_kv(_p(hidden), hidden.stride(0), _p(w_k), _p(w_v), N, Hd, Dout, _p(k_out), _p(v_out),
                                 k_out.stride(0), dt, _stream(stream)))
+
+
+def _i32_cuda(*ts):
+    for t in ts:
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+            raise ValueError("index tensors are contiguous int32")
+
+
+def sd_commit_tokens(proposals, n_accepted, next_token, ctx_len, out_tokens, out_len, anchor, ctx_cap,
+                     path=None, draft_ctx=None, status=None, stream=None):
+    """proposals int32 [B, P] (chain drafts, or tree node tokens with path
+    [B, T]); out_tokens int32 [B, out_cap]; the rest int32 [B], updated in
+    place on the device."""
+    _need_cuda(proposals, n_accepted, next_token, ctx_len, out_tokens, out_len, anchor, path, draft_ctx, status)
+    _i32_cuda(proposals, n_accepted, next_token, ctx_len, out_tokens, out_len, anchor, path, draft_ctx, status)
+    B, P = proposals.shape
+    T = path.shape[1] if path is not None else P + 1
+    _check(load().sd_commit_tokens(_p(proposals), P, _p(path), _p(n_accepted), _p(next_token), B, T,
+                                   _p(ctx_len), int(ctx_cap), _p(draft_ctx), _p(out_tokens), _p(out_len),
+                                   out_tokens.shape[1], _p(anchor), _p(status), _stream(stream)))
+
+
+def sd_compact_tree_kv(k_cache, v_cache, ctx_len, path, n_accepted, stream=None):
+    """k_cache, v_cache [B, S, Hkv, D] (D contiguous, equal strides); path int32 [B, T]."""
+    _need_cuda(k_cache, v_cache, ctx_len, path, n_accepted)
+    _i32_cuda(ctx_len, path, n_accepted)
+    if k_cache.stride() != v_cache.stride() or k_cache.shape != v_cache.shape:
+        raise ValueError("K and V caches must share shape and strides")
+    B, S, Hkv, D = k_cache.shape
+    T = path.shape[1]
+    _check(load().sd_compact_tree_kv(_p(k_cache), _p(v_cache), _kv_strides(k_cache), _p(ctx_len), _p(path),
+                                     _p(n_accepted), B, T, S, Hkv, D, _dt(k_cache), _stream(stream)))
+
+
+def sd_project_kv_commit(hidden_block, w_k, w_v, n_accepted, draft_ctx, k_ctx, v_ctx, path=None, stream=None):
+    """hidden_block bf16 [B, T, Hd] (last axis contiguous); w_k, w_v bf16
+    [Dout, Hd]; k_ctx, v_ctx bf16 [B, S, Dout] (last axis contiguous, equal
+    strides); n_accepted, draft_ctx int32 [B]; path int32 [B, T] for a tree."""
+    _need_cuda(hidden_block, w_k, w_v, n_accepted, draft_ctx, k_ctx, v_ctx, path)
+    _i32_cuda(n_accepted, draft_ctx, path)
+    B, T, Hd = hidden_block.shape
+    Dout = w_k.shape[0]
+    if w_k.shape != (Dout, Hd) or w_v.shape != (Dout, Hd) or not (w_k.is_contiguous() and w_v.is_contiguous()):
+        raise ValueError("w_k and w_v are contiguous [Dout, Hd]")
+    if k_ctx.shape != v_ctx.shape or k_ctx.stride() != v_ctx.stride() or k_ctx.shape[2] != Dout:
+        raise ValueError("k_ctx and v_ctx are [B, S, Dout] with equal strides")
+    if hidden_block.stride(2) != 1 or k_ctx.stride(2) != 1:
+        raise ValueError("the last axis must be contiguous")
+    _check(load().sd_project_kv_commit(_p(hidden_block), hidden_block.stride(1), hidden_block.stride(0), _p(w_k),
+                                       _p(w_v), Hd, Dout, _p(n_accepted), _p(path), _p(draft_ctx), B, T,
+                                       _p(k_ctx), _p(v_ctx), k_ctx.stride(0), k_ctx.stride(1), k_ctx.shape[1],
+                                       _dt(hidden_block), _stream(stream)))
 
 
 def sd_set_projector_path(path: int) -> int:

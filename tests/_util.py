@@ -70,3 +70,23 @@ def sample_rows(B, T, Hq, n, seed=0):
 
 def to_dev(d, device="cuda"):
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def check_projection(got, h, w, rows=None, min_exact=0.99):
+    """Projector output (bf16, fp32 accumulation, one rounding) against the
+    fp64 oracle: every element within half a bf16 ulp of the exact value plus
+    the fp32 summation bound Hd * 2^-23 * sum_f |h_f w_f|, and at least
+    `min_exact` of them equal to the exact value rounded to bf16."""
+    ref = oracle.project_rows(h, w, rows)
+    absum = oracle.project_rows(np.abs(np.asarray(h.double() if hasattr(h, "double") else h, dtype=np.float64)),
+                                np.abs(np.asarray(w.double() if hasattr(w, "double") else w, dtype=np.float64)),
+                                rows)
+    acc = h.shape[1] * 2.0 ** -23 * absum
+    tol = 2.0 ** -8 * (np.abs(ref) + acc) + acc
+    g = got.double().numpy() if hasattr(got, "double") else np.asarray(got, dtype=np.float64)
+    g = g.reshape(ref.shape)
+    err = np.abs(g - ref)
+    assert (err <= tol).all(), (err.max(), np.unravel_index(np.argmax(err - tol), err.shape))
+    exact = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    frac = float((g == exact).mean())
+    assert frac >= min_exact, frac
