@@ -12,8 +12,10 @@ header for the passages each routine follows.
 Pins (tests/test_oracle_*.py) fix every routine to something other than
 itself: Philox known-answer vectors, textbook decode attention, closed forms
 (constant keys, one key), brute force on tiny shapes, the worked cycle of the
-VFlash-FM project page, the autoregressive-equivalence invariant and a
-chi-square test of the sampled rule.
+VFlash-FM project page, the autoregressive-equivalence invariant, a
+chi-square test of the sampled rule, and for the latent compressor closed
+forms (equal features, zero queries, a one-hot limit), a hand example and
+the library's scaled-dot-product attention.
 """
 from __future__ import annotations
 
@@ -95,6 +97,8 @@ def _load():
                                            _ip, _ip, _ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, _ip]
     lib.oracle_compact_tree_kv.restype = ctypes.c_int
+    lib.oracle_latent_compress.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp]
+    lib.oracle_latent_compress.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -254,6 +258,29 @@ def compact_tree_kv(k_cache, v_cache, ctx_len, path, n_accepted):
     if rc != 0:
         raise ValueError("oracle_compact_tree_kv rejected its arguments")
     return k, v, status
+
+
+def latent_compress(queries, features, values=None):
+    """SpecFLASH latent compressor, exact fp64: queries [Cq, d], features
+    [..., N, d] (a leading frame axis is allowed) -> [..., Cq, d] =
+    softmax(queries . features^T) . values, values defaulting to features."""
+    qv = _f64(queries)
+    f = _f64(features)
+    v = f if values is None else _f64(values)
+    lead = f.shape[:-2]
+    N, d = f.shape[-2:]
+    Cq = qv.shape[0]
+    f2 = f.reshape(-1, N, d)
+    v2 = v.reshape(-1, N, d)
+    out = np.zeros((f2.shape[0], Cq, d))
+    for i in range(f2.shape[0]):
+        o = np.zeros((Cq, d))
+        rc = _load().oracle_latent_compress(qv, np.ascontiguousarray(f2[i]), np.ascontiguousarray(v2[i]),
+                                            Cq, N, d, o)
+        if rc != 0:
+            raise ValueError("oracle_latent_compress rejected its arguments")
+        out[i] = o
+    return out.reshape(*lead, Cq, d)
 
 
 def lse_merge(o_parts, lse_parts):

@@ -552,3 +552,42 @@ int oracle_compact_tree_kv(uint8_t *kc, uint8_t *vc, long sb, long ss, long sh, 
     free(tmp);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Latent visual compressor                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * SpecFLASH latent visual compressor ("SpecFLASH" README, the first of the
+ * draft model's two components): a learned set of Cq query vectors attends
+ * over the N visual features of the second-to-top layer and returns Cq latent
+ * features, out = softmax(Q . F^T) . F, the softmax over the N features of
+ * each query.  The formula applies no scale to the scores, so none is applied
+ * here.  Keys and values are separate arguments (the method passes F for
+ * both) so that the same routine also gives sum_n p_n |F_n|, the weighted
+ * magnitude that bounds a kernel's rounding.
+ *   q [Cq, d], k [N, d], v [N, d], out [Cq, d]; exact fp64, max-subtracted.
+ */
+int oracle_latent_compress(const double *q, const double *k, const double *v, int Cq, int N, int d, double *out) {
+    if (Cq < 1 || N < 1 || d < 1) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s) return -1;
+    for (int c = 0; c < Cq; ++c) {
+        double m = -INFINITY;
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += q[(long)c * d + i] * k[(long)n * d + i];
+            s[n] = acc;
+            if (acc > m) m = acc;
+        }
+        double l = 0.0;
+        for (int n = 0; n < N; ++n) { s[n] = exp(s[n] - m); l += s[n]; }
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int n = 0; n < N; ++n) acc += s[n] * v[(long)n * d + i];
+            out[(long)c * d + i] = acc / l;
+        }
+    }
+    free(s);
+    return 0;
+}
