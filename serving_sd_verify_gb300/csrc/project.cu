@@ -7,13 +7,15 @@
 // the whole context (prefill) and then, every cycle, over the few positions
 // just committed (the incremental append).
 //
-// Prefill (many rows): a tcgen05 GEMM.  One CTA per (128-row tile, 256-column
-// tile of [K | V]); the hidden-state and weight tiles (64 features deep,
-// 128-byte swizzle) stream through a 4-stage TMA ring; one thread issues
-// M128 N256 K16 MMAs into a 256-column fp32 accumulator in tensor memory; four
-// warps convert it to bf16 and store it.
-// Append (a few rows): bound by reading the weights once, so CUDA cores: a
-// warp per output column, lanes over the features, kProjSmallRows rows per CTA.
+// Prefill (many rows): a tcgen05 GEMM.  One CTA per (128-row tile,
+// 256-column tile of [K | V]), the column tiles of a row tile adjacent in
+// launch order; the hidden-state and weight tiles (64 features deep, 128-byte
+// swizzle) stream through a 4-stage TMA ring; one thread issues M128 N256 K16
+// MMAs into a 256-column fp32 accumulator in tensor memory; four warps
+// convert it to bf16 and store it.
+// Append (a few rows): bound by reading the weights once, so CUDA cores: four
+// warps per output column, lanes over the features, up to kProjSmallRows rows
+// per CTA.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -36,8 +38,10 @@ constexpr int kPjOffMisc = kPjOffBar + 8 * kPjNumBars;
 constexpr int kPjSmem = kPjOffMisc + 16 + 1024;
 static_assert(kPjSmem <= 227 * 1024, "shared memory per CTA");
 
-constexpr int kSmallWarps = 8;
-constexpr int kSmallInFlight = 8;        // weight vectors per lane per batch
+constexpr int kSmallCols = 4;            // output columns per CTA of the CUDA-core kernel
+constexpr int kSmallSplitK = 4;          // warps sharing one column
+constexpr int kSmallThreads = kSmallCols * kSmallSplitK * 32;
+constexpr int kSmallInFlight = 4;        // weight vectors per lane per batch
 
 __global__ void __launch_bounds__(kPjThreads, 1)
 project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wk,
@@ -47,8 +51,10 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t *sbase = smem_raw + (base - raw_u32);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mt = blockIdx.x, nt = blockIdx.y;
+    // the column tiles of one row tile are adjacent in launch order, so the
+    // row tile's hidden states come from memory once and from L2 after that
     const int n_per = (p.Dout + kPjN - 1) / kPjN;   // column tiles per matrix
+    const int mt = blockIdx.x / (2 * n_per), nt = blockIdx.x % (2 * n_per);
     const bool is_v = nt >= n_per;
     const int col0 = (is_v ? nt - n_per : nt) * kPjN;
     const CUtensorMap *tw = is_v ? &tm_wv : &tm_wk;
@@ -167,25 +173,29 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
 }
 
-// Few rows: out[n][c] = sum_k h[n][k] w[c][k], a warp per output column c of
-// [K | V], lanes over 8-feature vectors; CTA (x, y) takes columns
-// [8x, 8x + 8) and rows [NR y, NR y + NR).  The CTA's hidden rows are copied
-// once into shared memory (cp.async, all in flight together) while the first
-// batch of weight vectors is already on its way; the weights stream from
-// memory once per row group, double-buffered in registers.
+// Few rows: out[n][c] = sum_k h[n][k] w[c][k].  CTA (x, y) takes output
+// columns [4x, 4x + 4) of [K | V] and rows [NR y, NR y + NR); each column is
+// shared by 4 warps, warp ks taking the 8-feature vectors ks, ks + 4, ...
+// interleaved over the lanes, and the 4 partial sums meet in shared memory
+// in a fixed order.  The CTA's hidden rows are copied once into shared
+// memory (cp.async, all in flight together) while each lane's weight vectors
+// are already on their way; the weights stream from memory once per row
+// group.  16 warps per CTA and two or more CTAs per SM keep enough
+// independent FMA chains in flight to cover their latency.
 // kGather (the commit-time append): CTA row y is sequence b, its rows are
 // 0..n_acc[b] of that sequence's block (row r >= 1 is tree node
 // path[b][r-1] when a path is given) and they land at output rows
 // dst_row0[b] + r; all three come from device memory.
 template <int NR, bool kGather>
-__global__ void __launch_bounds__(kSmallWarps * 32)
+__global__ void __launch_bounds__(kSmallThreads)
 project_small_kernel(const ProjParams p) {
     extern __shared__ uint4 hs[];                 // [nr][Hd / 8]: the hidden rows, bf16
     __shared__ long s_off[NR];                    // element offset of row r in p.h
+    __shared__ float red[kSmallSplitK][kSmallCols][NR];
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int nr;
     long out_row0;                                // element offset of output row 0
     if (kGather) {
@@ -215,44 +225,47 @@ project_small_kernel(const ProjParams p) {
     }
     __syncthreads();
     const int hv = p.Hd / 8;                      // 16-byte vectors per hidden row
-    for (int i = tid; i < nr * hv; i += kSmallWarps * 32) {
+    for (int i = tid; i < nr * hv; i += kSmallThreads) {
         const int r = i / hv, x = i - r * hv;
         cp_async16(smem_u32(hs + i), p.h + s_off[r] + 8 * x);
     }
 
-    const int c = min(blockIdx.x * kSmallWarps + (tid >> 5), 2 * p.Dout - 1);
+    const int col_in = warp % kSmallCols, ks = warp / kSmallCols;
+    const int c = min(blockIdx.x * kSmallCols + col_in, 2 * p.Dout - 1);
     const bool is_v = c >= p.Dout;
     const int cc = is_v ? c - p.Dout : c;
     const __nv_bfloat16 *w = (is_v ? p.wv : p.wk) + (long)cc * p.Hd;
     constexpr int kU = kSmallInFlight;
+    constexpr int kStep = 32 * kSmallSplitK;      // vectors between a lane's consecutive ones
     uint4 cur[kU], nxt[kU];
-    auto load = [&](uint4 (&dst)[kU], int k0) {
+    auto load = [&](uint4 (&dst)[kU], int v0) {
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            const int k = k0 + u * 256;
-            dst[u] = k < p.Hd ? ld_stream_u4(w + k) : make_uint4(0u, 0u, 0u, 0u);
+            const int v = v0 + u * kStep;
+            dst[u] = v < hv ? ld_stream_u4(w + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
-    load(cur, lane * 8);
+    const int v_first = lane + 32 * ks;
+    load(cur, v_first);
     cp_async_wait_all();
     __syncthreads();
 
     float acc[NR];
 #pragma unroll
     for (int n = 0; n < NR; ++n) acc[n] = 0.f;
-    for (int k0 = lane * 8; k0 < p.Hd; k0 += 256 * kU) {
-        if (k0 + 256 * kU < p.Hd) load(nxt, k0 + 256 * kU);
+    for (int v0 = v_first; v0 < hv; v0 += kStep * kU) {
+        if (v0 + kStep * kU < hv) load(nxt, v0 + kStep * kU);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            const int k = k0 + u * 256;
-            if (k < p.Hd) {
+            const int v = v0 + u * kStep;
+            if (v < hv) {
                 float wf[8];
                 unpack_bf16x8(cur[u], wf);
 #pragma unroll
                 for (int n = 0; n < NR; ++n) {
                     if (n < nr) {
                         float hf[8];
-                        unpack_bf16x8(hs[n * hv + (k >> 3)], hf);
+                        unpack_bf16x8(hs[n * hv + v], hf);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) acc[n] = fmaf(hf[e], wf[e], acc[n]);
                     }
@@ -267,11 +280,24 @@ project_small_kernel(const ProjParams p) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], o);
     }
-    if (lane < nr && blockIdx.x * kSmallWarps + (tid >> 5) < 2 * p.Dout) {
+    if (lane < nr) {
         float v = acc[0];
 #pragma unroll
         for (int n = 1; n < NR; ++n) v = lane == n ? acc[n] : v;
-        (is_v ? p.v_out : p.k_out)[out_row0 + (long)lane * p.ld_out + cc] = __float2bfloat16_rn(v);
+        red[ks][col_in][lane] = v;
+    }
+    __syncthreads();
+    if (tid < kSmallCols * NR) {
+        const int ci = tid / NR, n = tid % NR;
+        const int col = blockIdx.x * kSmallCols + ci;
+        if (n < nr && col < 2 * p.Dout) {
+            float v = red[0][ci][n];
+#pragma unroll
+            for (int q = 1; q < kSmallSplitK; ++q) v += red[q][ci][n];
+            const bool ov = col >= p.Dout;
+            (ov ? p.v_out : p.k_out)[out_row0 + (long)n * p.ld_out + (ov ? col - p.Dout : col)] =
+                __float2bfloat16_rn(v);
+        }
     }
 }
 
@@ -332,8 +358,7 @@ cudaError_t launch_small(const ProjParams &p, dim3 grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev] = true;
     }
-    return launch_pdl_pj(project_small_kernel<NR, kGather>, grid, dim3(kSmallWarps * 32), small_smem(NR, p.Hd), st,
-                         p);
+    return launch_pdl_pj(project_small_kernel<NR, kGather>, grid, dim3(kSmallThreads), small_smem(NR, p.Hd), st, p);
 }
 
 }  // namespace
@@ -353,7 +378,7 @@ bool project_small_supported(int rows_per_cta, int Hd) {
 }
 
 cudaError_t launch_project_commit(const ProjParams &p, cudaStream_t st) {
-    const dim3 grid((unsigned)((2 * p.Dout + kSmallWarps - 1) / kSmallWarps), (unsigned)p.B);
+    const dim3 grid((unsigned)((2 * p.Dout + kSmallCols - 1) / kSmallCols), (unsigned)p.B);
     return launch_small<kMaxT, true>(p, grid, st);
 }
 
@@ -361,7 +386,7 @@ cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st) {
     if (p.N <= 0) return cudaSuccess;
     if (path == 1) {
         const int nr = (p.N <= 8 || small_smem(kProjSmallRows, p.Hd) > kProjSmallSmemMax) ? 8 : kProjSmallRows;
-        const dim3 grid((unsigned)((2 * p.Dout + kSmallWarps - 1) / kSmallWarps), (unsigned)((p.N + nr - 1) / nr));
+        const dim3 grid((unsigned)((2 * p.Dout + kSmallCols - 1) / kSmallCols), (unsigned)((p.N + nr - 1) / nr));
         if (nr == 8) return launch_small<8, false>(p, grid, st);
         return launch_small<kProjSmallRows, false>(p, grid, st);
     }
@@ -378,7 +403,7 @@ cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev] = true;
     }
-    const dim3 grid((unsigned)((p.N + kPjM - 1) / kPjM), (unsigned)(2 * ((p.Dout + kPjN - 1) / kPjN)));
+    const dim3 grid((unsigned)(((p.N + kPjM - 1) / kPjM) * 2 * ((p.Dout + kPjN - 1) / kPjN)));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kPjThreads);
