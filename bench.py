@@ -76,6 +76,11 @@ BYTES = {
     "project_append": 2 * HKV * D * HD * 2 + APPEND * HD * 2 + 2 * APPEND * HKV * D * 2,
 }
 PROJ_PREFILL_FLOPS = 2 * CTX * HD * 2 * HKV * D
+# SpecFLASH latent compressor: 16 frames of LLaVA-1.5-7B visual features
+# (576 per frame, d 4096) compressed to 64 latents each
+LC_FRAMES, LC_N, LC_C, LC_D = 16, 576, 64, 4096
+LC_BYTES = LC_FRAMES * LC_N * LC_D * 2 + LC_C * LC_D * 2 + LC_FRAMES * LC_C * LC_D * 2
+LC_FLOPS = 2 * 2 * LC_FRAMES * LC_C * LC_N * LC_D
 
 
 # ---------------------------------------------------------------------------
@@ -666,6 +671,37 @@ def main():
         kernels["commit"]["note"] = ("the device-side commit alone: projector append of the committed rows "
                                      "(weights read once) + token / length update")
         del cyc, proj
+        # the SpecFLASH latent compressor (two launches), one graph replay after an L2 flush
+        from serving_sd_verify_gb300 import workloads as W
+        lq, lf = W.latent_inputs(frames=LC_FRAMES, N=LC_N, Cq=LC_C, d=LC_D, seed=16)
+        lq, lf = lq.to(device), lf.to(device)
+        lout = torch.empty(LC_FRAMES, LC_C, LC_D, dtype=torch.bfloat16, device=device)
+        lws = S.workspace(S.sd_latent_compress_workspace_size(LC_FRAMES, LC_N, LC_C, LC_D), device)
+        with torch.cuda.stream(stream):
+            S.sd_latent_compress(lq, lf, lout, lws, stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            S.sd_latent_compress(lq, lf, lout, lws, stream)
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(n_rep):
+                flush.zero_()
+                e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e_a.record(stream)
+                g.replay()
+                e_b.record(stream)
+                evs.append((e_a, e_b))
+        torch.cuda.synchronize()
+        del g, lq, lf, lout, lws
+        per = sum(a.elapsed_time(b) for a, b in evs[3:]) / 1e3 / (n_rep - 3)
+        kernels["latent_compress"] = {
+            "us_per_call": per * 1e6, "calls_per_step": 0, "kernel_launches_per_call": 2,
+            "algorithmic_bytes_per_call": LC_BYTES, "GBps": LC_BYTES / per / 1e9,
+            "TFLOPs": LC_FLOPS / per / 1e12,
+            "note": (f"SpecFLASH latent compressor softmax(Q.F^T).F: {LC_FRAMES} frames x {LC_N} visual features "
+                     f"(d {LC_D}, LLaVA-1.5-7B) -> {LC_C} latents each; scores kernel + output kernel; "
+                     "features read from HBM once, re-read from L2; not part of the step")}
         tpk, tsrc = bf16_peak(sustained=False)
         kp = kernels["project_prefill"]
         kp["TFLOPs"] = PROJ_PREFILL_FLOPS / (kp["us_per_call"] * 1e-6) / 1e12

@@ -337,6 +337,38 @@ sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int6
                                int max_rows, sd_dtype dtype, void *stream);
 
 /* ------------------------------------------------------------------------
+ * SpecFLASH latent visual compressor
+ *
+ * Source: "SpecFLASH" README, the first of the draft model's two components:
+ * a learned set of Cq query vectors attends over the N visual features of
+ * the target's second-to-top layer and compresses them into Cq latent
+ * features (LLaVA-1.5: 576 -> 64; Qwen2.5-VL: 324 -> 36), per frame i:
+ *   out[i] = softmax(Q . F[i]^T) . F[i]     (softmax over the N features;
+ *                                             no scale on the scores)
+ * Scores accumulate in fp32 on the tensor cores; the softmax weights are
+ * rounded to bf16 for the second product, which accumulates in fp32 and is
+ * rounded once to bf16.
+ *
+ *   queries    device bf16 [Cq, d] contiguous, 1 <= Cq <= 64
+ *   features   device bf16: frame i, feature n at
+ *              features + i * frame_stride + n * ld_features (d contiguous)
+ *   out        device bf16: frame i, query c at out + i * out_frame_stride +
+ *              c * ld_out (d contiguous)
+ *   workspace  at least sd_latent_compress_workspace_size() bytes, 16-byte
+ *              aligned, no initial contents needed (fp32 scores and softmax
+ *              statistics: about 33 KB per 128 features of each frame)
+ * Requires d a multiple of 64 (<= 65536), 1 <= frames <= 65535, strides
+ * multiples of 8 elements that cover a row / frame, 16-byte aligned
+ * pointers, sm_103 (else SD_ERR_UNSUPPORTED).  Two kernel launches.
+ * ------------------------------------------------------------------------ */
+sd_status sd_latent_compress(const void *queries, const void *features, int64_t ld_features,
+                             int64_t frame_stride, int frames, int N, int Cq, int d, void *out,
+                             int64_t ld_out, int64_t out_frame_stride, sd_dtype dtype,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+size_t sd_latent_compress_workspace_size(int frames, int N, int Cq, int d);
+
+/* ------------------------------------------------------------------------
  * Greedy acceptance without a caller workspace
  *
  * No counterpart in the method's pages: this is a convenience of the library.

@@ -595,6 +595,68 @@ sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const 
     return SD_OK;
 }
 
+namespace {
+struct LatentLayout {
+    size_t scores, stat_m, stat_l, total;
+};
+LatentLayout latent_layout(int frames, int N) {
+    const size_t tiles = (size_t)frames * ((N + 127) / 128);
+    LatentLayout l;
+    l.scores = 0;
+    l.stat_m = align_up(tiles * 128 * kLatentMaxQueries * sizeof(float), 256);
+    l.stat_l = l.stat_m + align_up(tiles * kLatentMaxQueries * sizeof(float), 256);
+    l.total = l.stat_l + align_up(tiles * kLatentMaxQueries * sizeof(float), 256);
+    return l;
+}
+bool latent_shape_ok(int frames, int N, int Cq, int d) {
+    return frames >= 1 && frames <= 65535 && N >= 1 && N <= (1 << 20) && Cq >= 1 && Cq <= kLatentMaxQueries &&
+           d >= 64 && d % 64 == 0 && d <= (1 << 16);
+}
+}  // namespace
+
+size_t sd_latent_compress_workspace_size(int frames, int N, int Cq, int d) {
+    if (!latent_shape_ok(frames, N, Cq, d)) return 0;
+    return latent_layout(frames, N).total;
+}
+
+sd_status sd_latent_compress(const void *queries, const void *features, int64_t ld_features, int64_t frame_stride,
+                             int frames, int N, int Cq, int d, void *out, int64_t ld_out, int64_t out_frame_stride,
+                             sd_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (dtype == SD_FP32) return fail(SD_ERR_UNSUPPORTED, "the latent compressor takes bf16 tensors only");
+    if (dtype != SD_BF16) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
+    if (!latent_shape_ok(frames, N, Cq, d))
+        return fail(SD_ERR_INVALID_ARG, "need frames in [1, 65535], N >= 1, Cq in [1, 64], d a multiple of 64");
+    if (ld_features < d || ld_features % 8 != 0 || frame_stride < (int64_t)N * ld_features || frame_stride % 8 != 0)
+        return fail(SD_ERR_INVALID_ARG, "feature strides must cover a frame and be multiples of 8 elements");
+    if (ld_out < d || ld_out % 8 != 0 || out_frame_stride < (int64_t)Cq * ld_out || out_frame_stride % 8 != 0)
+        return fail(SD_ERR_INVALID_ARG, "output strides must cover a frame and be multiples of 8 elements");
+    if (!queries || !features || !out) return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(queries) || !aligned16(features) || !aligned16(out))
+        return fail(SD_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
+    const LatentLayout ll = latent_layout(frames, N);
+    if (!workspace || workspace_bytes < ll.total)
+        return fail(SD_ERR_WORKSPACE, "latent workspace too small: need %zu bytes, got %zu", ll.total, workspace_bytes);
+    if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    if (!latent_supported()) return fail(SD_ERR_UNSUPPORTED, "the latent compressor needs sm_103 and 200 KB shared memory");
+    char *w = static_cast<char *>(workspace);
+    LatentParams p = {};
+    p.q = static_cast<const __nv_bfloat16 *>(queries);
+    p.f = static_cast<const __nv_bfloat16 *>(features);
+    p.ld_f = (long)ld_features; p.f_fstride = (long)frame_stride;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ld_out = (long)ld_out; p.out_fstride = (long)out_frame_stride;
+    p.frames = frames; p.N = N; p.Cq = Cq; p.d = d;
+    p.n_tiles = (N + 127) / 128;
+    p.scores = reinterpret_cast<float *>(w + ll.scores);
+    p.stat_m = reinterpret_cast<float *>(w + ll.stat_m);
+    p.stat_l = reinterpret_cast<float *>(w + ll.stat_l);
+    p.fault = fault_ptr();
+    if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    cudaError_t e = launch_latent(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "latent compressor launch");
+    return SD_OK;
+}
+
 int sd_set_projector_path(int path) {
     if (path < 0 || path > 2) path = 0;
     return g_force_proj_path.exchange(path);

@@ -169,6 +169,23 @@ struct CompactParams {
 };
 cudaError_t launch_compact_tree_kv(const CompactParams &p, cudaStream_t st);
 
+// SpecFLASH latent compressor: out[i] = softmax(q . f[i]^T) . f[i] per frame i.
+constexpr int kLatentMaxQueries = 64;
+struct LatentParams {
+    const __nv_bfloat16 *q;         // [Cq, d] contiguous
+    const __nv_bfloat16 *f;         // frame i, feature n at f + i * f_fstride + n * ld_f
+    long ld_f, f_fstride;
+    __nv_bfloat16 *out;             // frame i, query c at out + i * out_fstride + c * ld_out
+    long ld_out, out_fstride;
+    int frames, N, Cq, d;
+    int n_tiles;                    // ceil(N / 128)
+    float *scores;                  // [frames, n_tiles * 128, 64] S^T (fp32)
+    float *stat_m, *stat_l;         // [frames, n_tiles, 64] per-tile max and sum of exp
+    unsigned int *fault;
+};
+cudaError_t launch_latent(const LatentParams &p, cudaStream_t st);
+bool latent_supported();
+
 cudaError_t launch_philox(const uint32_t *ctr, uint64_t key, uint32_t *out, int64_t n,
                           cudaStream_t st);
 

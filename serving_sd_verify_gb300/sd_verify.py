@@ -31,6 +31,7 @@ SYMBOLS = [
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
     "sd_project_kv", "sd_set_projector_path", "sd_last_projector_path",
     "sd_commit_tokens", "sd_compact_tree_kv", "sd_project_kv_commit",
+    "sd_latent_compress", "sd_latent_compress_workspace_size",
 ]
 
 
@@ -113,6 +114,10 @@ def load():
     lib.sd_project_kv_commit.argtypes = [_vp, _i64, _i64, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp,
                                          _i64, _i64, _i, _i, _vp]
     lib.sd_project_kv_commit.restype = _i
+    lib.sd_latent_compress.argtypes = [_vp, _vp, _i64, _i64, _i, _i, _i, _i, _vp, _i64, _i64, _i, _vp, _sz, _vp]
+    lib.sd_latent_compress.restype = _i
+    lib.sd_latent_compress_workspace_size.argtypes = [_i] * 4
+    lib.sd_latent_compress_workspace_size.restype = _sz
     lib.sd_set_projector_path.argtypes = [_i]
     lib.sd_set_projector_path.restype = _i
     lib.sd_last_projector_path.argtypes = []
@@ -365,6 +370,25 @@ def sd_project_kv_commit(hidden_block, w_k, w_v, n_accepted, draft_ctx, k_ctx, v
                                        _p(w_v), Hd, Dout, _p(n_accepted), _p(path), _p(draft_ctx), B, T,
                                        _p(k_ctx), _p(v_ctx), k_ctx.stride(0), k_ctx.stride(1), k_ctx.shape[1],
                                        _dt(hidden_block), _stream(stream)))
+
+
+def sd_latent_compress_workspace_size(frames, N, Cq, d) -> int:
+    return int(load().sd_latent_compress_workspace_size(frames, N, Cq, d))
+
+
+def sd_latent_compress(queries, features, out, ws, stream=None):
+    """queries bf16 [Cq, d] contiguous; features bf16 [F, N, d] (last axis
+    contiguous); out bf16 [F, Cq, d] (last axis contiguous)."""
+    _need_cuda(queries, features, out, ws)
+    F, N, d = features.shape
+    Cq = queries.shape[0]
+    if queries.shape != (Cq, d) or not queries.is_contiguous():
+        raise ValueError("queries are contiguous [Cq, d]")
+    if out.shape != (F, Cq, d) or out.stride(2) != 1 or features.stride(2) != 1:
+        raise ValueError("out is [F, Cq, d]; the last axes must be contiguous")
+    _check(load().sd_latent_compress(_p(queries), _p(features), features.stride(1), features.stride(0), F, N, Cq, d,
+                                     _p(out), out.stride(1), out.stride(0), _dt(features), _p(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def sd_set_projector_path(path: int) -> int:

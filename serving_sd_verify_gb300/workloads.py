@@ -182,6 +182,15 @@ def sample_inputs(*, B, T, V, sd=3.0, noise_sd=1.0, seed=0, draft_seed=None,
 # the five measured workloads
 # --------------------------------------------------------------------------
 
+def latent_inputs(*, frames, N, Cq, d, seed=0):
+    """SpecFLASH compressor inputs: visual features bf16 [frames, N, d] ~ N(0,1)
+    and learned queries bf16 [Cq, d] ~ N(0, 1/d) (so the scores are ~ N(0,1))."""
+    rng = np.random.default_rng(seed)
+    f = _to(_normal(rng, (frames, N, d)), torch.bfloat16)
+    q = _to(_normal(rng, (Cq, d), sd=1.0 / math.sqrt(d)), torch.bfloat16)
+    return q, f
+
+
 CONFIG_NAMES = {
     1: "tiny-verify-ctx512-h4kv1-d64-fp32",
     2: "llava-ov-7b-verify-ctx25119-h28kv4-d128-bf16",
