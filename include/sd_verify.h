@@ -355,11 +355,12 @@ sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int6
  *   out        device bf16: frame i, query c at out + i * out_frame_stride +
  *              c * ld_out (d contiguous)
  *   workspace  at least sd_latent_compress_workspace_size() bytes, 16-byte
- *              aligned, no initial contents needed (fp32 scores and softmax
- *              statistics: about 33 KB per 128 features of each frame)
+ *              aligned, no initial contents needed (fp32 partial scores,
+ *              one copy per slice of d, and the bf16 weights)
  * Requires d a multiple of 64 (<= 65536), 1 <= frames <= 65535, strides
  * multiples of 8 elements that cover a row / frame, 16-byte aligned
- * pointers, sm_103 (else SD_ERR_UNSUPPORTED).  Two kernel launches.
+ * pointers, sm_103 (else SD_ERR_UNSUPPORTED).  Three kernel launches; the
+ * result does not depend on how d is sliced across them (fixed order).
  * ------------------------------------------------------------------------ */
 sd_status sd_latent_compress(const void *queries, const void *features, int64_t ld_features,
                              int64_t frame_stride, int frames, int N, int Cq, int d, void *out,

@@ -597,15 +597,24 @@ sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const 
 
 namespace {
 struct LatentLayout {
-    size_t scores, stat_m, stat_l, total;
+    int n_splits, ksteps;
+    size_t scores, probs, total;
 };
-LatentLayout latent_layout(int frames, int N) {
-    const size_t tiles = (size_t)frames * ((N + 127) / 128);
+// slices of d for the scores kernel: enough CTAs for every SM, at least 2
+// stages of kLatentStageD per slice
+LatentLayout latent_layout(int frames, int N, int Cq, int d) {
     LatentLayout l;
+    const long ctas = (long)frames * ((N + 127) / 128);
+    const int steps = (d + kLatentStageD - 1) / kLatentStageD;
+    int splits = (int)std::min<long>((device_sm_count() + ctas - 1) / ctas, std::max(1, steps / 2));
+    splits = std::max(1, std::min(splits, 16));
+    l.ksteps = (steps + splits - 1) / splits;
+    l.n_splits = (steps + l.ksteps - 1) / l.ksteps;
+    const size_t ld_s = (size_t)((N + 127) / 128) * 128;
+    const size_t ld_p = align_up((size_t)N, 8);
     l.scores = 0;
-    l.stat_m = align_up(tiles * 128 * kLatentMaxQueries * sizeof(float), 256);
-    l.stat_l = l.stat_m + align_up(tiles * kLatentMaxQueries * sizeof(float), 256);
-    l.total = l.stat_l + align_up(tiles * kLatentMaxQueries * sizeof(float), 256);
+    l.probs = align_up((size_t)l.n_splits * frames * kLatentMaxQueries * ld_s * sizeof(float), 256);
+    l.total = l.probs + align_up((size_t)frames * Cq * ld_p * 2, 256);
     return l;
 }
 bool latent_shape_ok(int frames, int N, int Cq, int d) {
@@ -616,7 +625,7 @@ bool latent_shape_ok(int frames, int N, int Cq, int d) {
 
 size_t sd_latent_compress_workspace_size(int frames, int N, int Cq, int d) {
     if (!latent_shape_ok(frames, N, Cq, d)) return 0;
-    return latent_layout(frames, N).total;
+    return latent_layout(frames, N, Cq, d).total;
 }
 
 sd_status sd_latent_compress(const void *queries, const void *features, int64_t ld_features, int64_t frame_stride,
@@ -633,7 +642,7 @@ sd_status sd_latent_compress(const void *queries, const void *features, int64_t 
     if (!queries || !features || !out) return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
     if (!aligned16(queries) || !aligned16(features) || !aligned16(out))
         return fail(SD_ERR_INVALID_ARG, "tensor base addresses must be 16-byte aligned");
-    const LatentLayout ll = latent_layout(frames, N);
+    const LatentLayout ll = latent_layout(frames, N, Cq, d);
     if (!workspace || workspace_bytes < ll.total)
         return fail(SD_ERR_WORKSPACE, "latent workspace too small: need %zu bytes, got %zu", ll.total, workspace_bytes);
     if (!aligned16(workspace)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -647,9 +656,12 @@ sd_status sd_latent_compress(const void *queries, const void *features, int64_t 
     p.ld_out = (long)ld_out; p.out_fstride = (long)out_frame_stride;
     p.frames = frames; p.N = N; p.Cq = Cq; p.d = d;
     p.n_tiles = (N + 127) / 128;
+    p.n_splits = ll.n_splits;
+    p.ksteps_per_split = ll.ksteps;
     p.scores = reinterpret_cast<float *>(w + ll.scores);
-    p.stat_m = reinterpret_cast<float *>(w + ll.stat_m);
-    p.stat_l = reinterpret_cast<float *>(w + ll.stat_l);
+    p.ld_s = (long)p.n_tiles * 128;
+    p.probs = reinterpret_cast<__nv_bfloat16 *>(w + ll.probs);
+    p.ld_p = (long)align_up((size_t)N, 8);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     cudaError_t e = launch_latent(p, static_cast<cudaStream_t>(stream));

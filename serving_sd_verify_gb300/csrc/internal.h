@@ -171,6 +171,7 @@ cudaError_t launch_compact_tree_kv(const CompactParams &p, cudaStream_t st);
 
 // SpecFLASH latent compressor: out[i] = softmax(q . f[i]^T) . f[i] per frame i.
 constexpr int kLatentMaxQueries = 64;
+constexpr int kLatentStageD = 256;  // d per stage of the scores kernel
 struct LatentParams {
     const __nv_bfloat16 *q;         // [Cq, d] contiguous
     const __nv_bfloat16 *f;         // frame i, feature n at f + i * f_fstride + n * ld_f
@@ -179,8 +180,11 @@ struct LatentParams {
     long ld_out, out_fstride;
     int frames, N, Cq, d;
     int n_tiles;                    // ceil(N / 128)
-    float *scores;                  // [frames, n_tiles * 128, 64] S^T (fp32)
-    float *stat_m, *stat_l;         // [frames, n_tiles, 64] per-tile max and sum of exp
+    int n_splits, ksteps_per_split; // slices of d in the scores kernel, kLatentStageD-wide stages each
+    float *scores;                  // [n_splits, frames, 64, ld_s] partial S (fp32), ld_s = n_tiles * 128
+    long ld_s;
+    __nv_bfloat16 *probs;           // [frames, Cq, ld_p] P (bf16), ld_p = N rounded up to 8
+    long ld_p;
     unsigned int *fault;
 };
 cudaError_t launch_latent(const LatentParams &p, cudaStream_t st);

@@ -7,17 +7,21 @@
 // features of the target's second-to-top layer and replaces them with a few
 // latent features (LLaVA-1.5: 576 -> 64; Qwen2.5-VL: 324 -> 36).
 //
-// Two tensor-core kernels, F read twice (the second time mostly from L2):
-//  scores (CTA per (frame, 128-feature tile)): S^T = F_tile . Q^T, M 128
-//    features x N 64 queries x K d, with TMA tiles of F and Q through a
-//    6-stage ring; the epilogue writes S^T (fp32) and the tile's softmax
-//    statistics per query (max, sum of exp) to the workspace.
-//  output (CTA per (frame, 256-wide slice of d)): combines the statistics,
-//    builds P = softmax rows as bf16 tiles [128 query rows x 64 features] in
-//    a 3-slot ring (rows >= Cq stay zero) while TMA brings the matching F
-//    tiles [64 features x 256 d] (MN-major B operand), and accumulates
-//    O = P . F in tensor memory (M 128 x N 256 x K 16 MMAs); frames in
-//    reverse order, so the last frames the scores kernel read come first.
+// Three launches, F read twice (the second time mostly from L2):
+//  scores (tensor cores, CTA per (128-feature tile, frame, slice of d)):
+//    S^T = F_tile . Q^T over the CTA's slice of d, M 128 features x N 64
+//    queries x K 16 MMAs over TMA tiles of F and Q, 256 of d per stage (512
+//    contiguous bytes of every feature row per copy), through a 2-stage ring;
+//    the epilogue writes the partial S as [query][feature] (fp32).  Slicing d
+//    gives enough CTAs to fill the GPU when frames x tiles alone do not.
+//  softmax (CTA per (query, frame)): sums the slices in a fixed order, takes
+//    the row's max and sum of exp, and writes the normalised weights P
+//    [query][feature] as bf16.
+//  output (tensor cores, CTA per (frame, 256-wide slice of d)): O = P . F,
+//    M 128 (query rows, zero beyond Cq) x N 256 x K 16 MMAs over TMA tiles
+//    of P [128 x 64 features] and F [64 features x 256 d] (MN-major B
+//    operand) through a 4-stage ring; frames in reverse order, so the frames
+//    the scores kernel read last are re-read first, from L2.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -33,27 +37,29 @@ constexpr int kLcQ = kLatentMaxQueries;  // query columns (zero beyond Cq)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- scores kernel ----
-constexpr int kScStages = 6;
-constexpr int kScABytes = 128 * 128;     // [128 features x 64 d] bf16
-constexpr int kScBBytes = kLcQ * 128;    // [64 queries x 64 d] bf16
+constexpr int kScStages = 2;
+constexpr int kScChunks = kLatentStageD / 64;      // 64-wide chunks of d per stage
+constexpr int kScABytes = kScChunks * 128 * 128;   // [128 features x 256 d] bf16, as 4 chunks of 16 KB
+constexpr int kScBBytes = kScChunks * kLcQ * 128;  // [64 queries x 256 d] bf16, as 4 chunks of 8 KB
 constexpr int kScStageBytes = kScABytes + kScBBytes;
 constexpr int kScOffBar = kScStages * kScStageBytes;
 constexpr int kScNumBars = 2 * kScStages + 1;
 constexpr int kScOffMisc = kScOffBar + 8 * kScNumBars;
 constexpr int kScSmem = kScOffMisc + 16 + 1024;
-constexpr int kScRowStride = kLcQ + 1;   // floats per staged score row (bank-conflict free)
-static_assert(128 * kScRowStride * 4 + 2 * 2 * kLcQ * 4 <= kScOffBar, "staging fits the ring");
 static_assert(kScSmem <= 227 * 1024, "shared memory per CTA");
 
+// ---- softmax kernel ----
+constexpr int kSmThreads = 256;
+
 // ---- output kernel ----
-constexpr int kOutStages = 3;
+constexpr int kOutStages = 4;
 constexpr int kOutN = 256;               // d columns per CTA
 constexpr int kOutKeys = 64;             // features per stage
-constexpr int kOutFBytes = kOutKeys * kOutN * 2;   // 32 KB
-constexpr int kOutPBytes = 128 * kOutKeys * 2;     // 16 KB
-constexpr int kOutOffP = kOutStages * kOutFBytes;
-constexpr int kOutOffBar = kOutOffP + kOutStages * kOutPBytes;
-constexpr int kOutNumBars = 3 * kOutStages + 1;
+constexpr int kOutPBytes = 128 * kOutKeys * 2;     // [128 query rows x 64 features] bf16, 16 KB
+constexpr int kOutFBytes = kOutKeys * kOutN * 2;   // [64 features x 256 d] bf16, 32 KB
+constexpr int kOutStageBytes = kOutPBytes + kOutFBytes;
+constexpr int kOutOffBar = kOutStages * kOutStageBytes;
+constexpr int kOutNumBars = 2 * kOutStages + 1;
 constexpr int kOutOffMisc = kOutOffBar + 8 * kOutNumBars;
 constexpr int kOutSmem = kOutOffMisc + 16 + 1024;
 static_assert(kOutSmem <= 227 * 1024, "shared memory per CTA");
@@ -66,8 +72,9 @@ latent_scores_kernel(const __grid_constant__ CUtensorMap tm_f, const __grid_cons
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t *sbase = smem_raw + (base - raw_u32);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x, frame = blockIdx.y;
-    const int nk = p.d / 64;
+    const int tile = blockIdx.x, frame = blockIdx.y, split = blockIdx.z;
+    const int kt0 = split * p.ksteps_per_split;
+    const int nk = min((p.d + kLatentStageD - 1) / kLatentStageD - kt0, p.ksteps_per_split);   // stages of d
 
     const uint32_t bar0 = base + kScOffBar;
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
@@ -108,8 +115,8 @@ latent_scores_kernel(const __grid_constant__ CUtensorMap tm_f, const __grid_cons
                     break;
                 const uint32_t a = base + st * kScStageBytes;
                 mbar_arrive_expect_tx(full_bar(st), (uint32_t)kScStageBytes);
-                tma_load_3d(a, &tm_f, full_bar(st), kt * 64, tile * 128, frame);
-                tma_load_2d(a + kScABytes, &tm_q, full_bar(st), kt * 64, 0);
+                tma_load_4d(a, &tm_f, full_bar(st), 0, tile * 128, (kt0 + kt) * kScChunks, frame);
+                tma_load_3d(a + kScABytes, &tm_q, full_bar(st), 0, 0, (kt0 + kt) * kScChunks);
                 issued = kt + 1;
             }
             if (*abort_flag)
@@ -126,68 +133,38 @@ latent_scores_kernel(const __grid_constant__ CUtensorMap tm_f, const __grid_cons
                 tc_fence_after();
                 const uint32_t a = base + st * kScStageBytes, b = a + kScABytes;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_ss(tmem, sw128_desc(a + kk * 32, 16, 1024), sw128_desc(b + kk * 32, 16, 1024), idesc,
-                            (kt > 0 || kk > 0) ? 1u : 0u);
+                for (int c = 0; c < kScChunks; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_ss(tmem, sw128_desc(a + c * (128 * 128) + kk * 32, 16, 1024),
+                                sw128_desc(b + c * (kLcQ * 128) + kk * 32, 16, 1024), idesc,
+                                (kt > 0 || c > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(empty_bar(st));
             }
             umma_commit(done_bar);
         }
         __syncwarp();
-    }
-    // warps 4-7: thread = feature row of the tile = tensor-memory lane
-    const bool epi = warp >= 4;
-    const int r = (warp & 3) * 32 + lane;
-    const int key = tile * 128 + r;
-    float *stage = reinterpret_cast<float *>(sbase);   // [128][kScRowStride], over the ring once all MMAs are done
-    bool ok = true;
-    if (epi) {
-        ok = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, p.fault));
+    } else if (warp >= 4) {
+        // thread = feature row of the tile = tensor-memory lane; S_split[frame][query][feature]:
+        // for each query the warp's 32 features are contiguous
+        const int r = (warp & 3) * 32 + lane;
+        const int key = tile * 128 + r;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, p.fault));
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        uint32_t v[32];
-        float *srow = p.scores + (((long)frame * p.n_tiles + tile) * 128 + r) * kLcQ;
+        float *scol = p.scores + ((long)split * p.frames + frame) * kLcQ * p.ld_s + key;
 #pragma unroll
         for (int h = 0; h < kLcQ / 32; ++h) {
+            uint32_t v[32];
             tmem_ld32_async(taddr + (uint32_t)(32 * h), v);
             tmem_ld_wait();
             tmem_ld_bind(v);
+            if (ok && !*abort_flag && key < p.N) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stage[r * kScRowStride + 32 * h + c] = __uint_as_float(v[c]);
-            if (ok && key < p.N) {
-                float4 *dst = reinterpret_cast<float4 *>(srow + 32 * h);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    dst[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+                for (int c = 0; c < 32; ++c) scol[(long)(32 * h + c) * p.ld_s] = __uint_as_float(v[c]);
             }
         }
         tc_fence_before();
-    }
-    __syncthreads();
-    // the tile's statistics per query: thread t takes query t % 64 over half the rows
-    if (epi) {
-        const int t = tid - 128;
-        const int q = t % kLcQ, half = t / kLcQ;
-        const int r0 = half * 64, r1 = min(r0 + 64, p.N - tile * 128);
-        float m = -INFINITY;
-        for (int rr = r0; rr < r1; ++rr) m = fmaxf(m, stage[rr * kScRowStride + q]);
-        float l = 0.f;
-        if (m != -INFINITY)
-            for (int rr = r0; rr < r1; ++rr) l += ex2((stage[rr * kScRowStride + q] - m) * kLog2e);
-        float *xs = stage + 128 * kScRowStride;   // [2 halves][2][kLcQ]
-        xs[(half * 2 + 0) * kLcQ + q] = m;
-        xs[(half * 2 + 1) * kLcQ + q] = l;
-        named_sync(1, 128);
-        if (half == 0 && ok && !*abort_flag) {
-            const float m1 = xs[(2 + 0) * kLcQ + q], l1 = xs[(2 + 1) * kLcQ + q];
-            const float mm = fmaxf(m, m1);
-            const float ll = (m == -INFINITY ? 0.f : l * ex2((m - mm) * kLog2e)) +
-                             (m1 == -INFINITY ? 0.f : l1 * ex2((m1 - mm) * kLog2e));
-            const long si = ((long)frame * p.n_tiles + tile) * kLcQ + q;
-            p.stat_m[si] = mm;
-            p.stat_l[si] = ll;
-        }
     }
     __syncthreads();
     if (warp == 1) {
@@ -198,8 +175,50 @@ latent_scores_kernel(const __grid_constant__ CUtensorMap tm_f, const __grid_cons
     }
 }
 
+// CTA per (query row, frame): S[q][n] = sum of the slices' partial scores
+// (in slice order), then P[q][n] = exp(S[q][n] - max_n S[q]) / sum_n exp(...)
+// as bf16.  Each thread keeps a running (max, sum of exp) over its features;
+// the CTA combines them in a fixed tree order.
+__global__ void __launch_bounds__(kSmThreads) latent_softmax_kernel(const LatentParams p) {
+#if __CUDA_ARCH__ >= 900
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+    const int q = blockIdx.x, frame = blockIdx.y, tid = threadIdx.x;
+    __shared__ float s_m[kSmThreads / 32], s_l[kSmThreads / 32];
+    const long slice = (long)p.frames * kLcQ * p.ld_s;
+    const float *srow = p.scores + ((long)frame * kLcQ + q) * p.ld_s;
+    auto score = [&](int n) {
+        float v = srow[n];
+        for (int s2 = 1; s2 < p.n_splits; ++s2) v += srow[s2 * slice + n];
+        return v * kLog2e;
+    };
+    float m = -INFINITY, l = 0.f;
+    for (int n = tid; n < p.N; n += kSmThreads) {
+        const float v = score(n);
+        if (v > m) { l = l * ex2(m - v) + 1.f; m = v; }
+        else l += ex2(v - m);
+    }
+    auto combine = [](float &m1, float &l1, float m2, float l2) {
+        const float mm = fmaxf(m1, m2);
+        l1 = (m1 == -INFINITY ? 0.f : l1 * ex2(m1 - mm)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mm));
+        m1 = mm;
+    };
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) combine(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
+    if ((tid & 31) == 0) { s_m[tid >> 5] = m; s_l[tid >> 5] = l; }
+    __syncthreads();
+    m = s_m[0];
+    l = s_l[0];
+    for (int w = 1; w < kSmThreads / 32; ++w) combine(m, l, s_m[w], s_l[w]);
+    const float invL = 1.f / l;
+    __nv_bfloat16 *prow = p.probs + ((long)frame * p.Cq + q) * p.ld_p;
+    for (int n = tid; n < p.N; n += kSmThreads) prow[n] = __float2bfloat16_rn(ex2(score(n) - m) * invL);
+}
+
 __global__ void __launch_bounds__(kLcThreads, 1)
-latent_output_kernel(const __grid_constant__ CUtensorMap tm_f4, const LatentParams p) {
+latent_output_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_f4,
+                     const LatentParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -209,26 +228,18 @@ latent_output_kernel(const __grid_constant__ CUtensorMap tm_f4, const LatentPara
     const int nkt = (p.N + kOutKeys - 1) / kOutKeys;
 
     const uint32_t bar0 = base + kOutOffBar;
-    auto f_full = [&](int i) { return bar0 + 8u * i; };
-    auto p_full = [&](int i) { return bar0 + 8u * (kOutStages + i); };
-    auto empty_bar = [&](int i) { return bar0 + 8u * (2 * kOutStages + i); };
-    const uint32_t done_bar = bar0 + 8u * (3 * kOutStages);
+    auto full_bar = [&](int i) { return bar0 + 8u * i; };
+    auto empty_bar = [&](int i) { return bar0 + 8u * (kOutStages + i); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kOutStages);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + kOutOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + kOutOffMisc + 8);
 
-    // P slots start as zeros: rows >= Cq are never written again
-    for (int i = tid; i < kOutStages * kOutPBytes / 16; i += kLcThreads)
-        reinterpret_cast<uint4 *>(sbase + kOutOffP)[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     if (tid == 0) {
-        for (int i = 0; i < kOutStages; ++i) {
-            mbar_init(f_full(i), 1);
-            mbar_init(p_full(i), 128);
-            mbar_init(empty_bar(i), 1);
-        }
+        for (int i = 0; i < kOutStages; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_p)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_f4)) : "memory");
     }
     if (warp == 1) {
@@ -253,13 +264,15 @@ latent_output_kernel(const __grid_constant__ CUtensorMap tm_f4, const LatentPara
                 if (kt >= kOutStages &&
                     !mbar_wait(empty_bar(st), ((kt / kOutStages) - 1) & 1, abort_flag, p.fault))
                     break;
-                mbar_arrive_expect_tx(f_full(st), (uint32_t)kOutFBytes);
-                tma_load_4d(base + st * kOutFBytes, &tm_f4, f_full(st), 0, kt * kOutKeys, dt * (kOutN / 64), frame);
+                const uint32_t a = base + st * kOutStageBytes;
+                mbar_arrive_expect_tx(full_bar(st), (uint32_t)kOutStageBytes);
+                tma_load_3d(a, &tm_p, full_bar(st), kt * kOutKeys, 0, frame);
+                tma_load_4d(a + kOutPBytes, &tm_f4, full_bar(st), 0, kt * kOutKeys, dt * (kOutN / 64), frame);
                 issued = kt + 1;
             }
             if (*abort_flag)
                 for (int u = max(0, issued - kOutStages); u < issued; ++u)
-                    mbar_wait(f_full(u % kOutStages), (u / kOutStages) & 1, nullptr, p.fault);
+                    mbar_wait(full_bar(u % kOutStages), (u / kOutStages) & 1, nullptr, p.fault);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -267,11 +280,9 @@ latent_output_kernel(const __grid_constant__ CUtensorMap tm_f4, const LatentPara
             const uint32_t idesc = idesc_bf16(128, kOutN, true);
             for (int kt = 0; kt < nkt; ++kt) {
                 const int st = kt % kOutStages;
-                const uint32_t par = (kt / kOutStages) & 1;
-                if (!mbar_wait(f_full(st), par, abort_flag, p.fault)) break;
-                if (!mbar_wait(p_full(st), par, abort_flag, p.fault)) break;
+                if (!mbar_wait(full_bar(st), (kt / kOutStages) & 1, abort_flag, p.fault)) break;
                 tc_fence_after();
-                const uint32_t fb = base + st * kOutFBytes, pa = base + kOutOffP + st * kOutPBytes;
+                const uint32_t pa = base + st * kOutStageBytes, fb = pa + kOutPBytes;
 #pragma unroll
                 for (int kk = 0; kk < kOutKeys / 16; ++kk)
                     umma_ss(tmem, sw128_desc(pa + kk * 32, 16, 1024),
@@ -282,49 +293,6 @@ latent_output_kernel(const __grid_constant__ CUtensorMap tm_f4, const LatentPara
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // P builders: thread t takes query q = t % 64 and features [32 h, 32 h + 32) of each tile
-        const int t = tid - 128;
-        const int q = t % kLcQ, h = t / kLcQ;
-        const bool live = q < p.Cq;
-        float M = -INFINITY, invL = 0.f;
-        if (live) {
-            for (int i = 0; i < p.n_tiles; ++i)
-                M = fmaxf(M, p.stat_m[((long)frame * p.n_tiles + i) * kLcQ + q]);
-            float L = 0.f;
-            for (int i = 0; i < p.n_tiles; ++i) {
-                const long si = ((long)frame * p.n_tiles + i) * kLcQ + q;
-                const float mi = p.stat_m[si];
-                if (mi != -INFINITY) L += p.stat_l[si] * ex2((mi - M) * kLog2e);
-            }
-            invL = 1.f / L;
-        }
-        const float Ml = M * kLog2e;
-        const float *sc = p.scores + (long)frame * p.n_tiles * 128 * kLcQ + q;
-        bool ok = true;
-        for (int kt = 0; kt < nkt; ++kt) {
-            const int st = kt % kOutStages;
-            if (kt >= kOutStages)
-                ok = ok && mbar_wait(empty_bar(st), ((kt / kOutStages) - 1) & 1, abort_flag, p.fault);
-            if (ok && live) {
-                uint8_t *slot = sbase + kOutOffP + st * kOutPBytes;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int k0 = kt * kOutKeys + 32 * h + 8 * c;
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int ka = k0 + 2 * e, kb = ka + 1;
-                        const float pa = ka < p.N ? ex2(fmaf(sc[(long)ka * kLcQ], kLog2e, -Ml)) * invL : 0.f;
-                        const float pb = kb < p.N ? ex2(fmaf(sc[(long)kb * kLcQ], kLog2e, -Ml)) * invL : 0.f;
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(pa, pb);
-                        pk[e] = *reinterpret_cast<const uint32_t *>(&v2);
-                    }
-                    *reinterpret_cast<uint4 *>(slot + sw128_off(q, 4 * h + c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-                fence_proxy_async_smem();
-            }
-            mbar_arrive(p_full(st));
-        }
         // epilogue: thread = query row = tensor-memory lane (warps 4-7 own lanes 0-127)
         const bool done = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, p.fault));
         tc_fence_after();
@@ -337,7 +305,7 @@ latent_output_kernel(const __grid_constant__ CUtensorMap tm_f4, const LatentPara
             tmem_ld32_async(taddr + (uint32_t)c0, v);
             tmem_ld_wait();
             tmem_ld_bind(v);
-            if (done && ok && !*abort_flag && row < p.Cq && dt * kOutN + c0 < p.d) {
+            if (done && !*abort_flag && row < p.Cq && dt * kOutN + c0 < p.d) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -386,10 +354,10 @@ bool encode(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, c
 }
 
 template <typename K, typename... A>
-cudaError_t launch_lc(K kern, dim3 grid, int smem, cudaStream_t st, A... args) {
+cudaError_t launch_lc(K kern, dim3 grid, int threads, int smem, cudaStream_t st, A... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kLcThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -413,18 +381,24 @@ bool latent_supported() {
 }
 
 cudaError_t launch_latent(const LatentParams &p, cudaStream_t st) {
-    alignas(64) CUtensorMap mf, mq, mf4;
-    {   // F as (d, N, frames): box 64 d x 128 features
-        const cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.frames};
-        const cuuint64_t strides[2] = {(cuuint64_t)p.ld_f * 2, (cuuint64_t)p.f_fstride * 2};
-        const cuuint32_t box[3] = {64, 128, 1};
-        if (!encode(&mf, p.f, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap mf, mq, mp, mf4;
+    {   // F as (d % 64, N, d / 64, frames): box 64 x 128 features x 4 chunks (512 contiguous bytes per row)
+        const cuuint64_t dims[4] = {64, (cuuint64_t)p.N, (cuuint64_t)(p.d / 64), (cuuint64_t)p.frames};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.ld_f * 2, 128, (cuuint64_t)p.f_fstride * 2};
+        const cuuint32_t box[4] = {64, 128, (cuuint32_t)kScChunks, 1};
+        if (!encode(&mf, p.f, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    {   // Q as (d, Cq): box 64 d x 64 queries (rows >= Cq read as zeros)
-        const cuuint64_t dims[2] = {(cuuint64_t)p.d, (cuuint64_t)p.Cq};
-        const cuuint64_t strides[1] = {(cuuint64_t)p.d * 2};
-        const cuuint32_t box[2] = {64, (cuuint32_t)kLcQ};
-        if (!encode(&mq, p.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    {   // Q as (d % 64, Cq, d / 64): box 64 x 64 queries x 4 chunks (rows >= Cq read as zeros)
+        const cuuint64_t dims[3] = {64, (cuuint64_t)p.Cq, (cuuint64_t)(p.d / 64)};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.d * 2, 128};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kLcQ, (cuuint32_t)kScChunks};
+        if (!encode(&mq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {   // P as (N, Cq, frames): box 64 features x 128 query rows (rows >= Cq read as zeros)
+        const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.Cq, (cuuint64_t)p.frames};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.ld_p * 2, (cuuint64_t)p.ld_p * 2 * p.Cq};
+        const cuuint32_t box[3] = {(cuuint32_t)kOutKeys, 128, 1};
+        if (!encode(&mp, p.probs, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {   // F as (d % 64, N, d / 64, frames): box 64 x 64 features x 4 chunks = [64 features x 256 d]
         const cuuint64_t dims[4] = {64, (cuuint64_t)p.N, (cuuint64_t)(p.d / 64), (cuuint64_t)p.frames};
@@ -443,10 +417,13 @@ cudaError_t launch_latent(const LatentParams &p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev] = true;
     }
-    e = launch_lc(latent_scores_kernel, dim3((unsigned)p.n_tiles, (unsigned)p.frames), kScSmem, st, mf, mq, p);
+    e = launch_lc(latent_scores_kernel, dim3((unsigned)p.n_tiles, (unsigned)p.frames, (unsigned)p.n_splits), kLcThreads,
+                  kScSmem, st, mf, mq, p);
     if (e != cudaSuccess) return e;
-    return launch_lc(latent_output_kernel, dim3((unsigned)((p.d + kOutN - 1) / kOutN), (unsigned)p.frames), kOutSmem,
-                     st, mf4, p);
+    e = launch_lc(latent_softmax_kernel, dim3((unsigned)p.Cq, (unsigned)p.frames), kSmThreads, 0, st, p);
+    if (e != cudaSuccess) return e;
+    return launch_lc(latent_output_kernel, dim3((unsigned)((p.d + kOutN - 1) / kOutN), (unsigned)p.frames),
+                     kLcThreads, kOutSmem, st, mp, mf4, p);
 }
 
 }  // namespace sdv
