@@ -359,8 +359,10 @@ sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int6
  *              one copy per slice of d, and the bf16 weights)
  * Requires d a multiple of 64 (<= 65536), 1 <= frames <= 65535, strides
  * multiples of 8 elements that cover a row / frame, 16-byte aligned
- * pointers, sm_103 (else SD_ERR_UNSUPPORTED).  Three kernel launches; the
- * result does not depend on how d is sliced across them (fixed order).
+ * pointers, sm_103 (else SD_ERR_UNSUPPORTED).  Three kernel launches.
+ * Deterministic: the scores kernel may slice d (how many slices depends on
+ * the shape and the GPU's SM count) and the slices are summed in a fixed
+ * order.
  * ------------------------------------------------------------------------ */
 sd_status sd_latent_compress(const void *queries, const void *features, int64_t ld_features,
                              int64_t frame_stride, int frames, int N, int Cq, int d, void *out,
