@@ -702,6 +702,50 @@ def main():
             "note": (f"SpecFLASH latent compressor softmax(Q.F^T).F: {LC_FRAMES} frames x {LC_N} visual features "
                      f"(d {LC_D}, LLaVA-1.5-7B) -> {LC_C} latents each; scores, softmax and output kernels; "
                      "features read from HBM once, re-read from L2; not part of the step")}
+        # acceptance at the batched workloads -- greedy over the ragged batch's
+        # logits (B 8) and the sampled rule of the 72B-shaped workload (B 4) --
+        # issued back to back in one graph over 4 input copies (more than L2)
+        acceptance = {}
+        g8 = W.greedy_inputs(B=8, T=T, V=V, seed=103)
+        s4 = W.sample_inputs(B=4, T=T, V=V, seed=105, draft_seed=1235)
+        n_copies = 4
+        for name, Bn, make, call, nbytes in (
+                ("greedy_b8", 8,
+                 lambda: (g8["draft"].to(device), g8["logits"].to(device),
+                          S.workspace(S.sd_accept_greedy_workspace_size(8, T, V), device)),
+                 lambda c, n_, x_: S.sd_accept_greedy(c[0], c[1], n_, x_, c[2], stream),
+                 8 * (T * V * 2 + (T - 1) * 4 + 8)),
+                ("sample_b4", 4,
+                 lambda: (s4["draft"].to(device), s4["q"].to(device), s4["logits"].to(device),
+                          S.workspace(S.sd_accept_sample_workspace_size(4, T, V), device)),
+                 lambda c, n_, x_: S.sd_accept_sample(c[0], c[1], c[2], 1.0, 1234, 0, n_, x_, c[3], stream),
+                 4 * (T * V * 2 + V * 2 + V * 4 + (T - 1) * 8 + 8))):
+            cps = [make() for _ in range(n_copies)]
+            n_ = torch.zeros(Bn, dtype=torch.int32, device=device)
+            x_ = torch.zeros(Bn, dtype=torch.int32, device=device)
+            with torch.cuda.stream(stream):
+                for c in cps:
+                    call(c, n_, x_)
+            torch.cuda.synchronize()
+            ga = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ga, stream=stream):
+                for i in range(2 * n_copies):
+                    call(cps[i % n_copies], n_, x_)
+            reps_a = 25
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    ga.replay()
+                e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e_a.record(stream)
+                for _ in range(reps_a):
+                    ga.replay()
+                e_b.record(stream)
+            torch.cuda.synchronize()
+            del ga, cps
+            per = e_a.elapsed_time(e_b) / 1e3 / (reps_a * 2 * n_copies)
+            acceptance[name] = {"us_per_call": per * 1e6, "algorithmic_bytes_per_call": nbytes,
+                                "GBps": nbytes / per / 1e9}
+        del g8, s4
         tpk, tsrc = bf16_peak(sustained=False)
         kp = kernels["project_prefill"]
         kp["TFLOPs"] = PROJ_PREFILL_FLOPS / (kp["us_per_call"] * 1e-6) / 1e12
@@ -777,6 +821,11 @@ def main():
         for name, kk in kernels.items():
             if "GBps" in kk:
                 kk["frac_of_peak"] = kk["GBps"] / peak
+        for name, kk in acceptance.items():
+            kk["frac_of_peak"] = kk["GBps"] / peak
+        roofline["acceptance_back_to_back"] = dict(acceptance, note=(
+            "acceptance kernels at the batched workloads (greedy over 8 sequences' logits, the sampled rule "
+            "over 4), calls issued back to back in one graph over 4 input copies larger than L2"))
 
     # ---- end to end: host buffers, copies inside the timed region ----
     e2e = None

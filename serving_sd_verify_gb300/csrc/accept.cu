@@ -26,6 +26,9 @@ namespace sdv {
 namespace {
 
 constexpr int kAccThreads = 256;
+constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
+constexpr int kFinRows = 8;       // rows per warp whose chunk partials a finisher loads together
+constexpr int kDrawChunksStaged = 512;  // chunk sums the draw finisher stages in shared memory
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10
@@ -176,36 +179,74 @@ __device__ __forceinline__ bool elect_last(unsigned int *counter, unsigned int t
 // ----------------------------------------------------------------------------
 // greedy acceptance
 // ----------------------------------------------------------------------------
-template <typename Tin, int NV>
+// 16-byte vector of logits -> floats
+template <typename Tin> struct Vec16;
+template <> struct Vec16<float> {
+    static constexpr int PV = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&f)[4]) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+};
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int PV = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&f)[8]) { unpack_bf16x8(u, f); }
+};
+
+// CTA (c, row) streams chunk c of one row: the unaligned head and tail
+// element by element, the 16-byte-aligned body in batches of kGreedyBatch
+// vectors per thread, the next batch in flight while this one is reduced
+template <typename Tin>
 __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams p) {
     grid_dependency_wait();
-    const int c = blockIdx.x, row = blockIdx.y;
+    constexpr int PV = Vec16<Tin>::PV;
+    const int c = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
     const Tin *lg = static_cast<const Tin *>(p.logits) + (long)row * p.V;
-    ChunkRegs<Tin, NV> cr;
-    cr.load(lg, lo, hi, -INFINITY);
+    const uintptr_t base = reinterpret_cast<uintptr_t>(lg);
+    int a0 = lo;                                   // first 16-byte aligned index >= lo
+    while (a0 < hi && ((base + (uintptr_t)a0 * sizeof(Tin)) & 15u)) ++a0;
+    const int nvec = (hi - a0) / PV, a1 = a0 + nvec * PV;
+    const uint4 *vp = reinterpret_cast<const uint4 *>(lg + a0);
     float bv = -INFINITY;
     int bi = INT_MAX;
-    // ascending index order within the thread keeps the lowest index on ties
-    for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) {
+    for (int i = lo + tid; i < a0; i += kAccThreads) {
         const float x = Elem<Tin>::load(lg + i);
         if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
     }
+    uint4 cur[kGreedyBatch], nxt[kGreedyBatch];
+    auto load = [&](uint4 (&d)[kGreedyBatch], int v0) {
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        if (!cr.valid(v)) break;
-#pragma unroll
-        for (int e = 0; e < ChunkRegs<Tin, NV>::PV; ++e) {
-            const int i = cr.index(v, e);
-            if (argmax_better(cr.x[v][e], i, bv, bi)) { bv = cr.x[v][e]; bi = i; }
+        for (int u = 0; u < kGreedyBatch; ++u) {
+            const int vi = v0 + u * kAccThreads;
+            d[u] = vi < nvec ? ld_stream_u4(vp + vi) : make_uint4(0u, 0u, 0u, 0u);
         }
+    };
+    load(cur, tid);
+    for (int v0 = tid; v0 < nvec; v0 += kAccThreads * kGreedyBatch) {
+        if (v0 + kAccThreads * kGreedyBatch < nvec) load(nxt, v0 + kAccThreads * kGreedyBatch);
+#pragma unroll
+        for (int u = 0; u < kGreedyBatch; ++u) {
+            const int vi = v0 + u * kAccThreads;
+            if (vi < nvec) {
+                float f[PV];
+                Vec16<Tin>::unpack(cur[u], f);
+#pragma unroll
+                for (int e = 0; e < PV; ++e) {
+                    const int i = a0 + vi * PV + e;
+                    if (argmax_better(f[e], i, bv, bi)) { bv = f[e]; bi = i; }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kGreedyBatch; ++u) cur[u] = nxt[u];
     }
-    for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) {
+    for (int i = a1 + tid; i < hi; i += kAccThreads) {
         const float x = Elem<Tin>::load(lg + i);
         if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
     }
     block_argmax(bv, bi);
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         p.pval[(long)row * p.n_chunks + c] = bv;
         p.pidx[(long)row * p.n_chunks + c] = bi;
     }
@@ -218,19 +259,36 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     const int R = p.B * p.T;
     const int W = (kAccThreads / p.T) * p.T;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kAccThreads / 32;
     for (int r0 = 0; r0 < R; r0 += W) {
-        for (int r = r0 + warp; r < min(R, r0 + W); r += kAccThreads / 32) {
-            float v = -INFINITY;
-            int i = INT_MAX;
-            for (int k = lane; k < p.n_chunks; k += 32) {
-                const float pv = __ldcg(p.pval + (long)r * p.n_chunks + k);
-                const int pi = __ldcg(p.pidx + (long)r * p.n_chunks + k);
-                if (argmax_better(pv, pi, v, i)) { v = pv; i = pi; }
+        const int nr = min(R - r0, W);
+        // warp w takes rows w, w + 8, ... of the window, kFinRows at a time with
+        // all their partial loads in flight together; lanes over the chunks
+        for (int rb = 0; rb < nr; rb += kWarps * kFinRows) {
+            float v[kFinRows];
+            int ix[kFinRows];
+#pragma unroll
+            for (int k = 0; k < kFinRows; ++k) { v[k] = -INFINITY; ix[k] = INT_MAX; }
+            for (int k0 = lane; k0 < p.n_chunks; k0 += 32) {
+#pragma unroll
+                for (int k = 0; k < kFinRows; ++k) {
+                    const int r = rb + warp + kWarps * k;
+                    if (r < nr) {
+                        const long o = (long)(r0 + r) * p.n_chunks + k0;
+                        const float pv = __ldcg(p.pval + o);
+                        const int pi = __ldcg(p.pidx + o);
+                        if (argmax_better(pv, pi, v[k], ix[k])) { v[k] = pv; ix[k] = pi; }
+                    }
+                }
             }
-            warp_argmax(v, i);
-            if (lane == 0) {
-                if (i == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); i = 0; }
-                am[r - r0] = i;
+#pragma unroll
+            for (int k = 0; k < kFinRows; ++k) {
+                warp_argmax(v[k], ix[k]);
+                const int r = rb + warp + kWarps * k;
+                if (lane == 0 && r < nr) {
+                    if (ix[k] == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); ix[k] = 0; }
+                    am[r] = ix[k];
+                }
             }
         }
         __syncthreads();
@@ -332,34 +390,62 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     const int R = p.B * p.T;
     const int W = (kAccThreads / p.T) * p.T;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kAccThreads / 32;
     for (int r0 = 0; r0 < R; r0 += W) {
-        for (int r = r0 + warp; r < min(R, r0 + W); r += kAccThreads / 32) {
-            float M = -INFINITY;
-            for (int k = lane; k < p.n_chunks; k += 32) M = fmaxf(M, __ldcg(p.pm + (long)r * p.n_chunks + k));
+        const int nr = min(R - r0, W);
+        // warp w takes rows w, w + 8, ... of the window, kFinRows at a time with
+        // the loads of all of them in flight together; lanes over the chunks
+        for (int rb = 0; rb < nr; rb += kWarps * kFinRows) {
+            float M[kFinRows];
+            double Z[kFinRows];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            double Z = 0.0;
-            for (int k = lane; k < p.n_chunks; k += 32) {
-                const float mk = __ldcg(p.pm + (long)r * p.n_chunks + k);
-                if (mk != -INFINITY) Z += (double)__ldcg(p.pz + (long)r * p.n_chunks + k) * (double)expf(mk - M);
+            for (int k = 0; k < kFinRows; ++k) { M[k] = -INFINITY; Z[k] = 0.0; }
+            for (int k0 = lane; k0 < p.n_chunks; k0 += 32) {
+#pragma unroll
+                for (int k = 0; k < kFinRows; ++k) {
+                    const int r = rb + warp + kWarps * k;
+                    if (r < nr) M[k] = fmaxf(M[k], __ldcg(p.pm + (long)(r0 + r) * p.n_chunks + k0));
+                }
             }
-            Z = warp_sum(Z);
-            if (lane == 0) {
-                const int b = r / p.T, j = r % p.T;
-                int accept = 0;
-                if (j < p.T - 1) {
-                    const int d = p.draft[(long)b * (p.T - 1) + j];
-                    if (d >= 0 && d < p.V) {
-                        const float2 lq = __ldcg(p.row_stats + r);
-                        const double pd = (double)expf(lq.x * it - M) / Z;
-                        const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
-                        accept = u * (double)lq.y < pd ? 1 : 0;
-                    } else {
-                        set_fault(p.fault, FAULT_BAD_DRAFT_ID);
+#pragma unroll
+            for (int k = 0; k < kFinRows; ++k)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) M[k] = fmaxf(M[k], __shfl_xor_sync(0xffffffffu, M[k], o));
+            for (int k0 = lane; k0 < p.n_chunks; k0 += 32) {
+#pragma unroll
+                for (int k = 0; k < kFinRows; ++k) {
+                    const int r = rb + warp + kWarps * k;
+                    if (r < nr) {
+                        const long o = (long)(r0 + r) * p.n_chunks + k0;
+                        const float mk = __ldcg(p.pm + o);
+                        const float zk = __ldcg(p.pz + o);
+                        if (mk != -INFINITY) Z[k] += (double)zk * (double)expf(mk - M[k]);
                     }
                 }
-                acc_s[r - r0] = accept;
-                mz_s[r - r0] = make_float2(M, (float)Z);
+            }
+#pragma unroll
+            for (int k = 0; k < kFinRows; ++k) Z[k] = warp_sum(Z[k]);
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < kFinRows; ++k) {
+                    const int r = rb + warp + kWarps * k;
+                    if (r >= nr) continue;
+                    const int gr = r0 + r, b = gr / p.T, j = gr % p.T;
+                    int accept = 0;
+                    if (j < p.T - 1) {
+                        const int d = p.draft[(long)b * (p.T - 1) + j];
+                        if (d >= 0 && d < p.V) {
+                            const float2 lq = __ldcg(p.row_stats + gr);
+                            const double pd = (double)expf(lq.x * it - M[k]) / Z[k];
+                            const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
+                            accept = u * (double)lq.y < pd ? 1 : 0;
+                        } else {
+                            set_fault(p.fault, FAULT_BAD_DRAFT_ID);
+                        }
+                    }
+                    acc_s[r] = accept;
+                    mz_s[r] = make_float2(M[k], (float)Z[k]);
+                }
             }
         }
         __syncthreads();
@@ -442,20 +528,30 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     }
     if (!elect_last(p.row_counter + b, gridDim.x)) return;
 
-    // last CTA of sequence b: which chunk holds u' * S
+    // last CTA of sequence b: which chunk holds u' * S.  The chunk sums are
+    // first staged in shared memory by the whole CTA (one round trip).
     __shared__ int sel_chunk, sel_res;
     __shared__ double sel_base, sel_x;
+    __shared__ double s_rs[kDrawChunksStaged], s_ps[kDrawChunksStaged];
+    const bool staged = p.n_draw_chunks <= kDrawChunksStaged;
+    if (staged)
+        for (int k = threadIdx.x; k < p.n_draw_chunks; k += kAccThreads) {
+            s_rs[k] = __ldcg(p.rs + (long)b * p.n_draw_chunks + k);
+            s_ps[k] = __ldcg(p.ps + (long)b * p.n_draw_chunks + k);
+        }
+    __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         double Sr = 0.0, Sp = 0.0;
         for (int k = lane; k < p.n_draw_chunks; k += 32) {
-            Sr += __ldcg(p.rs + (long)b * p.n_draw_chunks + k);
-            Sp += __ldcg(p.ps + (long)b * p.n_draw_chunks + k);
+            Sr += staged ? s_rs[k] : __ldcg(p.rs + (long)b * p.n_draw_chunks + k);
+            Sp += staged ? s_ps[k] : __ldcg(p.ps + (long)b * p.n_draw_chunks + k);
         }
         Sr = warp_sum(Sr);
         Sp = warp_sum(Sp);
         const bool use_r = rejected && Sr > 0.0;
-        const double *cs = (use_r ? p.rs : p.ps) + (long)b * p.n_draw_chunks;
+        const double *gcs = (use_r ? p.rs : p.ps) + (long)b * p.n_draw_chunks;
+        auto cs_at = [&](int k) { return staged ? (use_r ? s_rs[k] : s_ps[k]) : __ldcg(gcs + k); };
         const double S = use_r ? Sr : Sp;
         const double x = (double)philox_uniform(p.seed, (uint32_t)n, (uint32_t)b, 1u, p.offset) * S;
         // inclusive prefix over the chunk sums, 32 chunks at a time
@@ -464,7 +560,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
         double found_base = 0.0;
         for (int k0 = 0; k0 < p.n_draw_chunks && found < 0; k0 += 32) {
             const int k = k0 + lane;
-            const double v = k < p.n_draw_chunks ? __ldcg(cs + k) : 0.0;
+            const double v = k < p.n_draw_chunks ? cs_at(k) : 0.0;
             double incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -484,7 +580,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
         if (found < 0) {  // x reached the total through rounding: the last non-empty chunk
             found = last_pos < 0 ? 0 : last_pos;
             double base = 0.0;
-            for (int k = lane; k < found; k += 32) base += __ldcg(cs + k);
+            for (int k = lane; k < found; k += 32) base += cs_at(k);
             found_base = warp_sum(base);
         }
         if (lane == 0) { sel_chunk = found; sel_base = found_base; sel_x = x; sel_res = use_r ? 1 : 0; }
@@ -585,8 +681,8 @@ cudaError_t launch_pdl(void (*kern)(const P), dim3 grid, cudaStream_t st, const 
 cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st) {
     dim3 grid(p.n_chunks, p.B * p.T);
     cudaError_t e;
-    if (p.dt == SD_BF16) SDV_DISPATCH_NV(greedy_kernel, __nv_bfloat16, vec_per_thread<__nv_bfloat16>(p.chunk), grid, st, p, e);
-    else SDV_DISPATCH_NV(greedy_kernel, float, vec_per_thread<float>(p.chunk), grid, st, p, e);
+    if (p.dt == SD_BF16) e = launch_pdl(greedy_kernel<__nv_bfloat16>, grid, st, p);
+    else e = launch_pdl(greedy_kernel<float>, grid, st, p);
     return e;
 }
 

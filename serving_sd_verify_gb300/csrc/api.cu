@@ -177,16 +177,23 @@ size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max
 // ----------------------------------------------------------------------------
 // acceptance planning
 // ----------------------------------------------------------------------------
-int accept_chunk(int rows, int V, int cap) {
-    const int sms = device_sm_count();
-    const long target = 2L * sms;  // CTAs: about two per SM (fewer finisher tickets, one wave)
-    long chunk = ((long)rows * V + target - 1) / target;
+// chunk length of the acceptance pass-1 kernels: every row is cut into
+// floor(per_sm * SMs / rows) chunks (at least one), so the grid fits in one
+// wave of per_sm CTAs per SM (greedy streams its chunk: 3 per SM; the sampled
+// pass 1 holds its chunk in registers: 2 per SM)
+int accept_chunk(int rows, int V, int cap, int per_sm) {
+    const long slots = (long)per_sm * device_sm_count();
+    const long per_row = std::max(1L, slots / std::max(1, rows));
+    long chunk = (V + per_row - 1) / per_row;
     chunk = std::max(2048L, std::min(chunk, (long)cap));
     chunk = (chunk + 7) / 8 * 8;
     return (int)std::min<long>(chunk, (long)V);
 }
 
-int greedy_cap(sd_dtype dt) { return dt == SD_BF16 ? kGreedyChunkMaxBf16 : kGreedyChunkMaxF32; }
+// the greedy pass streams its chunk, so its chunks are sized only by the grid;
+// the sampled pass 1 holds its chunk in registers: at most 8 vectors per thread
+int greedy_cap(sd_dtype) { return 1 << 30; }
+int sample_cap(sd_dtype dt) { return dt == SD_BF16 ? 8 * 8 * 256 : 8 * 4 * 256; }
 
 // greedy workspace: [header: CTAs-finished counter][pval][pidx]
 struct GreedyLayout {
@@ -351,7 +358,7 @@ size_t sd_verify_tree_attention_workspace_size(int B, int T, int Hq, int Hkv, in
 
 size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
-    return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype))).total;
+    return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype), 3)).total;
 }
 
 sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, int B, int T, int V,
@@ -366,7 +373,7 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
     GreedyParams p = {};
     p.draft = draft_ids; p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
     p.n_acc = n_accepted; p.corr = correction_id;
-    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype));
+    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype), 3);
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
     const GreedyLayout gl = greedy_layout(B, T, V, p.chunk);
     if (!workspace || workspace_bytes < gl.total)
@@ -400,7 +407,7 @@ sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, c
     p.draft = tokens; p.parents = parents; p.path = path;
     p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
     p.n_acc = n_accepted; p.corr = correction_id;
-    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype));
+    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype), 3);
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
     const GreedyLayout gl = greedy_layout(B, T, V, p.chunk);
     if (!workspace || workspace_bytes < gl.total)
@@ -421,7 +428,7 @@ sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, c
 size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype) {
     (void)dtype;
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
-    return sample_layout(B, T, V, accept_chunk(B * T, V, kSampleChunkMax), draw_chunk_for(B, V)).total;
+    return sample_layout(B, T, V, accept_chunk(B * T, V, sample_cap(dtype), 2), draw_chunk_for(B, V)).total;
 }
 
 sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, const void *target_logits,
@@ -441,7 +448,7 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.draft = draft_ids; p.q = draft_probs; p.logits = target_logits; p.B = B; p.T = T; p.V = V;
     p.dt = dtype; p.inv_tau = 1.0f / temperature; p.seed = philox_seed; p.offset = philox_offset;
     p.n_acc = n_accepted; p.next_id = next_id;
-    p.chunk = accept_chunk(B * T, V, kSampleChunkMax);
+    p.chunk = accept_chunk(B * T, V, sample_cap(dtype), 2);
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
     p.draw_chunk = draw_chunk_for(B, V);
     p.n_draw_chunks = (V + p.draw_chunk - 1) / p.draw_chunk;

@@ -97,7 +97,7 @@ struct SampleParams {
     uint64_t seed;
     uint32_t offset;
     int32_t *n_acc, *next_id;
-    int chunk, n_chunks;            // pass 1 chunks, chunk <= kSampleChunkMax
+    int chunk, n_chunks;            // pass 1 chunks (streamed)
     int draw_chunk, n_draw_chunks;  // pass 2 chunks, draw_chunk <= kDrawChunkMax
     unsigned int *counters;         // [0]: CTAs of pass 1 finished
     unsigned int *row_counter;      // [B] CTAs of pass 2 finished per sequence
@@ -107,10 +107,7 @@ struct SampleParams {
     double *rs, *ps;                // [B, n_draw_chunks] residual / p chunk sums
     unsigned int *fault;
 };
-constexpr int kSampleChunkMax = 8192;
 constexpr int kDrawChunkMax = 4096;  // pass 2 chunk bound: 16 elements per thread of the in-chunk search
-constexpr int kGreedyChunkMaxBf16 = 16384;
-constexpr int kGreedyChunkMaxF32 = 8192;
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);
 
 // Drafter K/V projector: k_out[n] = h[n] . wk^T, v_out[n] = h[n] . wv^T for

@@ -66,8 +66,9 @@ def test_no_alloc_matches_workspace_entry_point_twice(S):
 def test_no_alloc_rejects_shapes_beyond_its_scratch(S):
     logits = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
     lib = S.load()
-    # a workspace far beyond the fixed scratch: no launch, a clear status
-    status = lib.sd_accept_greedy_noalloc(None, ctypes.c_void_p(logits.data_ptr()), 4096, 16, 1 << 24,
+    # a workspace far beyond the fixed scratch (262,144 rows x 8 bytes of
+    # partials, one chunk per row): no launch, a clear status
+    status = lib.sd_accept_greedy_noalloc(None, ctypes.c_void_p(logits.data_ptr()), 16384, 16, 1 << 24,
                                           S.SD_BF16, None, None, None)
     assert status == S.SD_ERR_WORKSPACE
     assert b"1 MiB" in lib.sd_last_error()
