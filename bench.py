@@ -483,6 +483,27 @@ def reference_arm(args, host=None):
 
 
 # ---------------------------------------------------------------------------
+# ranks (one replica per GPU; no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values (every rank passes its own): the
+    timed region of a run is that of its slowest rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, steps_per_rank, secs):
+    """Blocks verified by all ranks together per second of the slowest rank."""
+    return world * steps_per_rank / secs
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -577,14 +598,10 @@ def main():
     if world > 1:
         dist.barrier()
     sampler.stop()
-    secs = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([secs], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
     clocks = sampler.summary(t_wall0, t_wall1)
     ms_per_step = 1e3 * secs / steps_done
-    value = world * steps_done / secs
+    value = whole_job_value(world, steps_done, secs)
     assert S.sd_fault_word() == 0, "device guard fired during the timed region"
 
     # ---- per-call timing of each kernel class: L2 flushed before every call,
