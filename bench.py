@@ -816,7 +816,7 @@ def main():
                       "us_per_call_back_to_back: average over calls issued back to back in one graph, inputs "
                       f"rotating over {len(sets)} copies ({len(sets) * 52} MB of K/V, more than L2)")
 
-    # ---- roofline: the verify attention (the spec kernel) ----
+    # ---- roofline: the verify attention (the headline kernel) ----
     roofline = None
     if kernels:
         peak, peak_src = hbm_peak(sustained=False)
