@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kAccThreads = 256;
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
-constexpr int kFinRows = 8;       // rows per warp whose chunk partials a finisher loads together
+constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
 constexpr int kDrawChunksStaged = 512;  // chunk sums the draw finisher stages in shared memory
 
 // ----------------------------------------------------------------------------

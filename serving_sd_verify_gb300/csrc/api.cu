@@ -179,8 +179,9 @@ size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max
 // ----------------------------------------------------------------------------
 // chunk length of the acceptance pass-1 kernels: every row is cut into
 // floor(per_sm * SMs / rows) chunks (at least one), so the grid fits in one
-// wave of per_sm CTAs per SM (greedy streams its chunk: 3 per SM; the sampled
-// pass 1 holds its chunk in registers: 2 per SM)
+// wave of per_sm CTAs per SM (greedy streams its chunk: 3 per SM for 64 rows
+// and more, 2 below, where larger chunks mean fewer partials and tickets; the
+// sampled pass 1 holds its chunk in registers: 2 per SM)
 int accept_chunk(int rows, int V, int cap, int per_sm) {
     const long slots = (long)per_sm * device_sm_count();
     const long per_row = std::max(1L, slots / std::max(1, rows));
@@ -193,6 +194,7 @@ int accept_chunk(int rows, int V, int cap, int per_sm) {
 // the greedy pass streams its chunk, so its chunks are sized only by the grid;
 // the sampled pass 1 holds its chunk in registers: at most 8 vectors per thread
 int greedy_cap(sd_dtype) { return 1 << 30; }
+int greedy_per_sm(int rows) { return rows >= 64 ? 3 : 2; }
 int sample_cap(sd_dtype dt) { return dt == SD_BF16 ? 8 * 8 * 256 : 8 * 4 * 256; }
 
 // greedy workspace: [header: CTAs-finished counter][pval][pidx]
@@ -358,7 +360,7 @@ size_t sd_verify_tree_attention_workspace_size(int B, int T, int Hq, int Hkv, in
 
 size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
     if (B < 1 || T < 1 || T > kMaxT || V < 1) return 0;
-    return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype), 3)).total;
+    return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype), greedy_per_sm(B * T))).total;
 }
 
 sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, int B, int T, int V,
@@ -373,7 +375,7 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
     GreedyParams p = {};
     p.draft = draft_ids; p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
     p.n_acc = n_accepted; p.corr = correction_id;
-    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype), 3);
+    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype), greedy_per_sm(B * T));
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
     const GreedyLayout gl = greedy_layout(B, T, V, p.chunk);
     if (!workspace || workspace_bytes < gl.total)
@@ -407,7 +409,7 @@ sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, c
     p.draft = tokens; p.parents = parents; p.path = path;
     p.logits = target_logits; p.B = B; p.T = T; p.V = V; p.dt = dtype;
     p.n_acc = n_accepted; p.corr = correction_id;
-    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype), 3);
+    p.chunk = accept_chunk(B * T, V, greedy_cap(dtype), greedy_per_sm(B * T));
     p.n_chunks = (V + p.chunk - 1) / p.chunk;
     const GreedyLayout gl = greedy_layout(B, T, V, p.chunk);
     if (!workspace || workspace_bytes < gl.total)
