@@ -44,16 +44,20 @@ sd_status cuda_fail(cudaError_t e, const char *what) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// device address of the fault word, looked up once per device (the lookup is
+// idempotent, so threads that race on a first call store the same value)
 unsigned int *fault_ptr() {
-    static unsigned int *ptrs[kMaxDevices] = {};
+    static std::atomic<unsigned int *> ptrs[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!ptrs[dev]) {
+    unsigned int *f = ptrs[dev].load(std::memory_order_acquire);
+    if (!f) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_sd_fault_word) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<unsigned int *>(p);
+        f = static_cast<unsigned int *>(p);
+        ptrs[dev].store(f, std::memory_order_release);
     }
-    return ptrs[dev];
+    return f;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -242,15 +246,15 @@ SampleLayout sample_layout(int B, int T, int V, int chunk, int draw_chunk) {
 }  // namespace
 
 int device_sm_count() {
-    static int cache[kMaxDevices] = {};
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-    if (!cache[dev]) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 sd_status report_error(sd_status s, const char *msg) { return fail(s, "%s", msg); }

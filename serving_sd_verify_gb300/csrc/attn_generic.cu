@@ -16,6 +16,7 @@
 #include "common.cuh"
 
 #include <math.h>
+#include <atomic>
 
 namespace sdv {
 
@@ -246,14 +247,14 @@ cudaError_t launch_generic_t(const AttnParams &p, cudaStream_t st) {
     const size_t smem = sizeof(float) * (kGenTile * (D + 1) + kGenTile * D + 2 * RC * D + 2 * RC);
     auto kern = attn_split_generic_kernel<Tin, D>;
     // the shared-memory opt-in is set once per device, before any graph capture
-    static bool opted_in[64] = {};
+    static std::atomic<bool> opted_in[64];  // per device: shared-memory limit raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+        if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     dim3 grid(p.n_splits, p.Hkv, p.B);
     kern<<<grid, kGenThreads, smem, st>>>(p);

@@ -52,6 +52,7 @@
 
 #include <math.h>
 #include <string.h>
+#include <atomic>
 
 namespace sdv {
 
@@ -695,16 +696,15 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once; the initialisation of a function-local static is thread-safe
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -747,14 +747,14 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B)) return cudaErrorInvalidValue;
     if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B)) return cudaErrorInvalidValue;
     constexpr int smem = Layout::kSmemBytes;
-    static bool opted_in[64] = {};
+    static std::atomic<bool> opted_in[64];  // per device: shared-memory limit raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(attn_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+        if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B);

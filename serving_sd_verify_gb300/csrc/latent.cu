@@ -27,6 +27,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 
 namespace sdv {
 
@@ -330,16 +331,15 @@ latent_output_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_cons
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_lc() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once; the initialisation of a function-local static is thread-safe
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -406,16 +406,16 @@ cudaError_t launch_latent(const LatentParams &p, cudaStream_t st) {
         const cuuint32_t box[4] = {64, (cuuint32_t)kOutKeys, (cuuint32_t)(kOutN / 64), 1};
         if (!encode(&mf4, p.f, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    static bool opted_in[64] = {};
+    static std::atomic<bool> opted_in[64];  // per device: shared-memory limit raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(latent_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScSmem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(latent_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+        if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     e = launch_lc(latent_scores_kernel, dim3((unsigned)p.n_tiles, (unsigned)p.frames, (unsigned)p.n_splits), kLcThreads,
                   kScSmem, st, mf, mq, p);

@@ -21,6 +21,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 
 namespace sdv {
 
@@ -302,16 +303,15 @@ project_small_kernel(const ProjParams p) {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_pj() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once; the initialisation of a function-local static is thread-safe
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -348,15 +348,15 @@ size_t small_smem(int NR, int Hd) { return (size_t)NR * Hd * 2; }
 
 template <int NR, bool kGather>
 cudaError_t launch_small(const ProjParams &p, dim3 grid, cudaStream_t st) {
-    static bool opted_in[64] = {};
+    static std::atomic<bool> opted_in[64];  // per device: shared-memory limit raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(project_small_kernel<NR, kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kProjSmallSmemMax);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+        if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     return launch_pdl_pj(project_small_kernel<NR, kGather>, grid, dim3(kSmallThreads), small_smem(NR, p.Hd), st, p);
 }
@@ -394,14 +394,14 @@ cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st) {
     if (!make_map_2d(&mh, p.h, p.N, p.Hd, p.ld_h, kPjM)) return cudaErrorInvalidValue;
     if (!make_map_2d(&mk, p.wk, p.Dout, p.Hd, p.Hd, kPjN)) return cudaErrorInvalidValue;
     if (!make_map_2d(&mv, p.wv, p.Dout, p.Hd, p.Hd, kPjN)) return cudaErrorInvalidValue;
-    static bool opted_in[64] = {};
+    static std::atomic<bool> opted_in[64];  // per device: shared-memory limit raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !opted_in[dev]) {
+    if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPjSmem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) opted_in[dev] = true;
+        if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     const dim3 grid((unsigned)(((p.N + kPjM - 1) / kPjM) * 2 * ((p.Dout + kPjN - 1) / kPjN)));
     cudaLaunchConfig_t cfg = {};
