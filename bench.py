@@ -892,38 +892,61 @@ def e2e_pass(S, host, ds, device, stream, steps):
     host memory: each step copies them in, runs the step, and reads the results
     back.  The long-context K/V (target cache, projected drafter context) is
     resident state built at prefill and is not re-sent per block; the block's
-    own new K/V slots are written into the cache each step."""
+    own new K/V slots are written into the cache each step.  The per-block
+    inputs sit in two packed pinned buffers (what the attention calls read;
+    what the acceptance calls read) mirrored by two device buffers whose views
+    the calls take, so a block costs a handful of copies, not one per tensor."""
+    import types
     import torch
     a, g, d, s = host["attn"], host["greedy"], host["drafter"], host["sample"]
-    pin = lambda t: t.contiguous().pin_memory()
-    h_q = pin(a["q"])
-    h_blk_k = pin(a["k"][:, CTX - 1:CTX + T - 1])
-    h_blk_v = pin(a["v"][:, CTX - 1:CTX + T - 1])
-    h_layers = [(pin(L["q"]), pin(L["kb"]), pin(L["vb"])) for L in d["layers"]]
-    h_logits, h_draft = pin(g["logits"]), pin(g["draft"])
-    h_sq, h_sdraft = pin(s["q"]), pin(s["draft"])
+
+    def packed(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        hbuf = torch.empty(n, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(n, dtype=torch.uint8, device=device)
+        views = []
+        for t, o in zip(tensors, offs):
+            nb = t.numel() * t.element_size()
+            hbuf[o:o + nb].view(t.dtype).view(t.shape).copy_(t)
+            views.append(dbuf[o:o + nb].view(t.dtype).view(t.shape))
+        return hbuf, dbuf, views
+
+    att_in = [a["q"].contiguous()] + [x.contiguous() for L in d["layers"] for x in (L["q"], L["kb"], L["vb"])]
+    acc_in = [g["logits"].contiguous(), g["draft"].contiguous(), s["q"].contiguous(), s["draft"].contiguous()]
+    h_att, d_att, v_att = packed(att_in)
+    h_acc, d_acc, v_acc = packed(acc_in)
+    h_blk_k = a["k"][:, CTX - 1:CTX + T - 1].contiguous().pin_memory()
+    h_blk_v = a["v"][:, CTX - 1:CTX + T - 1].contiguous().pin_memory()
+    res = torch.zeros(4, dtype=torch.int32, device=device)
+    e2 = types.SimpleNamespace(**vars(ds))
+    e2.q = v_att[0]
+    e2.layers = [tuple(v_att[1 + 3 * li: 4 + 3 * li]) for li in range(LAYERS)]
+    e2.logits, e2.draft, e2.sq, e2.sdraft = v_acc
+    e2.n, e2.c, e2.sn, e2.snx = res[0:1], res[1:2], res[2:3], res[3:4]
     h_out = torch.empty(1, T, HQ, D).pin_memory()
     h_res = torch.empty(4, dtype=torch.int32).pin_memory()
-    res = torch.empty(4, dtype=torch.int32, device=device)
-    h2d = sum(t.numel() * t.element_size() for t in
-              [h_q, h_blk_k, h_blk_v, h_logits, h_draft, h_sq, h_sdraft] + [x for L in h_layers for x in L])
+    h2d = h_att.numel() + h_acc.numel() + h_blk_k.numel() * 2 + h_blk_v.numel() * 2
     d2h = h_out.numel() * 4 + h_res.numel() * 4
+    side = torch.cuda.Stream(device)
 
     def body():
-        ds.q.copy_(h_q, non_blocking=True)
+        cur = torch.cuda.current_stream()
+        # the acceptance inputs (target logits, draft ids and probabilities:
+        # 14.6 of the 15.3 MB) travel on a side stream while the attention
+        # calls run, and join before the acceptance calls
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            d_acc.copy_(h_acc, non_blocking=True)
+        d_att.copy_(h_att, non_blocking=True)
         ds.k[:, CTX - 1:CTX + T - 1].copy_(h_blk_k, non_blocking=True)
         ds.v[:, CTX - 1:CTX + T - 1].copy_(h_blk_v, non_blocking=True)
-        for (dq, dkb, dvb), (hq, hkb, hvb) in zip(ds.layers, h_layers):
-            dq.copy_(hq, non_blocking=True)
-            dkb.copy_(hkb, non_blocking=True)
-            dvb.copy_(hvb, non_blocking=True)
-        ds.logits.copy_(h_logits, non_blocking=True)
-        ds.draft.copy_(h_draft, non_blocking=True)
-        ds.sq.copy_(h_sq, non_blocking=True)
-        ds.sdraft.copy_(h_sdraft, non_blocking=True)
-        run_step(S, ds, stream)
-        res[0:1].copy_(ds.n); res[1:2].copy_(ds.c); res[2:3].copy_(ds.sn); res[3:4].copy_(ds.snx)
-        h_out.copy_(ds.out, non_blocking=True)
+        run_step(S, e2, stream, ("draft", "verify"))
+        cur.wait_stream(side)
+        run_step(S, e2, stream, ("greedy", "sample"))
+        h_out.copy_(e2.out, non_blocking=True)
         h_res.copy_(res, non_blocking=True)
 
     def one():
@@ -958,9 +981,11 @@ def e2e_pass(S, host, ds, device, stream, steps):
         del g
     return {"value": steps / sec, "unit": "blocks/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "eager_value": steps / sec_eager,
-            "note": "per-block inputs from pinned host memory, results read back every step, the host waiting "
-                    "for them; the step (copies and C-ABI calls) replayed from one CUDA graph (eager_value: the "
-                    "same step issued call by call from Python); context K/V resident"}
+            "note": "per-block inputs from pinned host memory (two packed buffers plus the block's K/V slots), "
+                    "results read back every step, the host waiting for them; the acceptance inputs copied on "
+                    "a side stream while the attention calls run; the step (copies and C-ABI calls) replayed "
+                    "from one CUDA graph (eager_value: the same step issued call by call from Python); context "
+                    "K/V resident"}
 
 
 if __name__ == "__main__":
