@@ -7,12 +7,12 @@
 // the whole context (prefill) and then, every cycle, over the few positions
 // just committed (the incremental append).
 //
-// Prefill (many rows): a tcgen05 GEMM.  One CTA per (128-row tile,
-// 256-column tile of [K | V]), the column tiles of a row tile adjacent in
-// launch order; the hidden-state and weight tiles (64 features deep, 128-byte
-// swizzle) stream through a 4-stage TMA ring; one thread issues M128 N256 K16
-// MMAs into a 256-column fp32 accumulator in tensor memory; four warps
-// convert it to bf16 and store it.
+// Prefill (many rows): a persistent tcgen05 GEMM, one CTA per SM walking the
+// (128-row tile, 256-column tile of [K | V]) tiles; the hidden-state and
+// weight tiles (64 features deep, 128-byte swizzle) stream through a 4-stage
+// TMA ring that runs on across tiles; one thread issues M128 N256 K16 MMAs
+// into one of two 256-column fp32 accumulators in tensor memory while four
+// warps convert the other to bf16 and store it.
 // Append (a few rows): bound by reading the weights once, so CUDA cores: four
 // warps per output column, lanes over the features, up to kProjSmallRows rows
 // per CTA.
@@ -21,6 +21,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <algorithm>
 #include <atomic>
 
 namespace sdv {
@@ -34,7 +35,7 @@ constexpr int kPjABytes = kPjM * 128;   // [128 rows x 64 features] bf16
 constexpr int kPjBBytes = kPjN * 128;   // [256 out-columns x 64 features] bf16
 constexpr int kPjStageBytes = kPjABytes + kPjBBytes;
 constexpr int kPjOffBar = kPjStages * kPjStageBytes;
-constexpr int kPjNumBars = 2 * kPjStages + 1;
+constexpr int kPjNumBars = 2 * kPjStages + 5;   // ring full/empty, accumulator full/empty x 2, done
 constexpr int kPjOffMisc = kPjOffBar + 8 * kPjNumBars;
 constexpr int kPjSmem = kPjOffMisc + 16 + 1024;
 static_assert(kPjSmem <= 227 * 1024, "shared memory per CTA");
@@ -52,33 +53,36 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t *sbase = smem_raw + (base - raw_u32);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the column tiles of one row tile are adjacent in launch order, so the
-    // row tile's hidden states come from memory once and from L2 after that
+    // persistent: CTA b takes tiles b, b + grid, ...; tile t is (row tile
+    // t / (2 n_per), column tile t % (2 n_per)), so the CTAs working at the
+    // same time share row tiles and the hidden states come from L2 after the
+    // first read
     const int n_per = (p.Dout + kPjN - 1) / kPjN;   // column tiles per matrix
-    const int mt = blockIdx.x / (2 * n_per), nt = blockIdx.x % (2 * n_per);
-    const bool is_v = nt >= n_per;
-    const int col0 = (is_v ? nt - n_per : nt) * kPjN;
-    const CUtensorMap *tw = is_v ? &tm_wv : &tm_wk;
+    const int n_tiles = ((p.N + kPjM - 1) / kPjM) * 2 * n_per;
     const int nk = (p.Hd + kPjK - 1) / kPjK;
 
     const uint32_t bar0 = base + kPjOffBar;
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (kPjStages + i); };
-    const uint32_t done_bar = bar0 + 8u * (2 * kPjStages);
+    auto acc_full = [&](int i) { return bar0 + 8u * (2 * kPjStages + i); };
+    auto acc_empty = [&](int i) { return bar0 + 8u * (2 * kPjStages + 2 + i); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kPjStages + 4);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + kPjOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + kPjOffMisc + 8);
 
     if (tid == 0) {
         for (int i = 0; i < kPjStages; ++i) { mbar_init(full_bar(i), 1); mbar_init(empty_bar(i), 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full(i), 1); mbar_init(acc_empty(i), 128); }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_h)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tw)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_wk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_wv)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_holder)), "r"(256) : "memory");
+                         smem_u32(tmem_holder)), "r"(2 * kPjN) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 #if __CUDA_ARCH__ >= 900
@@ -93,20 +97,28 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kt = 0; kt < nk; ++kt) {
-                const int st = kt % kPjStages;
-                if (kt >= kPjStages &&
-                    !mbar_wait(empty_bar(st), ((kt / kPjStages) - 1) & 1, abort_flag, p.fault))
-                    break;
-                const uint32_t a = base + st * kPjStageBytes;
-                mbar_arrive_expect_tx(full_bar(st), (uint32_t)kPjStageBytes);
-                tma_load_2d(a, &tm_h, full_bar(st), kt * kPjK, mt * kPjM);
-                tma_load_2d(a + kPjABytes, tw, full_bar(st), kt * kPjK, col0);
-                issued = kt + 1;
+            int g = 0;                               // (tile, k step) pairs issued
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+                const int mt = t / (2 * n_per), nt = t % (2 * n_per);
+                const bool is_v = nt >= n_per;
+                const CUtensorMap *tw = is_v ? &tm_wv : &tm_wk;
+                const int col0 = (is_v ? nt - n_per : nt) * kPjN;
+                for (int kt = 0; kt < nk; ++kt, ++g) {
+                    const int st = g % kPjStages;
+                    if (g >= kPjStages &&
+                        !mbar_wait(empty_bar(st), ((g / kPjStages) - 1) & 1, abort_flag, p.fault)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a = base + st * kPjStageBytes;
+                    mbar_arrive_expect_tx(full_bar(st), (uint32_t)kPjStageBytes);
+                    tma_load_2d(a, &tm_h, full_bar(st), kt * kPjK, mt * kPjM);
+                    tma_load_2d(a + kPjABytes, tw, full_bar(st), kt * kPjK, col0);
+                }
             }
             if (*abort_flag)  // let the copies already issued land before the CTA exits
-                for (int u = max(0, issued - kPjStages); u < issued; ++u)
+                for (int u = max(0, g - kPjStages); u < g; ++u)
                     mbar_wait(full_bar(u % kPjStages), (u / kPjStages) & 1, nullptr, p.fault);
         }
         __syncwarp();
@@ -114,56 +126,77 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kPjM, kPjN, false);
-            for (int kt = 0; kt < nk; ++kt) {
-                const int st = kt % kPjStages;
-                if (!mbar_wait(full_bar(st), (kt / kPjStages) & 1, abort_flag, p.fault)) break;
+            int g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x, i = 0; ok && t < n_tiles; t += gridDim.x, ++i) {
+                const int acc = i & 1;
+                // the epilogue has drained this accumulator's previous tile
+                if (i >= 2 && !mbar_wait(acc_empty(acc), ((i >> 1) - 1) & 1, abort_flag, p.fault)) break;
                 tc_fence_after();
-                const uint32_t a = base + st * kPjStageBytes, bm = a + kPjABytes;
+                const uint32_t d = tmem + (uint32_t)(acc * kPjN);
+                for (int kt = 0; kt < nk; ++kt, ++g) {
+                    const int st = g % kPjStages;
+                    if (!mbar_wait(full_bar(st), (g / kPjStages) & 1, abort_flag, p.fault)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = base + st * kPjStageBytes, bm = a + kPjABytes;
 #pragma unroll
-                for (int kk = 0; kk < kPjK / 16; ++kk)
-                    umma_ss(tmem, sw128_desc(a + kk * 32, 16, 1024), sw128_desc(bm + kk * 32, 16, 1024), idesc,
-                            (kt > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(empty_bar(st));
+                    for (int kk = 0; kk < kPjK / 16; ++kk)
+                        umma_ss(d, sw128_desc(a + kk * 32, 16, 1024), sw128_desc(bm + kk * 32, 16, 1024), idesc,
+                                (kt > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(empty_bar(st));
+                }
+                if (ok) umma_commit(acc_full(acc));
             }
-            umma_commit(done_bar);  // every MMA issued, complete or not, before the epilogue and teardown
+            umma_commit(done_bar);  // every MMA issued, complete or not, before teardown
         }
         __syncwarp();
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- epilogue
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, p.fault));
-        tc_fence_after();
         const int r = (warp - 4) * 32 + lane;   // tensor-memory lane = tile row
-        const long grow = (long)mt * kPjM + r;
-        const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        __nv_bfloat16 *out = (is_v ? p.v_out : p.k_out) + grow * p.ld_out + col0;
+        for (int t = blockIdx.x, i = 0; t < n_tiles; t += gridDim.x, ++i) {
+            const int acc = i & 1;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full(acc), (i >> 1) & 1, abort_flag, p.fault));
+            if (!ok) break;
+            tc_fence_after();
+            const int mt = t / (2 * n_per), nt = t % (2 * n_per);
+            const bool is_v = nt >= n_per;
+            const int col0 = (is_v ? nt - n_per : nt) * kPjN;
+            const long grow = (long)mt * kPjM + r;
+            const uint32_t taddr = tmem + (uint32_t)(acc * kPjN) + ((uint32_t)((warp & 3) * 32) << 16);
+            __nv_bfloat16 *out = (is_v ? p.v_out : p.k_out) + grow * p.ld_out + col0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kPjN; c0 += 32) {
-            uint32_t acc[32];
-            tmem_ld32_async(taddr + (uint32_t)c0, acc);   // warp-wide: before any divergence
-            tmem_ld_wait();
-            tmem_ld_bind(acc);
-            if (ok && !*abort_flag && grow < p.N && col0 + c0 < p.Dout) {
-                uint32_t pk[16];
+            for (int c0 = 0; c0 < kPjN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32_async(taddr + (uint32_t)c0, v);   // warp-wide: before any divergence
+                tmem_ld_wait();
+                tmem_ld_bind(v);
+                if (!*abort_flag && grow < p.N && col0 + c0 < p.Dout) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const __nv_bfloat162 h2 =
-                        __floats2bfloat162_rn(__uint_as_float(acc[2 * e]), __uint_as_float(acc[2 * e + 1]));
-                    pk[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                    for (int e = 0; e < 16; ++e) {
+                        const __nv_bfloat162 h2 =
+                            __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                        pk[e] = *reinterpret_cast<const uint32_t *>(&h2);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + c0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(out + c0);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
+            tc_fence_before();
+            mbar_arrive(acc_empty(acc));            // this thread's lane of the accumulator is read
         }
-        tc_fence_before();
     }
     __syncthreads();
     if (warp == 1) {
-        // the epilogue waited on done_bar: every MMA has completed
-        if (*abort_flag && lane == 0) mbar_wait(done_bar, 0, nullptr, p.fault);
+        // every MMA has completed before the tensor memory is freed
+        if (lane == 0) mbar_wait(done_bar, 0, nullptr, p.fault);
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kPjN) : "memory");
     }
 }
 
@@ -403,7 +436,8 @@ cudaError_t launch_project(const ProjParams &p, int path, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
-    const dim3 grid((unsigned)(((p.N + kPjM - 1) / kPjM) * 2 * ((p.Dout + kPjN - 1) / kPjN)));
+    const long n_tiles = (long)((p.N + kPjM - 1) / kPjM) * 2 * ((p.Dout + kPjN - 1) / kPjN);
+    const dim3 grid((unsigned)std::min<long>(n_tiles, device_sm_count()));   // persistent: one CTA per SM
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kPjThreads);
