@@ -26,6 +26,7 @@ namespace sdv {
 namespace {
 
 constexpr int kAccThreads = 256;
+constexpr int kArgChains = 4;     // independent argmax chains per thread in the greedy stream
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
 constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
 constexpr int kDrawChunksStaged = 512;  // chunk sums the draw finisher stages in shared memory
@@ -208,11 +209,17 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     while (a0 < hi && ((base + (uintptr_t)a0 * sizeof(Tin)) & 15u)) ++a0;
     const int nvec = (hi - a0) / PV, a1 = a0 + nvec * PV;
     const uint4 *vp = reinterpret_cast<const uint4 *>(lg + a0);
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+    // kArgChains independent (value, index) chains per thread, so that
+    // consecutive compares do not wait on each other; merged at the end by
+    // the same rule (larger value, then lower index), so the result does not
+    // depend on which chain saw which element
+    float cv[kArgChains];
+    int ci[kArgChains];
+#pragma unroll
+    for (int k = 0; k < kArgChains; ++k) { cv[k] = -INFINITY; ci[k] = INT_MAX; }
     for (int i = lo + tid; i < a0; i += kAccThreads) {
         const float x = Elem<Tin>::load(lg + i);
-        if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
+        if (argmax_better(x, i, cv[0], ci[0])) { cv[0] = x; ci[0] = i; }
     }
     uint4 cur[kGreedyBatch], nxt[kGreedyBatch];
     auto load = [&](uint4 (&d)[kGreedyBatch], int v0) {
@@ -233,8 +240,8 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
                 Vec16<Tin>::unpack(cur[u], f);
 #pragma unroll
                 for (int e = 0; e < PV; ++e) {
-                    const int i = a0 + vi * PV + e;
-                    if (argmax_better(f[e], i, bv, bi)) { bv = f[e]; bi = i; }
+                    const int i = a0 + vi * PV + e, k = e % kArgChains;
+                    if (argmax_better(f[e], i, cv[k], ci[k])) { cv[k] = f[e]; ci[k] = i; }
                 }
             }
         }
@@ -243,8 +250,13 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     }
     for (int i = a1 + tid; i < hi; i += kAccThreads) {
         const float x = Elem<Tin>::load(lg + i);
-        if (argmax_better(x, i, bv, bi)) { bv = x; bi = i; }
+        if (argmax_better(x, i, cv[0], ci[0])) { cv[0] = x; ci[0] = i; }
     }
+    float bv = cv[0];
+    int bi = ci[0];
+#pragma unroll
+    for (int k = 1; k < kArgChains; ++k)
+        if (argmax_better(cv[k], ci[k], bv, bi)) { bv = cv[k]; bi = ci[k]; }
     block_argmax(bv, bi);
     if (tid == 0) {
         p.pval[(long)row * p.n_chunks + c] = bv;
