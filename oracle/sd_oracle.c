@@ -17,7 +17,9 @@
  *    values by a linear map of hidden states the target has already cached.
  *  - "SpecFLASH" README, section on inference: the target checks all drafted
  *    tokens at once under the usual speculative accept/reject test, which
- *    keeps the output distribution equal to the target's (lossless).
+ *    keeps the output distribution equal to the target's (lossless); and the
+ *    first of its draft model's two components, the latent visual compressor
+ *    softmax(C . F_V^T) . F_V over a frame's visual features.
  *  - Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *    Easy as 1, 2, 3", SC'11, section 3.2 (the Philox round and key schedule).
  *
@@ -31,6 +33,13 @@
  *    whose inclusive ascending cumulative sum of max(p - q, 0) exceeds u' * S.
  *  - Philox counter = (row j, batch b, stream, offset), key = (seed lo, seed
  *    hi); the uniform is (word0 >> 8) * 2^-24.
+ *  - a tree has at most 16 nodes; node j sees the context before the anchor
+ *    and the block slots of its ancestors and itself; the committed path ends
+ *    at the deepest accepted node (lowest index among equals).
+ *  - commit: committed tokens = kept proposals + the next token, ctx_len
+ *    advances by their count, the next token becomes the anchor; a tree's
+ *    kept K/V rows move to consecutive positions after the anchor.
+ *  - the compressor applies no scale to its scores (the formula has none).
  */
 #include <math.h>
 #include <stdint.h>
