@@ -116,3 +116,55 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sd_verify, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         sd_verify.load()
+
+
+def test_host_validation_of_the_tree_projector_commit_and_compressor_calls(S):
+    lib = S.load()
+    st = S.Strides(100 * 4 * 128, 4 * 128, 128)
+    fake = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+    # tree verify: no tree mask
+    r = lib.sd_verify_tree_attention(fake, fake, fake, st, fake, 100, None, fake, 1, 16, 28, 4, 128, 0, 1.0, fake,
+                                     1 << 30, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # tree greedy: no parents
+    r = lib.sd_accept_tree_greedy(fake, None, fake, 1, 16, 100, 0, fake, fake, fake, fake, 1 << 20, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # projector: fp32 unsupported, Dout not a multiple of 32, N = 0 is a no-op
+    assert lib.sd_project_kv(fake, 64, fake, fake, 4, 64, 64, fake, fake, 64, 1, None) == S.SD_ERR_UNSUPPORTED
+    assert lib.sd_project_kv(fake, 64, fake, fake, 4, 64, 48, fake, fake, 64, 0, None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_project_kv(fake, 64, fake, fake, 0, 64, 64, fake, fake, 64, 0, None) == S.SD_OK
+    assert lib.sd_last_projector_path() == 0
+    # commit-time append: 16 rows of Hd = 8000 do not fit its shared memory
+    r = lib.sd_project_kv_commit(fake, 8000, 16 * 8000, fake, fake, 8000, 64, fake, None, fake, 1, 16, fake, fake,
+                                 64 * 100, 64, 100, 0, None)
+    assert r == S.SD_ERR_UNSUPPORTED
+    # commit: T out of range, proposal stride too small for a chain
+    r = lib.sd_commit_tokens(fake, 15, None, fake, fake, 1, 17, fake, 1000, None, fake, fake, 64, fake, None, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    r = lib.sd_commit_tokens(fake, 14, None, fake, fake, 1, 16, fake, 1000, None, fake, fake, 64, fake, None, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # tree K/V compaction: a (position, head) row over 512 bytes, a missing path
+    big = S.Strides(100 * 512, 512, 512)
+    r = lib.sd_compact_tree_kv(fake, fake, big, fake, fake, fake, 1, 16, 100, 1, 512, 0, None)
+    assert r == S.SD_ERR_UNSUPPORTED
+    r = lib.sd_compact_tree_kv(fake, fake, st, fake, None, fake, 1, 16, 100, 4, 128, 0, None)
+    assert r == S.SD_ERR_INVALID_ARG
+    # compressor: 65 queries, d not a multiple of 64, fp32, a workspace too small
+    ws = S.sd_latent_compress_workspace_size(2, 576, 64, 256)
+    assert ws > 0 and S.sd_latent_compress_workspace_size(2, 576, 65, 256) == 0
+    assert lib.sd_latent_compress(fake, fake, 256, 576 * 256, 2, 576, 65, 256, fake, 256, 65 * 256, 0, fake, ws,
+                                  None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_latent_compress(fake, fake, 96, 576 * 96, 2, 576, 64, 96, fake, 96, 64 * 96, 0, fake, ws,
+                                  None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_latent_compress(fake, fake, 256, 576 * 256, 2, 576, 64, 256, fake, 256, 64 * 256, 1, fake, ws,
+                                  None) == S.SD_ERR_UNSUPPORTED
+    assert lib.sd_latent_compress(fake, fake, 256, 576 * 256, 2, 576, 64, 256, fake, 256, 64 * 256, 0, fake, 64,
+                                  None) == S.SD_ERR_WORKSPACE
+
+
+def test_next_row_workspace_sizes(S):
+    assert S.sd_verify_tree_attention_workspace_size(1, 16, 28, 4, 128, 25_119) > 256
+    assert S.sd_accept_tree_greedy_workspace_size(1, 16, 152_064) == S.sd_accept_greedy_workspace_size(1, 16, 152_064)
+    a = S.sd_latent_compress_workspace_size(16, 576, 64, 4096)
+    b = S.sd_latent_compress_workspace_size(32, 576, 64, 4096)
+    assert 0 < a < b
