@@ -29,6 +29,7 @@ constexpr int kAccThreads = 256;
 constexpr int kArgChains = 4;     // independent argmax chains per thread in the greedy stream
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
 constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
+constexpr int kFinStaged = 1024;  // chunk partials the greedy finisher stages in shared memory at once
 constexpr int kDrawChunksStaged = 512;  // chunk sums the draw finisher stages in shared memory
 
 // ----------------------------------------------------------------------------
@@ -272,11 +273,34 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     const int W = (kAccThreads / p.T) * p.T;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kWarps = kAccThreads / 32;
+    __shared__ float fin_v[kFinStaged];
+    __shared__ int fin_i[kFinStaged];
     for (int r0 = 0; r0 < R; r0 += W) {
         const int nr = min(R - r0, W);
-        // warp w takes rows w, w + 8, ... of the window, kFinRows at a time with
-        // all their partial loads in flight together; lanes over the chunks
-        for (int rb = 0; rb < nr; rb += kWarps * kFinRows) {
+        const int np = nr * p.n_chunks;   // the window's partials, contiguous in pval / pidx
+        if (np <= kFinStaged) {
+            // all of them in flight at once (the grids are sized so that this
+            // is the usual case), then a thread per row over its chunks
+            for (int u = threadIdx.x; u < np; u += kAccThreads) {
+                fin_v[u] = __ldcg(p.pval + (long)r0 * p.n_chunks + u);
+                fin_i[u] = __ldcg(p.pidx + (long)r0 * p.n_chunks + u);
+            }
+            __syncthreads();
+            for (int r = threadIdx.x; r < nr; r += kAccThreads) {
+                float v = -INFINITY;
+                int ix = INT_MAX;
+                for (int k = 0; k < p.n_chunks; ++k) {
+                    const float pv = fin_v[r * p.n_chunks + k];
+                    const int pi = fin_i[r * p.n_chunks + k];
+                    if (argmax_better(pv, pi, v, ix)) { v = pv; ix = pi; }
+                }
+                if (ix == INT_MAX) { set_fault(p.fault, FAULT_NAN_ROW); ix = 0; }
+                am[r] = ix;
+            }
+        }
+        // otherwise warp w takes rows w, w + 8, ... of the window, kFinRows at a
+        // time with all their partial loads in flight together; lanes over the chunks
+        for (int rb = 0; np > kFinStaged && rb < nr; rb += kWarps * kFinRows) {
             float v[kFinRows];
             int ix[kFinRows];
 #pragma unroll
