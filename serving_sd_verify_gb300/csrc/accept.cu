@@ -427,11 +427,49 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     const int W = (kAccThreads / p.T) * p.T;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kWarps = kAccThreads / 32;
+    // the accept test of row gr with its max M and normaliser Z
+    auto test_row = [&](int gr, float Mr, double Zr) {
+        const int b = gr / p.T, j = gr % p.T;
+        int accept = 0;
+        if (j < p.T - 1) {
+            const int d = p.draft[(long)b * (p.T - 1) + j];
+            if (d >= 0 && d < p.V) {
+                const float2 lq = __ldcg(p.row_stats + gr);
+                const double pd = (double)expf(lq.x * it - Mr) / Zr;
+                const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
+                accept = u * (double)lq.y < pd ? 1 : 0;
+            } else {
+                set_fault(p.fault, FAULT_BAD_DRAFT_ID);
+            }
+        }
+        return accept;
+    };
+    __shared__ float fin_m[kFinStaged], fin_z[kFinStaged];
     for (int r0 = 0; r0 < R; r0 += W) {
         const int nr = min(R - r0, W);
-        // warp w takes rows w, w + 8, ... of the window, kFinRows at a time with
-        // the loads of all of them in flight together; lanes over the chunks
-        for (int rb = 0; rb < nr; rb += kWarps * kFinRows) {
+        const int np = nr * p.n_chunks;   // the window's partials, contiguous in pm / pz
+        if (np <= kFinStaged) {
+            // all of them in flight at once, then a thread per row
+            for (int u = threadIdx.x; u < np; u += kAccThreads) {
+                fin_m[u] = __ldcg(p.pm + (long)r0 * p.n_chunks + u);
+                fin_z[u] = __ldcg(p.pz + (long)r0 * p.n_chunks + u);
+            }
+            __syncthreads();
+            for (int r = threadIdx.x; r < nr; r += kAccThreads) {
+                float Mr = -INFINITY;
+                for (int k = 0; k < p.n_chunks; ++k) Mr = fmaxf(Mr, fin_m[r * p.n_chunks + k]);
+                double Zr = 0.0;
+                for (int k = 0; k < p.n_chunks; ++k) {
+                    const float mk = fin_m[r * p.n_chunks + k];
+                    if (mk != -INFINITY) Zr += (double)fin_z[r * p.n_chunks + k] * (double)expf(mk - Mr);
+                }
+                acc_s[r] = test_row(r0 + r, Mr, Zr);
+                mz_s[r] = make_float2(Mr, (float)Zr);
+            }
+        }
+        // otherwise warp w takes rows w, w + 8, ... of the window, kFinRows at a
+        // time with the loads of all of them in flight together; lanes over the chunks
+        for (int rb = 0; np > kFinStaged && rb < nr; rb += kWarps * kFinRows) {
             float M[kFinRows];
             double Z[kFinRows];
 #pragma unroll
@@ -466,20 +504,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
                 for (int k = 0; k < kFinRows; ++k) {
                     const int r = rb + warp + kWarps * k;
                     if (r >= nr) continue;
-                    const int gr = r0 + r, b = gr / p.T, j = gr % p.T;
-                    int accept = 0;
-                    if (j < p.T - 1) {
-                        const int d = p.draft[(long)b * (p.T - 1) + j];
-                        if (d >= 0 && d < p.V) {
-                            const float2 lq = __ldcg(p.row_stats + gr);
-                            const double pd = (double)expf(lq.x * it - M[k]) / Z[k];
-                            const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
-                            accept = u * (double)lq.y < pd ? 1 : 0;
-                        } else {
-                            set_fault(p.fault, FAULT_BAD_DRAFT_ID);
-                        }
-                    }
-                    acc_s[r] = accept;
+                    acc_s[r] = test_row(r0 + r, M[k], Z[k]);
                     mz_s[r] = make_float2(M[k], (float)Z[k]);
                 }
             }
