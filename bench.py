@@ -246,6 +246,92 @@ def kernels_per_step():
     return LAYERS * ATTN_LAUNCHES["draft"] + ATTN_LAUNCHES["verify"] + 1 + 2
 
 
+def verify_bytes(ctx_list, T_, Hq, Hkv, D_):
+    """Algorithmic bytes of one verify call: every cache key a row can see,
+    K and V (bf16), read once; Q read once (bf16); the output written once (fp32)."""
+    n_keys = sum(int(c) + T_ - 1 for c in ctx_list)
+    B = len(ctx_list)
+    return 2 * n_keys * Hkv * D_ * 2 + B * T_ * Hq * D_ * 2 + B * T_ * Hq * D_ * 4
+
+
+def time_back_to_back(calls, n_copies, stream, reps=10):
+    """Average seconds per call of calls[i % n_copies] issued 2 x n_copies times
+    in one CUDA graph, replayed `reps` times after 3 warm-up replays."""
+    import torch
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(2 * n_copies):
+            calls[i % n_copies]()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e_b.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e_a.elapsed_time(e_b) / 1e3 / (reps * 2 * n_copies)
+
+
+def config_verify_pass(S, device, stream, n):
+    """Verify attention of the ragged batch (workload 3) or the 72B-shaped
+    batch (workload 5) at full size, calls back to back over 2 input copies
+    (each copy alone is larger than L2).  Returns (seconds per call, bytes)."""
+    import torch
+    from serving_sd_verify_gb300 import workloads as W
+    att = W.config(n)["attn"]
+    B_, T_, Hq, D_ = att["q"].shape
+    Hkv = att["k"].shape[2]
+    max_ctx = att["max_ctx"]
+    copies = []
+    for _ in range(2):
+        q, k, v, ctx = (att[x].to(device).contiguous() for x in ("q", "k", "v", "ctx"))
+        out = torch.zeros(B_, T_, Hq, D_, device=device)
+        ws = S.workspace(S.sd_verify_attention_workspace_size(B_, T_, Hq, Hkv, D_, att["max_ctx"]), device)
+        copies.append((q, k, v, ctx, out, ws))
+    del att
+
+    def call(c):
+        return lambda: S.sd_verify_attention(c[0], c[1], c[2], c[3], max_ctx, c[4], 1.0, c[5], stream)
+    calls = [call(c) for c in copies]
+    per = time_back_to_back(calls, len(copies), stream)
+    ctx_list = copies[0][3].cpu().tolist()
+    del copies, calls
+    torch.cuda.empty_cache()
+    return per, verify_bytes(ctx_list, T_, Hq, Hkv, D_)
+
+
+def drafter_layer_pass(S, ds, stream, flush, reps=20):
+    """The step's 4 drafter layers, one graph replay after an L2 flush, with
+    events between the calls: layer 1 streams the projected context from HBM,
+    layers 2-4 find it in L2.  Returns (layer-1 seconds, mean of layers 2-4)."""
+    import torch
+    with torch.cuda.stream(stream):
+        run_step(S, ds, stream, ("draft",))
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(LAYERS + 1)]
+    t1, t234 = [], []
+    for i in range(reps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            evs[0].record(stream)
+            for li, (q, kb, vb) in enumerate(ds.layers):
+                S.sd_draft_block_attention(q, ds.kc, ds.vc, ds.nctx, CTX, kb, vb, ds.dout[li], 1.0, ds.ws_d,
+                                           stream)
+                evs[li + 1].record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            t1.append(evs[0].elapsed_time(evs[1]) / 1e3)
+            t234.append(evs[1].elapsed_time(evs[LAYERS]) / 1e3 / (LAYERS - 1))
+    return statistics.median(t1), statistics.median(t234)
+
+
 def run_step(S, ds, stream=None, parts=("draft", "verify", "greedy", "sample")):
     if "draft" in parts:
         for li, (q, kb, vb) in enumerate(ds.layers):
@@ -419,11 +505,15 @@ def time_graph(g, reps, stream):
 # CPU baseline: the oracle on a bounded sample of one step
 # ---------------------------------------------------------------------------
 
-def cpu_step_sample(host, rows_per_call):
+def cpu_step_sample(host, rows_per_call, threads=1):
     """Oracle time of one step, extrapolated from `rows_per_call` query rows per
-    attention call (all rows of both acceptance calls run in full)."""
+    attention call (all rows of both acceptance calls run in full).  With
+    threads > 1 each attention call's rows are cut into that many slices run
+    by a thread pool (the oracle's C routines release the GIL), so the
+    attention part uses that many host cores; the acceptance calls stay on one."""
     import numpy as np
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     a, g, d, s = host["attn"], host["greedy"], host["drafter"], host["sample"]
     G = HQ // HKV
     rng = np.random.default_rng(0)
@@ -437,17 +527,35 @@ def cpu_step_sample(host, rows_per_call):
     lay = [sliced(L["q"], d["kc"], d["vc"], CTX, L["kb"], L["vb"]) for L in d["layers"]]
     lg = g["logits"].double().numpy()
     sq = s["q"].double().numpy()
+    slices = [sl for sl in np.array_split(rows, max(1, threads)) if sl.size]
+    pool = ThreadPoolExecutor(max_workers=len(slices)) if len(slices) > 1 else None
+
+    def attn(*a, **kw):
+        if pool is None:
+            oracle.attention_rows(*a, rows=rows, **kw)
+        else:
+            list(pool.map(lambda sl: oracle.attention_rows(*a, rows=sl, **kw), slices))
     t0 = time.perf_counter()
     for (q, kk, vv, kb, vb) in lay:
-        oracle.attention_rows(q, kk, vv, [CTX], 1.0, mode=1, kb=kb, vb=vb, rows=rows)
-    oracle.attention_rows(qv, kv_, vv_, [CTX], 1.0, rows=rows)
+        attn(q, kk, vv, [CTX], 1.0, mode=1, kb=kb, vb=vb)
+    attn(qv, kv_, vv_, [CTX], 1.0)
     t_attn = time.perf_counter() - t0
+    if pool is not None:
+        pool.shutdown()
     t1 = time.perf_counter()
     oracle.accept_greedy(g["draft"].numpy(), lg)
     oracle.accept_sample(s["draft"].numpy(), sq, lg, 1.0, 1234, 0)
     t_acc = time.perf_counter() - t1
     step = t_attn * (total_rows / rows_per_call) + t_acc
     return step, t_attn + t_acc
+
+
+def host_cores():
+    """Host cores this process may run on (the thread count of the all-core legs)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def reference_arm(args, host=None):
@@ -457,25 +565,27 @@ def reference_arm(args, host=None):
     if host is None:
         import torch
         host = make_inputs("cuda" if torch.cuda.is_available() else "cpu")
-    rows = args.ref_rows
+    cores = host_cores()
+    rows = min(T * HQ, args.ref_rows * cores)
     for _ in range(args.warmup):
-        cpu_step_sample(host, max(2, rows // 4))
+        cpu_step_sample(host, max(cores, rows // 4), cores)
     times, work = [], 0.0
     for _ in range(args.steps):
-        st, w = cpu_step_sample(host, rows)
+        st, w = cpu_step_sample(host, rows, cores)
         times.append(st)
         work += w
     ms = 1e3 * statistics.mean(times)
     v = 1e3 / ms
-    sample = (f"each step: {rows} of {T * HQ} query rows per attention call (4 drafter + 1 verify), "
-              f"scaled by {T * HQ}/{rows}; greedy and sampled acceptance over all 16 x {V} logits in full")
+    sample = (f"each step: {rows} of {T * HQ} query rows per attention call (4 drafter + 1 verify) sliced over "
+              f"{cores} threads, scaled by {T * HQ}/{rows}; greedy and sampled acceptance over all 16 x {V} "
+              "logits in full on one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "blocks/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": CTX, "parallelism": "none (1 host thread)",
-                   "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": 1, "kind": "oracle", "sample": sample,
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": CTX,
+                   "parallelism": f"none ({cores} host threads)", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": "blocks/s", "cores": cores, "kind": "oracle", "sample": sample,
                          "cpu_seconds": work},
         "e2e": {"value": v, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -763,6 +873,13 @@ def main():
             acceptance[name] = {"us_per_call": per * 1e6, "algorithmic_bytes_per_call": nbytes,
                                 "GBps": nbytes / per / 1e9}
         del g8, s4
+        # verify attention of the ragged batch and of the 72B-shaped batch at
+        # full size, and the drafter's layers split into the HBM-cold first one
+        # and the L2-resident rest
+        per_config = {}
+        for n in (3, 5):
+            per_config[n] = config_verify_pass(S, device, stream, n)
+        per_config["draft"] = drafter_layer_pass(S, sets[0], stream, flush)
         tpk, tsrc = bf16_peak(sustained=False)
         kp = kernels["project_prefill"]
         kp["TFLOPs"] = PROJ_PREFILL_FLOPS / (kp["us_per_call"] * 1e-6) / 1e12
@@ -840,6 +957,31 @@ def main():
                 kk["frac_of_peak"] = kk["GBps"] / peak
         for name, kk in acceptance.items():
             kk["frac_of_peak"] = kk["GBps"] / peak
+        # short scalar keys, one figure each, per workload
+        t3, b3 = per_config[3]
+        t5, b5 = per_config[5]
+        tg8 = acceptance["greedy_b8"]["us_per_call"] * 1e-6
+        ts4 = acceptance["sample_b4"]["us_per_call"] * 1e-6
+        t_l1, t_l234 = per_config["draft"]
+        draft_flops = 2 * 2 * T * HQ * (CTX + T) * D
+        tpk_, _ = bf16_peak(sustained=False)
+        roofline.update({
+            "cfg2_verify_us": k["us_per_call_back_to_back"],
+            "cfg3_verify_us": t3 * 1e6, "cfg3_verify_GBps": b3 / t3 / 1e9, "cfg3_verify_frac": b3 / t3 / 1e9 / peak,
+            "cfg3_verify_bytes": b3,
+            "cfg5_verify_us": t5 * 1e6, "cfg5_verify_GBps": b5 / t5 / 1e9, "cfg5_verify_frac": b5 / t5 / 1e9 / peak,
+            "cfg5_verify_bytes": b5,
+            "accept_greedy_b8_us": tg8 * 1e6, "accept_greedy_b8_frac": acceptance["greedy_b8"]["frac_of_peak"],
+            "accept_sample_b4_us": ts4 * 1e6, "accept_sample_b4_frac": acceptance["sample_b4"]["frac_of_peak"],
+            "accept_greedy_b1_us": kernels["accept_greedy"]["us_per_call"],
+            "accept_sample_b1_us": kernels["accept_sample"]["us_per_call"],
+            "cfg3_blocks_per_s": 8 / (t3 + tg8),
+            "cfg5_blocks_per_s": 4 / (t5 + ts4),
+            "draft_l1_us": t_l1 * 1e6, "draft_l1_frac": BYTES["draft_attention"] / t_l1 / 1e9 / peak,
+            "draft_l234_us": t_l234 * 1e6,
+            "draft_l234_tensor_frac": draft_flops / t_l234 / 1e12 / tpk_,
+            "cfg4_draft_blocks_per_s": 1.0 / (t_l1 + (LAYERS - 1) * t_l234),
+        })
         roofline["acceptance_back_to_back"] = dict(acceptance, note=(
             "acceptance kernels at the batched workloads (greedy over 8 sequences' logits, the sampled rule "
             "over 4), calls issued back to back in one graph over 4 input copies larger than L2"))
@@ -854,16 +996,24 @@ def main():
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         import oracle
         oracle.build()
-        n_s, total, work = 0, 0.0, 0.0
-        while work < 10.0 and n_s < 20:
-            st, w = cpu_step_sample(host, args.cpu_rows)
-            total += st
-            work += w
-            n_s += 1
-        cpu = {"value": n_s / total, "unit": "blocks/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n_s} steps; per step {args.cpu_rows} of {T * HQ} query rows per attention call "
-                         f"(scaled by {T * HQ}/{args.cpu_rows}), both acceptance calls in full; "
-                         f"{work:.1f} s of CPU work"}
+        cores = host_cores()
+        legs = {}
+        for threads, rows_per_call in ((1, args.cpu_rows), (cores, args.cpu_rows * cores)):
+            n_s, total, work = 0, 0.0, 0.0
+            while work < 6.0 and n_s < 20:
+                st, w = cpu_step_sample(host, rows_per_call, threads)
+                total += st
+                work += w
+                n_s += 1
+            legs[threads] = (n_s / total, n_s, work, rows_per_call)
+        v_all, n_all, w_all, r_all = legs[cores]
+        v_one, n_one, w_one, r_one = legs[1]
+        cpu = {"value": v_all, "unit": "blocks/s", "cores": cores, "kind": "oracle",
+               "value_1_thread": v_one,
+               "sample": f"{n_all} steps on {cores} threads (attention rows sliced over them), per step "
+                         f"{r_all} of {T * HQ} query rows per attention call scaled by {T * HQ}/{r_all}, "
+                         f"acceptance in full on one thread, {w_all:.1f} s wall; value_1_thread: {n_one} steps "
+                         f"of {r_one} rows per call on one thread, {w_one:.1f} s"}
 
     if rank == 0:
         line = {

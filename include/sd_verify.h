@@ -80,8 +80,11 @@ typedef struct {
  *   logits are scale * q.k; softmax and accumulation in fp32
  *   T in [1, 16]; D in {64, 128}; Hq % Hkv == 0; (Hq / Hkv) * T <= 256
  *
- * workspace: zero-filled before the first call on it (it holds per-(sequence,
- * kv head) counters of the splits that every completed call returns to zero).
+ * workspace: zero-filled before the first call on it.  It holds one counter
+ * per (sequence, kv head) for the splits that merge inside the kernel; every
+ * call returns them to zero when its kernel ends, including a call whose
+ * bounded wait gave up (fault bit 3; its output is then incomplete), so the
+ * workspace never needs clearing again.
  * ------------------------------------------------------------------------ */
 sd_status sd_verify_attention(const void *q, const void *k_cache, const void *v_cache,
                               sd_strides kv, const int32_t *ctx_len, int max_ctx,

@@ -193,9 +193,12 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int
                 make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
         }
     }
-    // back to zero once every split of the group has merged
+    // every split takes a second ticket, whether or not its wait succeeded, so
+    // the counter sees exactly 2n increments per launch and the last of them
+    // returns it to zero: a launch whose wait gave up (fault bit set, its rows
+    // left unmerged) still leaves the workspace ready for the next call
     __syncthreads();
-    if (tid == 0 && *go) {
+    if (tid == 0) {
         const unsigned int ticket = atomicAdd(ctr, 1u);
         if (ticket == 2u * (unsigned int)n - 1u) atomicExch(ctr, 0u);
     }

@@ -226,3 +226,68 @@ def test_sample_diag_reports_the_draw():
             assert d["u"][b, j] < d["ratio"][b, j]
         if n[b] < 15:
             assert not (d["u"][b, n[b]] < d["ratio"][b, n[b]])
+
+
+def _all_accepted_setup(B, V, seed):
+    """p = q on rows 0..T-2 (every proposal accepted), a different p on row T-1."""
+    T = 16
+    rng = np.random.default_rng(seed)
+    p_rows = _softmax(rng.standard_normal((T, V)) * 1.5)
+    q_rows = p_rows.copy()
+    # the last row must differ from the one before it, or a draw from the
+    # wrong row would go unnoticed
+    assert np.abs(p_rows[T - 1] - p_rows[T - 2]).sum() > 0.5
+    return T, p_rows, q_rows
+
+
+def test_all_accepted_bonus_follows_last_row_chi_square():
+    """With every proposal accepted, the extra token is drawn from p of the last
+    row (the standard rule: the target's distribution after the last accepted
+    proposal), so its frequencies follow that row and not the one before."""
+    stats = pytest.importorskip("scipy.stats")
+    V, B = 16, 200_000
+    T, p_rows, q_rows = _all_accepted_setup(B, V, 31)
+    logits = np.log(np.broadcast_to(p_rows, (B, T, V)))
+    q = np.ascontiguousarray(np.broadcast_to(q_rows, (B, T, V)))
+    rng = np.random.default_rng(4321)
+    cq = np.cumsum(q_rows, axis=-1)
+    drafts = np.stack([np.searchsorted(cq[j], rng.random(B), side="right")
+                       for j in range(T - 1)], axis=1).clip(0, V - 1)
+    n, nx = oracle.accept_sample(drafts, q, logits, 1.0, 4321, 0)
+    assert (n == T - 1).all()
+    counts = np.bincount(nx, minlength=V)
+    _, pv = stats.chisquare(counts, B * p_rows[T - 1])
+    assert pv > 1e-3, pv
+    # the row before it is clearly rejected by the same test
+    _, pv_wrong = stats.chisquare(counts, B * p_rows[T - 2])
+    assert pv_wrong < 1e-12, pv_wrong
+
+
+def test_all_accepted_bonus_uses_last_row_resample_stream():
+    """The extra token's uniform is Philox word (row T-1, batch b, stream 1,
+    offset), and the token is the inverse CDF of the last row's p at u'·S,
+    recomputed here in numpy from the logits."""
+    V, B = 40, 64
+    T, p_rows, q_rows = _all_accepted_setup(B, V, 32)
+    logits = np.log(np.broadcast_to(p_rows, (B, T, V)))
+    q = np.ascontiguousarray(np.broadcast_to(q_rows, (B, T, V)))
+    rng = np.random.default_rng(5)
+    cq = np.cumsum(q_rows, axis=-1)
+    drafts = np.stack([np.searchsorted(cq[j], rng.random(B), side="right")
+                       for j in range(T - 1)], axis=1).clip(0, V - 1)
+    for seed, offset in ((1234, 0), (77, 9)):
+        n, nx, diag = oracle.accept_sample(drafts, q, logits, 1.0, seed, offset, return_diag=True)
+        d = oracle.split_diag(diag, T)
+        assert (n == T - 1).all()
+        p_last = _softmax(logits[0, T - 1])
+        cdf = np.cumsum(p_last)
+        for b in range(B):
+            u2 = oracle.uniform(seed, T - 1, b, 1, offset)
+            assert d["u2"][b] == u2
+            # neither the accept stream of that row nor the row before it
+            assert u2 != oracle.uniform(seed, T - 1, b, 0, offset)
+            assert u2 != oracle.uniform(seed, T - 2, b, 1, offset)
+            x = u2 * cdf[-1]
+            want = int(np.searchsorted(cdf, x, side="right"))
+            near = np.min(np.abs(cdf - x)) < 1e-12
+            assert int(nx[b]) == want or near, (b, int(nx[b]), want)
