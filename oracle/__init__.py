@@ -36,6 +36,7 @@ _dp = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _ip = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
 _lp = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
 _up = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+_u64p = np.ctypeslib.ndpointer(dtype=np.uint64, flags="C_CONTIGUOUS")
 
 
 def build(force: bool = False) -> str:
@@ -80,7 +81,7 @@ def _load():
     lib.oracle_accept_sample.restype = ctypes.c_int
     _up32 = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
     lib.oracle_tree_attention_rows.argtypes = [
-        _dp, _dp, _dp, _ip, _up32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        _dp, _dp, _dp, _ip, _u64p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_long, _dp]
     lib.oracle_tree_attention_rows.restype = ctypes.c_int
     lib.oracle_accept_tree_greedy.argtypes = [_ip, _ip, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -173,13 +174,14 @@ def tree_attention_rows(q, k, v, nctx, tree_mask, scale, *, rows=None):
 
     Node j of sequence b attends to cache keys [0, nctx-1) and to the block
     slots k (cache slot nctx-1+k) whose bit is set in tree_mask[b, j].
-    q [B,T,Hq,D]; k, v [B,Sc,Hkv,D]; tree_mask [B,T] (uint32).  Returns out [n_rows, D].
+    q [B,T,Hq,D] (T <= 64); k, v [B,Sc,Hkv,D]; tree_mask [B,T] (bit k of a 64-bit
+    word per node).  Returns out [n_rows, D].
     """
     qd, kd, vd = _f64(q), _f64(k), _f64(v)
     B, T, Hq, D = qd.shape
     _, Sc, Hkv, _ = kd.shape
     n = _i32(nctx).reshape(B)
-    m = np.ascontiguousarray(np.asarray(tree_mask, dtype=np.uint32).reshape(B * T))
+    m = np.ascontiguousarray(np.asarray(tree_mask).astype(np.uint64).reshape(B * T))
     rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
     n_rows = B * T * Hq if rows_a is None else rows_a.size
     out = np.zeros((n_rows, D), dtype=np.float64)

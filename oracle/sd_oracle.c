@@ -33,7 +33,7 @@
  *    whose inclusive ascending cumulative sum of max(p - q, 0) exceeds u' * S.
  *  - Philox counter = (row j, batch b, stream, offset), key = (seed lo, seed
  *    hi); the uniform is (word0 >> 8) * 2^-24.
- *  - a tree has at most 16 nodes; node j sees the context before the anchor
+ *  - a tree has at most 64 nodes; node j sees the context before the anchor
  *    and the block slots of its ancestors and itself; the committed path ends
  *    at the deepest accepted node (lowest index among equals).
  *  - commit: committed tokens = kept proposals + the next token, ctx_len
@@ -200,14 +200,15 @@ int oracle_attention_rows(const double *q, const double *kc, const double *vc,
  * node 0 the anchor; their K/V sit at cache slots ctx-1 .. ctx-2+T as in the
  * chain case.  Node j attends to the context before the anchor, cache keys
  * [0, ctx-1), and to the block slots k whose bit is set in mask[b*T + j]
- * (its ancestors and itself), in increasing k.  A chain mask (bits 0..j)
+ * (its ancestors and itself), in increasing k; T <= 64, so a 64-bit word per
+ * node holds its mask.  A chain mask (bits 0..j)
  * gives exactly the keys [0, ctx+j) of oracle_attention_rows, in the same
  * order.  Arguments as there; mask is [B*T].
  */
 int oracle_tree_attention_rows(const double *q, const double *kc, const double *vc, const int *nctx,
-                               const unsigned int *mask, int B, int T, int Hq, int Hkv, int D, int Sc,
+                               const uint64_t *mask, int B, int T, int Hq, int Hkv, int D, int Sc,
                                double scale, const long *rows, long n_rows, double *out) {
-    if (B < 1 || T < 1 || T > 32 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return -1;
+    if (B < 1 || T < 1 || T > 64 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return -1;
     const int G = Hq / Hkv;
     long total_rows = (long)B * T * Hq;
     if (rows == NULL) n_rows = total_rows;
@@ -228,7 +229,7 @@ int oracle_tree_attention_rows(const double *q, const double *kc, const double *
         long n = 0;
         for (long i = 0; i < c - 1; ++i) ki[n++] = i;
         for (int k = 0; k < T; ++k)
-            if ((mask[(long)b * T + j] >> k) & 1u) ki[n++] = c - 1 + k;
+            if ((mask[(long)b * T + j] >> k) & 1u) ki[n++] = c - 1 + k;   /* 64-bit mask, k < 64 */
         double *o = out + r * D;
         for (int d = 0; d < D; ++d) o[d] = 0.0;
         if (n == 0) continue;

@@ -31,14 +31,14 @@ def _random_tree(rng, T):
 
 def _masks_from_parents(parents):
     T = len(parents)
-    m = np.zeros(T, dtype=np.uint32)
+    m = np.zeros(T, dtype=np.uint64)
     for j in range(T):
         v = j
         bits = 0
         while v != -1:
-            bits |= 1 << v
+            bits |= 1 << int(v)
             v = parents[v]
-        m[j] = bits
+        m[j] = np.uint64(bits)
     return m
 
 
@@ -46,19 +46,21 @@ def _chain_parents(T):
     return np.arange(-1, T - 1, dtype=np.int32)
 
 
-def test_chain_tree_equals_chain_attention_exactly():
-    inp = W.verify_inputs(B=2, T=6, Hq=4, Hkv=2, D=8, ctx=[7, 3], dtype=torch.float32, seed=11)
-    B, T = 2, 6
+@pytest.mark.parametrize("T", [6, 60, 64])
+def test_chain_tree_equals_chain_attention_exactly(T):
+    """A chain of up to 64 nodes (mask bits up to 63) is the chain verify."""
+    inp = W.verify_inputs(B=2, T=T, Hq=4, Hkv=2, D=8, ctx=[7, 3], dtype=torch.float32, seed=11)
+    B = 2
     mask = np.stack([_masks_from_parents(_chain_parents(T))] * B)
     got = oracle.tree_attention_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], mask, 0.3)
     want = oracle.attention_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], 0.3, mode=0)
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("seed", [0, 1, 2])
-def test_random_trees_match_sdpa_with_the_ancestor_mask(seed):
+@pytest.mark.parametrize("seed,T", [(0, 8), (1, 8), (2, 8), (3, 60), (4, 64)])
+def test_random_trees_match_sdpa_with_the_ancestor_mask(seed, T):
     rng = np.random.default_rng(seed)
-    B, T, Hq, Hkv, D = 2, 8, 6, 2, 16
+    B, Hq, Hkv, D = 2, 6, 2, 16
     ctx = [5, 12]
     inp = W.verify_inputs(B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, ctx=ctx, dtype=torch.float32, seed=20 + seed)
     parents = np.stack([_random_tree(rng, T) for _ in range(B)])
@@ -81,6 +83,26 @@ def test_random_trees_match_sdpa_with_the_ancestor_mask(seed):
         o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=am, scale=0.25)
         want[b] = o.permute(1, 0, 2).numpy()
     assert np.abs(got - want.reshape(-1, D)).max() < 1e-12
+
+
+def test_last_of_64_nodes_sees_only_context_anchor_and_itself():
+    """Mask bit 63: in a 64-node star, node 63 attends to the context, the
+    anchor and itself, which equals plain attention over those keys."""
+    T, n = 64, 10
+    inp = W.verify_inputs(B=1, T=T, Hq=2, Hkv=1, D=8, ctx=[n], dtype=torch.float32, seed=6)
+    parents = np.array([-1] + [0] * (T - 1), dtype=np.int32)
+    mask = _masks_from_parents(parents)[None]
+    assert int(mask[0, 63]) == (1 << 63) | 1
+    got = oracle.tree_attention_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], mask, 0.5).reshape(T, 2, 8)
+    keys = list(range(n)) + [n - 1 + 63]
+    for h in range(2):
+        qv = inp["q"][0, 63, h].double().numpy()
+        kk = inp["k"][0, keys, 0].double().numpy()
+        vv = inp["v"][0, keys, 0].double().numpy()
+        s_ = 0.5 * kk @ qv
+        w = np.exp(s_ - s_.max())
+        want = (w / w.sum()) @ vv
+        assert np.abs(got[63, h] - want).max() < 1e-12
 
 
 def test_star_tree_node_sees_context_anchor_and_itself():
