@@ -123,7 +123,7 @@ def make_inputs(device):
     am = cfg2["greedy"]["logits"].float().numpy().argmax(-1)[0]
     tokens = np.array([0] + [int(am[parents[j]]) if trng.random() < 0.7 else int(trng.integers(0, V))
                              for j in range(1, T)], dtype=np.int32)
-    tree = {"mask": torch.from_numpy(mask.astype(np.int32)).reshape(1, T),
+    tree = {"mask": torch.from_numpy(mask).reshape(1, T),
             "parents": torch.from_numpy(parents).reshape(1, T), "tokens": torch.from_numpy(tokens).reshape(1, T)}
     # the drafter K/V projector in a linear layer's [out, in] layout, bf16
     proj = {"h": h, "wk": wk.t().contiguous().to(torch.bfloat16), "wv": wv.t().contiguous().to(torch.bfloat16)}
@@ -305,6 +305,63 @@ def config_verify_pass(S, device, stream, n):
     del copies, calls
     torch.cuda.empty_cache()
     return per, verify_bytes(ctx_list, T_, Hq, Hkv, D_)
+
+
+def tree60_pass(S, device, stream, n_nodes=60):
+    """The pages' Tree-60 at the 25,119-token workload: verify attention over a
+    seeded 60-node draft tree (each node's parent among the 3 before it) and
+    greedy tree acceptance over its [1, 60, V] logits, each back to back over
+    input copies larger than L2 in total.  Returns (attention s, acceptance s,
+    attention bytes, acceptance bytes)."""
+    import numpy as np
+    import torch
+    from serving_sd_verify_gb300 import workloads as W
+    Tt = n_nodes
+    att = W.verify_inputs(B=1, T=Tt, Hq=HQ, Hkv=HKV, D=D, ctx=CTX, seed=2)
+    rng = np.random.default_rng(61)
+    parents = np.full(Tt, -1, dtype=np.int32)
+    for j in range(1, Tt):
+        parents[j] = rng.integers(max(0, j - 3), j)
+    mask = np.zeros(Tt, dtype=np.uint64)
+    for j in range(Tt):
+        v, bits = j, 0
+        while v != -1:
+            bits |= 1 << int(v)
+            v = parents[v]
+        mask[j] = np.uint64(bits)
+    tm = torch.from_numpy(mask.view(np.int64)).reshape(1, Tt).to(device)
+    acopies = []
+    for _ in range(4):   # 4 x 51.6 MB of K/V
+        q, k, v, ctx = (att[x].to(device).contiguous() for x in ("q", "k", "v", "ctx"))
+        out = torch.zeros(1, Tt, HQ, D, device=device)
+        ws = S.workspace(S.sd_verify_tree_attention_workspace_size(1, Tt, HQ, HKV, D, CTX), device)
+        acopies.append((q, k, v, ctx, out, ws))
+    del att
+    calls = [(lambda c=c: S.sd_verify_tree_attention(c[0], c[1], c[2], c[3], CTX, tm, c[4], 1.0, c[5], stream))
+             for c in acopies]
+    t_att = time_back_to_back(calls, len(acopies), stream)
+    a_bytes = verify_bytes([CTX], Tt, HQ, HKV, D) + Tt * 8
+    del acopies, calls
+    g = W.greedy_inputs(B=1, T=Tt, V=V, seed=160, k=0)
+    am = g["logits"].float().numpy().argmax(-1)[0]
+    tokens = np.array([0] + [int(am[parents[j]]) if rng.random() < 0.7 else int(rng.integers(0, V))
+                             for j in range(1, Tt)], dtype=np.int32)
+    tok = torch.from_numpy(tokens).reshape(1, Tt).to(device)
+    par = torch.from_numpy(parents).reshape(1, Tt).to(device)
+    gcopies = []
+    for _ in range(8):   # 8 x 18.2 MB of logits
+        lg = g["logits"].to(device)
+        n_ = torch.zeros(1, dtype=torch.int32, device=device)
+        c_ = torch.zeros(1, dtype=torch.int32, device=device)
+        path = torch.zeros(1, Tt, dtype=torch.int32, device=device)
+        ws = S.workspace(S.sd_accept_tree_greedy_workspace_size(1, Tt, V), device)
+        gcopies.append((lg, n_, c_, path, ws))
+    calls = [(lambda c=c: S.sd_accept_tree_greedy(tok, par, c[0], c[1], c[2], c[3], c[4], stream)) for c in gcopies]
+    t_acc = time_back_to_back(calls, len(gcopies), stream)
+    g_bytes = Tt * V * 2 + Tt * 8 + Tt * 4 + 8
+    del gcopies, calls
+    torch.cuda.empty_cache()
+    return t_att, t_acc, a_bytes, g_bytes
 
 
 def drafter_layer_pass(S, ds, stream, flush, reps=20):
@@ -880,6 +937,7 @@ def main():
         for n in (3, 5):
             per_config[n] = config_verify_pass(S, device, stream, n)
         per_config["draft"] = drafter_layer_pass(S, sets[0], stream, flush)
+        per_config["tree60"] = tree60_pass(S, device, stream)
         tpk, tsrc = bf16_peak(sustained=False)
         kp = kernels["project_prefill"]
         kp["TFLOPs"] = PROJ_PREFILL_FLOPS / (kp["us_per_call"] * 1e-6) / 1e12
@@ -981,6 +1039,14 @@ def main():
             "draft_l234_us": t_l234 * 1e6,
             "draft_l234_tensor_frac": draft_flops / t_l234 / 1e12 / tpk_,
             "cfg4_draft_blocks_per_s": 1.0 / (t_l1 + (LAYERS - 1) * t_l234),
+        })
+        t_tv, t_ta, b_tv, b_ta = per_config["tree60"]
+        roofline.update({
+            "tree60_verify_us": t_tv * 1e6, "tree60_verify_frac": b_tv / t_tv / 1e9 / peak,
+            "tree60_accept_us": t_ta * 1e6, "tree60_accept_frac": b_ta / t_ta / 1e9 / peak,
+            "tree60_blocks_per_s": 1.0 / (t_tv + t_ta),
+            "chain16_blocks_per_s": 1.0 / (k["us_per_call_back_to_back"] * 1e-6 +
+                                           kernels["accept_greedy"]["us_per_call"] * 1e-6),
         })
         roofline["acceptance_back_to_back"] = dict(acceptance, note=(
             "acceptance kernels at the batched workloads (greedy over 8 sequences' logits, the sampled rule "

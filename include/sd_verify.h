@@ -78,7 +78,7 @@ typedef struct {
  *   out      device fp32 [B, T, Hq, D] contiguous
  *   query head h reads kv head h / (Hq / Hkv)
  *   logits are scale * q.k; softmax and accumulation in fp32
- *   T in [1, 16]; D in {64, 128}; Hq % Hkv == 0; (Hq / Hkv) * T <= 256
+ *   T in [1, 16]; D in {64, 128}; Hq % Hkv == 0; Hq <= 4096
  *
  * workspace: zero-filled before the first call on it.  It holds one counter
  * per (sequence, kv head) for the splits that merge inside the kernel; every
@@ -135,13 +135,18 @@ size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, in
  * and to the slots ctx_len-1+k of every bit k set in tree_mask[b][j] (its
  * ancestors and itself).  A chain mask (bits 0..j) gives sd_verify_attention.
  *
- *   tree_mask  device uint32 [B, T]; bit k < T (T <= 16 here: the tensor-core
- *              kernel holds all G*T rows of a kv head in one 128-row tile)
- *   everything else as for sd_verify_attention (same workspace size)
+ *   tree_mask  device uint64 [B, T], 8-byte aligned; bit k (k < T) of node j's
+ *              word set when node j sees block slot k
+ *   T          nodes, in [1, 64] (the page's "Tree-60" is about 60 nodes);
+ *              the tensor-core kernel cuts a kv head's (Hq/Hkv)*T query rows
+ *              into blocks of whole nodes of at most 128 rows, which read
+ *              the same K/V tiles
+ *   everything else as for sd_verify_attention; the workspace size comes
+ *   from sd_verify_tree_attention_workspace_size
  * ------------------------------------------------------------------------ */
 sd_status sd_verify_tree_attention(const void *q, const void *k_cache, const void *v_cache,
                                    sd_strides kv, const int32_t *ctx_len, int max_ctx,
-                                   const uint32_t *tree_mask, float *out, int B, int T, int Hq,
+                                   const uint64_t *tree_mask, float *out, int B, int T, int Hq,
                                    int Hkv, int D, sd_dtype dtype, float scale,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
@@ -217,6 +222,7 @@ size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype);
  * greatest depth (the lowest index among equals), so a chain tree gives
  * sd_accept_greedy.
  *
+ *   T              nodes, in [1, 64]
  *   tokens         device int32 [B, T]: tokens[b][j] is node j's proposal
  *                  (tokens[b][0], the anchor, is not read)
  *   parents        device int32 [B, T]: parents[b][0] = -1, parents[b][j] in
@@ -225,7 +231,8 @@ size_t sd_accept_sample_workspace_size(int B, int T, int V, sd_dtype dtype);
  *   n_accepted     device int32 [B]: depth of that node (proposals kept)
  *   correction_id  device int32 [B]: a_node (the target's next token)
  *   path           device int32 [B, T]: the kept nodes at depth 1..n, then -1
- *   workspace      as for sd_accept_greedy (same size)
+ *   workspace      at least sd_accept_tree_greedy_workspace_size bytes,
+ *                  zero-filled before its first call (as for sd_accept_greedy)
  * ------------------------------------------------------------------------ */
 sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, const void *target_logits,
                                 int B, int T, int V, sd_dtype dtype, int32_t *n_accepted,
@@ -281,6 +288,7 @@ sd_status sd_project_kv(const void *hidden, int64_t ld_hidden, const void *w_k, 
  * Conventions (those of the attention calls): ctx_len counts the anchor;
  * block slot k of sequence b is cache position ctx_len[b] - 1 + k; the
  * drafter's context is every position before the anchor (ctx_len - 1 rows).
+ * T is the block's slot count: at most 16 for a chain, at most 64 for a tree.
  * ------------------------------------------------------------------------ */
 
 /* Tokens and lengths.  With n = n_accepted[b]:
@@ -331,8 +339,8 @@ sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const 
  *                that would pass it is skipped and sets the fault word)
  *   draft_ctx    device int32 [B]: the drafter's context length before the
  *                commit (sd_commit_tokens advances it afterwards)
- * Requirements as for sd_project_kv, and Hd <= 6400 (the block's 16 hidden
- * rows are staged in 200 KB of shared memory; else SD_ERR_UNSUPPORTED). */
+ * Requirements as for sd_project_kv, and Hd <= 6400 (the rows go in groups of
+ * 16 per CTA, staged in 200 KB of shared memory; else SD_ERR_UNSUPPORTED). */
 sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int64_t hidden_bstride,
                                const void *w_k, const void *w_v, int Hd, int Dout,
                                const int32_t *n_accepted, const int32_t *path, const int32_t *draft_ctx,

@@ -336,16 +336,16 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
                 // equals the target's pick after the parent; the deepest accepted
                 // node (lowest index among equals) ends the committed path
                 const int32_t *par = p.parents + (long)b * p.T, *tok = p.draft + (long)b * p.T;
-                uint32_t acc = 1u;  // bit j: node j accepted (the anchor always)
-                int depth[kMaxT];
+                uint64_t acc = 1ull;  // bit j: node j accepted (the anchor always)
+                int depth[kMaxTreeT];
                 depth[0] = 0;
                 int best = 0;
                 for (int j = 1; j < p.T; ++j) {
                     const int pj = par[j];
                     if (pj < 0 || pj >= j) { set_fault(p.fault, FAULT_BAD_TREE); depth[j] = 0; continue; }
                     depth[j] = depth[pj] + 1;
-                    if (((acc >> pj) & 1u) && tok[j] == am[rb + pj]) {
-                        acc |= 1u << j;
+                    if (((acc >> pj) & 1ull) && tok[j] == am[rb + pj]) {
+                        acc |= 1ull << j;
                         if (depth[j] > depth[best]) best = j;
                     }
                 }

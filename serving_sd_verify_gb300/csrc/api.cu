@@ -70,7 +70,15 @@ size_t esize(sd_dtype dt) { return dt == SD_BF16 ? 2 : 4; }
 struct AttnPlan {
     int path;           // 1 CUDA-core, 2 tensor-core
     int n_splits, keys_per_split;
+    int n_mblk, mblk_nodes;   // tensor-core row blocks per kv head and block rows in each
 };
+
+// row blocks of the tensor-core kernel: whole block rows, at most 128 query rows each
+void row_blocks(int G, int T, int *n_mblk, int *mblk_nodes) {
+    const int nodes = std::max(1, std::min(T, 128 / std::max(1, G)));
+    *mblk_nodes = nodes;
+    *n_mblk = (T + nodes - 1) / nodes;
+}
 
 // keys of the longest sequence's key space
 int max_keys(int mode, int max_ctx, int T) { return mode == 1 ? max_ctx + T : max_ctx + T - 1; }
@@ -78,9 +86,12 @@ int max_keys(int mode, int max_ctx, int T) { return mode == 1 ? max_ctx + T : ma
 AttnPlan plan_attention(const AttnParams &p, int path) {
     const int sms = device_sm_count();
     const int N = max_keys(p.mode, p.max_ctx, p.T);
-    const int units = p.B * p.Hkv;
     AttnPlan pl;
     pl.path = path;
+    pl.n_mblk = 1;
+    pl.mblk_nodes = p.T;
+    if (path >= 2) row_blocks(p.Hq / p.Hkv, p.T, &pl.n_mblk, &pl.mblk_nodes);
+    const int units = p.B * p.Hkv * pl.n_mblk;
     int ctas_per_sm, min_keys, gran;
     if (path >= 2) { ctas_per_sm = 1; min_keys = 2 * kTcTileKeys; gran = kTcTileKeys; }
     else { ctas_per_sm = 2; min_keys = 128; gran = 32; }
@@ -96,11 +107,14 @@ AttnPlan plan_attention(const AttnParams &p, int path) {
     return pl;
 }
 
-// attention workspace: [header][merge counters, B * Hkv][o_part][lse_part]
-size_t attn_counters_bytes(int B, int Hkv) { return align_up((size_t)B * Hkv * sizeof(unsigned int), 256); }
-size_t attn_workspace(int B, int T, int Hq, int Hkv, int D, int n_splits) {
+// attention workspace: [header][merge counters, B * Hkv * n_mblk][o_part][lse_part]
+size_t attn_counters_bytes(int B, int Hkv, int n_mblk) {
+    return align_up((size_t)B * Hkv * n_mblk * sizeof(unsigned int), 256);
+}
+size_t attn_workspace(int B, int T, int Hq, int Hkv, int D, int n_splits, int n_mblk) {
     const size_t rows = (size_t)B * T * Hq;
-    return kHeader + attn_counters_bytes(B, Hkv) + align_up((size_t)n_splits * rows * D * sizeof(float), 256) +
+    return kHeader + attn_counters_bytes(B, Hkv, n_mblk) +
+           align_up((size_t)n_splits * rows * D * sizeof(float), 256) +
            align_up((size_t)n_splits * rows * sizeof(float), 256);
 }
 
@@ -109,11 +123,17 @@ sd_status validate_attention(const AttnParams &p) {
         return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
     if (p.mode == 1 && (!p.kb || !p.vb)) return fail(SD_ERR_INVALID_ARG, "null block key/value pointer");
     if (p.mode == 2 && !p.tree_mask) return fail(SD_ERR_INVALID_ARG, "null tree mask");
-    if (p.B < 1 || p.T < 1 || p.T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    if (p.mode == 2 && (reinterpret_cast<uintptr_t>(p.tree_mask) & 7u))
+        return fail(SD_ERR_INVALID_ARG, "tree mask must be 8-byte aligned");
+    if (p.mode == 2) {
+        if (p.B < 1 || p.T < 1 || p.T > kMaxTreeT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 64]");
+    } else if (p.B < 1 || p.T < 1 || p.T > kMaxT) {
+        return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    }
     if (p.Hq < 1 || p.Hkv < 1 || p.Hq % p.Hkv) return fail(SD_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+    if (p.Hq > 4096) return fail(SD_ERR_UNSUPPORTED, "Hq must be <= 4096");
     if (p.D != 64 && p.D != 128) return fail(SD_ERR_UNSUPPORTED, "D must be 64 or 128");
     if (p.dt != SD_BF16 && p.dt != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
-    if ((p.Hq / p.Hkv) * p.T > 256) return fail(SD_ERR_UNSUPPORTED, "(Hq/Hkv)*T must be <= 256");
     if (p.max_ctx < 1) return fail(SD_ERR_INVALID_ARG, "max_ctx must be >= 1");
     if (!(p.scale == p.scale)) return fail(SD_ERR_INVALID_ARG, "scale is NaN");
     const size_t es = esize(p.dt);
@@ -138,24 +158,26 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     else if (force >= 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
     else path = 1;
     AttnPlan pl = plan_attention(p, path);
-    const size_t need = attn_workspace(p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits);
+    const size_t need = attn_workspace(p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits, pl.n_mblk);
     if (!ws || ws_bytes < need)
         return fail(SD_ERR_WORKSPACE, "attention workspace too small: need %zu bytes, got %zu", need, ws_bytes);
     if (!aligned16(ws)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     const size_t rows = (size_t)p.B * p.T * p.Hq;
     p.merge_ctr = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + kHeader);
-    char *w = static_cast<char *>(ws) + kHeader + attn_counters_bytes(p.B, p.Hkv);
+    char *w = static_cast<char *>(ws) + kHeader + attn_counters_bytes(p.B, p.Hkv, pl.n_mblk);
     p.o_part = reinterpret_cast<float *>(w);
     p.lse_part = reinterpret_cast<float *>(w + align_up((size_t)pl.n_splits * rows * p.D * sizeof(float), 256));
     p.n_splits = pl.n_splits;
     p.keys_per_split = pl.keys_per_split;
+    p.n_mblk = pl.n_mblk;
+    p.mblk_nodes = pl.mblk_nodes;
     // tensor-core path: one split writes the output itself; several merge
     // inside the kernel when the whole grid is resident at once (at most one
     // CTA per SM), else in the merge kernel
     p.merge = 0;
     if (path == 2) {
         if (pl.n_splits == 1) p.merge = 2;
-        else if ((long)pl.n_splits * p.Hkv * p.B <= device_sm_count()) p.merge = 1;
+        else if ((long)pl.n_splits * p.Hkv * p.B * pl.n_mblk <= device_sm_count()) p.merge = 1;
     }
     cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
@@ -170,12 +192,14 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
 }
 
 size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max_ctx, sd_dtype dt) {
-    if (B < 1 || T < 1 || T > kMaxT || Hq < 1 || Hkv < 1 || max_ctx < 1 || (D != 64 && D != 128)) return 0;
+    if (B < 1 || T < 1 || T > (mode == 2 ? kMaxTreeT : kMaxT) || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq > 4096 ||
+        max_ctx < 1 || (D != 64 && D != 128))
+        return 0;
     AttnParams p = {};
     p.mode = mode; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dt; p.max_ctx = max_ctx;
-    size_t need = attn_workspace(B, T, Hq, Hkv, D, plan_attention(p, 1).n_splits);
-    need = std::max(need, attn_workspace(B, T, Hq, Hkv, D, plan_attention(p, 2).n_splits));
-    return need;
+    const AttnPlan p1 = plan_attention(p, 1), p2 = plan_attention(p, 2);
+    return std::max(attn_workspace(B, T, Hq, Hkv, D, p1.n_splits, p1.n_mblk),
+                    attn_workspace(B, T, Hq, Hkv, D, p2.n_splits, p2.n_mblk));
 }
 
 // ----------------------------------------------------------------------------
@@ -345,7 +369,7 @@ size_t sd_draft_block_attention_workspace_size(int B, int T, int Hq, int Hkv, in
 }
 
 sd_status sd_verify_tree_attention(const void *q, const void *k_cache, const void *v_cache, sd_strides kv,
-                                   const int32_t *ctx_len, int max_ctx, const uint32_t *tree_mask, float *out,
+                                   const int32_t *ctx_len, int max_ctx, const uint64_t *tree_mask, float *out,
                                    int B, int T, int Hq, int Hkv, int D, sd_dtype dtype, float scale,
                                    void *workspace, size_t workspace_bytes, void *stream) {
     AttnParams p = {};
@@ -397,13 +421,15 @@ sd_status sd_accept_greedy(const int32_t *draft_ids, const void *target_logits, 
 }
 
 size_t sd_accept_tree_greedy_workspace_size(int B, int T, int V, sd_dtype dtype) {
-    return sd_accept_greedy_workspace_size(B, T, V, dtype);
+    if (B < 1 || T < 1 || T > kMaxTreeT || V < 1) return 0;
+    return greedy_layout(B, T, V, accept_chunk(B * T, V, greedy_cap(dtype), greedy_per_sm(B * T))).total;
 }
 
 sd_status sd_accept_tree_greedy(const int32_t *tokens, const int32_t *parents, const void *target_logits, int B,
                                 int T, int V, sd_dtype dtype, int32_t *n_accepted, int32_t *correction_id,
                                 int32_t *path, void *workspace, size_t workspace_bytes, void *stream) {
-    if (B < 1 || T < 1 || T > kMaxT || V < 1) return fail(SD_ERR_INVALID_ARG, "need B >= 1, T in [1, 16], V >= 1");
+    if (B < 1 || T < 1 || T > kMaxTreeT || V < 1)
+        return fail(SD_ERR_INVALID_ARG, "need B >= 1, T in [1, 64], V >= 1");
     if (!target_logits || !n_accepted || !correction_id || !tokens || !parents || !path)
         return fail(SD_ERR_INVALID_ARG, "null tensor pointer");
     if (dtype != SD_BF16 && dtype != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
@@ -526,7 +552,7 @@ sd_status sd_project_kv_commit(const void *hidden_block, int64_t ld_hidden, int6
                                int64_t ctx_bstride, int64_t ld_out, int max_rows, sd_dtype dtype, void *stream) {
     if (dtype == SD_FP32) return fail(SD_ERR_UNSUPPORTED, "the projector takes bf16 tensors only");
     if (dtype != SD_BF16) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
-    if (B < 1 || T < 1 || T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    if (B < 1 || T < 1 || T > kMaxTreeT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 64]");
     if (Hd < 8 || Hd % 8 != 0 || Hd > (1 << 20)) return fail(SD_ERR_INVALID_ARG, "need Hd a positive multiple of 8");
     if (Dout < 32 || Dout % 32 != 0 || Dout > (1 << 20))
         return fail(SD_ERR_INVALID_ARG, "need Dout a positive multiple of 32");
@@ -564,7 +590,7 @@ sd_status sd_commit_tokens(const int32_t *proposals, int proposal_stride, const 
                            const int32_t *n_accepted, const int32_t *next_token, int B, int T, int32_t *ctx_len,
                            int ctx_cap, int32_t *draft_ctx, int32_t *out_tokens, int32_t *out_len, int out_cap,
                            int32_t *anchor, int32_t *status, void *stream) {
-    if (B < 1 || T < 1 || T > kMaxT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 16]");
+    if (B < 1 || T < 1 || T > kMaxTreeT) return fail(SD_ERR_INVALID_ARG, "need B >= 1 and T in [1, 64]");
     if (proposal_stride < (path ? T : T - 1)) return fail(SD_ERR_INVALID_ARG, "proposal_stride too small");
     if (ctx_cap < 1 || out_cap < 1) return fail(SD_ERR_INVALID_ARG, "need ctx_cap >= 1 and out_cap >= 1");
     if ((T > 1 && !proposals) || !n_accepted || !next_token || !ctx_len || !out_tokens || !out_len || !anchor)
@@ -585,8 +611,8 @@ sd_status sd_commit_tokens(const int32_t *proposals, int proposal_stride, const 
 sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const int32_t *ctx_len,
                              const int32_t *path, const int32_t *n_accepted, int B, int T, int max_slots, int Hkv,
                              int D, sd_dtype dtype, void *stream) {
-    if (B < 1 || T < 1 || T > kMaxT || Hkv < 1 || D < 1 || max_slots < T)
-        return fail(SD_ERR_INVALID_ARG, "need B, Hkv, D >= 1, T in [1, 16] and max_slots >= T");
+    if (B < 1 || T < 1 || T > kMaxTreeT || Hkv < 1 || D < 1 || max_slots < T)
+        return fail(SD_ERR_INVALID_ARG, "need B, Hkv, D >= 1, T in [1, 64] and max_slots >= T");
     if (dtype != SD_BF16 && dtype != SD_FP32) return fail(SD_ERR_INVALID_ARG, "unknown dtype");
     const int es = (int)esize(dtype);
     if ((D * es) % 16 != 0 || D * es > kMaxHeadBytes)

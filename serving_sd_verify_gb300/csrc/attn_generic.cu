@@ -121,7 +121,7 @@ attn_split_generic_kernel(const AttnParams p) {
                 if (p.mode == 2) {
                     // tree: the context before the anchor, then the slots of the node's mask
                     const int slot = key - (nb - 1);
-                    valid = key < k1 && (slot < 0 || (slot < T && ((p.tree_mask[(long)b * T + j] >> slot) & 1u)));
+                    valid = key < k1 && (slot < 0 || (slot < T && ((p.tree_mask[(long)b * T + j] >> slot) & 1ull)));
                 } else {
                     valid = key < min(k1, p.mode == 0 ? nb + j : N_b);
                 }

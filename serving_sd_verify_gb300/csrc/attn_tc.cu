@@ -105,17 +105,18 @@ __device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int ta
     }
 }
 
-// Every split of sequence b, kv head g has written its partial (rows
-// normalised by their own sum, plus their log-sum-exp); once all of them have
-// arrived, split s combines rows s, s + n, s + 2n, ... of the group's M rows
-// (n = splits): out = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max).
+// Every split of sequence b, kv head g, row block mb has written its partial
+// (rows normalised by their own sum, plus their log-sum-exp); once all of them
+// have arrived, split s combines rows s, s + n, s + 2n, ... of the group's M
+// rows (n = splits; row rr is block row j0 + rr / G, query head g G + rr % G):
+// out = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max).
 // The whole grid is resident (at most one CTA per SM), so the wait ends.  The
 // counter is returned to zero by the last split to finish merging.  `scratch`
 // is idle shared memory (the K/V rings).
 constexpr int kMergeBatch = 12;  // loads one merge thread keeps in flight
-__device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int G, long rows_total,
-                            volatile int *go, uint8_t *scratch) {
-    unsigned int *ctr = p.merge_ctr + ((long)b * p.Hkv + g);
+__device__ void merge_group(const AttnParams &p, int s, int g, int b, int mb, int j0, int M, int G,
+                            long rows_total, volatile int *go, uint8_t *scratch) {
+    unsigned int *ctr = p.merge_ctr + (((long)b * p.Hkv + g) * p.n_mblk + mb);
     const int n = (int)gridDim.x;
     const int tid = threadIdx.x;
     __threadfence();  // this thread's partial stores are visible device-wide
@@ -137,7 +138,7 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int M, int
     float4 *part = reinterpret_cast<float4 *>(scratch + ((R * n + R) * 4 + 15) / 16 * 16);  // [K][R][32]
     auto frow_of = [&](int ri) {
         const int rr = s + ri * n;
-        return ((long)b * p.T + rr / G) * p.Hq + g * G + rr % G;
+        return ((long)b * p.T + j0 + rr / G) * p.Hq + g * G + rr % G;
     };
     if (*go && R > 0) {
         for (int i = tid; i < R * n; i += kTcThreads)
@@ -216,7 +217,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t *sbase = smem_raw + (base - raw_u32);
 
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // grid: (split, kv head x row block, sequence)
+    const int s = blockIdx.x, g = blockIdx.y / p.n_mblk, mb = blockIdx.y % p.n_mblk, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const uint32_t sQ = base + L::kOffQ, sK = base + L::kOffK, sV = base + L::kOffV;
@@ -258,12 +260,16 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs of an upstream kernel are visible now
 #endif
 
-    const int T = p.T, G = p.Hq / p.Hkv, M = G * T;
+    // this CTA's rows: block rows [j0, j0 + Tb) of the G query heads of kv head g
+    const int T = p.T, G = p.Hq / p.Hkv;
+    const int j0 = mb * p.mblk_nodes, Tb = min(p.mblk_nodes, T - j0), M = G * Tb;
+    const int MQ = G * p.mblk_nodes;  // rows the Q copy writes (those past block row T - 1 as zeros)
     if (producer) {
-        // Q first: rows r = j*G + hl of this kv head, two 64-column halves
-        mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * M));
-        tma_load_4d(sQ, &tmap_q, qready_bar, 0, g * G, 0, b);
-        tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, g * G, 0, b);
+        // Q first: rows r = (j - j0)*G + hl of this kv head, two 64-column halves;
+        // the copy always moves the whole box (out-of-range rows are zero-filled)
+        mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * MQ));
+        tma_load_4d(sQ, &tmap_q, qready_bar, 0, g * G, j0, b);
+        tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, g * G, j0, b);
     }
     const bool drafter = p.mode == 1;
     int nb = p.nctx[b];
@@ -317,7 +323,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         if (producer) mbar_wait(qready_bar, 0, nullptr, p.fault);
         for (int idx = tid; idx < M * 32; idx += kTcThreads) {
             const int rr = idx >> 5, c4 = idx & 31;
-            const long frow = ((long)b * T + rr / G) * p.Hq + g * G + rr % G;
+            const long frow = ((long)b * T + j0 + rr / G) * p.Hq + g * G + rr % G;
             float *dst = p.merge == 2 ? p.out + frow * 128 : p.o_part + ((long)s * rows_total + frow) * 128;
             reinterpret_cast<float4 *>(dst)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c4 == 0 && p.merge != 2) p.lse_part[(long)s * rows_total + frow] = -INFINITY;
@@ -386,10 +392,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
-        // Q rows past the M real ones are zero, so the padding rows of S are
-        // finite (the copy writes rows [0, M) only)
-        for (int idx = lane; idx < (128 - M) * 16; idx += 32) {
-            const int row = M + (idx >> 4), ch = idx & 15;
+        // Q rows past the MQ the copy writes are zero, so the padding rows of S
+        // are finite (the copy itself zero-fills rows [M, MQ))
+        for (int idx = lane; idx < (128 - MQ) * 16; idx += 32) {
+            const int row = MQ + (idx >> 4), ch = idx & 15;
             *reinterpret_cast<uint4 *>(sbase + L::kOffQ + (ch >> 3) * (128 * 128) + sw128_off(row, ch & 7)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
@@ -466,7 +472,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         const int wg = sidx >> 7;                   // key half of every tile
         const int r = sidx & 127;                   // query row = tensor-memory lane (warp % 4 picks the lanes)
         const bool row_ok = r < M;
-        const int j = row_ok ? r / G : 0;
+        const int j = row_ok ? j0 + r / G : 0;   // block row (tree node) of this query row
         const float qk = p.scale * kLog2e;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t o_col = tmem + lane_off + 64u * wg;   // this warpgroup's half of O (rescale, epilogue)
@@ -498,10 +504,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     vis = prefix(T - 64 * wg);
                 } else if (tree) {
                     vis = prefix(min(cend, nb - 1) - key0h);
-                    const uint32_t tm = p.tree_mask[(long)b * T + j];
+                    const uint64_t tm = p.tree_mask[(long)b * T + j];
                     for (int k = 0; k < T; ++k) {
                         const int pos = nb - 1 + k - key0h;
-                        if (pos >= 0 && pos < 64 && key0h + pos < cend && ((tm >> k) & 1u)) vis |= 1ull << pos;
+                        if (pos >= 0 && pos < 64 && key0h + pos < cend && ((tm >> k) & 1ull)) vis |= 1ull << pos;
                     }
                 } else {
                     vis = prefix((drafter ? cend : min(cend, nb + j)) - key0h);
@@ -674,8 +680,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // copy them out as contiguous float4 runs, block row by block row
             // (no divisions in the loop)
             float *obase = p.merge == 2 ? p.out : p.o_part + (long)s * rows_total * 128;
-            for (int jj = 0; jj < T; ++jj) {
-                float4 *dst = reinterpret_cast<float4 *>(obase + (((long)b * T + jj) * p.Hq + g * G) * 128);
+            for (int jj = 0; jj < Tb; ++jj) {
+                float4 *dst = reinterpret_cast<float4 *>(obase + (((long)b * T + j0 + jj) * p.Hq + g * G) * 128);
                 const float *src = ostage + jj * G * kOStride;
                 for (int rem = sidx; rem < G * 32; rem += 256)
                     dst[rem] = *reinterpret_cast<const float4 *>(src + (rem >> 5) * kOStride + (rem & 31) * 4);
@@ -691,8 +697,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                      : "memory");
     }
     if (p.merge == 1)
-        merge_group(p, s, g, b, M, G, rows_total, reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 12),
-                    sbase + L::kOffK);
+        merge_group(p, s, g, b, mb, j0, M, G, rows_total,
+                    reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 12), sbase + L::kOffK);
 }
 
 // ---------------------------------------------------------------------------
@@ -727,15 +733,16 @@ bool make_map(CUtensorMap *m, const void *ptr, const sd_strides &kv, int S, int 
     return r == CUDA_SUCCESS;
 }
 
-// 4-D map over the contiguous queries [B, T, Hq, D]; box: 64 d x G heads x T rows x 1,
-// which lands in shared memory as rows j*G + hl of 128 bytes
+// 4-D map over the contiguous queries [B, T, Hq, D]; box: 64 d x G heads x
+// mblk_nodes block rows x 1, which lands in shared memory as rows (j - j0)*G + hl
+// of 128 bytes
 bool make_q_map(CUtensorMap *m, const AttnParams &p) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const int G = p.Hq / p.Hkv;
     cuuint64_t dims[4] = {128, (cuuint64_t)p.Hq, (cuuint64_t)p.T, (cuuint64_t)p.B};
     cuuint64_t strides[3] = {256, (cuuint64_t)p.Hq * 256, (cuuint64_t)p.T * p.Hq * 256};
-    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)p.T, 1}, estr[4] = {1, 1, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)p.mblk_nodes, 1}, estr[4] = {1, 1, 1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.q), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -760,7 +767,7 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
         if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_splits, p.Hkv, p.B);
+    cfg.gridDim = dim3(p.n_splits, p.Hkv * p.n_mblk, p.B);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -775,8 +782,8 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
 }  // namespace
 
 bool attn_tc_supported(const AttnParams &p) {
-    if (p.dt != SD_BF16 || p.D != 128 || p.T < 1 || p.T > kMaxT) return false;
-    if ((p.Hq / p.Hkv) * p.T > 128) return false;
+    if (p.dt != SD_BF16 || p.D != 128 || p.T < 1 || p.T > (p.mode == 2 ? kMaxTreeT : kMaxT)) return false;
+    if (p.Hq / p.Hkv > 128) return false;   // a row block holds at least one block row
     if ((long)p.max_ctx + p.T > (1L << 30)) return false;
     if (!encode_fn()) return false;
     int dev = 0, optin = 0;

@@ -31,17 +31,23 @@ __global__ void __launch_bounds__(kCommitWarps * 32) commit_tokens_kernel(const 
     const int c = p.ctx_len[b];
     const int ol = p.out_len[b];
     bool ok = n >= 0 && n <= p.T - 1;
-    int tok = 0;
-    if (ok && lane < n) {
-        int src = lane;
-        if (p.path) {
-            const int node = p.path[(long)b * p.T + lane];
-            ok = node >= 1 && node < p.T;
-            src = node;
+    // committed token i (i <= n, at most 64): kept proposal i, then the next token;
+    // lane l takes tokens l and l + 32
+    int tok[2] = {0, 0};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = lane + 32 * k;
+        if (ok && i < n) {
+            int src = i;
+            if (p.path) {
+                const int node = p.path[(long)b * p.T + i];
+                ok = node >= 1 && node < p.T;
+                src = node;
+            }
+            if (ok) tok[k] = p.prop[(long)b * p.ps + src];
         }
-        if (ok) tok = p.prop[(long)b * p.ps + src];
+        if (i == n) tok[k] = p.next_tok[b];
     }
-    if (lane == n) tok = p.next_tok[b];
     ok = __all_sync(0xffffffffu, ok);
     ok = ok && (long)c + n + 1 <= p.ctx_cap && ol >= 0 && (long)ol + n + 1 <= p.out_cap && c >= 1;
     if (!ok) {
@@ -51,7 +57,9 @@ __global__ void __launch_bounds__(kCommitWarps * 32) commit_tokens_kernel(const 
         }
         return;
     }
-    if (lane <= n) p.out_tokens[(long)b * p.out_cap + ol + lane] = tok;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        if (lane + 32 * k <= n) p.out_tokens[(long)b * p.out_cap + ol + lane + 32 * k] = tok[k];
     if (lane == 0) {
         p.out_len[b] = ol + n + 1;
         p.ctx_len[b] = c + n + 1;
@@ -62,13 +70,14 @@ __global__ void __launch_bounds__(kCommitWarps * 32) commit_tokens_kernel(const 
 }
 
 // CTA (b, h): moves the rows of the kept nodes of sequence b, kv head h, to
-// positions ctx-1+1 .. ctx-1+n, K and V.  Every kept row is read into shared
-// memory before any is written: a destination may be another depth's source.
+// positions ctx-1+1 .. ctx-1+n, K then V.  Every kept row of a cache is read
+// into shared memory before any is written: a destination may be another
+// depth's source.
 __global__ void __launch_bounds__(kCompactThreads) compact_tree_kv_kernel(const CompactParams p) {
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
-    __shared__ uint4 stage[2][kMaxT - 1][kMaxHeadBytes / 16];
+    __shared__ uint4 stage[kMaxTreeT - 1][kMaxHeadBytes / 16];
     const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int n = p.n_acc[b], c = p.ctx_len[b];
     bool ok = n >= 0 && n <= p.T - 1 && c >= 1 && (long)c - 1 + p.T <= p.S;
@@ -83,17 +92,19 @@ __global__ void __launch_bounds__(kCompactThreads) compact_tree_kv_kernel(const 
     const int vec = p.D * p.es / 16;              // 16-byte words per row
     const long es = p.es;
     const long base = ((long)b * p.kv.b + (long)h * p.kv.h) * es;
-    for (int i = tid; i < 2 * n * vec; i += kCompactThreads) {
-        const int kv = i / (n * vec), r = i % (n * vec), d = r / vec, x = r % vec;
-        const int node = p.path[(long)b * p.T + d];
-        const char *src = static_cast<const char *>(kv ? p.vc : p.kc) + base + (long)(c - 1 + node) * p.kv.s * es;
-        stage[kv][d][x] = reinterpret_cast<const uint4 *>(src)[x];
-    }
-    __syncthreads();
-    for (int i = tid; i < 2 * n * vec; i += kCompactThreads) {
-        const int kv = i / (n * vec), r = i % (n * vec), d = r / vec, x = r % vec;
-        char *dst = static_cast<char *>(kv ? p.vc : p.kc) + base + (long)(c + d) * p.kv.s * es;
-        reinterpret_cast<uint4 *>(dst)[x] = stage[kv][d][x];
+    for (int kv = 0; kv < 2; ++kv) {
+        char *cache = static_cast<char *>(kv ? p.vc : p.kc);
+        for (int i = tid; i < n * vec; i += kCompactThreads) {
+            const int d = i / vec, x = i % vec;
+            const int node = p.path[(long)b * p.T + d];
+            stage[d][x] = reinterpret_cast<const uint4 *>(cache + base + (long)(c - 1 + node) * p.kv.s * es)[x];
+        }
+        __syncthreads();
+        for (int i = tid; i < n * vec; i += kCompactThreads) {
+            const int d = i / vec, x = i % vec;
+            reinterpret_cast<uint4 *>(cache + base + (long)(c + d) * p.kv.s * es)[x] = stage[d][x];
+        }
+        __syncthreads();   // the stage is reused by the next cache
     }
 }
 

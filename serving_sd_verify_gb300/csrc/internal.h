@@ -23,6 +23,7 @@ enum FaultBits : unsigned int {
 };
 
 constexpr int kMaxT = 16;           // block rows (anchor + 15 proposals)
+constexpr int kMaxTreeT = 64;       // nodes of a draft tree (one 64-bit ancestor mask per node)
 constexpr int kTileKeys = 64;       // keys per tile of the CUDA-core attention kernel
 constexpr int kTcTileKeys = 128;    // keys per tile of the tensor-core attention kernel
 constexpr int kMaxHeadBytes = 512;  // bytes of one (position, kv head) row the tree compaction moves
@@ -36,6 +37,9 @@ constexpr int kMaxHeadBytes = 512;  // bytes of one (position, kv head) row the 
 //                     [0, nctx[b] - 1) and block slot nctx[b] - 1 + k for every
 //                     bit k set in tree_mask[b * T + j]
 //  split s covers keys [s * keys_per_split, (s + 1) * keys_per_split) of that space.
+//  The tensor-core kernel cuts a kv head's G*T query rows into n_mblk row
+//  blocks of mblk_nodes whole block rows (G * mblk_nodes <= 128 rows each);
+//  the blocks of one split read the same K/V tiles.
 struct AttnParams {
     const void *q;                  // [B, T, Hq, D]
     const void *kc, *vc;            // [B, S, Hkv, D] with strides kv
@@ -43,7 +47,7 @@ struct AttnParams {
     const int32_t *nctx;            // [B]
     int mode;
     const void *kb, *vb;            // [B, T, Hkv, D] (mode 1)
-    const uint32_t *tree_mask;      // [B, T] (mode 2)
+    const uint64_t *tree_mask;      // [B, T] (mode 2)
     float *out;                     // [B, T, Hq, D]
     int B, T, Hq, Hkv, D;
     sd_dtype dt;
@@ -51,12 +55,13 @@ struct AttnParams {
     int max_ctx;                    // host bound of nctx
     int s_rows;                     // cache slots available per sequence (derived bound)
     int n_splits, keys_per_split;
+    int n_mblk, mblk_nodes;         // tensor-core kernel: row blocks per kv head, block rows per row block
     float *o_part;                  // [n_splits, B*T*Hq, D]
     float *lse_part;                // [n_splits, B*T*Hq]
     // how the splits are combined: 0 a separate merge kernel, 1 merged inside
-    // the split kernel once every split of a (sequence, kv head) has arrived
-    // (counters merge_ctr[B * Hkv], zero between calls), 2 a single split that
-    // writes the output itself
+    // the split kernel once every split of a (sequence, kv head, row block) has
+    // arrived (counters merge_ctr[B * Hkv * n_mblk], zero between calls), 2 a
+    // single split that writes the output itself
     int merge;
     unsigned int *merge_ctr;
     unsigned int *fault;

@@ -216,10 +216,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // are already on their way; the weights stream from memory once per row
 // group.  16 warps per CTA and two or more CTAs per SM keep enough
 // independent FMA chains in flight to cover their latency.
-// kGather (the commit-time append): CTA row y is sequence b, its rows are
-// 0..n_acc[b] of that sequence's block (row r >= 1 is tree node
-// path[b][r-1] when a path is given) and they land at output rows
-// dst_row0[b] + r; all three come from device memory.
+// kGather (the commit-time append): CTA row y is row group gi of sequence b
+// (y = b * groups + gi, groups = ceil(T / NR)); the sequence's rows are
+// 0..n_acc[b] of its block (row r >= 1 is tree node path[b][r-1] when a path
+// is given), the group takes rows [NR gi, NR gi + NR) of them, and row r lands
+// at output row dst_row0[b] + r; all three come from device memory.
 template <int NR, bool kGather>
 __global__ void __launch_bounds__(kSmallThreads)
 project_small_kernel(const ProjParams p) {
@@ -233,24 +234,27 @@ project_small_kernel(const ProjParams p) {
     int nr;
     long out_row0;                                // element offset of output row 0
     if (kGather) {
-        const int b = blockIdx.y;
+        const int groups = (p.T + NR - 1) / NR;
+        const int b = blockIdx.y / groups, r0 = (blockIdx.y % groups) * NR;
         const int n = p.n_acc[b];
         const int d0 = p.dst_row0[b];
-        bool ok = n >= 0 && n < p.T && n < NR && d0 >= 0 && (long)d0 + n + 1 <= p.max_rows;
+        bool ok = n >= 0 && n < p.T && d0 >= 0 && (long)d0 + n + 1 <= p.max_rows;
         for (int r = 1; ok && r <= n; ++r) {
             const int src = p.path ? p.path[(long)b * p.T + r - 1] : r;
             ok = src >= 1 && src < p.T;
         }
         if (!ok) {                                // uniform over the CTA
-            if (blockIdx.x == 0 && tid == 0) set_fault(p.fault, FAULT_BAD_COMMIT);
+            if (blockIdx.x == 0 && r0 == 0 && tid == 0) set_fault(p.fault, FAULT_BAD_COMMIT);
             return;
         }
-        nr = n + 1;
+        nr = min(NR, n + 1 - r0);
+        if (nr <= 0) return;                      // uniform: this group holds none of the rows
         if (tid < nr) {
-            const int src = tid == 0 ? 0 : p.path ? p.path[(long)b * p.T + tid - 1] : tid;
+            const int r = r0 + tid;
+            const int src = r == 0 ? 0 : p.path ? p.path[(long)b * p.T + r - 1] : r;
             s_off[tid] = (long)b * p.h_bstride + (long)src * p.ld_h;
         }
-        out_row0 = (long)b * p.out_bstride + (long)d0 * p.ld_out;
+        out_row0 = (long)b * p.out_bstride + (long)(d0 + r0) * p.ld_out;
     } else {
         const int n0 = blockIdx.y * NR;
         nr = min(NR, p.N - n0);
@@ -411,7 +415,8 @@ bool project_small_supported(int rows_per_cta, int Hd) {
 }
 
 cudaError_t launch_project_commit(const ProjParams &p, cudaStream_t st) {
-    const dim3 grid((unsigned)((2 * p.Dout + kSmallCols - 1) / kSmallCols), (unsigned)p.B);
+    const int groups = (p.T + kMaxT - 1) / kMaxT;   // row groups of kMaxT rows per sequence
+    const dim3 grid((unsigned)((2 * p.Dout + kSmallCols - 1) / kSmallCols), (unsigned)(p.B * groups));
     return launch_small<kMaxT, true>(p, grid, st);
 }
 

@@ -240,7 +240,8 @@ def sd_accept_tree_greedy_workspace_size(B, T, V, dtype=SD_BF16) -> int:
 
 
 def sd_verify_tree_attention(q, k_cache, v_cache, ctx_len, max_ctx, tree_mask, out, scale, ws, stream=None):
-    """As sd_verify_attention, plus tree_mask int32/uint32 [B,T] (bit k: node sees block slot k)."""
+    """As sd_verify_attention, plus tree_mask int64 [B,T] (bit k of node j's 64-bit word: node j
+    sees block slot k); T <= 64."""
     _need_cuda(q, k_cache, v_cache, ctx_len, tree_mask, out, ws)
     B, T, Hq, D = q.shape
     Hkv = k_cache.shape[2]
@@ -248,8 +249,8 @@ def sd_verify_tree_attention(q, k_cache, v_cache, ctx_len, max_ctx, tree_mask, o
         raise ValueError("q and out must be contiguous; out fp32")
     if ctx_len.dtype != torch.int32 or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
         raise ValueError("ctx_len int32; q, k_cache, v_cache of one dtype")
-    if tree_mask.dtype not in (torch.int32, torch.uint32) or tree_mask.numel() != B * T or not tree_mask.is_contiguous():
-        raise ValueError("tree_mask: contiguous 32-bit [B, T]")
+    if tree_mask.dtype != torch.int64 or tree_mask.numel() != B * T or not tree_mask.is_contiguous():
+        raise ValueError("tree_mask: contiguous int64 [B, T] (one 64-bit mask word per node)")
     if k_cache.stride() != v_cache.stride():
         raise ValueError("k_cache and v_cache must share strides")
     _check(load().sd_verify_tree_attention(_p(q), _p(k_cache), _p(v_cache), _kv_strides(k_cache), _p(ctx_len),

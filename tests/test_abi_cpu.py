@@ -102,6 +102,17 @@ def test_workspace_sizes_are_positive_and_monotone(S):
     assert S.sd_verify_attention_workspace_size(1, 17, 28, 4, 128, 100) == 0
 
 
+def test_tree_calls_take_up_to_64_nodes(S):
+    # a tree of up to 64 nodes (the pages' Tree-60); chains stay at 16 slots
+    assert S.sd_verify_tree_attention_workspace_size(1, 60, 28, 4, 128, 25_119) > \
+        S.sd_verify_tree_attention_workspace_size(1, 16, 28, 4, 128, 25_119) > 256
+    assert S.sd_verify_tree_attention_workspace_size(1, 64, 28, 4, 128, 100) > 0
+    assert S.sd_verify_tree_attention_workspace_size(1, 65, 28, 4, 128, 100) == 0
+    assert S.sd_accept_tree_greedy_workspace_size(2, 64, 152_064) > 256
+    assert S.sd_accept_tree_greedy_workspace_size(2, 65, 152_064) == 0
+    assert S.sd_accept_greedy_workspace_size(1, 17, 1000) == 0
+
+
 def test_binding_refuses_cpu_tensors(S):
     import torch
     q = torch.zeros(1, 16, 28, 128, dtype=torch.bfloat16)

@@ -35,7 +35,8 @@ def _automatic_path(S):
 
 
 def tc_applies(dtype, D, G, T):
-    return dtype == torch.bfloat16 and D == 128 and G * T <= 128
+    # the tensor-core kernel cuts G*T rows into row blocks of whole block rows
+    return dtype == torch.bfloat16 and D == 128 and G <= 128
 
 
 def run_verify(S, inp, path, max_ctx=None, out_rows=None):
@@ -86,7 +87,9 @@ VERIFY_CASES = [
     (3, 1, 28, 4, 128, [5, 64, 1000], torch.bfloat16),  # T = 1: decode
     (2, 2, 8, 8, 128, [63, 65], torch.bfloat16),    # MHA
     (1, 16, 64, 8, 128, [2000], torch.bfloat16),    # 72B-shaped, G*T = 128
-    (2, 16, 16, 1, 64, [300, 77], torch.bfloat16),  # MQA, G*T = 256 (CUDA-core only)
+    (2, 16, 16, 1, 64, [300, 77], torch.bfloat16),  # MQA, G*T = 256 (CUDA-core only: D 64)
+    (2, 16, 16, 1, 128, [300, 77], torch.bfloat16),  # MQA, G*T = 256: two row blocks of 8 block rows
+    (1, 16, 24, 1, 128, [390], torch.bfloat16),      # G 24: 5 block rows per row block, the last with 1
     (1, 5, 7, 1, 128, [333], torch.float32),
 ]
 
@@ -189,6 +192,7 @@ DRAFT_CASES = [
     (2, 16, 28, 4, 128, [1, 700], torch.bfloat16),
     (1, 16, 4, 1, 64, [300], torch.float32),
     (2, 3, 8, 2, 128, [64, 129], torch.bfloat16),
+    (1, 16, 32, 2, 128, [500], torch.bfloat16),   # G*T = 256: two row blocks
 ]
 
 

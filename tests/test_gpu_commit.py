@@ -44,12 +44,24 @@ def random_paths(rng, B, T, V=50):
     return tokens, parents, logits, n, c, path
 
 
-@pytest.mark.parametrize("tree", [False, True])
-def test_commit_tokens_match_oracle(S, tree):
-    rng = np.random.default_rng(3 + tree)
-    B, T, cap = 40, 16, 64
+def deep_first(n, path, T):
+    """Sequence 0 keeps a whole chain of T - 1 nodes (the deepest commit a tree
+    of T nodes allows), so trees of up to 64 nodes reach their last rows."""
+    n, path = n.copy(), path.copy()
+    n[0] = T - 1
+    path[0, :] = np.arange(1, T + 1)
+    path[0, T - 1] = -1
+    return n, path
+
+
+@pytest.mark.parametrize("tree,T", [(False, 16), (True, 16), (True, 64)])
+def test_commit_tokens_match_oracle(S, tree, T):
+    rng = np.random.default_rng(3 + tree + (T if T > 16 else 0))
+    B, cap = 40, 64 if T <= 16 else 2 * T + 40
     if tree:
         prop, _, _, n, nx, path = random_paths(rng, B, T)
+        if T > 16:
+            n, path = deep_first(n, path, T)
     else:
         prop = rng.integers(0, 1000, (B, T - 1)).astype(np.int32)
         n = rng.integers(0, T, B).astype(np.int32)
@@ -92,12 +104,18 @@ def test_commit_tokens_match_oracle(S, tree):
     assert (dctx.cpu().numpy()[~ok] == -5).all()
 
 
-@pytest.mark.parametrize("dtype,D,strided", [(torch.bfloat16, 128, False), (torch.bfloat16, 128, True),
-                                             (torch.float32, 64, False)])
-def test_compact_tree_kv_matches_oracle(S, dtype, D, strided):
-    rng = np.random.default_rng(D + strided)
-    B, Sl, Hkv, T = 5, 160, 4, 16
+@pytest.mark.parametrize("dtype,D,strided,T", [(torch.bfloat16, 128, False, 16), (torch.bfloat16, 128, True, 16),
+                                               (torch.float32, 64, False, 16), (torch.bfloat16, 128, True, 60)])
+def test_compact_tree_kv_matches_oracle(S, dtype, D, strided, T):
+    rng = np.random.default_rng(D + strided + (T if T > 16 else 0))
+    B, Sl, Hkv = 5, 160, 4
     _, _, _, n, _, path = random_paths(rng, B, T)
+    if T > 16:
+        n, path = deep_first(n, path, T)
+        # sequence 4: a deep path over every other node
+        path[4, :] = -1
+        path[4, :T // 2 - 1] = np.arange(2, T, 2)[: T // 2 - 1]
+        n[4] = T // 2 - 1
     ctx = rng.integers(1, Sl - T + 2, B).astype(np.int32)
     ctx[0] = 1
     ctx[1] = Sl - T + 1                     # block ends at the last position
@@ -123,16 +141,18 @@ def test_compact_tree_kv_matches_oracle(S, dtype, D, strided):
     assert torch.equal(big_k[:, Sl:].cpu(), pad_k) and torch.equal(big_v[:, Sl:].cpu(), pad_v)
 
 
-@pytest.mark.parametrize("tree", [False, True])
-def test_project_kv_commit_matches_oracle(S, tree):
-    rng = np.random.default_rng(11 + tree)
-    B, T, Hd, Dout, Sd = 4, 16, 512, 256, 100
+@pytest.mark.parametrize("tree,T", [(False, 16), (True, 16), (True, 60)])
+def test_project_kv_commit_matches_oracle(S, tree, T):
+    rng = np.random.default_rng(11 + tree + (T if T > 16 else 0))
+    B, Hd, Dout, Sd = 4, 512, 256, 100
     g = torch.Generator().manual_seed(5)
     hid = torch.randn(B, T, Hd, generator=g).to(torch.bfloat16)
     wk = (torch.randn(Dout, Hd, generator=g) * 0.05).to(torch.bfloat16)
     wv = (torch.randn(Dout, Hd, generator=g) * 0.05).to(torch.bfloat16)
     if tree:
         _, _, _, n, _, path = random_paths(rng, B, T)
+        if T > 16:
+            n, path = deep_first(n, path, T)   # 60 rows: four row groups of 16
     else:
         n, path = np.array([0, 7, 15, 3], np.int32), None
     d0 = np.array([10, 50, Sd - 1 - int(n[2]), Sd - int(n[3])], np.int32)   # last: one row too many

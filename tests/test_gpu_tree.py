@@ -34,13 +34,14 @@ def random_tree(rng, T, span=3):
 
 
 def masks(parents):
-    m = np.zeros(len(parents), dtype=np.uint32)
+    """One 64-bit ancestor mask per node (bit k: node k is the node or an ancestor)."""
+    m = np.zeros(len(parents), dtype=np.uint64)
     for j in range(len(parents)):
         v, bits = j, 0
         while v != -1:
-            bits |= 1 << v
+            bits |= 1 << int(v)
             v = parents[v]
-        m[j] = bits
+        m[j] = np.uint64(bits)
     return m
 
 
@@ -49,7 +50,7 @@ def run_tree_attention(S, inp, mask, path):
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     mc = inp["max_ctx"]
-    tm = torch.from_numpy(mask.astype(np.int64).astype(np.int32)).reshape(B, T).cuda()
+    tm = torch.from_numpy(np.ascontiguousarray(mask, dtype=np.uint64).view(np.int64)).reshape(B, T).cuda()
     out = torch.full((B, T, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
     ws = S.workspace(S.sd_verify_tree_attention_workspace_size(B, T, Hq, Hkv, D, mc, S._dt(q)))
     S.sd_set_attention_path(path)
@@ -67,6 +68,10 @@ TREE_CASES = [
     (2, 16, 28, 4, 128, [700, 130], torch.bfloat16, (1, 2)),   # several tiles, ragged tails
     (1, 16, 28, 4, 128, [1], torch.bfloat16, (1, 2)),          # the anchor is the only context key
     (2, 8, 4, 1, 64, [300, 5], torch.float32, (1,)),           # CUDA-core kernel only
+    (1, 60, 28, 4, 128, [700], torch.bfloat16, (1, 2)),        # Tree-60: 4 row blocks of 18/18/18/6 nodes
+    (2, 64, 8, 1, 128, [300, 40], torch.bfloat16, (1, 2)),     # 64 nodes (mask bit 63): 4 row blocks of 16
+    (2, 33, 28, 4, 128, [129, 1], torch.bfloat16, (1, 2)),     # mask bit 32, the anchor alone as context
+    (1, 40, 4, 1, 64, [100], torch.float32, (1,)),             # CUDA-core kernel, 40 nodes
 ]
 
 
@@ -106,6 +111,24 @@ def test_tree_attention_full_size_workload(S):
         check_attention(run_tree_attention(S, inp, mask, path)[rows], want)
 
 
+def tree60(rng, T=60, span=3):
+    """A seeded draft tree of T nodes, each node's parent among the span nodes before it."""
+    return random_tree(rng, T, span)
+
+
+def test_tree60_attention_full_size_workload(S):
+    """The pages' Tree-60 at the 25,119-token workload (LLaVA-OneVision-7B
+    shape): 60 nodes verified in one call, sampled rows against the oracle."""
+    T = 60
+    inp = W.verify_inputs(B=1, T=T, Hq=28, Hkv=4, D=128, ctx=25_119, seed=2)
+    rng = np.random.default_rng(61)
+    mask = masks(tree60(rng, T))[None]
+    rows = sample_rows(1, T, 28, 96, seed=61)
+    want = oracle.tree_attention_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], mask, inp["scale"], rows=rows)
+    for path in (0, 2):
+        check_attention(run_tree_attention(S, inp, mask, path)[rows], want)
+
+
 def run_tree_greedy(S, tokens, parents, logits):
     B, T, V = logits.shape
     n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
@@ -121,7 +144,8 @@ def run_tree_greedy(S, tokens, parents, logits):
 
 
 @pytest.mark.parametrize("B,T,V,dtype", [(4, 16, 152_064, torch.bfloat16), (8, 9, 1_000, torch.float32),
-                                         (3, 1, 500, torch.bfloat16)])
+                                         (3, 1, 500, torch.bfloat16), (2, 60, 152_064, torch.bfloat16),
+                                         (5, 64, 2_000, torch.bfloat16), (3, 33, 700, torch.float32)])
 def test_tree_greedy_matches_oracle(S, B, T, V, dtype):
     rng = np.random.default_rng(B * T)
     g = W.greedy_inputs(B=B, T=T, V=V, dtype=dtype, seed=B + T)
