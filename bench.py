@@ -716,6 +716,7 @@ def main():
 
     host = make_inputs(device)
     sets = [DeviceSet(host, device, S) for _ in range(args.copies)]
+    torch.cuda.synchronize()   # inputs and zeroed workspaces are written before another stream reads them
     resident = sum(s.nbytes() for s in sets)
     log(f"[bench] {args.copies} input copies, {resident / 1e6:.0f} MB resident (L2 {L2_BYTES / 1e6:.0f} MB)")
     stream = torch.cuda.Stream(device)

@@ -72,6 +72,10 @@ constexpr int kOStride = 132;               // floats per staged output row (ban
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// A tile whose weights are all at most kLoFrac of the running sum (in every
+// row) is multiplied with P rounded to nearest bf16 alone; any other tile
+// with the two-term P (hi + lo).
+constexpr float kLoFrac = 0.25f;
 
 struct Layout {
     static constexpr int kOffQ = 0;
@@ -82,10 +86,11 @@ struct Layout {
     static constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 3 * kSP + 2;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                 // tmem base, abort flag, merge flag
     static constexpr int kOffX = kOffMisc + 16;                             // [2][128] per-row exchange
+    static constexpr int kOffLo = kOffX + 2 * 128 * 4;                      // [kSP] tile + 1 when its P needs lo
     // epilogue, once every copy and MMA is done: the staged output rows, in the
     // (then idle) K ring
     static constexpr int kOffOStage = kOffK;
-    static constexpr int kSmemBytes = kOffX + 2 * 128 * 4 + 1024;           // + alignment slack
+    static constexpr int kSmemBytes = kOffLo + 16 + 1024;                   // + alignment slack
     static_assert(128 * kOStride * 4 <= kKSlots * kTileBytes, "staging fits in the K ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
@@ -130,68 +135,79 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int mb, in
     __syncthreads();
     const int R = s < M ? (M - s + n - 1) / n : 0;   // rows of this split
     // the splits of a row are cut into K chunks, so that about one (row, 4
-    // columns, chunk) unit falls to each thread
+    // columns, chunk) unit falls to each thread; a unit loads its chunk's
+    // partials and their log-sum-exps together (one round trip), weighs them
+    // against the chunk's own largest log-sum-exp, and the K chunk results are
+    // then combined against the largest of those
     const int K = max(1, min(n, kTcThreads / max(1, R * 32)));
     const int chunk = (n + K - 1) / K;
-    float *wgt = reinterpret_cast<float *>(scratch);                     // [R][n] lse, then weights
-    float *inv = wgt + R * n;                                            // [R] 1 / sum of weights
-    float4 *part = reinterpret_cast<float4 *>(scratch + ((R * n + R) * 4 + 15) / 16 * 16);  // [K][R][32]
+    float4 *pacc = reinterpret_cast<float4 *>(scratch);                    // [K][R][32] weighted sums
+    float *pm = reinterpret_cast<float *>(scratch + (size_t)K * R * 32 * 16);  // [K][R][32] chunk reference
+    float *pw = pm + K * R * 32;                                           // [K][R][32] sum of weights
     auto frow_of = [&](int ri) {
         const int rr = s + ri * n;
         return ((long)b * p.T + j0 + rr / G) * p.Hq + g * G + rr % G;
     };
     if (*go && R > 0) {
-        for (int i = tid; i < R * n; i += kTcThreads)
-            wgt[i] = __ldcg(p.lse_part + (long)(i % n) * rows_total + frow_of(i / n));
-        __syncthreads();
-        for (int ri = tid; ri < R; ri += kTcThreads) {
-            float m = -INFINITY;
-            for (int sp = 0; sp < n; ++sp) m = fmaxf(m, wgt[ri * n + sp]);
-            float sum = 0.f;
-            for (int sp = 0; sp < n; ++sp) {
-                const float l = wgt[ri * n + sp];
-                const float w = l == -INFINITY ? 0.f : __expf(l - m);  // an empty split weighs 0
-                wgt[ri * n + sp] = w;
-                sum += w;
-            }
-            inv[ri] = sum > 0.f ? 1.f / sum : 0.f;
-        }
-        __syncthreads();
         for (int u = tid; u < K * R * 32; u += kTcThreads) {
             const int k = u / (R * 32), ri = (u / 32) % R, c4 = u & 31;
             const long frow = frow_of(ri);
             const int sp0 = k * chunk, sp1 = min(n, sp0 + chunk);
+            float m_run = -INFINITY, w_run = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int sb = sp0; sb < sp1; sb += kMergeBatch) {
                 // branch-free, so that the batch's loads are all in flight at
-                // once: past the chunk's end, re-read its last split with weight 0
+                // once: past the chunk's end, re-read its last split and drop it
                 float4 v[kMergeBatch];
-                float w[kMergeBatch];
+                float l[kMergeBatch];
 #pragma unroll
                 for (int e = 0; e < kMergeBatch; ++e) {
                     const int sp = min(sb + e, sp1 - 1);
                     v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ((long)sp * rows_total + frow) * 128) + c4);
-                    w[e] = sb + e < sp1 ? wgt[ri * n + sp] : 0.f;
+                    l[e] = sb + e < sp1 ? __ldcg(p.lse_part + (long)sp * rows_total + frow) : -INFINITY;
+                }
+                float bm = l[0];
+#pragma unroll
+                for (int e = 1; e < kMergeBatch; ++e) bm = fmaxf(bm, l[e]);
+                if (bm == -INFINITY) continue;                 // only empty splits so far in this batch
+                if (bm > m_run) {                              // a new reference: rescale what is held
+                    const float f = m_run == -INFINITY ? 0.f : __expf(m_run - bm);
+                    acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+                    w_run *= f;
+                    m_run = bm;
                 }
 #pragma unroll
                 for (int e = 0; e < kMergeBatch; ++e) {
-                    acc.x = fmaf(w[e], v[e].x, acc.x); acc.y = fmaf(w[e], v[e].y, acc.y);
-                    acc.z = fmaf(w[e], v[e].z, acc.z); acc.w = fmaf(w[e], v[e].w, acc.w);
+                    const float w = __expf(l[e] - m_run);       // 0 for an empty split (l = -inf)
+                    w_run += w;
+                    acc.x = fmaf(w, v[e].x, acc.x); acc.y = fmaf(w, v[e].y, acc.y);
+                    acc.z = fmaf(w, v[e].z, acc.z); acc.w = fmaf(w, v[e].w, acc.w);
                 }
             }
-            part[u] = acc;
+            pacc[u] = acc;
+            pm[u] = m_run;
+            pw[u] = w_run;
         }
         __syncthreads();
         for (int i = tid; i < R * 32; i += kTcThreads) {
             const int ri = i / 32, c4 = i & 31;
-            float4 acc = part[i];
-            for (int k = 1; k < K; ++k) {
-                const float4 v = part[k * R * 32 + i];
-                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            float M = -INFINITY;
+            for (int k = 0; k < K; ++k) M = fmaxf(M, pm[k * R * 32 + i]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float wsum = 0.f;
+            if (M != -INFINITY) {
+                for (int k = 0; k < K; ++k) {
+                    const float mk = pm[k * R * 32 + i];
+                    const float f = mk == -INFINITY ? 0.f : __expf(mk - M);
+                    const float4 a = pacc[k * R * 32 + i];
+                    acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y);
+                    acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
+                    wsum = fmaf(f, pw[k * R * 32 + i], wsum);
+                }
             }
-            const float f = inv[ri];
+            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
             reinterpret_cast<float4 *>(p.out + frow_of(ri) * 128)[c4] =
-                make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
     }
     // every split takes a second ticket, whether or not its wait succeeded, so
@@ -236,6 +252,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sbase + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 8);
     float *xrow = reinterpret_cast<float *>(sbase + L::kOffX);  // [2][128]: one value per row and warpgroup
+    // lo_flag[i] == t + 1: tile t, in S/P buffer i, is multiplied with the two-term P
+    volatile int *lo_flag = reinterpret_cast<volatile int *>(sbase + L::kOffLo);
 
     const bool producer = warp == kProducerWarp && lane == 0;
     if (producer) {
@@ -245,6 +263,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         mbar_init(qready_bar, 1);  // the Q copy, with its bytes
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        for (int i = 0; i < kSP; ++i) lo_flag[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
@@ -412,17 +431,19 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             for (uint32_t spin = 0; ok && npv < n_tiles;) {
                 if (npv < ns && mbar_test(pfull_bar(npv % kSP), (npv / kSP) & 1) &&
                     mbar_test(vfull_bar(npv % kVSlots), (npv / kVSlots) & 1)) {
-                    // P.V(npv): O += P_hi . V + P_lo . V over the 128 keys
+                    // P.V(npv): O += P_hi . V (+ P_lo . V when the softmax warps asked
+                    // for the two-term P) over the 128 keys
                     tc_fence_after();
                     const uint32_t vb = sV + (npv % kVSlots) * kTileBytes;
                     const uint32_t pb = tmem + 128u + 128u * (npv % kSP);
+                    const bool two_term = lo_flag[npv % kSP] == npv + 1;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         // 16 keys: V rows 16 kk.., P columns of the 64-key half kk / 4
                         const uint64_t bd = sw128_desc(vb + kk * 16 * 128, kBN * 128, 1024);
                         const uint32_t a = pb + 64u * (kk >> 2) + 8u * (kk & 3);
                         umma_ts(tmem, a, bd, idO, (npv > 0 || kk > 0) ? 1u : 0u);
-                        umma_ts(tmem, a + 32u, bd, idO, 1u);
+                        if (two_term) umma_ts(tmem, a + 32u, bd, idO, 1u);
                     }
                     umma_commit(pempty_bar(npv % kSP));
                     umma_commit(vempty_bar(npv % kVSlots));
@@ -547,9 +568,17 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             }
             const float hmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            // the two-term P is needed for the split's first tile, and for any tile
+            // where a row's largest weight, in the reference of the tiles before,
+            // exceeds kLoFrac of that row's running sum; the vote of all rows is
+            // one flag, read after the barrier by every softmax warp and, after
+            // the P arrival, by the MMA issuer
+            const bool vote = t == 0 || (row_ok && !(ex2(hmax * qk - m_used) <= kLoFrac * l));
+            if (__any_sync(0xffffffffu, vote) && lane == 0) lo_flag[bi] = t + 1;
             xrow[wg * 128 + r] = hmax;
             named_sync(1, 256);
             const float omax = xrow[(wg ^ 1) * 128 + r];
+            const bool two_term = lo_flag[bi] == t + 1;
             named_sync(1, 256);  // both read before the next tile writes
             const float tmax = fmaxf(hmax, omax) * qk;
             // move the reference max only when it grows by more than 2^8
@@ -580,10 +609,6 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const float neg_m = live ? -m_used : 0.f;
             if (!live) vis = 0ull;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            // P of this 64-key half over the S columns it came from: hi in [0,32),
-            // lo in [32,64).  hi = p truncated to bf16; lo = the exact fp32
-            // remainder truncated to bf16: |p - hi - lo| < 2^-14 p.  Byte
-            // permutes instead of conversion instructions.
             // the masked keys of an edge tile are cleared in the scores first
             // (-inf gives a weight of 0), so the exponential loop has no selects
             if (!whole || !live) {
@@ -593,23 +618,49 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     if (!((vis >> (32 + c)) & 1ull)) sb[c] = 0xff800000u;
                 }
             }
+            if (two_term) {
+                // P of this 64-key half over the S columns it came from: hi in
+                // [0,32), lo in [32,64).  hi = p truncated to bf16; lo = the exact
+                // fp32 remainder truncated to bf16: |p - hi - lo| < 2^-14 p.  Byte
+                // permutes instead of conversion instructions.
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {   // 32 keys at a time
-                const uint32_t *sq = q == 0 ? sa : sb;
-                uint32_t pk[16], pl[16];
+                for (int q = 0; q < 2; ++q) {   // 32 keys at a time
+                    const uint32_t *sq = q == 0 ? sa : sb;
+                    uint32_t pk[16], pl[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
-                    const float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
-                    ls[c & 3] += p0 + p1;
-                    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-                    pk[c] = __byte_perm(b0, b1, 0x7632);
-                    const uint32_t q0 = __float_as_uint(p0 - __uint_as_float(b0 & 0xffff0000u));
-                    const uint32_t q1 = __float_as_uint(p1 - __uint_as_float(b1 & 0xffff0000u));
-                    pl[c] = __byte_perm(q0, q1, 0x7632);
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
+                        ls[c & 3] += p0 + p1;
+                        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                        pk[c] = __byte_perm(b0, b1, 0x7632);
+                        const uint32_t q0 = __float_as_uint(p0 - __uint_as_float(b0 & 0xffff0000u));
+                        const uint32_t q1 = __float_as_uint(p1 - __uint_as_float(b1 & 0xffff0000u));
+                        pl[c] = __byte_perm(q0, q1, 0x7632);
+                    }
+                    tmem_st16(sp_col + 16u * q, pk);
+                    tmem_st16(sp_col + 32u + 16u * q, pl);
                 }
-                tmem_st16(sp_col + 16u * q, pk);
-                tmem_st16(sp_col + 32u + 16u * q, pl);
+            } else {
+                // P rounded to nearest bf16 in [0,32), and the running sum taken
+                // over the rounded weights themselves, so that the output is the
+                // exact average under those weights (rounding common to all of
+                // them cancels)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t *sq = q == 0 ? sa : sb;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);   // .x = p0 in the low half
+                        const uint32_t h = *reinterpret_cast<const uint32_t *>(&h2);
+                        pk[c] = h;
+                        ls[c & 3] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
+                    }
+                    tmem_st16(sp_col + 16u * q, pk);
+                }
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // value rows past the split's last cache key may hold anything (P is
@@ -673,19 +724,17 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     Lsum > 0.f ? m_used * kLn2 + logf(Lsum) : -INFINITY;
             }
         }
+        if (!abort_seen) fence_proxy_async_smem();   // the staged rows, for the copy engine
         tc_fence_before();
         named_sync(1, 256);
-        if (!abort_seen) {
-            // rows (j, hl) of one j are G consecutive rows of the partial output:
-            // copy them out as contiguous float4 runs, block row by block row
-            // (no divisions in the loop)
+        if (!abort_seen && sidx < M) {
+            // one 512-byte bulk copy per row, by the copy engine; the thread waits
+            // for its copy to land before the CTA announces its partial
+            const int rr = sidx;
             float *obase = p.merge == 2 ? p.out : p.o_part + (long)s * rows_total * 128;
-            for (int jj = 0; jj < Tb; ++jj) {
-                float4 *dst = reinterpret_cast<float4 *>(obase + (((long)b * T + j0 + jj) * p.Hq + g * G) * 128);
-                const float *src = ostage + jj * G * kOStride;
-                for (int rem = sidx; rem < G * 32; rem += 256)
-                    dst[rem] = *reinterpret_cast<const float4 *>(src + (rem >> 5) * kOStride + (rem & 31) * 4);
-            }
+            float *dst = obase + (((long)b * T + j0 + rr / G) * p.Hq + g * G + rr % G) * 128;
+            bulk_store_s2g(dst, smem_u32(ostage + rr * kOStride), 128 * 4);
+            bulk_store_wait_all();
         }
     }
 
@@ -784,6 +833,7 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
 bool attn_tc_supported(const AttnParams &p) {
     if (p.dt != SD_BF16 || p.D != 128 || p.T < 1 || p.T > (p.mode == 2 ? kMaxTreeT : kMaxT)) return false;
     if (p.Hq / p.Hkv > 128) return false;   // a row block holds at least one block row
+    if (!(p.scale > 0.f)) return false;      // the row max is taken on the raw scores
     if ((long)p.max_ctx + p.T > (1L << 30)) return false;
     if (!encode_fn()) return false;
     int dev = 0, optin = 0;

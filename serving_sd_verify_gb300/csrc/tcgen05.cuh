@@ -105,6 +105,17 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// shared to global memory by the copy engine, tracked in this thread's bulk group
+__device__ __forceinline__ void bulk_store_s2g(void *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+// waits until this thread's bulk copies have written global memory, then
+// orders them before its later generic accesses
+__device__ __forceinline__ void bulk_store_wait_all() {
+    asm volatile("cp.async.bulk.commit_group;\n cp.async.bulk.wait_group 0;\n fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int threads) {
