@@ -434,7 +434,10 @@ sd_status sd_fault_word(uint32_t *out, int clear);
 int sd_set_attention_path(int path);
 
 /* Which kernel the last attention call on this thread launched (1 or 2 as
- * above) and how many key splits it used. */
+ * above) and its split count: for the CUDA-core kernel the key splits of every
+ * (sequence, kv head); for the tensor-core kernel the CTAs of its grid, which
+ * the kernel spreads over the (sequence, kv head, row block) units by their
+ * lengths (a unit left with one CTA writes its output itself). */
 int sd_last_attention_path(int *n_splits);
 
 /* How many kernels the last attention call on this thread launched: 1 when the

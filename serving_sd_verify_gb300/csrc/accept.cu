@@ -10,11 +10,16 @@
 // Both are vocabulary-wide reductions over B*T rows.  A grid of (chunk, row)
 // CTAs reads every row once: each thread pulls its share of the chunk into
 // registers with 16-byte loads issued together, reduces it, and the CTA
-// reduces across warps (shuffles, then shared memory) into one partial.  The
-// last CTA of a row to finish (a per-row ticket counter) combines that row's
-// partials; the last row to finish (a second counter) runs the per-sequence
-// scan.  Every counter is returned to zero by the CTA that read it last, so a
-// zero-filled workspace stays reusable.  No CTA ever waits for another.
+// reduces across warps (shuffles, then shared memory) into one partial.  One
+// grid-wide ticket counter elects the CTA that finishes last; that CTA
+// combines every row's partials (the greedy finisher stages them in shared
+// memory, the sampled one takes a warp per row) and runs the per-sequence
+// scan.  The sampled rule's second kernel works on the row that decides each
+// sequence's next token; a ticket counter per sequence elects the CTA that
+// picks the chunk and then the element.  The CTA that takes a counter's last
+// ticket returns it to zero, so a zero-filled workspace stays reusable.  No
+// CTA ever waits for another.  Sums over a whole vocabulary are carried as
+// float-float values (two fp32 words), not in the slow fp64 pipe.
 #include "common.cuh"
 
 #include <float.h>
@@ -30,7 +35,6 @@ constexpr int kArgChains = 4;     // independent argmax chains per thread in the
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
 constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
 constexpr int kFinStaged = 1024;  // chunk partials the greedy finisher stages in shared memory at once
-constexpr int kDrawChunksStaged = 512;  // chunk sums the draw finisher stages in shared memory
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10
@@ -137,24 +141,19 @@ __device__ __forceinline__ T block_sum(T x) {
     return t;
 }
 
-__device__ __forceinline__ float block_max(float x) {
-    __shared__ float sh[kAccThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    __syncthreads();
-    if (lane == 0) sh[warp] = x;
-    __syncthreads();
-    float t = sh[0];
-    for (int w = 1; w < kAccThreads / 32; ++w) t = fmaxf(t, sh[w]);
-    return t;
-}
 
 // Programmatic dependent launch: the kernel may start while the previous one in
 // the stream drains; wait here until its results are visible.
 __device__ __forceinline__ void grid_dependency_wait() {
 #if __CUDA_ARCH__ >= 900
     asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+// lets the next kernel in the stream launch (it still waits for this one's
+// results in its own grid_dependency_wait)
+__device__ __forceinline__ void grid_launch_dependents() {
+#if __CUDA_ARCH__ >= 900
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
 }
 
@@ -368,19 +367,96 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
 }
 
 // ----------------------------------------------------------------------------
+// float-float sums: a value held as hi + lo, two fp32 words with hi the fp32
+// rounding of the pair, added with Knuth's error-free two-sum; about 48
+// significant bits, enough for sums over a whole vocabulary, without the slow
+// fp64 pipe
+// ----------------------------------------------------------------------------
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_norm(float s, float e) {   // s + e with |e| small next to |s|
+    const float h = s + e;
+    return FF{h, e - (h - s)};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const float s = a.hi + b.hi;
+    const float bv = s - a.hi;
+    const float e = ((a.hi - (s - bv)) + (b.hi - bv)) + (a.lo + b.lo);
+    return ff_norm(s, e);
+}
+__device__ __forceinline__ FF ff_add(FF a, float b) { return ff_add(a, FF{b, 0.f}); }
+// a * f, f a plain fp32 factor
+__device__ __forceinline__ FF ff_scale(FF a, float f) {
+    const float p = a.hi * f;
+    return ff_norm(p, fmaf(a.hi, f, -p) + a.lo * f);
+}
+// a * b
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+    const float p = a.hi * b.hi;
+    return ff_norm(p, fmaf(a.hi, b.hi, -p) + (a.hi * b.lo + a.lo * b.hi));
+}
+// the exact product of two fp32 numbers
+__device__ __forceinline__ FF ff_prod(float a, float b) {
+    const float p = a * b;
+    return FF{p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ bool ff_lt(FF a, FF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ bool ff_gt0(FF a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int o) {
+    return FF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ FF ff_shfl_up(FF a, int o) {
+    return FF{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ FF ff_warp_sum(FF x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
+    return x;
+}
+// block-wide sum; result valid in every thread
+__device__ __forceinline__ FF ff_block_sum(FF x) {
+    __shared__ FF sh[kAccThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    x = ff_warp_sum(x);
+    __syncthreads();
+    if (lane == 0) sh[warp] = x;
+    __syncthreads();
+    FF t = sh[0];
+    for (int w = 1; w < kAccThreads / 32; ++w) t = ff_add(t, sh[w]);
+    return t;
+}
+
+__device__ __forceinline__ float block_max(float x) {
+    __shared__ float sh[kAccThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    __syncthreads();
+    if (lane == 0) sh[warp] = x;
+    __syncthreads();
+    float t = sh[0];
+    for (int w = 1; w < kAccThreads / 32; ++w) t = fmaxf(t, sh[w]);
+    return t;
+}
+
+// ----------------------------------------------------------------------------
 // sampled acceptance, pass 1: per-row max and normaliser of softmax(l / tau);
-// the last CTA of a row also tests that row's proposal, the last row finds
-// the first rejection of every sequence
+// the last CTA tests every row's proposal and finds the first rejection of
+// every sequence
 // ----------------------------------------------------------------------------
 template <typename Tin, int NV>
 __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleParams p) {
     grid_dependency_wait();
+    // the draw kernel may take its place on the SMs now and wait there
+    grid_launch_dependents();
     const int c = blockIdx.x, row = blockIdx.y;
     const int lo = c * p.chunk, hi = min(p.V, lo + p.chunk);
     const Tin *lg = static_cast<const Tin *>(p.logits) + (long)row * p.V;
     const float it = p.inv_tau;
     ChunkRegs<Tin, NV> cr;
     cr.load(lg, lo, hi, -INFINITY);
+    // the chunk's max, then its sum of exp against it (float-float)
     float m = -INFINITY;
 #pragma unroll
     for (int v = 0; v < NV; ++v)
@@ -389,24 +465,22 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) m = fmaxf(m, Elem<Tin>::load(lg + i) * it);
     for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) m = fmaxf(m, Elem<Tin>::load(lg + i) * it);
     m = block_max(m);
-    double z = 0.0;
+    FF z = FF{0.f, 0.f};
     if (m != -INFINITY) {
-        float zf = 0.f;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             float zv = 0.f;
 #pragma unroll
             for (int e = 0; e < ChunkRegs<Tin, NV>::PV; ++e) zv += expf(cr.x[v][e] * it - m);  // fill -inf -> 0
-            zf += zv;
+            z = ff_add(z, zv);
         }
-        z = zf;
-        for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) z += expf(Elem<Tin>::load(lg + i) * it - m);
-        for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) z += expf(Elem<Tin>::load(lg + i) * it - m);
+        for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) z = ff_add(z, expf(Elem<Tin>::load(lg + i) * it - m));
+        for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) z = ff_add(z, expf(Elem<Tin>::load(lg + i) * it - m));
     }
-    z = block_sum<double>(z);
+    z = ff_block_sum(z);
     if (threadIdx.x == 0) {
         p.pm[(long)row * p.n_chunks + c] = m;
-        p.pz[(long)row * p.n_chunks + c] = (float)z;
+        p.pz[(long)row * p.n_chunks + c] = make_float2(z.hi, z.lo);
         // the CTA whose chunk holds this row's proposal records its logit and q
         const int b = row / p.T, j = row % p.T;
         if (j < p.T - 1) {
@@ -417,97 +491,101 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
     }
     if (!elect_last(p.counters, gridDim.x * gridDim.y)) return;
 
-    // last CTA: every row's max M and normaliser Z (a warp per row, lanes over
-    // chunks) and the test of its proposal (rows 0..T-2): accept iff
-    // u * q(d) < p(d); then the first rejection of every sequence, over windows
-    // of W rows that hold whole sequences
+    // last CTA: every row's max M and normaliser Z (from the chunk partials,
+    // below) and the test of its proposal (rows 0..T-2): accept iff
+    // u * q(d) < p(d) = exp(l(d) / tau - M) / Z, taken as u * q(d) * Z < exp(..)
+    // with the product exact; then the first rejection of every sequence, over
+    // windows of W rows that hold whole sequences
     __shared__ int acc_s[kAccThreads];
     __shared__ float2 mz_s[kAccThreads];
     const int R = p.B * p.T;
     const int W = (kAccThreads / p.T) * p.T;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int kWarps = kAccThreads / 32;
-    // the accept test of row gr with its max M and normaliser Z
-    auto test_row = [&](int gr, float Mr, double Zr) {
+    auto test_row = [&](int gr, float Mr, FF Zr, float u) {
         const int b = gr / p.T, j = gr % p.T;
         int accept = 0;
         if (j < p.T - 1) {
             const int d = p.draft[(long)b * (p.T - 1) + j];
             if (d >= 0 && d < p.V) {
                 const float2 lq = __ldcg(p.row_stats + gr);
-                const double pd = (double)expf(lq.x * it - Mr) / Zr;
-                const double u = (double)philox_uniform(p.seed, (uint32_t)j, (uint32_t)b, 0u, p.offset);
-                accept = u * (double)lq.y < pd ? 1 : 0;
+                const float ed = expf(lq.x * it - Mr);
+                accept = ff_lt(ff_mul(ff_prod(u, lq.y), Zr), FF{ed, 0.f}) ? 1 : 0;
             } else {
                 set_fault(p.fault, FAULT_BAD_DRAFT_ID);
             }
         }
         return accept;
     };
-    __shared__ float fin_m[kFinStaged], fin_z[kFinStaged];
+    // the window's partials (contiguous in pm / pz) are staged kFinStaged at a
+    // time with all their loads in flight: the row maxima by a thread per row,
+    // then every partial rescaled to its row's maximum by a thread per
+    // partial, then the rows' float-float sums by a thread per row
+    __shared__ float fin_m[kFinStaged];
+    __shared__ FF fin_z[kFinStaged];
+    __shared__ float row_m[kAccThreads];
+    __shared__ FF row_z[kAccThreads];
     for (int r0 = 0; r0 < R; r0 += W) {
         const int nr = min(R - r0, W);
-        const int np = nr * p.n_chunks;   // the window's partials, contiguous in pm / pz
-        if (np <= kFinStaged) {
-            // all of them in flight at once, then a thread per row
-            for (int u = threadIdx.x; u < np; u += kAccThreads) {
-                fin_m[u] = __ldcg(p.pm + (long)r0 * p.n_chunks + u);
-                fin_z[u] = __ldcg(p.pz + (long)r0 * p.n_chunks + u);
+        const int np = nr * p.n_chunks;
+        for (int r = threadIdx.x; r < nr; r += kAccThreads) { row_m[r] = -INFINITY; row_z[r] = FF{0.f, 0.f}; }
+        // this thread's row's uniform (row r0 + threadIdx.x), drawn while the loads below are in flight
+        float u_own = 0.f;
+        if ((int)threadIdx.x < nr) {
+            const int gr = r0 + (int)threadIdx.x;
+            u_own = philox_uniform(p.seed, (uint32_t)(gr % p.T), (uint32_t)(gr / p.T), 0u, p.offset);
+        }
+        for (int k0 = 0; k0 < np; k0 += kFinStaged) {
+            const int nk = min(kFinStaged, np - k0);
+            for (int u = threadIdx.x; u < nk; u += kAccThreads) {
+                const long o = (long)r0 * p.n_chunks + k0 + u;
+                fin_m[u] = __ldcg(p.pm + o);
+                const float2 zk = __ldcg(p.pz + o);
+                fin_z[u] = FF{zk.x, zk.y};
             }
             __syncthreads();
+            // the rows' maxima over this part
             for (int r = threadIdx.x; r < nr; r += kAccThreads) {
-                float Mr = -INFINITY;
-                for (int k = 0; k < p.n_chunks; ++k) Mr = fmaxf(Mr, fin_m[r * p.n_chunks + k]);
-                double Zr = 0.0;
-                for (int k = 0; k < p.n_chunks; ++k) {
-                    const float mk = fin_m[r * p.n_chunks + k];
-                    if (mk != -INFINITY) Zr += (double)fin_z[r * p.n_chunks + k] * (double)expf(mk - Mr);
+                const int u0 = max(0, r * p.n_chunks - k0), u1 = min(nk, (r + 1) * p.n_chunks - k0);
+                float mr = row_m[r];
+                for (int u = u0; u < u1; ++u) mr = fmaxf(mr, fin_m[u]);
+                row_m[r] = mr;
+            }
+            __syncthreads();
+            if (k0 + nk >= np || np <= kFinStaged) {
+                // every part's maxima are in: rescale each partial to its row's max
+                for (int u = threadIdx.x; u < nk; u += kAccThreads) {
+                    const int r = (k0 + u) / p.n_chunks;
+                    const float mk = fin_m[u];
+                    fin_z[u] = mk == -INFINITY ? FF{0.f, 0.f} : ff_scale(fin_z[u], expf(mk - row_m[r]));
                 }
-                acc_s[r] = test_row(r0 + r, Mr, Zr);
-                mz_s[r] = make_float2(Mr, (float)Zr);
+                __syncthreads();
+                for (int r = threadIdx.x; r < nr; r += kAccThreads) {
+                    const int u0 = max(0, r * p.n_chunks - k0), u1 = min(nk, (r + 1) * p.n_chunks - k0);
+                    FF zr = row_z[r];
+                    for (int u = u0; u < u1; ++u) zr = ff_add(zr, fin_z[u]);
+                    row_z[r] = zr;
+                }
+                __syncthreads();
             }
         }
-        // otherwise warp w takes rows w, w + 8, ... of the window, kFinRows at a
-        // time with the loads of all of them in flight together; lanes over the chunks
-        for (int rb = 0; np > kFinStaged && rb < nr; rb += kWarps * kFinRows) {
-            float M[kFinRows];
-            double Z[kFinRows];
-#pragma unroll
-            for (int k = 0; k < kFinRows; ++k) { M[k] = -INFINITY; Z[k] = 0.0; }
-            for (int k0 = lane; k0 < p.n_chunks; k0 += 32) {
-#pragma unroll
-                for (int k = 0; k < kFinRows; ++k) {
-                    const int r = rb + warp + kWarps * k;
-                    if (r < nr) M[k] = fmaxf(M[k], __ldcg(p.pm + (long)(r0 + r) * p.n_chunks + k0));
+        if (np > kFinStaged) {
+            // more partials than one stage: the maxima are final only now, so the
+            // sums are taken in a second sweep straight from L2
+            for (int r = threadIdx.x; r < nr; r += kAccThreads) {
+                const long o = (long)(r0 + r) * p.n_chunks;
+                const float mr = row_m[r];
+                FF zr = FF{0.f, 0.f};
+                for (int k = 0; k < p.n_chunks; ++k) {
+                    const float mk = __ldcg(p.pm + o + k);
+                    const float2 zk = __ldcg(p.pz + o + k);
+                    if (mk != -INFINITY) zr = ff_add(zr, ff_scale(FF{zk.x, zk.y}, expf(mk - mr)));
                 }
+                row_z[r] = zr;
             }
-#pragma unroll
-            for (int k = 0; k < kFinRows; ++k)
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) M[k] = fmaxf(M[k], __shfl_xor_sync(0xffffffffu, M[k], o));
-            for (int k0 = lane; k0 < p.n_chunks; k0 += 32) {
-#pragma unroll
-                for (int k = 0; k < kFinRows; ++k) {
-                    const int r = rb + warp + kWarps * k;
-                    if (r < nr) {
-                        const long o = (long)(r0 + r) * p.n_chunks + k0;
-                        const float mk = __ldcg(p.pm + o);
-                        const float zk = __ldcg(p.pz + o);
-                        if (mk != -INFINITY) Z[k] += (double)zk * (double)expf(mk - M[k]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kFinRows; ++k) Z[k] = warp_sum(Z[k]);
-            if (lane == 0) {
-#pragma unroll
-                for (int k = 0; k < kFinRows; ++k) {
-                    const int r = rb + warp + kWarps * k;
-                    if (r >= nr) continue;
-                    acc_s[r] = test_row(r0 + r, M[k], Z[k]);
-                    mz_s[r] = make_float2(M[k], (float)Z[k]);
-                }
-            }
+            __syncthreads();
+        }
+        for (int r = threadIdx.x; r < nr; r += kAccThreads) {   // nr <= W <= kAccThreads: r is threadIdx.x
+            acc_s[r] = test_row(r0 + r, row_m[r], row_z[r], u_own);
+            mz_s[r] = make_float2(row_m[r], row_z[r].hi + row_z[r].lo);
         }
         __syncthreads();
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
@@ -526,8 +604,9 @@ __global__ void __launch_bounds__(kAccThreads) sample_stats_kernel(const SampleP
 
 // ----------------------------------------------------------------------------
 // sampled acceptance, pass 2: on the row that decides the next token, chunk
-// sums of the residual r = max(p - q, 0) and of p; the last CTA of the
-// sequence picks the chunk where u' * S falls and searches inside it
+// sums of the residual r = max(p - q, 0) (after a rejection) or of p (every
+// proposal accepted); the last CTA of the sequence picks the chunk where
+// u' * S falls and searches inside it
 // ----------------------------------------------------------------------------
 // the weight of element i (the same fp32 arithmetic wherever it is used)
 __device__ __forceinline__ float residual_or_p(float x, float it, float M, float Z, float qi, bool residual) {
@@ -535,6 +614,27 @@ __device__ __forceinline__ float residual_or_p(float x, float it, float M, float
     if (!residual) return pi;
     const float r = pi - qi;
     return r > 0.f ? r : 0.f;
+}
+
+// q at the elements a chunk's registers hold (the vectors of ChunkRegs), with
+// 16-byte loads where the row allows them; zeros when not needed
+template <typename Tin, int NV, int PV>
+__device__ __forceinline__ void load_q(const float *qn, const ChunkRegs<Tin, NV> &cr, bool need, float (&qv)[NV][PV]) {
+    const bool vec4 = (reinterpret_cast<uintptr_t>(qn + cr.a0) & 15u) == 0;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const bool ok = need && cr.valid(v);
+        if (ok && vec4) {
+#pragma unroll
+            for (int e4 = 0; e4 < PV / 4; ++e4) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(qn + cr.index(v, 4 * e4)));
+                qv[v][4 * e4] = t.x; qv[v][4 * e4 + 1] = t.y; qv[v][4 * e4 + 2] = t.z; qv[v][4 * e4 + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < PV; ++e) qv[v][e] = ok ? __ldg(qn + cr.index(v, e)) : 0.f;
+        }
+    }
 }
 
 template <typename Tin, int NV>
@@ -552,155 +652,216 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     const int lo = c * p.draw_chunk, hi = min(p.V, lo + p.draw_chunk);
     ChunkRegs<Tin, NV> cr;
     cr.load(lg, lo, hi, -INFINITY);
-    // per-thread sums in fp32 (at most a few dozen terms), the CTA total in fp64
-    float srf = 0.f, spf = 0.f;
     constexpr int PV = ChunkRegs<Tin, NV>::PV;
     float qv[NV][PV];
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int e = 0; e < PV; ++e) qv[v][e] = (rejected && cr.valid(v)) ? __ldg(qn + cr.index(v, e)) : 0.f;
+    load_q(qn, cr, rejected, qv);
+    // per-vector fp32 sums of PV terms, accumulated as float-float; only the
+    // weights the draw uses (the residual after a rejection, else p)
+    FF sw = FF{0.f, 0.f};
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         if (!cr.valid(v)) break;
-        float sv = 0.f, rv = 0.f;
+        float wv = 0.f;
 #pragma unroll
-        for (int e = 0; e < PV; ++e) {
-            const float pi = expf(cr.x[v][e] * it - M) / Z;
-            sv += pi;
-            const float r = pi - qv[v][e];
-            rv += r > 0.f ? r : 0.f;
-        }
-        spf += sv;
-        srf += rv;
+        for (int e = 0; e < PV; ++e) wv += residual_or_p(cr.x[v][e], it, M, Z, qv[v][e], rejected);
+        sw = ff_add(sw, wv);
     }
-    auto scalar = [&](int i) {
-        const float pi = expf(Elem<Tin>::load(lg + i) * it - M) / Z;
-        spf += pi;
-        if (rejected) { const float r = pi - __ldg(qn + i); srf += r > 0.f ? r : 0.f; }
-    };
-    for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads) scalar(i);
-    for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads) scalar(i);
-    const double sr = block_sum<double>(rejected ? (double)srf : 0.0);
-    const double sp = block_sum<double>((double)spf);
-    if (threadIdx.x == 0) {
-        p.rs[(long)b * p.n_draw_chunks + c] = sr;
-        p.ps[(long)b * p.n_draw_chunks + c] = sp;
-    }
+    for (int i = lo + (int)threadIdx.x; i < cr.a0; i += kAccThreads)
+        sw = ff_add(sw, residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, rejected ? __ldg(qn + i) : 0.f, rejected));
+    for (int i = cr.a1 + (int)threadIdx.x; i < hi; i += kAccThreads)
+        sw = ff_add(sw, residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, rejected ? __ldg(qn + i) : 0.f, rejected));
+    sw = ff_block_sum(sw);
+    if (threadIdx.x == 0) p.rs[(long)b * p.n_draw_chunks + c] = make_float2(sw.hi, sw.lo);
     if (!elect_last(p.row_counter + b, gridDim.x)) return;
 
-    // last CTA of sequence b: which chunk holds u' * S.  The chunk sums are
-    // first staged in shared memory by the whole CTA (one round trip).
-    __shared__ int sel_chunk, sel_res;
-    __shared__ double sel_base, sel_x;
-    __shared__ double s_rs[kDrawChunksStaged], s_ps[kDrawChunksStaged];
-    const bool staged = p.n_draw_chunks <= kDrawChunksStaged;
-    if (staged)
-        for (int k = threadIdx.x; k < p.n_draw_chunks; k += kAccThreads) {
-            s_rs[k] = __ldcg(p.rs + (long)b * p.n_draw_chunks + k);
-            s_ps[k] = __ldcg(p.ps + (long)b * p.n_draw_chunks + k);
-        }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        double Sr = 0.0, Sp = 0.0;
-        for (int k = lane; k < p.n_draw_chunks; k += 32) {
-            Sr += staged ? s_rs[k] : __ldcg(p.rs + (long)b * p.n_draw_chunks + k);
-            Sp += staged ? s_ps[k] : __ldcg(p.ps + (long)b * p.n_draw_chunks + k);
-        }
-        Sr = warp_sum(Sr);
-        Sp = warp_sum(Sp);
-        const bool use_r = rejected && Sr > 0.0;
-        const double *gcs = (use_r ? p.rs : p.ps) + (long)b * p.n_draw_chunks;
-        auto cs_at = [&](int k) { return staged ? (use_r ? s_rs[k] : s_ps[k]) : __ldcg(gcs + k); };
-        const double S = use_r ? Sr : Sp;
-        const double x = (double)philox_uniform(p.seed, (uint32_t)n, (uint32_t)b, 1u, p.offset) * S;
-        // inclusive prefix over the chunk sums, 32 chunks at a time
-        double carry = 0.0;
-        int found = -1, last_pos = -1;
-        double found_base = 0.0;
-        for (int k0 = 0; k0 < p.n_draw_chunks && found < 0; k0 += 32) {
-            const int k = k0 + lane;
-            const double v = k < p.n_draw_chunks ? cs_at(k) : 0.0;
-            double incl = v;
+    // last CTA of sequence b: an inclusive float-float scan of the chunk sums
+    // by the whole CTA (thread k holds chunk k, in passes of kAccThreads),
+    // the first chunk whose prefix exceeds x = u' * S, then the element inside
+    // it, found in fp32 against x minus the chunks before it
+    __shared__ FF wsum[kAccThreads / 32];
+    __shared__ FF s_carry, s_base, s_x;
+    __shared__ int s_found, s_lastpos, s_res;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const float2 *gcs = p.rs + (long)b * p.n_draw_chunks;
+    // the deciding row's u' (every thread draws it; no barrier waits on it)
+    const float u2 = philox_uniform(p.seed, (uint32_t)n, (uint32_t)b, 1u, p.offset);
+    auto scan_select = [&](bool residual) {
+        // one inclusive scan over the chunk sums (thread k holds chunk k, in
+        // passes of kAccThreads): its last value is S; then the chunk whose
+        // interval [prefix - sum, prefix) holds x = u' * S
+        constexpr int kPass = 4;   // chunk sums a thread keeps from the scan (nd <= 4 * kAccThreads here)
+        FF incl_k[kPass], v_k[kPass];
+        if (threadIdx.x == 0) { s_carry = FF{0.f, 0.f}; s_found = INT_MAX; s_lastpos = -1; }
+        __syncthreads();
+        const int passes = (p.n_draw_chunks + kAccThreads - 1) / kAccThreads;
+        const bool keep = passes <= kPass;
+#pragma unroll
+        for (int q = 0; q < kPass; ++q) { incl_k[q] = FF{0.f, 0.f}; v_k[q] = FF{0.f, 0.f}; }
+        for (int q = 0; q < passes; ++q) {
+            const int k = q * kAccThreads + (int)threadIdx.x;
+            FF v = FF{0.f, 0.f};
+            if (k < p.n_draw_chunks) { const float2 t = __ldcg(gcs + k); v = FF{t.x, t.y}; }
+            FF incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+                const FF y = ff_shfl_up(incl, o);
+                if (lane >= o) incl = ff_add(incl, y);
             }
-            const unsigned pos = __ballot_sync(0xffffffffu, k < p.n_draw_chunks && v > 0.0);
-            if (pos) last_pos = k0 + 31 - __clz((int)pos);
-            const unsigned hit = __ballot_sync(0xffffffffu, k < p.n_draw_chunks && carry + incl > x);
-            if (hit) {
-                const int l = __ffs((int)hit) - 1;
-                found = k0 + l;
-                found_base = carry + __shfl_sync(0xffffffffu, incl - v, l);
+            if (lane == 31) wsum[wid] = incl;
+            __syncthreads();
+            FF pre = s_carry;
+            for (int w = 0; w < wid; ++w) pre = ff_add(pre, wsum[w]);
+            incl = ff_add(pre, incl);
+            if (k < p.n_draw_chunks && ff_gt0(v)) atomicMax(&s_lastpos, k);
+#pragma unroll
+            for (int qq = 0; qq < kPass; ++qq)
+                if (qq == q) { incl_k[qq] = incl; v_k[qq] = v; }
+            __syncthreads();
+            if (threadIdx.x == kAccThreads - 1) s_carry = incl;   // the total so far
+            __syncthreads();
+        }
+        const FF S = s_carry;
+        if (residual && !ff_gt0(S)) {   // residual zero everywhere: draw from p instead
+            if (threadIdx.x == 0) s_res = 2;
+            __syncthreads();
+            return;
+        }
+        const FF x = ff_mul(FF{u2, 0.f}, S);
+        if (keep) {
+#pragma unroll
+            for (int q = 0; q < kPass; ++q) {
+                const int k = q * kAccThreads + (int)threadIdx.x;
+                if (q < passes && k < p.n_draw_chunks) {
+                    const FF excl = ff_add(incl_k[q], FF{-v_k[q].hi, -v_k[q].lo});
+                    if (ff_lt(x, incl_k[q]) && !ff_lt(x, excl)) { s_found = k; s_base = excl; }   // one k at most
+                }
             }
-            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (found < 0) {  // x reached the total through rounding: the last non-empty chunk
-            found = last_pos < 0 ? 0 : last_pos;
-            double base = 0.0;
-            for (int k = lane; k < found; k += 32) base += cs_at(k);
-            found_base = warp_sum(base);
+        if (threadIdx.x == 0) { s_x = x; s_res = residual ? 1 : 0; }
+        __syncthreads();
+        if (s_found == INT_MAX) {
+            // more chunks than a thread keeps, or x reached the total through
+            // rounding: walk the chunk sums once more with one thread
+            if (threadIdx.x == 0) {
+                FF acc = FF{0.f, 0.f};
+                int found = -1;
+                for (int k = 0; k < p.n_draw_chunks; ++k) {
+                    const float2 t = __ldcg(gcs + k);
+                    const FF nxt = ff_add(acc, FF{t.x, t.y});
+                    if (ff_lt(x, nxt)) { found = k; break; }
+                    acc = nxt;
+                }
+                if (found < 0) {   // the last non-empty chunk, and the sum before it
+                    found = s_lastpos < 0 ? 0 : s_lastpos;
+                    acc = FF{0.f, 0.f};
+                    for (int k = 0; k < found; ++k) { const float2 t = __ldcg(gcs + k); acc = ff_add(acc, FF{t.x, t.y}); }
+                }
+                s_found = found;
+                s_base = acc;
+            }
+            __syncthreads();
         }
-        if (lane == 0) { sel_chunk = found; sel_base = found_base; sel_x = x; sel_res = use_r ? 1 : 0; }
+    };
+    scan_select(rejected);
+    if (s_res == 2) {
+        // a rejection whose residual is zero everywhere (p = q up to rounding):
+        // the draw is from p; rare enough to take the p chunk sums here
+        for (int k = 0; k < p.n_draw_chunks; ++k) {
+            const int klo = k * p.draw_chunk, khi = min(p.V, klo + p.draw_chunk);
+            FF part = FF{0.f, 0.f};
+            for (int i = klo + (int)threadIdx.x; i < khi; i += kAccThreads)
+                part = ff_add(part, residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, 0.f, false));
+            part = ff_block_sum(part);
+            if (threadIdx.x == 0) p.rs[(long)b * p.n_draw_chunks + k] = make_float2(part.hi, part.lo);
+        }
+        __syncthreads();
+        scan_select(false);
     }
-    __syncthreads();
 
-    // inside the chunk: thread t owns a contiguous run of elements; runs are
-    // combined by an exclusive scan over the threads, the owner of the
-    // crossing then walks its run
-    constexpr int kRun = 16;
-    static_assert(kRun * kAccThreads >= kDrawChunkMax, "the search covers a whole draw chunk");
+    // inside the chunk: its elements in registers as in the first phase
+    // (vector v of thread t holds 8 (bf16) or 4 (fp32) consecutive elements,
+    // vector slots in element order v-major), the weights recomputed with the
+    // same arithmetic, and for each vector slot an exclusive fp32 scan of the
+    // threads' vector sums from the chunk's start (the chunk is a small part of
+    // S, so fp32 holds these offsets to far better than 1e-6 S); the thread
+    // whose vector holds the crossing walks it.  The draw is the smallest index
+    // whose computed inclusive prefix exceeds x (the inverse CDF), reduced
+    // with a warp minimum before the shared atomic
+    const int sel_chunk = s_found;
+    const bool res = s_res != 0;
+    const float xl = ff_add(s_x, FF{-s_base.hi, -s_base.lo}).hi;   // x - base, to fp32
     const int clo = sel_chunk * p.draw_chunk, chi = min(p.V, clo + p.draw_chunk);
-    const int per = (chi - clo + kAccThreads - 1) / kAccThreads;  // <= kRun (draw chunk <= kDrawChunkMax)
-    const int tlo = min(chi, clo + (int)threadIdx.x * per), thi = min(chi, tlo + per);
-    const bool res = sel_res != 0;
-    float w[kRun], xin[kRun], qin[kRun];
-#pragma unroll
-    for (int e = 0; e < kRun; ++e) {
-        const int i = tlo + e;
-        xin[e] = i < thi ? Elem<Tin>::load(lg + i) : 0.f;
-        qin[e] = (i < thi && res) ? __ldg(qn + i) : 0.f;
+    ChunkRegs<Tin, NV> sr;
+    sr.load(lg, clo, chi, -INFINITY);
+    float qs[NV][PV];
+    load_q(qn, sr, res, qs);
+    __shared__ float wtot[kAccThreads / 32];
+    __shared__ int s_id, s_last;
+    if (threadIdx.x == 0) { s_id = INT_MAX; s_last = -1; }
+    // the unaligned head [clo, a0) (fewer than 8 elements) comes first in element order
+    float head = 0.f;
+    for (int i = clo; i < sr.a0; ++i) {
+        const float wi = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, res ? __ldg(qn + i) : 0.f, res);
+        if (wi > 0.f) { if (threadIdx.x == 0) atomicMax(&s_last, i); }
+        if (threadIdx.x == 0 && head + wi > xl) atomicMin(&s_id, i);
+        head += wi;
     }
-    float runf = 0.f;
+    float carry = head;
 #pragma unroll
-    for (int e = 0; e < kRun; ++e) {
-        w[e] = tlo + e < thi ? residual_or_p(xin[e], it, M, Z, qin[e], res) : 0.f;
-        runf += w[e];
-    }
-    // exclusive prefix of the runs over the threads: warp scans, then warp totals
-    const double run = (double)runf;
-    __shared__ double wtot[kAccThreads / 32];
-    __shared__ int s_id, s_lastpos;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    double incl = run;
+    for (int v = 0; v < NV; ++v) {
+        float wv[PV];
+        float sv = 0.f;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) wtot[wid] = incl;
-    if (threadIdx.x == 0) { s_id = INT_MAX; s_lastpos = -1; }
-    __syncthreads();
-    double before = 0.0;
-    for (int k = 0; k < wid; ++k) before += wtot[k];
-    double acc = sel_base + before + (incl - run);
-    int last_here = -1;
+        for (int e = 0; e < PV; ++e) {
+            wv[e] = sr.valid(v) ? residual_or_p(sr.x[v][e], it, M, Z, qs[v][e], res) : 0.f;
+            sv += wv[e];
+        }
+        float incl = sv;
 #pragma unroll
-    for (int e = 0; e < kRun; ++e) {
-        if (tlo + e >= thi) break;
-        if (w[e] > 0.f) last_here = tlo + e;
-        const double nxt = acc + (double)w[e];
-        if (nxt > sel_x && acc <= sel_x) { atomicMin(&s_id, tlo + e); break; }
-        acc = nxt;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __syncthreads();   // wtot of the previous slot is read
+        if (lane == 31) wtot[wid] = incl;
+        __syncthreads();
+        float acc = carry + (incl - sv);
+        float slot_tot = 0.f;
+        for (int k = 0; k < kAccThreads / 32; ++k) {
+            if (k < wid) acc += wtot[k];
+            slot_tot += wtot[k];
+        }
+        int cand = INT_MAX, last_here = -1;
+        if (sr.valid(v)) {
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+                if (wv[e] > 0.f) last_here = sr.index(v, e);
+                acc += wv[e];
+                if (acc > xl && cand == INT_MAX) cand = sr.index(v, e);
+            }
+        }
+        cand = __reduce_min_sync(0xffffffffu, cand);
+        last_here = __reduce_max_sync(0xffffffffu, last_here);
+        if (lane == 0) {
+            if (cand != INT_MAX) atomicMin(&s_id, cand);
+            if (last_here >= 0) atomicMax(&s_last, last_here);
+        }
+        carry += slot_tot;
     }
-    if (last_here >= 0) atomicMax(&s_lastpos, last_here);
+    // the unaligned tail [a1, chi) last
+    if (threadIdx.x == 0) {
+        float acc = carry;
+        for (int i = sr.a1; i < chi; ++i) {
+            const float wi = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, res ? __ldg(qn + i) : 0.f, res);
+            if (wi > 0.f) atomicMax(&s_last, i);
+            acc += wi;
+            if (acc > xl) atomicMin(&s_id, i);
+        }
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         int id = s_id;
-        if (id == INT_MAX) id = s_lastpos >= 0 ? s_lastpos : clo;  // rounding: last positive weight
+        if (id == INT_MAX) id = s_last >= 0 ? s_last : clo;  // rounding: last positive weight
         p.next_id[b] = id;
     }
 }

@@ -90,7 +90,31 @@ AttnPlan plan_attention(const AttnParams &p, int path) {
     pl.path = path;
     pl.n_mblk = 1;
     pl.mblk_nodes = p.T;
-    if (path >= 2) row_blocks(p.Hq / p.Hkv, p.T, &pl.n_mblk, &pl.mblk_nodes);
+    if (path >= 2) {
+        // tensor cores: one CTA per work slot, at most one per SM when the units
+        // fit (the kernel spreads the slots over the units by their sequences'
+        // lengths, read on the device), else one per unit
+        row_blocks(p.Hq / p.Hkv, p.T, &pl.n_mblk, &pl.mblk_nodes);
+        const long units = (long)p.B * p.Hkv * pl.n_mblk;
+        // tiles of the longest unit: its cache keys, plus the drafter's block tile
+        const long cache_keys = p.mode == 1 ? p.max_ctx : (long)p.max_ctx + p.T - 1;
+        const long max_tiles = (cache_keys + kTcTileKeys - 1) / kTcTileKeys + (p.mode == 1 ? 1 : 0);
+        if (units > sms) {
+            pl.n_splits = (int)units;
+        } else if (p.B == 1) {
+            // one sequence: every unit has max_tiles; the fewest splits per unit
+            // that reach the smallest load of any split count fitting the SMs
+            const long per = std::max(1L, std::min<long>(sms / units, max_tiles));
+            const long load = (max_tiles + per - 1) / per;
+            pl.n_splits = (int)(units * ((max_tiles + load - 1) / load));
+        } else {
+            // several sequences: the kernel spreads up to one CTA per SM over the
+            // units by their lengths
+            pl.n_splits = (int)std::min<long>(sms, units * max_tiles);
+        }
+        pl.keys_per_split = 0;
+        return pl;
+    }
     const int units = p.B * p.Hkv * pl.n_mblk;
     int ctas_per_sm, min_keys, gran;
     if (path >= 2) { ctas_per_sm = 1; min_keys = 2 * kTcTileKeys; gran = kTcTileKeys; }
@@ -111,11 +135,15 @@ AttnPlan plan_attention(const AttnParams &p, int path) {
 size_t attn_counters_bytes(int B, int Hkv, int n_mblk) {
     return align_up((size_t)B * Hkv * n_mblk * sizeof(unsigned int), 256);
 }
-size_t attn_workspace(int B, int T, int Hq, int Hkv, int D, int n_splits, int n_mblk) {
-    const size_t rows = (size_t)B * T * Hq;
-    return kHeader + attn_counters_bytes(B, Hkv, n_mblk) +
-           align_up((size_t)n_splits * rows * D * sizeof(float), 256) +
-           align_up((size_t)n_splits * rows * sizeof(float), 256);
+// partial rows: CUDA-core kernel [n_splits][B*T*Hq] rows; tensor-core kernel one
+// slot of 128 rows per CTA
+size_t attn_partial_rows(int path, int B, int T, int Hq, int n_splits) {
+    return path >= 2 ? (size_t)n_splits * 128 : (size_t)n_splits * B * T * Hq;
+}
+size_t attn_workspace(int path, int B, int T, int Hq, int Hkv, int D, int n_splits, int n_mblk) {
+    const size_t rows = attn_partial_rows(path, B, T, Hq, n_splits);
+    return kHeader + attn_counters_bytes(B, Hkv, n_mblk) + align_up(rows * D * sizeof(float), 256) +
+           align_up(rows * sizeof(float), 256);
 }
 
 sd_status validate_attention(const AttnParams &p) {
@@ -158,27 +186,26 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     else if (force >= 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
     else path = 1;
     AttnPlan pl = plan_attention(p, path);
-    const size_t need = attn_workspace(p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits, pl.n_mblk);
+    const size_t need = attn_workspace(path, p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits, pl.n_mblk);
     if (!ws || ws_bytes < need)
         return fail(SD_ERR_WORKSPACE, "attention workspace too small: need %zu bytes, got %zu", need, ws_bytes);
     if (!aligned16(ws)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    const size_t rows = (size_t)p.B * p.T * p.Hq;
+    const size_t rows = attn_partial_rows(path, p.B, p.T, p.Hq, pl.n_splits);
     p.merge_ctr = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + kHeader);
     char *w = static_cast<char *>(ws) + kHeader + attn_counters_bytes(p.B, p.Hkv, pl.n_mblk);
     p.o_part = reinterpret_cast<float *>(w);
-    p.lse_part = reinterpret_cast<float *>(w + align_up((size_t)pl.n_splits * rows * p.D * sizeof(float), 256));
+    p.lse_part = reinterpret_cast<float *>(w + align_up(rows * p.D * sizeof(float), 256));
     p.n_splits = pl.n_splits;
     p.keys_per_split = pl.keys_per_split;
     p.n_mblk = pl.n_mblk;
     p.mblk_nodes = pl.mblk_nodes;
-    // tensor-core path: one split writes the output itself; several merge
-    // inside the kernel when the whole grid is resident at once (at most one
-    // CTA per SM), else in the merge kernel
-    p.merge = 0;
-    if (path == 2) {
-        if (pl.n_splits == 1) p.merge = 2;
-        else if ((long)pl.n_splits * p.Hkv * p.B * pl.n_mblk <= device_sm_count()) p.merge = 1;
-    }
+    // one sequence: a (splits, units) grid, every unit as long as the others
+    p.plan_static = path == 2 && p.B == 1 && (long)p.Hkv * pl.n_mblk <= device_sm_count() ? 1 : 0;
+    // tensor-core path: the splits of a unit merge inside the kernel (its grid
+    // has at most one CTA per SM whenever a unit has several splits), and a
+    // unit's only split writes the output itself; the CUDA-core path merges
+    // in the merge kernel
+    p.merge = path == 2 ? 1 : 0;
     cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
     if (p.merge == 0) {
@@ -198,8 +225,8 @@ size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max
     AttnParams p = {};
     p.mode = mode; p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.dt = dt; p.max_ctx = max_ctx;
     const AttnPlan p1 = plan_attention(p, 1), p2 = plan_attention(p, 2);
-    return std::max(attn_workspace(B, T, Hq, Hkv, D, p1.n_splits, p1.n_mblk),
-                    attn_workspace(B, T, Hq, Hkv, D, p2.n_splits, p2.n_mblk));
+    return std::max(attn_workspace(1, B, T, Hq, Hkv, D, p1.n_splits, p1.n_mblk),
+                    attn_workspace(2, B, T, Hq, Hkv, D, p2.n_splits, p2.n_mblk));
 }
 
 // ----------------------------------------------------------------------------
@@ -238,19 +265,16 @@ GreedyLayout greedy_layout(int B, int T, int V, int chunk) {
     return l;
 }
 
-// chunk of the sampled rule's second pass (one row per sequence): about two
-// CTAs per SM over the B rows, at least 1024 elements
+// chunk of the sampled rule's second pass (the deciding row of each sequence):
+// the largest chunk the in-chunk search covers, so the chunk sums are few
 int draw_chunk_for(int B, int V) {
-    const int sms = device_sm_count();
-    long c = ((long)B * V + 2L * sms - 1) / (2L * sms);
-    c = std::max(1024L, std::min(c, (long)kDrawChunkMax));
-    c = (c + 7) / 8 * 8;
-    return (int)std::min<long>(c, (long)V);
+    (void)B;
+    return std::min(V, kDrawChunkMax);
 }
 
-// sample workspace: [header: pass-1 counter][per-sequence counters][pm][pz][row_stats][state][rs][ps]
+// sample workspace: [header: pass-1 counter][per-sequence counters][pm][pz][row_stats][state][rs]
 struct SampleLayout {
-    size_t row_ctr, pm, pz, row_stats, state, rs, ps, total;
+    size_t row_ctr, pm, pz, row_stats, state, rs, total;
 };
 SampleLayout sample_layout(int B, int T, int V, int chunk, int draw_chunk) {
     const size_t R = (size_t)B * T, nc = (V + chunk - 1) / chunk, parts = R * nc;
@@ -259,11 +283,10 @@ SampleLayout sample_layout(int B, int T, int V, int chunk, int draw_chunk) {
     l.row_ctr = kHeader;
     l.pm = l.row_ctr + align_up((size_t)B * 4, 256);
     l.pz = l.pm + align_up(parts * 4, 256);
-    l.row_stats = l.pz + align_up(parts * 4, 256);
+    l.row_stats = l.pz + align_up(parts * 8, 256);
     l.state = l.row_stats + align_up(R * 8, 256);
     l.rs = l.state + align_up((size_t)B * 16, 256);
-    l.ps = l.rs + align_up((size_t)B * nd * 8, 256);
-    l.total = l.ps + align_up((size_t)B * nd * 8, 256);
+    l.total = l.rs + align_up((size_t)B * nd * 8, 256);
     return l;
 }
 
@@ -492,11 +515,10 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.counters = reinterpret_cast<unsigned int *>(w);
     p.row_counter = reinterpret_cast<unsigned int *>(w + sl.row_ctr);
     p.pm = reinterpret_cast<float *>(w + sl.pm);
-    p.pz = reinterpret_cast<float *>(w + sl.pz);
+    p.pz = reinterpret_cast<float2 *>(w + sl.pz);
     p.row_stats = reinterpret_cast<float2 *>(w + sl.row_stats);
     p.state = reinterpret_cast<float4 *>(w + sl.state);
-    p.rs = reinterpret_cast<double *>(w + sl.rs);
-    p.ps = reinterpret_cast<double *>(w + sl.ps);
+    p.rs = reinterpret_cast<float2 *>(w + sl.rs);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
     cudaError_t e = launch_accept_sample(p, static_cast<cudaStream_t>(stream));

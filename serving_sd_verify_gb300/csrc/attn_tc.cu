@@ -87,13 +87,173 @@ struct Layout {
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;                 // tmem base, abort flag, merge flag
     static constexpr int kOffX = kOffMisc + 16;                             // [2][128] per-row exchange
     static constexpr int kOffLo = kOffX + 2 * 128 * 4;                      // [kSP] tile + 1 when its P needs lo
+    static constexpr int kOffPlan = kOffLo + 16;                            // the CtaPlan
     // epilogue, once every copy and MMA is done: the staged output rows, in the
     // (then idle) K ring
     static constexpr int kOffOStage = kOffK;
-    static constexpr int kSmemBytes = kOffLo + 16 + 1024;                   // + alignment slack
+    static constexpr int kSmemBytes = kOffPlan + 48 + 1024;                 // + alignment slack (CtaPlan: 48 B)
     static_assert(128 * kOStride * 4 <= kKSlots * kTileBytes, "staging fits in the K ring");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
+
+// ---------------------------------------------------------------------------
+// work plan: which keys of which (sequence, kv head, row block) this CTA takes
+// ---------------------------------------------------------------------------
+// The grid is one CTA per work slot.  Unit u = (b, g, mb) has tiles_u 128-key
+// tiles (its sequence's cache keys, plus the block tile that leads a drafter
+// unit) and gets n_u = ceil(tiles_u / L) splits, L the smallest load for which
+// sum n_u fits the C slots, so long sequences get more CTAs than short ones and
+// no CTA takes more than L tiles; split s of n takes tiles
+// [s tiles / n, (s + 1) tiles / n).  A unit's CTAs are consecutive: slot0 is
+// its first, and its partial slots are slot0 .. slot0 + n - 1.  CTAs past
+// sum n_u are idle.  Every CTA derives the same plan from ctx_len, so no plan
+// crosses the host.  With more units than kPlanUnits the grid holds one CTA
+// per unit.
+constexpr int kPlanUnits = 5 * 32;   // units a warp plans with its lanes' registers
+
+struct CtaPlan {      // 48 bytes, held in shared memory at Layout::kOffPlan
+    int b, g, mb;        // unit
+    int s, n, slot0;     // split s of n; the unit's first slot
+    int k0, k1;          // cache keys [k0, k1) of the sequence's key space (clipped later)
+    int block_tile;      // the drafter's block tile leads this split
+    int idle;
+    int nb;              // the sequence's ctx_len, clamped to [1, max_ctx]
+    int tiles;           // the unit's tiles (0: not yet read)
+};
+static_assert(sizeof(CtaPlan) == 48, "the plan's shared-memory slot");
+
+// tiles of unit u: its sequence's cache keys, plus the drafter's block tile
+__device__ __forceinline__ int unit_tiles(const AttnParams &p, int u) {
+    int nb = p.nctx[u / (p.Hkv * p.n_mblk)];
+    nb = max(1, min(nb, p.max_ctx));
+    const int keys = p.mode == 1 ? nb : nb + p.T - 1;
+    return (keys + kBN - 1) / kBN + (p.mode == 1 ? 1 : 0);
+}
+
+// ceil(t / d) for 0 <= t < 2^24, d >= 1: a float estimate, corrected by one
+__device__ __forceinline__ int ceil_div_small(int t, int d, float inv_d) {
+    int q = (int)ceilf((float)t * inv_d);
+    if (q > 0 && (q - 1) * d >= t) --q;
+    else if (q * d < t) ++q;
+    return q;
+}
+
+// Which unit and split this CTA serves (warp-collective, one full warp).
+// With one sequence every unit has the same length: the grid is (splits, units)
+// and the assignment needs neither a global load nor a division.  Otherwise
+// the grid is one CTA per work slot and the lanes search for the load L over
+// the units' tiles, read from ctx_len.
+__device__ CtaPlan plan_unit(const AttnParams &p) {
+    const int lane = threadIdx.x & 31;
+    const int U = p.B * p.Hkv * p.n_mblk;
+    const int C = (int)gridDim.x;
+    const int slot = (int)blockIdx.x;
+    CtaPlan pl = {};
+    pl.idle = 1;
+    if (p.plan_static) {
+        pl.idle = 0;
+        pl.b = (int)blockIdx.y;                // the unit, split into (b, g, mb) below
+        pl.s = slot;
+        pl.n = C;
+        pl.slot0 = (int)blockIdx.y * C;
+    } else if (U > kPlanUnits || U >= C) {     // one CTA per unit
+        if (slot < U) { pl.idle = 0; pl.b = slot; pl.s = 0; pl.n = 1; pl.slot0 = slot; }
+    } else {
+        const int kU = (U + 31) / 32;          // units per lane, <= kPlanUnits / 32
+        int tl[kPlanUnits / 32];
+        int tmax = 1;
+        long tot = 0;
+#pragma unroll
+        for (int k = 0; k < kPlanUnits / 32; ++k) {
+            const int u = lane + 32 * k;
+            tl[k] = (k < kU && u < U) ? unit_tiles(p, u) : 0;
+            tmax = max(tmax, tl[k]);
+            tot += tl[k];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        }
+        // smallest L in [ceil(tot / C), tmax] with sum ceil(tiles_u / L) <= C:
+        // each round the 32 lanes try 32 loads spread over the range at once
+        // (the count falls as L grows, and L = tmax always fits: U <= C)
+        int lo = (int)max(1L, (tot + C - 1) / C), hi = tmax;
+        while (lo < hi) {
+            const int span = hi - lo;
+            const int cand = lo + (int)((long)lane * span / 31);   // lane 0: lo, lane 31: hi
+            const float inv_c = 1.0f / (float)cand;
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < kPlanUnits / 32; ++k) {
+                if (k >= kU) break;
+#pragma unroll 8
+                for (int src = 0; src < 32; ++src) {
+                    const int t = __shfl_sync(0xffffffffu, tl[k], src);   // 0 past the last unit
+                    cnt += ceil_div_small(t, cand, inv_c);
+                }
+            }
+            const unsigned fits = __ballot_sync(0xffffffffu, cnt <= C);
+            const int f = __ffs((int)fits) - 1;                     // lane 31 (hi) always fits
+            const int new_hi = __shfl_sync(0xffffffffu, cand, f);
+            const int below = __shfl_sync(0xffffffffu, cand, max(f - 1, 0));
+            lo = f > 0 ? below + 1 : lo;
+            hi = new_hi;
+        }
+        const float inv = 1.0f / (float)lo;
+        int base = 0;
+#pragma unroll
+        for (int k = 0; k < kPlanUnits / 32; ++k) {
+            if (k >= kU) break;
+            const int u = lane + 32 * k;
+            const int nu = ceil_div_small(tl[k], lo, inv);   // 0 past the last unit
+            int incl = nu;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int excl = base + incl - nu;
+            const unsigned hit = __ballot_sync(0xffffffffu, u < U && slot >= excl && slot < excl + nu);
+            if (hit) {
+                const int src = __ffs((int)hit) - 1;
+                pl.idle = 0;
+                pl.b = 32 * k + src;   // the unit, split into (b, g, mb) below
+                pl.n = __shfl_sync(0xffffffffu, nu, src);
+                pl.slot0 = __shfl_sync(0xffffffffu, excl, src);
+                pl.s = slot - pl.slot0;
+                pl.tiles = __shfl_sync(0xffffffffu, tl[k], src);
+                break;
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    if (!pl.idle) {
+        const int u = pl.b;
+        if (p.n_mblk == 1) {
+            pl.b = p.B == 1 ? 0 : u / p.Hkv;
+            pl.g = p.B == 1 ? u : u - pl.b * p.Hkv;
+            pl.mb = 0;
+        } else {
+            pl.b = u / (p.Hkv * p.n_mblk);
+            pl.g = (u / p.n_mblk) % p.Hkv;
+            pl.mb = u % p.n_mblk;
+        }
+    }
+    return pl;
+}
+
+// the split's cache keys, from its unit's tiles (one global load)
+__device__ void plan_keys(const AttnParams &p, CtaPlan &pl) {
+    const int lead = p.mode == 1 ? 1 : 0;
+    pl.nb = max(1, min(p.nctx[pl.b], p.max_ctx));
+    if (pl.tiles == 0) pl.tiles = ((p.mode == 1 ? pl.nb : pl.nb + p.T - 1) + kBN - 1) / kBN + lead;  // < 2^24
+    const int tiles = pl.tiles;
+    const int a = pl.s * tiles / pl.n, e = (pl.s + 1) * tiles / pl.n;               // products < 2^31
+    pl.k0 = max(0, a - lead) * kBN;
+    pl.k1 = max(0, e - lead) * kBN;
+    pl.block_tile = lead && a == 0 && e > 0;   // an empty split [0, 0) takes nothing
+}
 
 // ---------------------------------------------------------------------------
 // merge of the splits inside the kernel
@@ -110,19 +270,20 @@ __device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int ta
     }
 }
 
-// Every split of sequence b, kv head g, row block mb has written its partial
-// (rows normalised by their own sum, plus their log-sum-exp); once all of them
-// have arrived, split s combines rows s, s + n, s + 2n, ... of the group's M
-// rows (n = splits; row rr is block row j0 + rr / G, query head g G + rr % G):
+// Every split of unit (b, g, mb) has written its partial into its slot (rows
+// normalised by their own sum, plus their log-sum-exp); once all n of them
+// have arrived, split s combines rows s, s + n, s + 2n, ... of the unit's M
+// rows (row rr is block row j0 + rr / G, query head g G + rr % G):
 // out = sum_s w_s o_s / sum_s w_s with w_s = exp(lse_s - max).
 // The whole grid is resident (at most one CTA per SM), so the wait ends.  The
 // counter is returned to zero by the last split to finish merging.  `scratch`
 // is idle shared memory (the K/V rings).
 constexpr int kMergeBatch = 12;  // loads one merge thread keeps in flight
-__device__ void merge_group(const AttnParams &p, int s, int g, int b, int mb, int j0, int M, int G,
-                            long rows_total, volatile int *go, uint8_t *scratch) {
-    unsigned int *ctr = p.merge_ctr + (((long)b * p.Hkv + g) * p.n_mblk + mb);
-    const int n = (int)gridDim.x;
+__device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int M, int G, volatile int *go,
+                            uint8_t *scratch) {
+    const int s = pl.s, g = pl.g, b = pl.b;
+    unsigned int *ctr = p.merge_ctr + (((long)b * p.Hkv + g) * p.n_mblk + pl.mb);
+    const int n = pl.n;
     const int tid = threadIdx.x;
     __threadfence();  // this thread's partial stores are visible device-wide
     __syncthreads();
@@ -151,7 +312,6 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int mb, in
     if (*go && R > 0) {
         for (int u = tid; u < K * R * 32; u += kTcThreads) {
             const int k = u / (R * 32), ri = (u / 32) % R, c4 = u & 31;
-            const long frow = frow_of(ri);
             const int sp0 = k * chunk, sp1 = min(n, sp0 + chunk);
             float m_run = -INFINITY, w_run = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -162,9 +322,9 @@ __device__ void merge_group(const AttnParams &p, int s, int g, int b, int mb, in
                 float l[kMergeBatch];
 #pragma unroll
                 for (int e = 0; e < kMergeBatch; ++e) {
-                    const int sp = min(sb + e, sp1 - 1);
-                    v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ((long)sp * rows_total + frow) * 128) + c4);
-                    l[e] = sb + e < sp1 ? __ldcg(p.lse_part + (long)sp * rows_total + frow) : -INFINITY;
+                    const long prow = (long)(pl.slot0 + min(sb + e, sp1 - 1)) * 128 + s + ri * n;  // slot, row
+                    v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + prow * 128) + c4);
+                    l[e] = sb + e < sp1 ? __ldcg(p.lse_part + prow) : -INFINITY;
                 }
                 float bm = l[0];
 #pragma unroll
@@ -233,8 +393,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t *sbase = smem_raw + (base - raw_u32);
 
-    // grid: (split, kv head x row block, sequence)
-    const int s = blockIdx.x, g = blockIdx.y / p.n_mblk, mb = blockIdx.y % p.n_mblk, b = blockIdx.z;
+    // grid: one CTA per work slot, or (split, unit) for one sequence (plan_unit)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const uint32_t sQ = base + L::kOffQ, sK = base + L::kOffK, sV = base + L::kOffV;
@@ -254,6 +413,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     float *xrow = reinterpret_cast<float *>(sbase + L::kOffX);  // [2][128]: one value per row and warpgroup
     // lo_flag[i] == t + 1: tile t, in S/P buffer i, is multiplied with the two-term P
     volatile int *lo_flag = reinterpret_cast<volatile int *>(sbase + L::kOffLo);
+    CtaPlan *plan_sh = reinterpret_cast<CtaPlan *>(sbase + L::kOffPlan);
 
     const bool producer = warp == kProducerWarp && lane == 0;
     if (producer) {
@@ -279,61 +439,93 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs of an upstream kernel are visible now
 #endif
 
-    // this CTA's rows: block rows [j0, j0 + Tb) of the G query heads of kv head g
+    // the plan: warp 0 works it out, and its lane 0 starts the Q copy and the
+    // first K/V copies before the CTA-wide barrier; the other warps read the
+    // plan after it
     const int T = p.T, G = p.Hq / p.Hkv;
-    const int j0 = mb * p.mblk_nodes, Tb = min(p.mblk_nodes, T - j0), M = G * Tb;
     const int MQ = G * p.mblk_nodes;  // rows the Q copy writes (those past block row T - 1 as zeros)
-    if (producer) {
-        // Q first: rows r = (j - j0)*G + hl of this kv head, two 64-column halves;
-        // the copy always moves the whole box (out-of-range rows are zero-filled)
-        mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * MQ));
-        tma_load_4d(sQ, &tmap_q, qready_bar, 0, g * G, j0, b);
-        tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, g * G, j0, b);
+    CtaPlan pl = {};
+    if (warp == kProducerWarp) {
+        pl = plan_unit(p);
+        if (producer && !pl.idle) {
+            // Q first: rows r = (j - j0)*G + hl of this kv head, two 64-column halves;
+            // the copy always moves the whole box (out-of-range rows are zero-filled)
+            mbar_arrive_expect_tx(qready_bar, (uint32_t)(256 * MQ));
+            tma_load_4d(sQ, &tmap_q, qready_bar, 0, pl.g * G, pl.mb * p.mblk_nodes, pl.b);
+            tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, pl.g * G, pl.mb * p.mblk_nodes, pl.b);
+        }
+        if (!pl.idle) plan_keys(p, pl);
+        if (lane == 0) *plan_sh = pl;
     }
+    // a split's tiles: the cache keys [k0, cend) of its sequence, after the
+    // drafter's block tile when it leads the split
+    struct Tiles {
+        int nb, k0, cend, n_tiles, first_tma;
+    };
+    auto tiles_of = [&](const CtaPlan &q) {
+        Tiles r;
+        r.nb = q.nb;
+        r.k0 = q.k0;
+        r.cend = p.mode == 1 ? min(q.k1, r.nb) : min(q.k1, r.nb + T - 1);
+        const int n_cache = r.cend > r.k0 ? (r.cend - r.k0 + kBN - 1) / kBN : 0;
+        r.first_tma = q.block_tile ? 1 : 0;   // tile 0 of a leading drafter split is the block
+        r.n_tiles = n_cache + r.first_tma;
+        return r;
+    };
+    // one copy per tile: map coordinates (d within a half, key, half, kv head, sequence)
+    auto issue_k = [&](const CtaPlan &q, const Tiles &r, int t) {
+        const int sl = t % kKSlots;
+        mbar_arrive_expect_tx(kfull_bar(sl), (uint32_t)kTileBytes);
+        tma_load_5d(sK + sl * kTileBytes, &tmap_k, kfull_bar(sl), 0, r.k0 + (t - r.first_tma) * kBN, 0, q.g, q.b);
+    };
+    auto issue_v = [&](const CtaPlan &q, const Tiles &r, int t) {
+        const int sl = t % kVSlots;
+        mbar_arrive_expect_tx(vfull_bar(sl), (uint32_t)kTileBytes);
+        tma_load_5d(sV + sl * kTileBytes, &tmap_v, vfull_bar(sl), 0, r.k0 + (t - r.first_tma) * kBN, 0, q.g, q.b);
+    };
+    // first wave, before the CTA-wide barrier: every slot of both rings
+    if (producer && !pl.idle) {
+        const Tiles r = tiles_of(pl);
+        for (int t = r.first_tma; t < min(r.n_tiles, kKSlots); ++t) {
+            issue_k(pl, r, t);
+            issue_v(pl, r, t);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp != kProducerWarp) pl = *plan_sh;
+    if (pl.idle) {
+        // no work for this slot: give the tensor memory back and leave
+        if (warp == kMmaWarp) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_holder),
+                         "r"(kTmemCols) : "memory");
+        }
+        return;
+    }
+    const int g = pl.g, mb = pl.mb, b = pl.b;
+    const int slot = pl.slot0 + pl.s;  // this split's partial slot
+    const bool direct = pl.n == 1;  // a unit's only split writes the output itself
+    // this CTA's rows: block rows [j0, j0 + Tb) of the G query heads of kv head g
+    const int j0 = mb * p.mblk_nodes, Tb = min(p.mblk_nodes, T - j0), M = G * Tb;
     const bool drafter = p.mode == 1;
-    int nb = p.nctx[b];
-    if (nb < 1 || nb > p.max_ctx) {
-        if (tid == 0) set_fault(p.fault, FAULT_BAD_CTX);
-        nb = max(1, min(nb, p.max_ctx));
-    }
-    const int k0 = s * p.keys_per_split;
-    const int k1 = k0 + p.keys_per_split;
-    const int cend = drafter ? min(k1, nb) : min(k1, nb + T - 1);  // end of this split's cache keys
-    const int n_cache_tiles = cend > k0 ? (cend - k0 + kBN - 1) / kBN : 0;
-    const bool has_block_tile = drafter && s == 0;
-    const int n_tiles = n_cache_tiles + (has_block_tile ? 1 : 0);
-    const int first_tma = has_block_tile ? 1 : 0;  // tile 0 of the drafter's split 0 is the block
-    const long rows_total = (long)p.B * T * p.Hq;
-    auto tile_key0 = [&](int t) { return k0 + (t - first_tma) * kBN; };
+    if (tid == 0 && (p.nctx[b] < 1 || p.nctx[b] > p.max_ctx)) set_fault(p.fault, FAULT_BAD_CTX);
+    const Tiles tr = tiles_of(pl);
+    const int nb = tr.nb, cend = tr.cend, n_tiles = tr.n_tiles, first_tma = tr.first_tma;
+    const bool has_block_tile = first_tma != 0;
+    auto tile_key0 = [&](int t) { return tr.k0 + (t - first_tma) * kBN; };
     auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
     // keys every row of the block sees: the drafter's context, the target's
     // cache before the block (before the anchor for a tree)
     const bool tree = p.mode == 2;
     const int all_see = min(cend, tree ? nb - 1 : nb);
+    // copies the first wave issued
+    int next_k = max(first_tma, min(n_tiles, kKSlots)), next_v = next_k;
+    static_assert(kKSlots == kVSlots, "the first wave fills both rings in step");
+    auto issue_k_t = [&](int t) { issue_k(pl, tr, t); };
+    auto issue_v_t = [&](int t) { issue_v(pl, tr, t); };
 
-    // one copy per tile: map coordinates (d within a half, key, half, kv head, sequence)
-    auto issue_k = [&](int t) {
-        const int slot = t % kKSlots;
-        mbar_arrive_expect_tx(kfull_bar(slot), (uint32_t)kTileBytes);
-        tma_load_5d(sK + slot * kTileBytes, &tmap_k, kfull_bar(slot), 0, tile_key0(t), 0, g, b);
-    };
-    auto issue_v = [&](int t) {
-        const int slot = t % kVSlots;
-        mbar_arrive_expect_tx(vfull_bar(slot), (uint32_t)kTileBytes);
-        tma_load_5d(sV + slot * kTileBytes, &tmap_v, vfull_bar(slot), 0, tile_key0(t), 0, g, b);
-    };
-    // first wave, before the CTA-wide sync: every slot of both rings
-    int next_k = first_tma, next_v = first_tma;
-    if (producer) {
-        for (; next_k < min(n_tiles, kKSlots); ++next_k) {
-            issue_k(next_k);
-            if (next_v < min(n_tiles, kVSlots)) issue_v(next_v++);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
     if (n_tiles == 0) {
@@ -343,9 +535,9 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         for (int idx = tid; idx < M * 32; idx += kTcThreads) {
             const int rr = idx >> 5, c4 = idx & 31;
             const long frow = ((long)b * T + j0 + rr / G) * p.Hq + g * G + rr % G;
-            float *dst = p.merge == 2 ? p.out + frow * 128 : p.o_part + ((long)s * rows_total + frow) * 128;
+            float *dst = direct ? p.out + frow * 128 : p.o_part + ((long)slot * 128 + rr) * 128;
             reinterpret_cast<float4 *>(dst)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c4 == 0 && p.merge != 2) p.lse_part[(long)s * rows_total + frow] = -INFINITY;
+            if (c4 == 0 && !direct) p.lse_part[(long)slot * 128 + rr] = -INFINITY;
         }
     } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ producer
@@ -377,13 +569,13 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             for (uint32_t spin = 0; next_k < n_tiles || next_v < n_tiles;) {
                 if (next_k < n_tiles &&
                     (next_k < kKSlots || mbar_test(kempty_bar(next_k % kKSlots), ((next_k / kKSlots) - 1) & 1))) {
-                    issue_k(next_k++);
+                    issue_k_t(next_k++);
                     t_last = global_timer();
                     continue;
                 }
                 if (next_v < n_tiles &&
                     (next_v < kVSlots || mbar_test(vempty_bar(next_v % kVSlots), ((next_v / kVSlots) - 1) & 1))) {
-                    issue_v(next_v++);
+                    issue_v_t(next_v++);
                     t_last = global_timer();
                     continue;
                 }
@@ -718,11 +910,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                         make_float4(__uint_as_float(oa[e]) * inv, __uint_as_float(oa[e + 1]) * inv,
                                     __uint_as_float(oa[e + 2]) * inv, __uint_as_float(oa[e + 3]) * inv);
             }
-            if (row_ok && wg == 0 && p.merge != 2) {
-                const int h = g * G + r % G;
-                p.lse_part[(long)s * rows_total + ((long)b * T + j) * p.Hq + h] =
-                    Lsum > 0.f ? m_used * kLn2 + logf(Lsum) : -INFINITY;
-            }
+            if (row_ok && wg == 0 && !direct)
+                p.lse_part[(long)slot * 128 + r] = Lsum > 0.f ? m_used * kLn2 + logf(Lsum) : -INFINITY;
         }
         if (!abort_seen) fence_proxy_async_smem();   // the staged rows, for the copy engine
         tc_fence_before();
@@ -731,8 +920,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // one 512-byte bulk copy per row, by the copy engine; the thread waits
             // for its copy to land before the CTA announces its partial
             const int rr = sidx;
-            float *obase = p.merge == 2 ? p.out : p.o_part + (long)s * rows_total * 128;
-            float *dst = obase + (((long)b * T + j0 + rr / G) * p.Hq + g * G + rr % G) * 128;
+            float *dst = direct ? p.out + (((long)b * T + j0 + rr / G) * p.Hq + g * G + rr % G) * 128
+                                : p.o_part + ((long)slot * 128 + rr) * 128;
             bulk_store_s2g(dst, smem_u32(ostage + rr * kOStride), 128 * 4);
             bulk_store_wait_all();
         }
@@ -745,9 +934,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
-    if (p.merge == 1)
-        merge_group(p, s, g, b, mb, j0, M, G, rows_total,
-                    reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 12), sbase + L::kOffK);
+    if (!direct)
+        merge_group(p, pl, j0, M, G, reinterpret_cast<volatile int *>(sbase + L::kOffMisc + 12), sbase + L::kOffK);
 }
 
 // ---------------------------------------------------------------------------
@@ -816,7 +1004,9 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
         if (dev >= 0 && dev < 64) opted_in[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_splits, p.Hkv * p.n_mblk, p.B);
+    // one CTA per work slot, or (splits, units) for one sequence (plan_unit)
+    cfg.gridDim = p.plan_static ? dim3(p.n_splits / (p.B * p.Hkv * p.n_mblk), p.B * p.Hkv * p.n_mblk)
+                                : dim3(p.n_splits);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;

@@ -56,6 +56,7 @@ struct AttnParams {
     int s_rows;                     // cache slots available per sequence (derived bound)
     int n_splits, keys_per_split;
     int n_mblk, mblk_nodes;         // tensor-core kernel: row blocks per kv head, block rows per row block
+    int plan_static;                // tensor-core kernel: grid (splits, units) instead of one CTA per work slot
     float *o_part;                  // [n_splits, B*T*Hq, D]
     float *lse_part;                // [n_splits, B*T*Hq]
     // how the splits are combined: 0 a separate merge kernel, 1 merged inside
@@ -106,10 +107,11 @@ struct SampleParams {
     int draw_chunk, n_draw_chunks;  // pass 2 chunks, draw_chunk <= kDrawChunkMax
     unsigned int *counters;         // [0]: CTAs of pass 1 finished
     unsigned int *row_counter;      // [B] CTAs of pass 2 finished per sequence
-    float *pm, *pz;                 // [B*T, n_chunks] chunk max and sum of exp
+    float *pm;                      // [B*T, n_chunks] chunk max
+    float2 *pz;                     // [B*T, n_chunks] chunk sum of exp (hi, lo: a float-float value)
     float2 *row_stats;              // [B*T] (logit, q) of the row's proposal
     float4 *state;                  // [B]: (n as int bits, M, Z, unused) of the deciding row
-    double *rs, *ps;                // [B, n_draw_chunks] residual / p chunk sums
+    float2 *rs;                     // [B, n_draw_chunks] chunk sums of the draw's weights (hi, lo)
     unsigned int *fault;
 };
 constexpr int kDrawChunkMax = 4096;  // pass 2 chunk bound: 16 elements per thread of the in-chunk search

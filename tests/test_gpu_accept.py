@@ -239,3 +239,22 @@ def test_accept_errors_are_reported_not_launched(S):
         S.sd_accept_sample(d, lg.float(), lg, 0.0, 1, 0, n, n, ws)
     assert e.value.status == S.SD_ERR_INVALID_ARG
     assert S.sd_fault_word() == 0
+
+
+def test_sample_zero_residual_draws_from_p(S):
+    """q = 2 p (unnormalised, taken as given): a proposal is rejected when
+    u >= 1/2, the residual max(p - q, 0) is zero everywhere, and the next token
+    is drawn from p, as the oracle does (its draw mode 1)."""
+    B, T, V = 16, 4, 20_000
+    g = torch.Generator().manual_seed(44)
+    lg = (torch.randn(B, T, V, generator=g) * 2).to(torch.bfloat16)
+    p = torch.softmax(lg.double(), -1)
+    q = (2.0 * p).float()
+    draft = torch.multinomial(p[:, :-1].reshape(-1, V), 1, generator=g).reshape(B, T - 1).int()
+    inp = {"logits": lg, "q": q, "draft": draft}
+    n, nx = run_sample(S, inp, 1.0, 99)
+    on, onx, exc = assert_sample_parity(inp, n, nx, 1.0, 99)
+    _, _, diag = oracle.accept_sample(draft, q, lg, 1.0, 99, return_diag=True)
+    modes = oracle.split_diag(diag, T)["mode"]
+    assert (on < T - 1).any() and (modes[on < T - 1] == 1).all()   # rejections drew from p
+    assert exc <= 1

@@ -90,6 +90,7 @@ VERIFY_CASES = [
     (2, 16, 16, 1, 64, [300, 77], torch.bfloat16),  # MQA, G*T = 256 (CUDA-core only: D 64)
     (2, 16, 16, 1, 128, [300, 77], torch.bfloat16),  # MQA, G*T = 256: two row blocks of 8 block rows
     (1, 16, 24, 1, 128, [390], torch.bfloat16),      # G 24: 5 block rows per row block, the last with 1
+    (5, 16, 28, 4, 128, [1, 3000, 40, 9000, 128], torch.bfloat16),  # ragged: 1 to 71 tiles, splits by length
     (1, 5, 7, 1, 128, [333], torch.float32),
 ]
 
@@ -278,10 +279,11 @@ def test_verify_in_kernel_merge_reuses_its_workspace(S):
     rows = sample_rows(B, T, Hq, 16, seed=22)
     want = oracle_verify_rows(inp["q"], inp["k"], inp["v"], inp["ctx"], inp["scale"], rows)
     check_attention(outs[1].numpy().reshape(B * T * Hq, D)[rows], want)
-    # a context short enough for one split: the kernel writes the output itself
-    small = W.verify_inputs(B=1, T=16, Hq=28, Hkv=4, D=128, ctx=[130], dtype=torch.bfloat16, seed=23)
+    # a context of one tile per kv head: one CTA per (sequence, kv head), each
+    # writing its output itself
+    small = W.verify_inputs(B=1, T=16, Hq=28, Hkv=4, D=128, ctx=[100], dtype=torch.bfloat16, seed=23)
     got, used = run_verify(S, small, 2)
-    assert used == (2, 1) and S.sd_last_attention_launches() == 1
+    assert used == (2, 4) and S.sd_last_attention_launches() == 1
     check_attention(got, oracle_verify_rows(small["q"], small["k"], small["v"], small["ctx"], small["scale"],
                                             list(range(16 * 28))))
     S.sd_set_attention_path(0)
