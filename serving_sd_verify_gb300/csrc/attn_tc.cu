@@ -1010,12 +1010,26 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    // the splits of a unit that merge inside the kernel wait for one another:
+    // with at most one CTA per SM the grid goes out as a cooperative launch,
+    // which makes every CTA resident at once; a device that cannot do that (a
+    // partitioned one) gets an ordinary launch, where a wait that gives up
+    // sets fault bit 3 instead of hanging
+    const bool coop = (long)cfg.gridDim.x * cfg.gridDim.y <= device_sm_count();
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
+    cfg.numAttrs = coop ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
+    if (e == cudaErrorCooperativeLaunchTooLarge && coop) {
+        (void)cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
+    }
+    return e;
 }
 
 }  // namespace
