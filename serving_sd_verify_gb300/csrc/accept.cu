@@ -31,7 +31,6 @@ namespace sdv {
 namespace {
 
 constexpr int kAccThreads = 256;
-constexpr int kArgChains = 4;     // independent argmax chains per thread in the greedy stream
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
 constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
 constexpr int kFinStaged = 1024;  // chunk partials the greedy finisher stages in shared memory at once
@@ -158,20 +157,19 @@ __device__ __forceinline__ void grid_launch_dependents() {
 }
 
 // Last-CTA election on `counter` among `total` arrivals: true in every thread of
-// the CTA that arrived last, which also returns the counter to zero.  Only
-// thread 0 of a CTA writes that CTA's partial results; its fence before the
-// ticket makes them visible to the elected CTA, which reads them from L2.
+// the CTA that arrived last, which also returns the counter to zero (seen by
+// the next launch once this grid has ended).  Only thread 0 of a CTA writes
+// that CTA's partial results; its ticket is an acquire-release atomic at GPU
+// scope, so the partials are released with it, and the last CTA's acquire
+// (then the barrier) orders its threads' reads of everyone's partials after it.
 __device__ __forceinline__ bool elect_last(unsigned int *counter, unsigned int total) {
     __shared__ bool is_last;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned int ticket = atomicAdd(counter, 1u);
+        unsigned int ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counter) : "memory");
         is_last = ticket == total - 1;
-        if (is_last) {
-            *counter = 0u;
-            __threadfence();
-        }
+        if (is_last) *counter = 0u;
     }
     __syncthreads();
     return is_last;
@@ -188,17 +186,33 @@ template <> struct Vec16<float> {
         f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
         f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
     }
+    // the largest ordered value of the vector (NaN loses; -inf if all are NaN)
+    __device__ __forceinline__ static float max(const uint4 &u) {
+        return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                     fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+    }
 };
 template <> struct Vec16<__nv_bfloat16> {
     static constexpr int PV = 8;
     __device__ __forceinline__ static void unpack(const uint4 &u, float (&f)[8]) { unpack_bf16x8(u, f); }
+    // the largest ordered value of the vector, from packed bf16x2 maxima (exact:
+    // a maximum picks one of its inputs; NaN loses to a number)
+    __device__ __forceinline__ static float max(const uint4 &u) {
+        const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x),
+                                         *reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+        const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&u.z),
+                                         *reinterpret_cast<const __nv_bfloat162 *>(&u.w));
+        const __nv_bfloat162 c = __hmax2(a, b);
+        return fmaxf(__low2float(c), __high2float(c));
+    }
 };
 
 // CTA (c, row) streams chunk c of one row: the unaligned head and tail
 // element by element, the 16-byte-aligned body in batches of kGreedyBatch
 // vectors per thread, the next batch in flight while this one is reduced
+// at most 3 CTAs per SM are resident by design (the grid is one such wave)
 template <typename Tin>
-__global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams p) {
+__global__ void __launch_bounds__(kAccThreads, 3) greedy_kernel(const GreedyParams p) {
     grid_dependency_wait();
     constexpr int PV = Vec16<Tin>::PV;
     const int c = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
@@ -209,19 +223,28 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     while (a0 < hi && ((base + (uintptr_t)a0 * sizeof(Tin)) & 15u)) ++a0;
     const int nvec = (hi - a0) / PV, a1 = a0 + nvec * PV;
     const uint4 *vp = reinterpret_cast<const uint4 *>(lg + a0);
-    // kArgChains independent (value, index) chains per thread, so that
-    // consecutive compares do not wait on each other; merged at the end by
-    // the same rule (larger value, then lower index), so the result does not
-    // depend on which chain saw which element
-    float cv[kArgChains];
-    int ci[kArgChains];
-#pragma unroll
-    for (int k = 0; k < kArgChains; ++k) { cv[k] = -INFINITY; ci[k] = INT_MAX; }
+    // the first finisher window's proposals, loaded by every CTA while its
+    // stream runs (only the last CTA uses them: at most 1 KB, from L2)
+    const int per_seq = p.parents ? p.T : p.T - 1;
+    const int R = p.B * p.T;
+    const int W = (kAccThreads / p.T) * p.T;
+    const int n_pre = min(R, W) / p.T * per_seq;
+    int pre_tok = 0, pre_par = 0;
+    if (tid < n_pre) {
+        pre_tok = p.draft[tid];
+        if (p.parents) pre_par = p.parents[tid];
+    }
+    // the thread's (value, index) argmax so far
+    float cv = -INFINITY;
+    int ci = INT_MAX;
     for (int i = lo + tid; i < a0; i += kAccThreads) {
         const float x = Elem<Tin>::load(lg + i);
-        if (argmax_better(x, i, cv[0], ci[0])) { cv[0] = x; ci[0] = i; }
+        if (argmax_better(x, i, cv, ci)) { cv = x; ci = i; }
     }
-    uint4 cur[kGreedyBatch], nxt[kGreedyBatch];
+    // a ring of three batches of kGreedyBatch vectors: while one is reduced
+    // the next two are in flight (12 vectors, 192 bytes per thread)
+    uint4 r0[kGreedyBatch], r1[kGreedyBatch], r2[kGreedyBatch];
+    constexpr int kStep = kAccThreads * kGreedyBatch;   // vectors per batch of the CTA
     auto load = [&](uint4 (&d)[kGreedyBatch], int v0) {
 #pragma unroll
         for (int u = 0; u < kGreedyBatch; ++u) {
@@ -229,34 +252,48 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
             d[u] = vi < nvec ? ld_stream_u4(vp + vi) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
-    load(cur, tid);
-    for (int v0 = tid; v0 < nvec; v0 += kAccThreads * kGreedyBatch) {
-        if (v0 + kAccThreads * kGreedyBatch < nvec) load(nxt, v0 + kAccThreads * kGreedyBatch);
+    // each vector: its largest value first (packed maxima), compared with the
+    // running best; only a vector that beats it (rare past the start) is
+    // searched for the lowest index holding that value.  A thread meets its
+    // indices in increasing order, so an equal value met later never wins;
+    // the first ordered value (even -inf) is taken, and NaN never is.
+    auto reduce = [&](const uint4 (&d)[kGreedyBatch], int v0) {
 #pragma unroll
         for (int u = 0; u < kGreedyBatch; ++u) {
             const int vi = v0 + u * kAccThreads;
             if (vi < nvec) {
-                float f[PV];
-                Vec16<Tin>::unpack(cur[u], f);
+                const float vmax = Vec16<Tin>::max(d[u]);
+                if (vmax > cv || (vmax == cv && ci == INT_MAX)) {
+                    float f[PV];
+                    Vec16<Tin>::unpack(d[u], f);
+                    int e0 = PV - 1;
 #pragma unroll
-                for (int e = 0; e < PV; ++e) {
-                    const int i = a0 + vi * PV + e, k = e % kArgChains;
-                    if (argmax_better(f[e], i, cv[k], ci[k])) { cv[k] = f[e]; ci[k] = i; }
+                    for (int e = PV - 1; e >= 0; --e)
+                        if (f[e] == vmax) e0 = e;
+                    cv = vmax;
+                    ci = a0 + vi * PV + e0;
                 }
             }
         }
-#pragma unroll
-        for (int u = 0; u < kGreedyBatch; ++u) cur[u] = nxt[u];
+    };
+    load(r0, tid);
+    load(r1, tid + kStep);
+    for (int v0 = tid; v0 < nvec; v0 += 3 * kStep) {
+        load(r2, v0 + 2 * kStep);
+        reduce(r0, v0);
+        if (v0 + kStep >= nvec) break;
+        load(r0, v0 + 3 * kStep);
+        reduce(r1, v0 + kStep);
+        if (v0 + 2 * kStep >= nvec) break;
+        load(r1, v0 + 4 * kStep);
+        reduce(r2, v0 + 2 * kStep);
     }
     for (int i = a1 + tid; i < hi; i += kAccThreads) {
         const float x = Elem<Tin>::load(lg + i);
-        if (argmax_better(x, i, cv[0], ci[0])) { cv[0] = x; ci[0] = i; }
+        if (argmax_better(x, i, cv, ci)) { cv = x; ci = i; }
     }
-    float bv = cv[0];
-    int bi = ci[0];
-#pragma unroll
-    for (int k = 1; k < kArgChains; ++k)
-        if (argmax_better(cv[k], ci[k], bv, bi)) { bv = cv[k]; bi = ci[k]; }
+    float bv = cv;
+    int bi = ci;
     block_argmax(bv, bi);
     if (tid == 0) {
         p.pval[(long)row * p.n_chunks + c] = bv;
@@ -268,15 +305,25 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
     // lanes over chunks), then the first-mismatch scan of every sequence, over
     // windows of W rows that hold whole sequences
     __shared__ int am[kAccThreads];
-    const int R = p.B * p.T;
-    const int W = (kAccThreads / p.T) * p.T;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int kWarps = kAccThreads / 32;
     __shared__ float fin_v[kFinStaged];
     __shared__ int fin_i[kFinStaged];
+    // the window's proposals (chain: T-1 drafts per sequence; tree: T node
+    // tokens and T parents), loaded together with the partials
+    __shared__ int s_tok[kAccThreads], s_par[kAccThreads];
     for (int r0 = 0; r0 < R; r0 += W) {
         const int nr = min(R - r0, W);
         const int np = nr * p.n_chunks;   // the window's partials, contiguous in pval / pidx
+        if (r0 == 0) {
+            if (tid < n_pre) { s_tok[tid] = pre_tok; s_par[tid] = pre_par; }
+        } else {
+            const int b0w = r0 / p.T, nseq = nr / p.T;
+            for (int u = threadIdx.x; u < nseq * per_seq; u += kAccThreads) {
+                s_tok[u] = p.draft[(long)b0w * per_seq + u];
+                if (p.parents) s_par[u] = p.parents[(long)b0w * p.T + u];
+            }
+        }
         if (np <= kFinStaged) {
             // all of them in flight at once (the grids are sized so that this
             // is the usual case), then a thread per row over its chunks
@@ -334,7 +381,7 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
                 // draft tree: node j is accepted when its parent is and its token
                 // equals the target's pick after the parent; the deepest accepted
                 // node (lowest index among equals) ends the committed path
-                const int32_t *par = p.parents + (long)b * p.T, *tok = p.draft + (long)b * p.T;
+                const int *par = s_par + bl * p.T, *tok = s_tok + bl * p.T;
                 uint64_t acc = 1ull;  // bit j: node j accepted (the anchor always)
                 int depth[kMaxTreeT];
                 depth[0] = 0;
@@ -352,11 +399,11 @@ __global__ void __launch_bounds__(kAccThreads) greedy_kernel(const GreedyParams 
                 p.corr[b] = am[rb + best];
                 int32_t *path = p.path + (long)b * p.T;
                 for (int k = depth[best]; k < p.T; ++k) path[k] = -1;
-                for (int v = best; v != 0; v = par[v]) path[depth[v] - 1] = v;
+                for (int v = best; v != 0; v = par[v]) path[depth[v] - 1] = v;   // par[v] < v: ends at 0
             } else {
                 int n = p.T - 1;
                 for (int j = 0; j < p.T - 1; ++j) {
-                    if (p.draft[(long)b * (p.T - 1) + j] != am[rb + j]) { n = j; break; }
+                    if (s_tok[bl * (p.T - 1) + j] != am[rb + j]) { n = j; break; }
                 }
                 p.n_acc[b] = n;
                 p.corr[b] = am[rb + n];

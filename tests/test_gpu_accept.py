@@ -76,6 +76,34 @@ def test_greedy_ties_lowest_index(S):
     assert c.tolist() == oc.tolist() == [17, 9999]
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_greedy_vector_max_edges(S, dtype):
+    """The stream takes each 16-byte vector's maximum first and searches a
+    vector for its lowest index only when that maximum is new: rows that are
+    all -inf, ties inside one vector and across vectors, a maximum in the
+    unaligned head or tail, and rising rows where every vector is new."""
+    V = 4_099                                      # odd: rows start unaligned
+    T = 8
+    lg = torch.randn(1, T, V).to(dtype)
+    lg[0, 0] = -float("inf")                       # all -inf: index 0
+    lg[0, 1, [1026, 1030, 3001]] = 9.0             # tie inside one vector, and a later one
+    lg[0, 2] = torch.arange(V, dtype=torch.float32).to(dtype) / V   # rising (bf16 ties at the top)
+    lg[0, 3, 0] = 20.0                             # in the unaligned head
+    lg[0, 4, V - 1] = 20.0                         # in the tail
+    lg[0, 5] = -float("inf")
+    lg[0, 5, [7, 4000]] = -1.0                     # only two ordered values above -inf
+    lg[0, 6] = 0.0                                 # all equal: index 0
+    draft = torch.zeros((1, T - 1), dtype=torch.int32)
+    on, oc, am = oracle.accept_greedy(draft, lg, return_argmax=True)
+    assert am[0].tolist()[:7] == [0, 1026, int(am[0, 2]), 0, V - 1, 7, 0]
+    for j in range(T):                             # each row as the rejected one
+        d = am[0:1, :T - 1].astype(np.int32).copy()
+        if j < T - 1:
+            d[0, j] = (am[0, j] + 1) % V
+        n, c = run_greedy(S, torch.from_numpy(d), lg)
+        assert int(n[0]) == j and int(c[0]) == int(am[0, j]), (j, n, c, am[0, j])
+
+
 def test_greedy_all_accepted_and_worked_cycle(S):
     import json, os
     g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_cycle.json")))
