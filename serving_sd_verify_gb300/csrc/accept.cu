@@ -374,39 +374,85 @@ __global__ void __launch_bounds__(kAccThreads, 3) greedy_kernel(const GreedyPara
             }
         }
         __syncthreads();
+        // a warp per sequence
         const int b0 = r0 / p.T, nbw = min(p.B - b0, W / p.T);
-        for (int bl = threadIdx.x; bl < nbw; bl += kAccThreads) {
+        for (int bl = warp; bl < nbw; bl += kWarps) {
             const int b = b0 + bl, rb = bl * p.T;
             if (p.parents) {
                 // draft tree: node j is accepted when its parent is and its token
                 // equals the target's pick after the parent; the deepest accepted
-                // node (lowest index among equals) ends the committed path
+                // node (lowest index among equals) ends the committed path.  Lane
+                // l holds nodes l and l + 32.  Pointer jumping over the parent
+                // links: each node carries the segment of its root path from
+                // itself up to (not including) node A -- all matched, its length,
+                // its node set -- and joins A's segment to its own until A is the
+                // root (six rounds cover 63 links)
                 const int *par = s_par + bl * p.T, *tok = s_tok + bl * p.T;
-                uint64_t acc = 1ull;  // bit j: node j accepted (the anchor always)
-                int depth[kMaxTreeT];
-                depth[0] = 0;
-                int best = 0;
-                for (int j = 1; j < p.T; ++j) {
-                    const int pj = par[j];
-                    if (pj < 0 || pj >= j) { set_fault(p.fault, FAULT_BAD_TREE); depth[j] = 0; continue; }
-                    depth[j] = depth[pj] + 1;
-                    if (((acc >> pj) & 1ull) && tok[j] == am[rb + pj]) {
-                        acc |= 1ull << j;
-                        if (depth[j] > depth[best]) best = j;
+                int A[2], okd[2];        // okd: bit 16 all matched, low bits the length
+                uint64_t M[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = lane + 32 * h;
+                    A[h] = 0; okd[h] = 1 << 16; M[h] = 0ull;   // the root (and nodes past T)
+                    if (j >= 1 && j < p.T) {
+                        const int pj = par[j];
+                        M[h] = 1ull << j;
+                        if (pj < 0 || pj >= j) { set_fault(p.fault, FAULT_BAD_TREE); okd[h] = 0; }
+                        else { A[h] = pj; okd[h] = ((tok[j] == am[rb + pj]) ? 1 << 16 : 0) | 1; }
                     }
                 }
-                p.n_acc[b] = depth[best];
-                p.corr[b] = am[rb + best];
-                int32_t *path = p.path + (long)b * p.T;
-                for (int k = depth[best]; k < p.T; ++k) path[k] = -1;
-                for (int v = best; v != 0; v = par[v]) path[depth[v] - 1] = v;   // par[v] < v: ends at 0
-            } else {
-                int n = p.T - 1;
-                for (int j = 0; j < p.T - 1; ++j) {
-                    if (s_tok[bl * (p.T - 1) + j] != am[rb + j]) { n = j; break; }
+#pragma unroll 1
+                for (int round = 0; round < 6; ++round) {
+                    int nA[2], nokd[2];
+                    uint64_t nM[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int src = A[h] & 31;
+                        const bool hi = A[h] >= 32;
+                        const int a0 = __shfl_sync(0xffffffffu, A[0], src), a1 = __shfl_sync(0xffffffffu, A[1], src);
+                        const int o0 = __shfl_sync(0xffffffffu, okd[0], src), o1 = __shfl_sync(0xffffffffu, okd[1], src);
+                        const uint64_t m0 = __shfl_sync(0xffffffffu, M[0], src), m1 = __shfl_sync(0xffffffffu, M[1], src);
+                        const int oa = hi ? o1 : o0;
+                        nA[h] = hi ? a1 : a0;
+                        nokd[h] = (okd[h] & oa & (1 << 16)) | ((okd[h] & 0xffff) + (oa & 0xffff));
+                        nM[h] = M[h] | (hi ? m1 : m0);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) { A[h] = nA[h]; okd[h] = nokd[h]; M[h] = nM[h]; }
                 }
-                p.n_acc[b] = n;
-                p.corr[b] = am[rb + n];
+                // deepest accepted node, lowest index among equals
+                int key = -1;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = lane + 32 * h;
+                    if (j < p.T && (okd[h] >> 16)) key = max(key, ((okd[h] & 0xffff) << 7) | (127 - j));
+                }
+                key = __reduce_max_sync(0xffffffffu, key);
+                const int best = 127 - (key & 127), dbest = key >> 7;
+                const uint64_t mb0 = __shfl_sync(0xffffffffu, M[0], best & 31);
+                const uint64_t mb1 = __shfl_sync(0xffffffffu, M[1], best & 31);
+                const uint64_t mbest = best >= 32 ? mb1 : mb0;   // the nodes of the committed path
+                if (lane == 0) {
+                    p.n_acc[b] = dbest;
+                    p.corr[b] = am[rb + best];
+                }
+                int32_t *path = p.path + (long)b * p.T;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = lane + 32 * h;
+                    if (j < p.T && j >= dbest) path[j] = -1;
+                    if (j >= 1 && j < p.T && ((mbest >> j) & 1ull)) path[(okd[h] & 0xffff) - 1] = j;
+                }
+            } else {
+                // chain: lane j tests proposal j (T - 1 <= 15); the first
+                // mismatch is the lowest set bit of the warp's ballot
+                const bool miss = lane < p.T - 1 && s_tok[bl * (p.T - 1) + lane] != am[rb + lane];
+                const unsigned int m = __ballot_sync(0xffffffffu, miss);
+                if (lane == 0) {
+                    const int n = m ? __ffs(m) - 1 : p.T - 1;
+                    p.n_acc[b] = n;
+                    p.corr[b] = am[rb + n];
+                }
             }
         }
         __syncthreads();
