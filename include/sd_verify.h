@@ -201,7 +201,8 @@ size_t sd_accept_greedy_workspace_size(int B, int T, int V, sd_dtype dtype);
  *   temperature  > 0 (temperature 0 is sd_accept_greedy)
  *   n_accepted, next_id  device int32 [B]
  *   workspace: zero-filled before the first call on it; each completed call
- *   leaves its counters zero again.
+ *   leaves its counters zero again (a call whose bounded wait gave up
+ *   included: the fault word says so).
  * ------------------------------------------------------------------------ */
 sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs,
                            const void *target_logits, int B, int T, int V, sd_dtype dtype,
@@ -445,6 +446,22 @@ int sd_last_attention_path(int *n_splits);
  * a separate merge kernel followed.  No counterpart on the pages: a count for
  * measurement. */
 int sd_last_attention_launches(void);
+
+/* Sampled-rule kernel selection, process-wide, for tests and measurement:
+ * 0 = automatic (the one-launch form where its grid fits on the device at
+ * once: 2 CTAs per SM, B*T and B at most that many, chunks of the deciding
+ * row within 4 vectors per thread, logits 16-byte aligned; else two kernels),
+ * 1 = force the two-kernel
+ * form, 2 = require the one-launch form (calls it cannot serve return
+ * SD_ERR_UNSUPPORTED).  Other values select 0.  Returns the previous setting.
+ * Both forms compute the same rule; their float-float sums group terms
+ * differently, so a draw may differ where it sits within rounding of a
+ * boundary. */
+int sd_set_sample_path(int path);
+
+/* Which form the last sd_accept_sample on this thread launched: 1 two
+ * kernels, 2 one cooperative launch, 0 none. */
+int sd_last_sample_path(void);
 
 /* Projector kernel selection, process-wide, for tests and measurement:
  * 0 = automatic (above), 1 = CUDA cores for every N, 2 = tensor cores for

@@ -20,8 +20,9 @@
 // ticket returns it to zero, so a zero-filled workspace stays reusable.  No
 // CTA ever waits for another.  Sums over a whole vocabulary are carried as
 // float-float values (two fp32 words), not in the slow fp64 pipe.
-#include "common.cuh"
+#include "tcgen05.cuh"
 
+#include <atomic>
 #include <float.h>
 #include <limits.h>
 #include <math.h>
@@ -34,6 +35,8 @@ constexpr int kAccThreads = 256;
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
 constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
 constexpr int kFinStaged = 1024;  // chunk partials the greedy finisher stages in shared memory at once
+constexpr int kFStages = 3;          // shared-memory stages of the one-launch sampled stream
+constexpr int kFStageBytes = 32768;  // bytes per stage
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10
@@ -730,6 +733,93 @@ __device__ __forceinline__ void load_q(const float *qn, const ChunkRegs<Tin, NV>
     }
 }
 
+// The draw inside chunk [clo, chi) of the deciding row, whose elements (and q
+// where the residual needs it) the CTA holds in registers as ChunkRegs: vector
+// v of thread t holds 8 (bf16) or 4 (fp32) consecutive elements, vector slots
+// in element order v-major.  The weights are recomputed with the same
+// arithmetic as the chunk sums, and for each vector slot an exclusive fp32 scan
+// of the threads' vector sums from the chunk's start (the chunk is a small part
+// of S, so fp32 holds these offsets to far better than 1e-6 S) lets the thread
+// whose vector holds the crossing walk it.  The draw is the smallest index
+// whose computed inclusive prefix exceeds xl (x minus the chunks before this
+// one: the inverse CDF), reduced with a warp minimum before the shared atomic;
+// if rounding leaves no such index, the last positive weight.  Every thread of
+// the CTA calls it; the id is returned in every thread.
+template <typename Tin, int NV>
+__device__ int search_chunk(const ChunkRegs<Tin, NV> &sr, const float (&qs)[NV][Elem<Tin>::kPerVec],
+                            const Tin *lg, const float *qn, int clo, int chi, float it, float M, float Z,
+                            bool res, float xl) {
+    constexpr int PV = Elem<Tin>::kPerVec;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    __shared__ float wtot[kAccThreads / 32];
+    __shared__ int s_id, s_last;
+    if (threadIdx.x == 0) { s_id = INT_MAX; s_last = -1; }
+    // the unaligned head [clo, a0) (fewer than 8 elements) comes first in element order
+    float head = 0.f;
+    for (int i = clo; i < sr.a0; ++i) {
+        const float wi = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, res ? __ldg(qn + i) : 0.f, res);
+        if (wi > 0.f) { if (threadIdx.x == 0) atomicMax(&s_last, i); }
+        if (threadIdx.x == 0 && head + wi > xl) atomicMin(&s_id, i);
+        head += wi;
+    }
+    float carry = head;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float wv[PV];
+        float sv = 0.f;
+#pragma unroll
+        for (int e = 0; e < PV; ++e) {
+            wv[e] = sr.valid(v) ? residual_or_p(sr.x[v][e], it, M, Z, qs[v][e], res) : 0.f;
+            sv += wv[e];
+        }
+        float incl = sv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __syncthreads();   // wtot of the previous slot is read
+        if (lane == 31) wtot[wid] = incl;
+        __syncthreads();
+        float acc = carry + (incl - sv);
+        float slot_tot = 0.f;
+        for (int k = 0; k < kAccThreads / 32; ++k) {
+            if (k < wid) acc += wtot[k];
+            slot_tot += wtot[k];
+        }
+        int cand = INT_MAX, last_here = -1;
+        if (sr.valid(v)) {
+#pragma unroll
+            for (int e = 0; e < PV; ++e) {
+                if (wv[e] > 0.f) last_here = sr.index(v, e);
+                acc += wv[e];
+                if (acc > xl && cand == INT_MAX) cand = sr.index(v, e);
+            }
+        }
+        cand = __reduce_min_sync(0xffffffffu, cand);
+        last_here = __reduce_max_sync(0xffffffffu, last_here);
+        if (lane == 0) {
+            if (cand != INT_MAX) atomicMin(&s_id, cand);
+            if (last_here >= 0) atomicMax(&s_last, last_here);
+        }
+        carry += slot_tot;
+    }
+    // the unaligned tail [a1, chi) last
+    if (threadIdx.x == 0) {
+        float acc = carry;
+        for (int i = sr.a1; i < chi; ++i) {
+            const float wi = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, res ? __ldg(qn + i) : 0.f, res);
+            if (wi > 0.f) atomicMax(&s_last, i);
+            acc += wi;
+            if (acc > xl) atomicMin(&s_id, i);
+        }
+    }
+    __syncthreads();
+    int id = s_id;
+    if (id == INT_MAX) id = s_last >= 0 ? s_last : clo;  // rounding: last positive weight
+    return id;
+}
+
 template <typename Tin, int NV>
 __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SampleParams p) {
     grid_dependency_wait();
@@ -871,15 +961,6 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
         scan_select(false);
     }
 
-    // inside the chunk: its elements in registers as in the first phase
-    // (vector v of thread t holds 8 (bf16) or 4 (fp32) consecutive elements,
-    // vector slots in element order v-major), the weights recomputed with the
-    // same arithmetic, and for each vector slot an exclusive fp32 scan of the
-    // threads' vector sums from the chunk's start (the chunk is a small part of
-    // S, so fp32 holds these offsets to far better than 1e-6 S); the thread
-    // whose vector holds the crossing walks it.  The draw is the smallest index
-    // whose computed inclusive prefix exceeds x (the inverse CDF), reduced
-    // with a warp minimum before the shared atomic
     const int sel_chunk = s_found;
     const bool res = s_res != 0;
     const float xl = ff_add(s_x, FF{-s_base.hi, -s_base.lo}).hi;   // x - base, to fp32
@@ -888,75 +969,469 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
     sr.load(lg, clo, chi, -INFINITY);
     float qs[NV][PV];
     load_q(qn, sr, res, qs);
-    __shared__ float wtot[kAccThreads / 32];
-    __shared__ int s_id, s_last;
-    if (threadIdx.x == 0) { s_id = INT_MAX; s_last = -1; }
-    // the unaligned head [clo, a0) (fewer than 8 elements) comes first in element order
-    float head = 0.f;
-    for (int i = clo; i < sr.a0; ++i) {
-        const float wi = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, res ? __ldg(qn + i) : 0.f, res);
-        if (wi > 0.f) { if (threadIdx.x == 0) atomicMax(&s_last, i); }
-        if (threadIdx.x == 0 && head + wi > xl) atomicMin(&s_id, i);
-        head += wi;
-    }
-    float carry = head;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        float wv[PV];
-        float sv = 0.f;
-#pragma unroll
-        for (int e = 0; e < PV; ++e) {
-            wv[e] = sr.valid(v) ? residual_or_p(sr.x[v][e], it, M, Z, qs[v][e], res) : 0.f;
-            sv += wv[e];
-        }
-        float incl = sv;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        __syncthreads();   // wtot of the previous slot is read
-        if (lane == 31) wtot[wid] = incl;
-        __syncthreads();
-        float acc = carry + (incl - sv);
-        float slot_tot = 0.f;
-        for (int k = 0; k < kAccThreads / 32; ++k) {
-            if (k < wid) acc += wtot[k];
-            slot_tot += wtot[k];
-        }
-        int cand = INT_MAX, last_here = -1;
-        if (sr.valid(v)) {
-#pragma unroll
-            for (int e = 0; e < PV; ++e) {
-                if (wv[e] > 0.f) last_here = sr.index(v, e);
-                acc += wv[e];
-                if (acc > xl && cand == INT_MAX) cand = sr.index(v, e);
-            }
-        }
-        cand = __reduce_min_sync(0xffffffffu, cand);
-        last_here = __reduce_max_sync(0xffffffffu, last_here);
-        if (lane == 0) {
-            if (cand != INT_MAX) atomicMin(&s_id, cand);
-            if (last_here >= 0) atomicMax(&s_last, last_here);
-        }
-        carry += slot_tot;
-    }
-    // the unaligned tail [a1, chi) last
+    const int id = search_chunk<Tin, NV>(sr, qs, lg, qn, clo, chi, it, M, Z, res, xl);
+    if (threadIdx.x == 0) p.next_id[b] = id;
+}
+
+// ----------------------------------------------------------------------------
+// sampled acceptance in one cooperative launch (every CTA resident at once):
+//   1. the B*T*V logits as equal segments, one per CTA, each reduced to the
+//      (max, sum of exp) of its pieces of at most two rows, online: a vector
+//      whose maximum is new rescales the running sum first; the records of
+//      the pieces (and of the proposals that fall in the segment) published;
+//      then a grid barrier;
+//   2. the CTAs of sequence b (n_fchunks of them) each read the partials
+//      of its T rows and combine them into (M, Z) -- all of them the same
+//      way, so with the same result -- test the proposals and find the
+//      deciding row n;
+//   3. each takes one chunk of row n into registers and publishes the chunk's
+//      sums of the residual max(p - q, 0) and of p;
+//   4. after a barrier of the sequence's CTAs, each scans the chunk sums; the
+//      CTA whose chunk holds x = u' * S draws from its registers.
+// The two waits are barriers (below), bounded in time; a CTA only ever waits
+// for CTAs that are resident and arrive before they wait themselves.
+// ----------------------------------------------------------------------------
+
+// A barrier of `n` CTAs on two counters: thread 0 arrives (a release
+// reduction, after the CTA's writes) and waits, bounded in time, for the count
+// to reach n (acquire loads); each CTA departs once, at its end, and the n-th
+// departure returns both counters to zero -- every CTA has stopped reading
+// them by then, whether or not its wait gave up.  The whole CTA calls the
+// wait; false (and the fault bit) if it gave up.
+__device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int n, unsigned int *fault) {
+    __shared__ int s_ok;
+    __syncthreads();
     if (threadIdx.x == 0) {
-        float acc = carry;
-        for (int i = sr.a1; i < chi; ++i) {
-            const float wi = residual_or_p(Elem<Tin>::load(lg + i), it, M, Z, res ? __ldg(qn + i) : 0.f, res);
-            if (wi > 0.f) atomicMax(&s_last, i);
-            acc += wi;
-            if (acc > xl) atomicMin(&s_id, i);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+        const unsigned long long t0 = global_timer();
+        int ok = 1;
+        for (uint32_t i = 0;; ++i) {
+            unsigned int v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+            if (v >= n) break;
+            if ((i & 15u) == 15u && global_timer() - t0 > kWaitLimitNs) { ok = 0; break; }
+            __nanosleep(20);
+        }
+        if (!ok) set_fault(fault, FAULT_WAIT_TIMEOUT);
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+__device__ __forceinline__ void barrier_depart(unsigned int *arrive, unsigned int *depart, unsigned int n) {
+    if (threadIdx.x == 0) {
+        if (atomicAdd(depart, 1u) == n - 1) { *arrive = 0u; *depart = 0u; }
+    }
+}
+
+// two block-wide maxima at once; results valid in every thread
+__device__ __forceinline__ void block_max2(float &a, float &b) {
+    __shared__ float sh[2][kAccThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    __syncthreads();
+    if (lane == 0) { sh[0][warp] = a; sh[1][warp] = b; }
+    __syncthreads();
+    a = sh[0][0]; b = sh[1][0];
+    for (int w = 1; w < kAccThreads / 32; ++w) { a = fmaxf(a, sh[0][w]); b = fmaxf(b, sh[1][w]); }
+}
+// two block-wide float-float sums at once; results valid in every thread
+__device__ __forceinline__ void ff_block_sum2(FF &a, FF &b) {
+    __shared__ FF sh[2][kAccThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    a = ff_warp_sum(a);
+    b = ff_warp_sum(b);
+    __syncthreads();
+    if (lane == 0) { sh[0][warp] = a; sh[1][warp] = b; }
+    __syncthreads();
+    a = sh[0][0]; b = sh[1][0];
+    for (int w = 1; w < kAccThreads / 32; ++w) { a = ff_add(a, sh[0][w]); b = ff_add(b, sh[1][w]); }
+}
+// block-wide inclusive float-float scan of one value per thread (thread order);
+// the total is returned in every thread
+__device__ __forceinline__ FF ff_block_scan(FF v, FF &total) {
+    __shared__ FF wsum[kAccThreads / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    FF incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const FF y = ff_shfl_up(incl, o);
+        if (lane >= o) incl = ff_add(incl, y);
+    }
+    __syncthreads();
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    FF pre = FF{0.f, 0.f}, tot = FF{0.f, 0.f};
+    for (int w = 0; w < kAccThreads / 32; ++w) {
+        if (w < wid) pre = ff_add(pre, wsum[w]);
+        tot = ff_add(tot, wsum[w]);
+    }
+    total = tot;
+    return ff_add(pre, incl);
+}
+
+// e^(y - m) for y <= m in the one-launch stream: 2^((y - m) log2 e) from the
+// ex2.approx unit (relative error about 2^-22), y - m rounded once
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float exp_rel(float y, float m) { return ex2((y - m) * kLog2e); }
+
+// online (max, sum of exp) of one row's piece: y = l / tau of a new element
+__device__ __forceinline__ void online_add(float &m, FF &z, float y) {
+    if (y > m) {
+        if (m != -INFINITY) z = ff_scale(z, exp_rel(m, y));
+        m = y;
+    }
+    if (m != -INFINITY) z = ff_add(z, exp_rel(y, m));
+}
+
+template <typename Tin, int NV>
+__global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_kernel(const SampleParams p) {
+    grid_dependency_wait();
+    constexpr int PV = Elem<Tin>::kPerVec;
+    constexpr int kWarps = kAccThreads / 32;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const float it = p.inv_tau;
+    const unsigned int C = gridDim.x;
+    const int R = p.B * p.T;
+    // the proposals of this CTA's sequence and the uniforms of its rows (the
+    // tests' u, the draw's u'), ready for steps 2 and 4
+    __shared__ int s_draft[kMaxT];
+    __shared__ float s_u[2][kMaxT];
+    {
+        const int bq = blockIdx.x / p.n_fchunks;
+        if (bq < p.B) {
+            if (tid < p.T - 1) s_draft[tid] = p.draft[(long)bq * (p.T - 1) + tid];
+            if (tid >= 32 && tid < 32 + 2 * p.T) {
+                const int j = (tid - 32) % p.T, st = (tid - 32) / p.T;
+                s_u[st][j] = philox_uniform(p.seed, (uint32_t)j, (uint32_t)bq, (uint32_t)st, p.offset);
+            }
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int id = s_id;
-        if (id == INT_MAX) id = s_last >= 0 ? s_last : clo;  // rounding: last positive weight
-        p.next_id[b] = id;
+
+    // ---- 1. segment blockIdx.x: [f0, f0 + len) of the flattened logits
+    if ((int)blockIdx.x < p.n_segs) {
+        const long N = (long)R * p.V;
+        const long f0 = (long)blockIdx.x * p.seg;
+        const int len = (int)min((long)p.seg, N - f0);
+        const int rA = (int)(f0 / p.V);
+        const int offA = (int)(f0 - (long)rA * p.V);   // row index of the first element
+        const int jb = p.V - offA;                     // where row rA + 1 starts (>= len: not here)
+        // threads 0 and 1: the proposal of row rA / rA + 1, if it falls in this
+        // segment -- its logit and q, loaded now, written with the partials
+        float2 prop = make_float2(0.f, 0.f);
+        int prop_row = -1;
+        if (tid < 2) {
+            const int r = rA + tid;
+            const int plo = tid == 0 ? offA : 0, phi = tid == 0 ? offA + min(len, jb) : len - jb;
+            if (r < R && plo < phi && (r % p.T) < p.T - 1) {
+                const int d = p.draft[(long)(r / p.T) * (p.T - 1) + r % p.T];
+                if (d >= plo && d < phi) {
+                    prop_row = r;
+                    prop = make_float2(Elem<Tin>::load(static_cast<const Tin *>(p.logits) + (long)r * p.V + d),
+                                       __ldg(p.q + (long)r * p.V + d));
+                }
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY;          // per thread, rows rA and rA + 1
+        FF z0 = FF{0.f, 0.f}, z1 = FF{0.f, 0.f};
+        // a vector: its maximum first (exact: it is one of its elements), the
+        // running sum rescaled when that is new, then the vector's sum of exp
+        auto vec = [&](const uint4 &d, float &m, FF &z) {
+            const float vm = Vec16<Tin>::max(d) * it;
+            if (vm > m) {
+                if (m != -INFINITY) z = ff_scale(z, exp_rel(m, vm));
+                m = vm;
+            }
+            if (m != -INFINITY) {
+                float f[PV];
+                Vec16<Tin>::unpack(d, f);
+                float w[PV];
+#pragma unroll
+                for (int e = 0; e < PV; ++e) w[e] = exp_rel(f[e] * it, m);
+#pragma unroll
+                for (int h = PV / 2; h > 0; h >>= 1)
+#pragma unroll
+                    for (int e = 0; e < h; ++e) w[e] += w[e + h];
+                z = ff_add(z, w[0]);
+            }
+        };
+        // two vectors of one row: one maximum, one rescale, 2 PV independent exps
+        auto vec2 = [&](const uint4 &d0, const uint4 &d1, float &m, FF &z) {
+            const float vm = fmaxf(Vec16<Tin>::max(d0), Vec16<Tin>::max(d1)) * it;
+            if (vm > m) {
+                if (m != -INFINITY) z = ff_scale(z, exp_rel(m, vm));
+                m = vm;
+            }
+            if (m != -INFINITY) {
+                float f0[PV], f1[PV];
+                Vec16<Tin>::unpack(d0, f0);
+                Vec16<Tin>::unpack(d1, f1);
+                float w[PV];
+#pragma unroll
+                for (int e = 0; e < PV; ++e) w[e] = exp_rel(f0[e] * it, m) + exp_rel(f1[e] * it, m);
+#pragma unroll
+                for (int h = PV / 2; h > 0; h >>= 1)
+#pragma unroll
+                    for (int e = 0; e < h; ++e) w[e] += w[e + h];
+                z = ff_add(z, w[0]);
+            }
+        };
+        // any one vector: its row's pair, or element by element across the row end
+        auto one = [&](const uint4 &d, int j) {
+            if (j + PV <= jb || j >= jb) {
+                const bool inB = j >= jb;
+                float m = inB ? m1 : m0;
+                FF z = inB ? z1 : z0;
+                vec(d, m, z);
+                if (inB) { m1 = m; z1 = z; } else { m0 = m; z0 = z; }
+            } else {
+                float f[PV];
+                Vec16<Tin>::unpack(d, f);
+#pragma unroll 1
+                for (int e = 0; e < PV; ++e) {
+                    const bool inB = j + e >= jb;
+                    float m = inB ? m1 : m0;
+                    FF z = inB ? z1 : z0;
+                    online_add(m, z, f[e] * it);
+                    if (inB) { m1 = m; z1 = z; } else { m0 = m; z0 = z; }
+                }
+            }
+        };
+        // the segment's bytes through a ring of kFStages shared-memory stages
+        // that the copy engine fills (a bulk copy per stage, completing on the
+        // stage's mbarrier): thread 0 keeps up to kFStages copies in flight, the
+        // CTA reads each stage once it has landed.  Segments start on 16-byte
+        // boundaries (the logits are 16-byte aligned, seg a multiple of 8); the
+        // last one's ragged end (under 16 bytes) is read directly.
+        const char *gsrc = reinterpret_cast<const char *>(static_cast<const Tin *>(p.logits) + f0);
+        const int bulk = (len * (int)sizeof(Tin)) & ~15;
+        const int n_st = (bulk + kFStageBytes - 1) / kFStageBytes;
+        extern __shared__ __align__(128) uint8_t fsm[];
+        __shared__ __align__(8) uint64_t fbar[kFStages];
+        if (tid == 0) {
+            for (int s = 0; s < kFStages; ++s) mbar_init(smem_u32(&fbar[s]), 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        auto issue = [&](int t) {
+            const int s = t % kFStages, off = t * kFStageBytes, nb = min(kFStageBytes, bulk - off);
+            mbar_arrive_expect_tx(smem_u32(&fbar[s]), (uint32_t)nb);
+            bulk_load_g2s(smem_u32(fsm + s * kFStageBytes), gsrc + off, (uint32_t)nb, smem_u32(&fbar[s]));
+        };
+        if (tid == 0)
+            for (int t = 0; t < min(n_st, kFStages); ++t) issue(t);
+        for (int t = 0; t < n_st; ++t) {
+            const int s = t % kFStages;
+            mbar_wait(smem_u32(&fbar[s]), (uint32_t)((t / kFStages) & 1), nullptr, p.fault);
+            const uint4 *sv = reinterpret_cast<const uint4 *>(fsm + s * kFStageBytes);
+            const int nvt = min(kFStageBytes, bulk - t * kFStageBytes) / 16;
+            const int j0 = t * (kFStageBytes / (int)sizeof(Tin));
+            // vectors i and i + kAccThreads of the stage together
+            for (int i = tid; i < nvt; i += 2 * kAccThreads) {
+                const int i2 = i + kAccThreads;
+                const int j = j0 + i * PV, j2 = j0 + i2 * PV;
+                const uint4 d0 = sv[i];
+                if (i2 < nvt && (j2 + PV <= jb || j >= jb)) {   // both in one row
+                    const uint4 d1 = sv[i2];
+                    const bool inB = j >= jb;
+                    float m = inB ? m1 : m0;
+                    FF z = inB ? z1 : z0;
+                    vec2(d0, d1, m, z);
+                    if (inB) { m1 = m; z1 = z; } else { m0 = m; z0 = z; }
+                } else {
+                    one(d0, j);
+                    if (i2 < nvt) one(sv[i2], j2);
+                }
+            }
+            __syncthreads();                               // stage s is read
+            if (tid == 0 && t + kFStages < n_st) {
+                fence_proxy_async_smem();
+                issue(t + kFStages);
+            }
+        }
+        const Tin *lg = static_cast<const Tin *>(p.logits) + f0;
+        for (int j = bulk / (int)sizeof(Tin) + tid; j < len; j += kAccThreads) {
+            const float y = Elem<Tin>::load(lg + j) * it;
+            if (j < jb) online_add(m0, z0, y); else online_add(m1, z1, y);
+        }
+        float M0 = m0, M1 = m1;
+        block_max2(M0, M1);
+        FF t0 = m0 == -INFINITY ? FF{0.f, 0.f} : ff_scale(z0, expf(m0 - M0));
+        FF t1 = m1 == -INFINITY ? FF{0.f, 0.f} : ff_scale(z1, expf(m1 - M1));
+        ff_block_sum2(t0, t1);
+        const float2 prop1 = make_float2(__shfl_sync(0xffffffffu, prop.x, 1), __shfl_sync(0xffffffffu, prop.y, 1));
+        const int prop_row1 = __shfl_sync(0xffffffffu, prop_row, 1);
+        if (tid == 0) {
+            p.pp[2L * blockIdx.x] = make_float4(M0, t0.hi, t0.lo, 0.f);
+            p.pp[2L * blockIdx.x + 1] = make_float4(M1, t1.hi, t1.lo, 0.f);
+            if (prop_row >= 0) p.row_stats[prop_row] = prop;
+            if (prop_row1 >= 0) p.row_stats[prop_row1] = prop1;
+        }
     }
+
+    // every segment's partials are in (a grid barrier)
+    barrier_arrive_wait(p.counters + 1, C, p.fault);
+    auto depart = [&]() { barrier_depart(p.counters + 1, p.counters + 2, C); };
+    const int b = blockIdx.x / p.n_fchunks, k = blockIdx.x % p.n_fchunks;
+    if (b >= p.B) {
+        depart();
+        return;
+    }
+
+    // ---- sequence b: every row's (M, Z), a warp per row (rows w and w + 8)
+    // and lanes over the segments that cover it; the proposal tests; the
+    // deciding row n
+    __shared__ float s_M[kMaxT];
+    __shared__ FF s_Z[kMaxT];
+    __shared__ int s_acc[kMaxT];
+    auto seg_lo = [&](int r) { return (int)((long)r * p.V / p.seg); };
+    auto seg_hi = [&](int r) { return (int)(((long)(r + 1) * p.V - 1) / p.seg); };
+    // row r is the first row of every segment that covers it but the first,
+    // when that one starts inside row r - 1
+    auto slot_of = [&](int r, int i) { return 2 * i + (((long)i * p.seg < (long)r * p.V) ? 1 : 0); };
+    static_assert(kMaxT <= 2 * kWarps, "two rows per warp");
+    // ---- 2. the partials of rows wid and wid + 8 (lanes over the segments
+    // that cover a row, the first 32 kept in registers) and lane 0 the
+    // proposal's (logit, q), all loads in flight together
+    float pm[2], pzh[2], pzl[2], mloc[2];
+    float2 lq[2];
+    int ni[2], i0[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = wid + kWarps * h, r = b * p.T + j;
+        pm[h] = -INFINITY; pzh[h] = 0.f; pzl[h] = 0.f; mloc[h] = -INFINITY;
+        lq[h] = make_float2(0.f, 0.f);
+        ni[h] = 0;
+        i0[h] = 0;
+        if (j < p.T) {
+            i0[h] = seg_lo(r);
+            ni[h] = seg_hi(r) - i0[h] + 1;
+            float mx = -INFINITY;
+            for (int t = lane; t < ni[h]; t += 32) {
+                const float4 q4 = __ldcg(p.pp + slot_of(r, i0[h] + t));
+                mx = fmaxf(mx, q4.x);
+                if (t == lane) { pm[h] = q4.x; pzh[h] = q4.y; pzl[h] = q4.z; }
+            }
+            mloc[h] = mx;
+            if (lane == 0 && j < p.T - 1) lq[h] = __ldcg(p.row_stats + r);
+        }
+    }
+    // ---- 3. (M, Z) of each row, the proposal test
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = wid + kWarps * h, r = b * p.T + j;
+        if (j >= p.T) continue;                            // warp-uniform
+        float mr = mloc[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+        FF zr = pm[h] == -INFINITY ? FF{0.f, 0.f} : ff_scale(FF{pzh[h], pzl[h]}, expf(pm[h] - mr));
+        for (int t = lane + 32; t < ni[h]; t += 32) {   // rows over more than 32 segments
+            const float4 q4 = __ldcg(p.pp + slot_of(r, i0[h] + t));
+            if (q4.x != -INFINITY) zr = ff_add(zr, ff_scale(FF{q4.y, q4.z}, expf(q4.x - mr)));
+        }
+        zr = ff_warp_sum(zr);
+        if (lane == 0) {
+            int accept = 0;
+            if (j < p.T - 1) {
+                const int d = s_draft[j];
+                if (d >= 0 && d < p.V) {
+                    // accept iff u * q(d) < p(d) = exp(l(d) / tau - M) / Z, as
+                    // u * q(d) * Z < exp(...) with the product exact
+                    const float ed = expf(lq[h].x * it - mr);
+                    accept = ff_lt(ff_mul(ff_prod(s_u[0][j], lq[h].y), zr), FF{ed, 0.f}) ? 1 : 0;
+                } else {
+                    set_fault(p.fault, FAULT_BAD_DRAFT_ID);
+                }
+            }
+            s_M[j] = mr;
+            s_Z[j] = zr;
+            s_acc[j] = accept;
+        }
+    }
+    __syncthreads();
+    const unsigned int rej = __ballot_sync(0xffffffffu, lane < p.T - 1 && !s_acc[lane]);
+    const int n = rej ? __ffs(rej) - 1 : p.T - 1;      // the first rejection, else T - 1
+    const float M = s_M[n], Z = s_Z[n].hi + s_Z[n].lo;
+    const bool rejected = n < p.T - 1;
+    if (k == 0 && tid == 0) p.n_acc[b] = n;
+
+    // ---- 3. chunk k of row n in registers; its sums of the residual and of p
+    const long row = (long)b * p.T + n;
+    const Tin *lg = static_cast<const Tin *>(p.logits) + row * p.V;
+    const float *qn = p.q + row * p.V;
+    const int clo = k * p.fchunk, chi = min(p.V, clo + p.fchunk);
+    ChunkRegs<Tin, NV> sr;
+    sr.load(lg, clo, chi, -INFINITY);
+    float qs[NV][PV];
+    load_q(qn, sr, rejected, qs);
+    const float u2 = s_u[1][n];   // the deciding row's u'
+    FF sres = FF{0.f, 0.f}, sp = FF{0.f, 0.f};
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        if (!sr.valid(v)) break;
+        float wr = 0.f, wp = 0.f;
+#pragma unroll
+        for (int e = 0; e < PV; ++e) {
+            wr += residual_or_p(sr.x[v][e], it, M, Z, qs[v][e], true);
+            wp += residual_or_p(sr.x[v][e], it, M, Z, 0.f, false);
+        }
+        sres = ff_add(sres, wr);
+        sp = ff_add(sp, wp);
+    }
+    // the unaligned head [clo, a0) and tail [a1, chi)
+    auto edge = [&](int i) {
+        const float x = Elem<Tin>::load(lg + i);
+        sres = ff_add(sres, residual_or_p(x, it, M, Z, rejected ? __ldg(qn + i) : 0.f, true));
+        sp = ff_add(sp, residual_or_p(x, it, M, Z, 0.f, false));
+    };
+    for (int i = clo + tid; i < sr.a0; i += kAccThreads) edge(i);
+    for (int i = sr.a1 + tid; i < chi; i += kAccThreads) edge(i);
+    ff_block_sum2(sres, sp);
+    if (tid == 0) p.fs[(long)b * p.n_fchunks + k] = make_float4(sres.hi, sres.lo, sp.hi, sp.lo);
+
+    // then the chunk where x = u' * S falls (residual after a rejection,
+    // unless it is zero everywhere, else p), then the element inside it
+    __shared__ int s_found, s_lastpos;
+    __shared__ FF s_excl[kAccThreads];
+    if (tid == 0) { s_found = INT_MAX; s_lastpos = -1; }
+    // ---- 4. every chunk sum of the sequence is in (a barrier of its CTAs)
+    barrier_arrive_wait(p.row_counter + b, (unsigned int)p.n_fchunks, p.fault);
+    FF vres = FF{0.f, 0.f}, vp = FF{0.f, 0.f};
+    if (tid < p.n_fchunks) {
+        const float4 t = __ldcg(p.fs + (long)b * p.n_fchunks + tid);
+        vres = FF{t.x, t.y};
+        vp = FF{t.z, t.w};
+    }
+    bool res = rejected;
+    FF v = res ? vres : vp, S;
+    FF incl = ff_block_scan(v, S);
+    if (res && !ff_gt0(S)) {   // p = q up to rounding: the draw is from p
+        res = false;
+        v = vp;
+        incl = ff_block_scan(v, S);
+    }
+    const FF x = ff_mul(FF{u2, 0.f}, S);
+    const FF excl = ff_add(incl, FF{-v.hi, -v.lo});
+    s_excl[tid] = excl;
+    if (tid < p.n_fchunks) {
+        if (ff_lt(x, incl) && !ff_lt(x, excl)) s_found = tid;   // one chunk at most
+        if (ff_gt0(v)) atomicMax(&s_lastpos, tid);
+    }
+    __syncthreads();
+    int found = s_found;
+    if (found == INT_MAX) found = s_lastpos < 0 ? 0 : s_lastpos;   // rounding: the last non-empty chunk
+    if (found == k) {
+        const float xl = ff_add(x, FF{-s_excl[found].hi, -s_excl[found].lo}).hi;
+        const int id = search_chunk<Tin, NV>(sr, qs, lg, qn, clo, chi, it, M, Z, res, xl);
+        if (tid == 0) p.next_id[b] = id;
+    }
+    barrier_depart(p.row_counter + b, p.row_counter + p.B + b, (unsigned int)p.n_fchunks);
+    depart();
 }
 
 }  // namespace
@@ -998,6 +1473,75 @@ cudaError_t launch_accept_greedy(const GreedyParams &p, cudaStream_t st) {
     cudaError_t e;
     if (p.dt == SD_BF16) e = launch_pdl(greedy_kernel<__nv_bfloat16>, grid, st, p);
     else e = launch_pdl(greedy_kernel<float>, grid, st, p);
+    return e;
+}
+
+int sample_vec_per_thread(sd_dtype dt, int chunk) {
+    return dt == SD_BF16 ? vec_per_thread<__nv_bfloat16>(chunk) : vec_per_thread<float>(chunk);
+}
+
+int sample_fused_per_sm(sd_dtype dt, int nv) {
+    // CTAs of the fused kernel that fit on one SM (cached per instantiation)
+    static std::atomic<int> cache[2][3][kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    const int di = dt == SD_BF16 ? 0 : 1, ni = nv <= 1 ? 0 : nv <= 2 ? 1 : 2;
+    int v = cache[di][ni][dev].load(std::memory_order_relaxed);
+    if (!v) {
+        int occ = 0;
+        const int smem = kFStages * kFStageBytes;
+        auto query = [&](auto kern) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAccThreads, smem);
+            return e;
+        };
+        cudaError_t e;
+        if (dt == SD_BF16) {
+            e = ni == 0 ? query(sample_fused_kernel<__nv_bfloat16, 1>)
+              : ni == 1 ? query(sample_fused_kernel<__nv_bfloat16, 2>)
+                        : query(sample_fused_kernel<__nv_bfloat16, 4>);
+        } else {
+            e = ni == 0 ? query(sample_fused_kernel<float, 1>)
+              : ni == 1 ? query(sample_fused_kernel<float, 2>)
+                        : query(sample_fused_kernel<float, 4>);
+        }
+        if (e != cudaSuccess) { (void)cudaGetLastError(); occ = 0; }
+        v = occ > 0 ? occ : -1;
+        cache[di][ni][dev].store(v, std::memory_order_relaxed);
+    }
+    return v < 0 ? 0 : std::min(v, kSampleFusedPerSm);
+}
+
+cudaError_t launch_accept_sample_fused(const SampleParams &p, int grid, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kAccThreads);
+    cfg.dynamicSmemBytes = kFStages * kFStageBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e;
+    const int NVv = p.dt == SD_BF16 ? vec_per_thread<__nv_bfloat16>(p.fchunk) : vec_per_thread<float>(p.fchunk);
+    if (p.dt == SD_BF16) {
+        switch (NVv) {
+            case 1: e = cudaLaunchKernelEx(&cfg, sample_fused_kernel<__nv_bfloat16, 1>, p); break;
+            case 2: e = cudaLaunchKernelEx(&cfg, sample_fused_kernel<__nv_bfloat16, 2>, p); break;
+            case 4: e = cudaLaunchKernelEx(&cfg, sample_fused_kernel<__nv_bfloat16, 4>, p); break;
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (NVv) {
+            case 1: e = cudaLaunchKernelEx(&cfg, sample_fused_kernel<float, 1>, p); break;
+            case 2: e = cudaLaunchKernelEx(&cfg, sample_fused_kernel<float, 2>, p); break;
+            case 4: e = cudaLaunchKernelEx(&cfg, sample_fused_kernel<float, 4>, p); break;
+            default: return cudaErrorInvalidValue;
+        }
+    }
     return e;
 }
 

@@ -26,9 +26,10 @@ thread_local int g_last_launches = 0;
 std::atomic<int> g_force_path{0};
 std::atomic<int> g_force_proj_path{0};
 thread_local int g_last_proj_path = 0;
+std::atomic<int> g_force_sample_path{0};
+thread_local int g_last_sample_path = 0;
 
 constexpr size_t kHeader = 256;  // counters; zero between calls
-constexpr int kMaxDevices = 64;
 
 sd_status fail(sd_status s, const char *fmt, ...) {
     va_list ap;
@@ -272,22 +273,57 @@ int draw_chunk_for(int B, int V) {
     return std::min(V, kDrawChunkMax);
 }
 
-// sample workspace: [header: pass-1 counter][per-sequence counters][pm][pz][row_stats][state][rs]
+// sample workspace: [header: counters][per-sequence counters]
+// [pm][pz][row_stats][state][rs] for the two-kernel form, then [pp][fs] for
+// the one-launch form (sized for a grid of kSampleFusedPerSm CTAs per SM)
 struct SampleLayout {
-    size_t row_ctr, pm, pz, row_stats, state, rs, total;
+    size_t row_ctr, pm, pz, row_stats, state, rs, pp, fs, total;
 };
 SampleLayout sample_layout(int B, int T, int V, int chunk, int draw_chunk) {
     const size_t R = (size_t)B * T, nc = (V + chunk - 1) / chunk, parts = R * nc;
     const size_t nd = (V + draw_chunk - 1) / draw_chunk;
+    const size_t cmax = (size_t)kSampleFusedPerSm * device_sm_count();
     SampleLayout l;
     l.row_ctr = kHeader;
-    l.pm = l.row_ctr + align_up((size_t)B * 4, 256);
+    l.pm = l.row_ctr + align_up((size_t)B * 8, 256);
     l.pz = l.pm + align_up(parts * 4, 256);
     l.row_stats = l.pz + align_up(parts * 8, 256);
     l.state = l.row_stats + align_up(R * 8, 256);
     l.rs = l.state + align_up((size_t)B * 16, 256);
-    l.total = l.rs + align_up((size_t)B * nd * 8, 256);
+    l.pp = l.rs + align_up((size_t)B * nd * 8, 256);
+    l.fs = l.pp + align_up(cmax * 2 * 16, 256);
+    l.total = l.fs + align_up(cmax * 16, 256);
     return l;
+}
+
+// The one-launch form of the sampled rule, where its grid fits on the device at
+// once (kSampleFusedPerSm CTAs per SM): segments of the B*T*V logits, at least
+// 2048 elements, a multiple of 8, no longer than a row, one per CTA; chunks of
+// the deciding row, at least 2048 elements, as many per sequence as the grid
+// holds, each within 4 vectors per thread.
+struct FusedPlan {
+    int grid, seg, n_segs, fchunk, n_fchunks;
+};
+bool plan_sample_fused(int B, int T, int V, sd_dtype dt, FusedPlan &f) {
+    const long R = (long)B * T;
+    const int sms = device_sm_count();
+    const int C = kSampleFusedPerSm * sms;
+    if (R > C || B > C) return false;
+    const int nb = std::max(1, std::min(C / B, (V + 2047) / 2048));
+    long fchunk = (V + nb - 1) / nb;
+    fchunk = (fchunk + 7) / 8 * 8;
+    f.fchunk = (int)std::min<long>(fchunk, V);
+    f.n_fchunks = (V + f.fchunk - 1) / f.fchunk;
+    const int nv = sample_vec_per_thread(dt, f.fchunk);
+    if (nv > 4) return false;   // (1, 2, 4 vectors per thread cover the chunk; 8 is the cap)
+    if (sample_fused_per_sm(dt, nv) < kSampleFusedPerSm) return false;
+    const long n = R * V;
+    long seg = (n + C - 1) / C;
+    seg = std::max(2048L, (seg + 7) / 8 * 8);
+    f.seg = (int)std::min<long>(seg, V);
+    f.n_segs = (int)((n + f.seg - 1) / f.seg);
+    f.grid = std::max(f.n_segs, B * f.n_fchunks);
+    return f.grid <= C;
 }
 
 }  // namespace
@@ -519,12 +555,37 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.row_stats = reinterpret_cast<float2 *>(w + sl.row_stats);
     p.state = reinterpret_cast<float4 *>(w + sl.state);
     p.rs = reinterpret_cast<float2 *>(w + sl.rs);
+    p.pp = reinterpret_cast<float4 *>(w + sl.pp);
+    p.fs = reinterpret_cast<float4 *>(w + sl.fs);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
-    cudaError_t e = launch_accept_sample(p, static_cast<cudaStream_t>(stream));
+    const int force = g_force_sample_path.load();
+    FusedPlan fp = {};
+    const bool fused = force != 1 && aligned16(target_logits) && plan_sample_fused(B, T, V, dtype, fp);
+    if (force == 2 && !fused) return fail(SD_ERR_UNSUPPORTED, "the one-launch sampled rule does not fit this call");
+    cudaError_t e;
+    if (fused) {
+        p.seg = fp.seg; p.n_segs = fp.n_segs; p.fchunk = fp.fchunk; p.n_fchunks = fp.n_fchunks;
+        e = launch_accept_sample_fused(p, fp.grid, static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) {
+            g_last_sample_path = 2;
+            return SD_OK;
+        }
+        if (e != cudaErrorCooperativeLaunchTooLarge || force == 2) return cuda_fail(e, "sampled accept launch");
+        (void)cudaGetLastError();   // the device is shared more than planned: two kernels instead
+    }
+    e = launch_accept_sample(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sampled accept launch");
+    g_last_sample_path = 1;
     return SD_OK;
 }
+
+int sd_set_sample_path(int path) {
+    if (path < 0 || path > 2) path = 0;
+    return g_force_sample_path.exchange(path);
+}
+
+int sd_last_sample_path(void) { return g_last_sample_path; }
 
 sd_status sd_project_kv(const void *hidden, int64_t ld_hidden, const void *w_k, const void *w_v, int N, int Hd,
                         int Dout, void *k_out, void *v_out, int64_t ld_out, sd_dtype dtype, void *stream) {

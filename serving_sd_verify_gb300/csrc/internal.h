@@ -112,10 +112,22 @@ struct SampleParams {
     float2 *row_stats;              // [B*T] (logit, q) of the row's proposal
     float4 *state;                  // [B]: (n as int bits, M, Z, unused) of the deciding row
     float2 *rs;                     // [B, n_draw_chunks] chunk sums of the draw's weights (hi, lo)
+    // the one-launch form: counters[1..2] its grid barrier (arrivals,
+    // departures), row_counter [2B] the barriers of the sequences
+    int seg, n_segs;                // the B*T*V logits as n_segs segments of seg (<= V) elements
+    int fchunk, n_fchunks;          // chunks of the deciding row, one CTA each
+    float4 *pp;                     // [n_segs, 2] (max, sum hi, sum lo, -) of a segment's two row pieces
+    float4 *fs;                     // [B, n_fchunks] (residual sum hi, lo, p sum hi, lo) of each chunk
     unsigned int *fault;
 };
+constexpr int kMaxDevices = 64;          // devices whose per-device caches the library keeps
+constexpr int kSampleFusedPerSm = 2;     // CTAs per SM of the one-launch sampled rule
 constexpr int kDrawChunkMax = 4096;  // pass 2 chunk bound: 16 elements per thread of the in-chunk search
 cudaError_t launch_accept_sample(const SampleParams &p, cudaStream_t st);
+// the one-launch form: a cooperative grid of `grid` CTAs, all resident
+cudaError_t launch_accept_sample_fused(const SampleParams &p, int grid, cudaStream_t st);
+int sample_fused_per_sm(sd_dtype dt, int nv);   // its resident CTAs per SM (0: none)
+int sample_vec_per_thread(sd_dtype dt, int chunk);
 
 // Drafter K/V projector: k_out[n] = h[n] . wk^T, v_out[n] = h[n] . wv^T for
 // rows n < N; h [N, Hd] row stride ld_h, wk / wv [Dout, Hd] contiguous,

@@ -30,6 +30,7 @@ SYMBOLS = [
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
     "sd_project_kv", "sd_set_projector_path", "sd_last_projector_path",
+    "sd_set_sample_path", "sd_last_sample_path",
     "sd_commit_tokens", "sd_compact_tree_kv", "sd_project_kv_commit",
     "sd_latent_compress", "sd_latent_compress_workspace_size",
 ]
@@ -120,6 +121,10 @@ def load():
     lib.sd_latent_compress_workspace_size.restype = _sz
     lib.sd_set_projector_path.argtypes = [_i]
     lib.sd_set_projector_path.restype = _i
+    lib.sd_set_sample_path.argtypes = [_i]
+    lib.sd_set_sample_path.restype = _i
+    lib.sd_last_sample_path.argtypes = []
+    lib.sd_last_sample_path.restype = _i
     lib.sd_last_projector_path.argtypes = []
     lib.sd_last_projector_path.restype = _i
     _lib = lib
@@ -398,6 +403,14 @@ def sd_set_projector_path(path: int) -> int:
 
 def sd_last_projector_path() -> int:
     return int(load().sd_last_projector_path())
+
+
+def sd_set_sample_path(path: int) -> int:
+    return load().sd_set_sample_path(int(path))
+
+
+def sd_last_sample_path() -> int:
+    return int(load().sd_last_sample_path())
 
 
 def sd_philox4x32_10(counters, key, out, stream=None):

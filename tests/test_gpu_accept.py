@@ -149,16 +149,25 @@ def test_greedy_repeated_calls_share_workspace(S):
 # sampled
 # --------------------------------------------------------------------------
 
-def run_sample(S, inp, tau, seed, offset=0, ws=None):
+def run_sample(S, inp, tau, seed, offset=0, ws=None, path=0):
+    """path 1: the two-kernel form; 2: the one-launch form (required); 0: automatic."""
     lg, q, d = inp["logits"], inp["q"], inp["draft"]
     B, T, V = lg.shape
     n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
     nx = torch.full((B,), -1, dtype=torch.int32, device="cuda")
     if ws is None:
         ws = S.workspace(S.sd_accept_sample_workspace_size(B, T, V, S._dt(lg)))
-    S.sd_accept_sample(d.cuda(), q.cuda(), lg.cuda(), tau, seed, offset, n, nx, ws)
+    prev = S.sd_set_sample_path(path)
+    try:
+        S.sd_accept_sample(d.cuda(), q.cuda(), lg.cuda(), tau, seed, offset, n, nx, ws)
+        if path:
+            assert S.sd_last_sample_path() == path
+    finally:
+        S.sd_set_sample_path(prev)
     torch.cuda.synchronize()
-    assert counters_zero(ws, 256 + 4 * B), "ticket counters not returned to zero"
+    # the counters: the 256-byte header, then two per sequence
+    assert counters_zero(ws, 256 + 8 * B), "ticket and barrier counters not returned to zero"
+    assert S.sd_fault_word() == 0
     return n.cpu().numpy(), nx.cpu().numpy()
 
 
@@ -214,30 +223,33 @@ def _draw_weights(inp, b, n, tau, mode):
     (2, 1, 3_000, 1.0, torch.bfloat16),
     (12, 4, 152_064, 1.0, torch.bfloat16),   # the largest draw chunk (4096 elements)
 ])
-def test_sample_matches_oracle(S, B, T, V, tau, dtype):
+@pytest.mark.parametrize("path", [1, 2])
+def test_sample_matches_oracle(S, B, T, V, tau, dtype, path):
     inp = W.sample_inputs(B=B, T=T, V=V, seed=B + V, dtype=dtype)
     for offset in (0, 7):
-        n, nx = run_sample(S, inp, tau, 1234, offset)
+        n, nx = run_sample(S, inp, tau, 1234, offset, path=path)
         on, onx, exc = assert_sample_parity(inp, n, nx, tau, 1234, offset)
         assert exc <= max(1, B // 20)
 
 
-def test_sample_workload5(S):
+@pytest.mark.parametrize("path", [1, 2])
+def test_sample_workload5(S, path):
     cfg = W.config(5)
-    n, nx = run_sample(S, cfg["sample"], cfg["temperature"], cfg["philox_seed"])
+    n, nx = run_sample(S, cfg["sample"], cfg["temperature"], cfg["philox_seed"], path=path)
     on, onx, exc = assert_sample_parity(cfg["sample"], n, nx, cfg["temperature"], cfg["philox_seed"])
     assert exc == 0
     assert (n == on).all() and (nx == onx).all()
 
 
-def test_sample_p_equals_q_accepts_all(S):
+@pytest.mark.parametrize("path", [1, 2])
+def test_sample_p_equals_q_accepts_all(S, path):
     B, T, V = 6, 16, 4_000
     g = torch.Generator().manual_seed(3)
     lg = (torch.randn(B, T, V, generator=g) * 2).to(torch.bfloat16)
     q = torch.softmax(lg.double(), -1).float()
     draft = torch.multinomial(q[:, :-1].reshape(-1, V).double(), 1, generator=g).reshape(B, T - 1).int()
     inp = {"logits": lg, "q": q, "draft": draft}
-    n, nx = run_sample(S, inp, 1.0, 42)
+    n, nx = run_sample(S, inp, 1.0, 42, path=path)
     on, onx, _ = assert_sample_parity(inp, n, nx, 1.0, 42)
     assert (n >= 14).all()
 
@@ -269,7 +281,8 @@ def test_accept_errors_are_reported_not_launched(S):
     assert S.sd_fault_word() == 0
 
 
-def test_sample_zero_residual_draws_from_p(S):
+@pytest.mark.parametrize("path", [1, 2])
+def test_sample_zero_residual_draws_from_p(S, path):
     """q = 2 p (unnormalised, taken as given): a proposal is rejected when
     u >= 1/2, the residual max(p - q, 0) is zero everywhere, and the next token
     is drawn from p, as the oracle does (its draw mode 1)."""
@@ -280,9 +293,37 @@ def test_sample_zero_residual_draws_from_p(S):
     q = (2.0 * p).float()
     draft = torch.multinomial(p[:, :-1].reshape(-1, V), 1, generator=g).reshape(B, T - 1).int()
     inp = {"logits": lg, "q": q, "draft": draft}
-    n, nx = run_sample(S, inp, 1.0, 99)
+    n, nx = run_sample(S, inp, 1.0, 99, path=path)
     on, onx, exc = assert_sample_parity(inp, n, nx, 1.0, 99)
     _, _, diag = oracle.accept_sample(draft, q, lg, 1.0, 99, return_diag=True)
     modes = oracle.split_diag(diag, T)["mode"]
     assert (on < T - 1).any() and (modes[on < T - 1] == 1).all()   # rejections drew from p
     assert exc <= 1
+
+
+def test_sample_one_launch_is_chosen_where_it_fits(S):
+    """The automatic choice takes the one-launch form for the batched workload
+    (4 sequences of 16 rows over a 152,064-token vocabulary) and for a single
+    sequence, and the two-kernel form where the grid cannot hold it (more
+    rows than two CTAs per SM)."""
+    for B, T, V, want in [(4, 16, 152_064, 2), (1, 16, 152_064, 2), (32, 16, 2_000, 1)]:
+        inp = W.sample_inputs(B=B, T=T, V=V, seed=7 + B)
+        n, nx = run_sample(S, inp, 1.0, 5, path=0)
+        assert S.sd_last_sample_path() == want, (B, T, V)
+        assert_sample_parity(inp, n, nx, 1.0, 5)
+
+
+def test_sample_one_launch_repeated_calls(S):
+    """Back-to-back one-launch calls on one workspace: the barrier counters
+    return to zero each time and the draws repeat, also after a call of
+    another shape on the same workspace."""
+    inp = W.sample_inputs(B=4, T=16, V=152_064, seed=21)
+    small = W.sample_inputs(B=2, T=8, V=152_064, seed=22)
+    ws = S.workspace(S.sd_accept_sample_workspace_size(4, 16, 152_064))
+    first = run_sample(S, inp, 0.8, 77, ws=ws, path=2)
+    for _ in range(4):
+        again = run_sample(S, inp, 0.8, 77, ws=ws, path=2)
+        assert (again[0] == first[0]).all() and (again[1] == first[1]).all()
+    n, nx = run_sample(S, small, 1.0, 3, ws=ws, path=2)
+    assert_sample_parity(small, n, nx, 1.0, 3)
+    assert (run_sample(S, inp, 0.8, 77, ws=ws, path=2)[1] == first[1]).all()
