@@ -893,18 +893,30 @@ def main():
         acceptance = {}
         g8 = W.greedy_inputs(B=8, T=T, V=V, seed=103)
         s4 = W.sample_inputs(B=4, T=T, V=V, seed=105, draft_seed=1235)
-        n_copies = 4
-        for name, Bn, make, call, nbytes in (
-                ("greedy_b8", 8,
+        g1 = W.greedy_inputs(B=1, T=T, V=V, seed=101)
+        s1 = W.sample_inputs(B=1, T=T, V=V, seed=106, draft_seed=1236)
+        for name, Bn, n_copies, make, call, nbytes in (
+                ("greedy_b8", 8, 4,
                  lambda: (g8["draft"].to(device), g8["logits"].to(device),
                           S.workspace(S.sd_accept_greedy_workspace_size(8, T, V), device)),
                  lambda c, n_, x_: S.sd_accept_greedy(c[0], c[1], n_, x_, c[2], stream),
                  8 * (T * V * 2 + (T - 1) * 4 + 8)),
-                ("sample_b4", 4,
+                ("sample_b4", 4, 4,
                  lambda: (s4["draft"].to(device), s4["q"].to(device), s4["logits"].to(device),
                           S.workspace(S.sd_accept_sample_workspace_size(4, T, V), device)),
                  lambda c, n_, x_: S.sd_accept_sample(c[0], c[1], c[2], 1.0, 1234, 0, n_, x_, c[3], stream),
-                 4 * (T * V * 2 + V * 2 + V * 4 + (T - 1) * 8 + 8))):
+                 4 * (T * V * 2 + V * 2 + V * 4 + (T - 1) * 8 + 8)),
+                # one sequence: 32 input copies, so that the copies exceed L2
+                ("greedy_b1", 1, 32,
+                 lambda: (g1["draft"].to(device), g1["logits"].to(device),
+                          S.workspace(S.sd_accept_greedy_workspace_size(1, T, V), device)),
+                 lambda c, n_, x_: S.sd_accept_greedy(c[0], c[1], n_, x_, c[2], stream),
+                 1 * (T * V * 2 + (T - 1) * 4 + 8)),
+                ("sample_b1", 1, 32,
+                 lambda: (s1["draft"].to(device), s1["q"].to(device), s1["logits"].to(device),
+                          S.workspace(S.sd_accept_sample_workspace_size(1, T, V), device)),
+                 lambda c, n_, x_: S.sd_accept_sample(c[0], c[1], c[2], 1.0, 1234, 0, n_, x_, c[3], stream),
+                 1 * (T * V * 2 + V * 2 + V * 4 + (T - 1) * 8 + 8))):
             cps = [make() for _ in range(n_copies)]
             n_ = torch.zeros(Bn, dtype=torch.int32, device=device)
             x_ = torch.zeros(Bn, dtype=torch.int32, device=device)
@@ -930,7 +942,7 @@ def main():
             per = e_a.elapsed_time(e_b) / 1e3 / (reps_a * 2 * n_copies)
             acceptance[name] = {"us_per_call": per * 1e6, "algorithmic_bytes_per_call": nbytes,
                                 "GBps": nbytes / per / 1e9}
-        del g8, s4
+        del g8, s4, g1, s1
         # verify attention of the ragged batch and of the 72B-shaped batch at
         # full size, and the drafter's layers split into the HBM-cold first one
         # and the L2-resident rest
@@ -1034,6 +1046,8 @@ def main():
             "accept_sample_b4_us": ts4 * 1e6, "accept_sample_b4_frac": acceptance["sample_b4"]["frac_of_peak"],
             "accept_greedy_b1_us": kernels["accept_greedy"]["us_per_call"],
             "accept_sample_b1_us": kernels["accept_sample"]["us_per_call"],
+            "accept_greedy_b1_us_back_to_back": acceptance["greedy_b1"]["us_per_call"],
+            "accept_sample_b1_us_back_to_back": acceptance["sample_b1"]["us_per_call"],
             "cfg3_blocks_per_s": 8 / (t3 + tg8),
             "cfg5_blocks_per_s": 4 / (t5 + ts4),
             "draft_l1_us": t_l1 * 1e6, "draft_l1_frac": BYTES["draft_attention"] / t_l1 / 1e9 / peak,
@@ -1051,7 +1065,8 @@ def main():
         })
         roofline["acceptance_back_to_back"] = dict(acceptance, note=(
             "acceptance kernels at the batched workloads (greedy over 8 sequences' logits, the sampled rule "
-            "over 4), calls issued back to back in one graph over 4 input copies larger than L2"))
+            "over 4; 4 input copies) and for one sequence (32 copies), calls issued back to back in one "
+            "graph over input copies larger than L2"))
 
     # ---- end to end: host buffers, copies inside the timed region ----
     e2e = None

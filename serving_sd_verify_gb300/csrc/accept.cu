@@ -35,8 +35,6 @@ constexpr int kAccThreads = 256;
 constexpr int kGreedyBatch = 4;   // 16-byte vectors per thread per batch of the pass-1 streams
 constexpr int kFinRows = 4;       // rows per warp whose chunk partials a finisher loads together
 constexpr int kFinStaged = 1024;  // chunk partials the greedy finisher stages in shared memory at once
-constexpr int kFStages = 3;          // shared-memory stages of the one-launch sampled stream
-constexpr int kFStageBytes = 32768;  // bytes per stage
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10
@@ -1202,60 +1200,36 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
                 }
             }
         };
-        // the segment's bytes through a ring of kFStages shared-memory stages
-        // that the copy engine fills (a bulk copy per stage, completing on the
-        // stage's mbarrier): thread 0 keeps up to kFStages copies in flight, the
-        // CTA reads each stage once it has landed.  Segments start on 16-byte
-        // boundaries (the logits are 16-byte aligned, seg a multiple of 8); the
-        // last one's ragged end (under 16 bytes) is read directly.
-        const char *gsrc = reinterpret_cast<const char *>(static_cast<const Tin *>(p.logits) + f0);
-        const int bulk = (len * (int)sizeof(Tin)) & ~15;
-        const int n_st = (bulk + kFStageBytes - 1) / kFStageBytes;
-        extern __shared__ __align__(128) uint8_t fsm[];
-        __shared__ __align__(8) uint64_t fbar[kFStages];
-        if (tid == 0) {
-            for (int s = 0; s < kFStages; ++s) mbar_init(smem_u32(&fbar[s]), 1);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        __syncthreads();
-        auto issue = [&](int t) {
-            const int s = t % kFStages, off = t * kFStageBytes, nb = min(kFStageBytes, bulk - off);
-            mbar_arrive_expect_tx(smem_u32(&fbar[s]), (uint32_t)nb);
-            bulk_load_g2s(smem_u32(fsm + s * kFStageBytes), gsrc + off, (uint32_t)nb, smem_u32(&fbar[s]));
-        };
-        if (tid == 0)
-            for (int t = 0; t < min(n_st, kFStages); ++t) issue(t);
-        for (int t = 0; t < n_st; ++t) {
-            const int s = t % kFStages;
-            mbar_wait(smem_u32(&fbar[s]), (uint32_t)((t / kFStages) & 1), nullptr, p.fault);
-            const uint4 *sv = reinterpret_cast<const uint4 *>(fsm + s * kFStageBytes);
-            const int nvt = min(kFStageBytes, bulk - t * kFStageBytes) / 16;
-            const int j0 = t * (kFStageBytes / (int)sizeof(Tin));
-            // vectors i and i + kAccThreads of the stage together
-            for (int i = tid; i < nvt; i += 2 * kAccThreads) {
-                const int i2 = i + kAccThreads;
-                const int j = j0 + i * PV, j2 = j0 + i2 * PV;
-                const uint4 d0 = sv[i];
-                if (i2 < nvt && (j2 + PV <= jb || j >= jb)) {   // both in one row
-                    const uint4 d1 = sv[i2];
-                    const bool inB = j >= jb;
-                    float m = inB ? m1 : m0;
-                    FF z = inB ? z1 : z0;
-                    vec2(d0, d1, m, z);
-                    if (inB) { m1 = m; z1 = z; } else { m0 = m; z0 = z; }
-                } else {
-                    one(d0, j);
-                    if (i2 < nvt) one(sv[i2], j2);
-                }
-            }
-            __syncthreads();                               // stage s is read
-            if (tid == 0 && t + kFStages < n_st) {
-                fence_proxy_async_smem();
-                issue(t + kFStages);
-            }
-        }
+        // the segment (16-byte aligned: the logits are, and seg is a multiple
+        // of 8) as vectors, thread t taking vectors t, t + 256, t + 512, ... in
+        // pairs, the next pair's loads in flight while a pair is reduced; the
+        // last segment's ragged end (under one vector) read element by element
         const Tin *lg = static_cast<const Tin *>(p.logits) + f0;
-        for (int j = bulk / (int)sizeof(Tin) + tid; j < len; j += kAccThreads) {
+        const uint4 *vp = reinterpret_cast<const uint4 *>(lg);
+        const int nvec = len / PV;
+        auto ld = [&](int i) { return i < nvec ? ld_stream_u4(vp + i) : make_uint4(0u, 0u, 0u, 0u); };
+        auto pair = [&](const uint4 &d0, const uint4 &d1, int i) {
+            const int i2 = i + kAccThreads;
+            const int j = i * PV, j2 = i2 * PV;
+            if (i2 < nvec && (j2 + PV <= jb || j >= jb)) {   // both in one row
+                const bool inB = j >= jb;
+                float m = inB ? m1 : m0;
+                FF z = inB ? z1 : z0;
+                vec2(d0, d1, m, z);
+                if (inB) { m1 = m; z1 = z; } else { m0 = m; z0 = z; }
+            } else {
+                one(d0, j);
+                if (i2 < nvec) one(d1, j2);
+            }
+        };
+        uint4 a0 = ld(tid), a1 = ld(tid + kAccThreads);
+        for (int i = tid; i < nvec; i += 2 * kAccThreads) {
+            const uint4 b0 = ld(i + 2 * kAccThreads), b1 = ld(i + 3 * kAccThreads);
+            pair(a0, a1, i);
+            a0 = b0;
+            a1 = b1;
+        }
+        for (int j = nvec * PV + tid; j < len; j += kAccThreads) {
             const float y = Elem<Tin>::load(lg + j) * it;
             if (j < jb) online_add(m0, z0, y); else online_add(m1, z1, y);
         }
@@ -1489,11 +1463,8 @@ int sample_fused_per_sm(sd_dtype dt, int nv) {
     int v = cache[di][ni][dev].load(std::memory_order_relaxed);
     if (!v) {
         int occ = 0;
-        const int smem = kFStages * kFStageBytes;
         auto query = [&](auto kern) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAccThreads, smem);
-            return e;
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAccThreads, 0);
         };
         cudaError_t e;
         if (dt == SD_BF16) {
@@ -1516,7 +1487,7 @@ cudaError_t launch_accept_sample_fused(const SampleParams &p, int grid, cudaStre
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kAccThreads);
-    cfg.dynamicSmemBytes = kFStages * kFStageBytes;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

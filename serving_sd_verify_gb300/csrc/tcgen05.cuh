@@ -102,12 +102,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
-// global to shared memory by the copy engine, completing on mbarrier `bar`
-__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
