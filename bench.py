@@ -307,6 +307,25 @@ def config_verify_pass(S, device, stream, n):
     return per, verify_bytes(ctx_list, T_, Hq, Hkv, D_)
 
 
+def profile_case(S, device, args):
+    """One call class alone for a profiler: verify attention of workload 3
+    (8 sequences, ragged contexts) or 5 (4 sequences, 64 query / 8 kv heads,
+    32,768-token contexts), launched --warmup + --steps times on one stream."""
+    import torch
+    from serving_sd_verify_gb300 import workloads as W
+    att = W.config(3 if args.profile_case == "cfg3-verify" else 5)["attn"]
+    B_, T_, Hq, D_ = att["q"].shape
+    Hkv = att["k"].shape[2]
+    q, k, v, ctx = (att[x].to(device).contiguous() for x in ("q", "k", "v", "ctx"))
+    out = torch.zeros(B_, T_, Hq, D_, device=device)
+    ws = S.workspace(S.sd_verify_attention_workspace_size(B_, T_, Hq, Hkv, D_, att["max_ctx"]), device)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        S.sd_verify_attention(q, k, v, ctx, att["max_ctx"], out, 1.0, ws)
+    torch.cuda.synchronize()
+    assert S.sd_fault_word() == 0
+
+
 def tree60_pass(S, device, stream, n_nodes=60):
     """The pages' Tree-60 at the 25,119-token workload: verify attention over a
     seeded 60-node draft tree (each node's parent among the 3 before it) and
@@ -687,6 +706,8 @@ def main():
     ap.add_argument("--no-soak", action="store_true", help="no 1.5 s soak before timing (profiling)")
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--cpu-rows", type=int, default=32)
+    ap.add_argument("--profile-case", choices=["cfg3-verify", "cfg5-verify"], default=None,
+                    help="profiling: run only this call, --warmup + --steps times eagerly, print nothing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -713,6 +734,10 @@ def main():
     if world > 1:
         dist.barrier()
     S.load()
+
+    if args.profile_case:
+        profile_case(S, device, args)
+        return 0
 
     host = make_inputs(device)
     sets = [DeviceSet(host, device, S) for _ in range(args.copies)]
