@@ -395,7 +395,9 @@ size_t sd_latent_compress_workspace_size(int frames, int N, int Cq, int d);
  * every GPU that loads it until the process exits); shapes whose workspace
  * (sd_accept_greedy_workspace_size) exceeds 1 MiB return SD_ERR_WORKSPACE.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for the process; make that first call
+ * before any stream capture.  A cudaDeviceReset ends the context that address
+ * belongs to: do not call this entry point on that device after one.
  * Every call clears and then uses the same array, so calls must not overlap
  * on the GPU: issue them on one stream (calls on different streams or from
  * different threads without ordering race).  Nothing on this path allocates.
@@ -462,6 +464,16 @@ int sd_set_sample_path(int path);
 /* Which form the last sd_accept_sample on this thread launched: 1 two
  * kernels, 2 one cooperative launch, 0 none. */
 int sd_last_sample_path(void);
+
+/* Failure-detection test hook, process-wide.  The in-kernel barriers (the
+ * tensor-core attention's merge of a unit's splits, the one-launch sampled
+ * rule's grid and sequence barriers) wait for `extra_arrivals` more CTAs than
+ * the grid has, giving up after `limit_ns` (0, or more than 2 s: 2 s, the
+ * normal limit).  A call made meanwhile sets fault bit 3 (a bounded wait gave
+ * up), returns with undefined outputs and leaves its counters zero, so the
+ * next call on the same workspace is exact.  (0, 0) restores normal
+ * operation.  SD_ERR_INVALID_ARG if extra_arrivals > 1024. */
+sd_status sd_set_wait_test(uint32_t extra_arrivals, uint64_t limit_ns);
 
 /* Projector kernel selection, process-wide, for tests and measurement:
  * 0 = automatic (above), 1 = CUDA cores for every N, 2 = tensor cores for

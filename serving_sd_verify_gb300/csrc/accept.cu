@@ -996,7 +996,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
 // departure returns both counters to zero -- every CTA has stopped reading
 // them by then, whether or not its wait gave up.  The whole CTA calls the
 // wait; false (and the fault bit) if it gave up.
-__device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int n, unsigned int *fault) {
+__device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int n, const WaitTest &wt, unsigned int *fault) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1006,8 +1006,8 @@ __device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int n, unsigned 
         for (uint32_t i = 0;; ++i) {
             unsigned int v;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-            if (v >= n) break;
-            if ((i & 15u) == 15u && global_timer() - t0 > kWaitLimitNs) { ok = 0; break; }
+            if (v >= n + wt.extra) break;
+            if ((i & 15u) == 15u && global_timer() - t0 > wt.limit_ns) { ok = 0; break; }
             __nanosleep(20);
         }
         if (!ok) set_fault(fault, FAULT_WAIT_TIMEOUT);
@@ -1249,7 +1249,7 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
     }
 
     // every segment's partials are in (a grid barrier)
-    barrier_arrive_wait(p.counters + 1, C, p.fault);
+    barrier_arrive_wait(p.counters + 1, C, p.wt, p.fault);
     auto depart = [&]() { barrier_depart(p.counters + 1, p.counters + 2, C); };
     const int b = blockIdx.x / p.n_fchunks, k = blockIdx.x % p.n_fchunks;
     if (b >= p.B) {
@@ -1374,7 +1374,7 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
     __shared__ FF s_excl[kAccThreads];
     if (tid == 0) { s_found = INT_MAX; s_lastpos = -1; }
     // ---- 4. every chunk sum of the sequence is in (a barrier of its CTAs)
-    barrier_arrive_wait(p.row_counter + b, (unsigned int)p.n_fchunks, p.fault);
+    barrier_arrive_wait(p.row_counter + b, (unsigned int)p.n_fchunks, p.wt, p.fault);
     FF vres = FF{0.f, 0.f}, vp = FF{0.f, 0.f};
     if (tid < p.n_fchunks) {
         const float4 t = __ldcg(p.fs + (long)b * p.n_fchunks + tid);

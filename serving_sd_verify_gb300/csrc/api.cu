@@ -27,6 +27,8 @@ std::atomic<int> g_force_path{0};
 std::atomic<int> g_force_proj_path{0};
 thread_local int g_last_proj_path = 0;
 std::atomic<int> g_force_sample_path{0};
+std::atomic<unsigned int> g_wait_extra{0};
+std::atomic<unsigned long long> g_wait_ns{kBarrierWaitNs};
 thread_local int g_last_sample_path = 0;
 
 constexpr size_t kHeader = 256;  // counters; zero between calls
@@ -186,37 +188,48 @@ sd_status run_attention(AttnParams &p, void *ws, size_t ws_bytes, cudaStream_t s
     else if (attn_tc_supported(p)) path = 2;
     else if (force >= 2) return fail(SD_ERR_UNSUPPORTED, "tensor-core attention does not cover this shape");
     else path = 1;
-    AttnPlan pl = plan_attention(p, path);
-    const size_t need = attn_workspace(path, p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits, pl.n_mblk);
-    if (!ws || ws_bytes < need)
-        return fail(SD_ERR_WORKSPACE, "attention workspace too small: need %zu bytes, got %zu", need, ws_bytes);
-    if (!aligned16(ws)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    const size_t rows = attn_partial_rows(path, p.B, p.T, p.Hq, pl.n_splits);
-    p.merge_ctr = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + kHeader);
-    char *w = static_cast<char *>(ws) + kHeader + attn_counters_bytes(p.B, p.Hkv, pl.n_mblk);
-    p.o_part = reinterpret_cast<float *>(w);
-    p.lse_part = reinterpret_cast<float *>(w + align_up(rows * p.D * sizeof(float), 256));
-    p.n_splits = pl.n_splits;
-    p.keys_per_split = pl.keys_per_split;
-    p.n_mblk = pl.n_mblk;
-    p.mblk_nodes = pl.mblk_nodes;
-    // one sequence: a (splits, units) grid, every unit as long as the others
-    p.plan_static = path == 2 && p.B == 1 && (long)p.Hkv * pl.n_mblk <= device_sm_count() ? 1 : 0;
-    // tensor-core path: the splits of a unit merge inside the kernel (its grid
-    // has at most one CTA per SM whenever a unit has several splits), and a
-    // unit's only split writes the output itself; the CUDA-core path merges
-    // in the merge kernel
-    p.merge = path == 2 ? 1 : 0;
-    cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
-    if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
-    if (p.merge == 0) {
-        e = launch_lse_merge(p, st);
-        if (e != cudaSuccess) return cuda_fail(e, "attention merge kernel launch");
+    for (;;) {
+        AttnPlan pl = plan_attention(p, path);
+        const size_t need = attn_workspace(path, p.B, p.T, p.Hq, p.Hkv, p.D, pl.n_splits, pl.n_mblk);
+        if (!ws || ws_bytes < need)
+            return fail(SD_ERR_WORKSPACE, "attention workspace too small: need %zu bytes, got %zu", need, ws_bytes);
+        if (!aligned16(ws)) return fail(SD_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        const size_t rows = attn_partial_rows(path, p.B, p.T, p.Hq, pl.n_splits);
+        p.merge_ctr = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + kHeader);
+        char *w = static_cast<char *>(ws) + kHeader + attn_counters_bytes(p.B, p.Hkv, pl.n_mblk);
+        p.o_part = reinterpret_cast<float *>(w);
+        p.lse_part = reinterpret_cast<float *>(w + align_up(rows * p.D * sizeof(float), 256));
+        p.n_splits = pl.n_splits;
+        p.keys_per_split = pl.keys_per_split;
+        p.n_mblk = pl.n_mblk;
+        p.mblk_nodes = pl.mblk_nodes;
+        // one sequence: a (splits, units) grid, every unit as long as the others
+        p.plan_static = path == 2 && p.B == 1 && (long)p.Hkv * pl.n_mblk <= device_sm_count() ? 1 : 0;
+        // tensor-core path: the splits of a unit merge inside the kernel (its grid
+        // has at most one CTA per SM whenever a unit has several splits), and a
+        // unit's only split writes the output itself; the CUDA-core path merges
+        // in the merge kernel
+        p.merge = path == 2 ? 1 : 0;
+        p.wt = wait_test();
+        cudaError_t e = path == 2 ? launch_attn_tc(p, st) : launch_attn_generic(p, st);
+        if (e == cudaErrorCooperativeLaunchTooLarge && path == 2) {
+            // the device cannot hold the whole grid at once (a partitioned one):
+            // the CUDA-core kernel and the merge kernel, whose CTAs never wait
+            (void)cudaGetLastError();
+            if (force >= 2) return fail(SD_ERR_UNSUPPORTED, "the device cannot hold the tensor-core grid at once");
+            path = 1;
+            continue;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "attention split kernel launch");
+        if (p.merge == 0) {
+            e = launch_lse_merge(p, st);
+            if (e != cudaSuccess) return cuda_fail(e, "attention merge kernel launch");
+        }
+        g_last_path = path;
+        g_last_splits = pl.n_splits;
+        g_last_launches = p.merge == 0 ? 2 : 1;
+        return SD_OK;
     }
-    g_last_path = path;
-    g_last_splits = pl.n_splits;
-    g_last_launches = p.merge == 0 ? 2 : 1;
-    return SD_OK;
 }
 
 size_t attention_ws_size(int mode, int B, int T, int Hq, int Hkv, int D, int max_ctx, sd_dtype dt) {
@@ -327,6 +340,13 @@ bool plan_sample_fused(int B, int T, int V, sd_dtype dt, FusedPlan &f) {
 }
 
 }  // namespace
+
+WaitTest wait_test() {
+    WaitTest w;
+    w.extra = g_wait_extra.load();
+    w.limit_ns = g_wait_ns.load();
+    return w;
+}
 
 int device_sm_count() {
     static std::atomic<int> cache[kMaxDevices];
@@ -559,6 +579,7 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     p.fs = reinterpret_cast<float4 *>(w + sl.fs);
     p.fault = fault_ptr();
     if (!p.fault) return fail(SD_ERR_CUDA, "no CUDA device / fault word unavailable");
+    p.wt = wait_test();
     const int force = g_force_sample_path.load();
     FusedPlan fp = {};
     const bool fused = force != 1 && aligned16(target_logits) && plan_sample_fused(B, T, V, dtype, fp);
@@ -577,6 +598,13 @@ sd_status sd_accept_sample(const int32_t *draft_ids, const float *draft_probs, c
     e = launch_accept_sample(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sampled accept launch");
     g_last_sample_path = 1;
+    return SD_OK;
+}
+
+sd_status sd_set_wait_test(uint32_t extra_arrivals, uint64_t limit_ns) {
+    if (extra_arrivals > 1024) return fail(SD_ERR_INVALID_ARG, "extra_arrivals must be <= 1024");
+    g_wait_ns.store(limit_ns == 0 || limit_ns > kBarrierWaitNs ? kBarrierWaitNs : (unsigned long long)limit_ns);
+    g_wait_extra.store(extra_arrivals);
     return SD_OK;
 }
 

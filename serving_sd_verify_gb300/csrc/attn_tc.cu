@@ -259,13 +259,13 @@ __device__ void plan_keys(const AttnParams &p, CtaPlan &pl) {
 // merge of the splits inside the kernel
 // ---------------------------------------------------------------------------
 // Bounded wait until the counter reaches `target`.
-__device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int target) {
+__device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int target, unsigned long long limit_ns) {
     const unsigned long long t0 = global_timer();
     for (uint32_t it = 0;; ++it) {
         unsigned int v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
         if (v >= target) return true;
-        if ((it & 15u) == 15u && global_timer() - t0 > kWaitLimitNs) return false;
+        if ((it & 15u) == 15u && global_timer() - t0 > limit_ns) return false;
         __nanosleep(32);
     }
 }
@@ -289,7 +289,7 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
     __syncthreads();
     if (tid == 0) {
         atomicAdd(ctr, 1u);
-        const bool ok = wait_count(ctr, (unsigned int)n);
+        const bool ok = wait_count(ctr, (unsigned int)n + p.wt.extra, p.wt.limit_ns);
         if (!ok) set_fault(p.fault, FAULT_WAIT_TIMEOUT);
         *go = ok ? 1 : 0;
     }
@@ -1012,9 +1012,9 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     cfg.stream = st;
     // the splits of a unit that merge inside the kernel wait for one another:
     // with at most one CTA per SM the grid goes out as a cooperative launch,
-    // which makes every CTA resident at once; a device that cannot do that (a
-    // partitioned one) gets an ordinary launch, where a wait that gives up
-    // sets fault bit 3 instead of hanging
+    // which makes every CTA resident at once; a device that cannot hold it (a
+    // partitioned one) refuses the launch, and the caller takes the CUDA-core
+    // kernel, whose splits never wait
     const bool coop = (long)cfg.gridDim.x * cfg.gridDim.y <= device_sm_count();
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1023,13 +1023,7 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = coop ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
-    if (e == cudaErrorCooperativeLaunchTooLarge && coop) {
-        (void)cudaGetLastError();
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
-    }
-    return e;
+    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
 }
 
 }  // namespace

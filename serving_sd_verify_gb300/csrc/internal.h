@@ -28,6 +28,17 @@ constexpr int kTileKeys = 64;       // keys per tile of the CUDA-core attention 
 constexpr int kTcTileKeys = 128;    // keys per tile of the tensor-core attention kernel
 constexpr int kMaxHeadBytes = 512;  // bytes of one (position, kv head) row the tree compaction moves
 
+constexpr unsigned long long kBarrierWaitNs = 2000000000ull;   // an in-kernel barrier wait gives up after 2 s
+
+// Failure-detection test hook (sd_set_wait_test): the in-kernel barriers
+// (attention merge, one-launch sampled rule) wait for `extra` arrivals more
+// than exist, giving up after `limit_ns`.  {0, kBarrierWaitNs} normally.
+struct WaitTest {
+    unsigned int extra;
+    unsigned long long limit_ns;
+};
+WaitTest wait_test();
+
 // Attention launch description (both the target verify and the drafter).
 //  key index space of sequence b:
 //   mode 0 (verify):  N_b = nctx[b] + T - 1 cache keys; row j sees [0, nctx[b] + j)
@@ -65,6 +76,7 @@ struct AttnParams {
     // single split that writes the output itself
     int merge;
     unsigned int *merge_ctr;
+    WaitTest wt;
     unsigned int *fault;
 };
 
@@ -118,6 +130,7 @@ struct SampleParams {
     int fchunk, n_fchunks;          // chunks of the deciding row, one CTA each
     float4 *pp;                     // [n_segs, 2] (max, sum hi, sum lo, -) of a segment's two row pieces
     float4 *fs;                     // [B, n_fchunks] (residual sum hi, lo, p sum hi, lo) of each chunk
+    WaitTest wt;
     unsigned int *fault;
 };
 constexpr int kMaxDevices = 64;          // devices whose per-device caches the library keeps

@@ -30,7 +30,7 @@ SYMBOLS = [
     "sd_philox4x32_10", "sd_status_string", "sd_last_error", "sd_version",
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
     "sd_project_kv", "sd_set_projector_path", "sd_last_projector_path",
-    "sd_set_sample_path", "sd_last_sample_path",
+    "sd_set_sample_path", "sd_last_sample_path", "sd_set_wait_test",
     "sd_commit_tokens", "sd_compact_tree_kv", "sd_project_kv_commit",
     "sd_latent_compress", "sd_latent_compress_workspace_size",
 ]
@@ -121,6 +121,8 @@ def load():
     lib.sd_latent_compress_workspace_size.restype = _sz
     lib.sd_set_projector_path.argtypes = [_i]
     lib.sd_set_projector_path.restype = _i
+    lib.sd_set_wait_test.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
+    lib.sd_set_wait_test.restype = _i
     lib.sd_set_sample_path.argtypes = [_i]
     lib.sd_set_sample_path.restype = _i
     lib.sd_last_sample_path.argtypes = []
@@ -403,6 +405,10 @@ def sd_set_projector_path(path: int) -> int:
 
 def sd_last_projector_path() -> int:
     return int(load().sd_last_projector_path())
+
+
+def sd_set_wait_test(extra_arrivals: int, limit_ns: int = 0) -> None:
+    _check(load().sd_set_wait_test(int(extra_arrivals), int(limit_ns)))
 
 
 def sd_set_sample_path(path: int) -> int:
