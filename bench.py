@@ -239,11 +239,11 @@ class CycleSet:
 
 
 # kernels of one step: 5 attention calls (1 launch each when the splits merge
-# inside the split kernel, else 2; set from the library after a warm-up
-# step), greedy 1, sampled 2
-ATTN_LAUNCHES = {"draft": 2, "verify": 2}
+# inside the split kernel, else 2), greedy 1, sampled 1 (one cooperative
+# launch) or 2; set from the library after a warm-up step
+ATTN_LAUNCHES = {"draft": 2, "verify": 2, "sample": 2}
 def kernels_per_step():
-    return LAYERS * ATTN_LAUNCHES["draft"] + ATTN_LAUNCHES["verify"] + 1 + 2
+    return LAYERS * ATTN_LAUNCHES["draft"] + ATTN_LAUNCHES["verify"] + 1 + ATTN_LAUNCHES["sample"]
 
 
 def verify_bytes(ctx_list, T_, Hq, Hkv, D_):
@@ -420,6 +420,7 @@ def run_step(S, ds, stream=None, parts=("draft", "verify", "greedy", "sample")):
         S.sd_accept_greedy(ds.draft, ds.logits, ds.n, ds.c, ds.ws_g, stream)
     if "sample" in parts:
         S.sd_accept_sample(ds.sdraft, ds.sq, ds.logits, 1.0, 1234, 0, ds.sn, ds.snx, ds.ws_s, stream)
+        ATTN_LAUNCHES["sample"] = 1 if S.sd_last_sample_path() == 2 else 2
     if "tree_verify" in parts:
         S.sd_verify_tree_attention(ds.q, ds.k, ds.v, ds.ctx, CTX, ds.tmask, ds.out, 1.0, ds.ws_tv, stream)
     if "tree_greedy" in parts:
@@ -996,7 +997,7 @@ def main():
                                      "the step, which uses the chain calls")
         for name, nl in (("draft_attention", ATTN_LAUNCHES["draft"]), ("verify_attention", ATTN_LAUNCHES["verify"]),
                          ("accept_greedy", 1),
-                         ("accept_sample", 2), ("verify_tree_attention", ATTN_LAUNCHES["verify"]),
+                         ("accept_sample", ATTN_LAUNCHES["sample"]), ("verify_tree_attention", ATTN_LAUNCHES["verify"]),
                          ("accept_tree_greedy", 1)):
             kernels[name]["kernel_launches_per_call"] = nl
 
