@@ -285,10 +285,12 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
     unsigned int *ctr = p.merge_ctr + (((long)b * p.Hkv + g) * p.n_mblk + pl.mb);
     const int n = pl.n;
     const int tid = threadIdx.x;
-    __threadfence();  // this thread's partial stores are visible device-wide
+    // the arrival is a release by thread 0 after the CTA barrier: it covers
+    // every thread's partial (the bulk copies each thread waited for, the
+    // log-sum-exps) for whoever acquires the count
     __syncthreads();
     if (tid == 0) {
-        atomicAdd(ctr, 1u);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
         const bool ok = wait_count(ctr, (unsigned int)n + p.wt.extra, p.wt.limit_ns);
         if (!ok) set_fault(p.fault, FAULT_WAIT_TIMEOUT);
         *go = ok ? 1 : 0;
