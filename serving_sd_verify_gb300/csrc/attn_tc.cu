@@ -279,6 +279,8 @@ __device__ __noinline__ bool wait_count(const unsigned int *ctr, unsigned int ta
 // counter is returned to zero by the last split to finish merging.  `scratch`
 // is idle shared memory (the K/V rings).
 constexpr int kMergeBatch = 12;  // loads one merge thread keeps in flight
+constexpr int kMergeSmall = 6;   // a chunk of at most this many splits takes the grouped path
+constexpr int kMergeUnits = 3;   // units a merge thread loads together on that path
 __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int M, int G, volatile int *go,
                             uint8_t *scratch) {
     const int s = pl.s, g = pl.g, b = pl.b;
@@ -312,6 +314,51 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
         return ((long)b * p.T + j0 + rr / G) * p.Hq + g * G + rr % G;
     };
     if (*go && R > 0) {
+        if (chunk <= kMergeSmall) {
+            // few splits per chunk: a thread's units go kMergeUnits at a time,
+            // every load of the group in flight together (one round trip for
+            // up to kMergeUnits units instead of one each)
+            for (int u0 = tid; u0 < K * R * 32; u0 += kMergeUnits * kTcThreads) {
+                float4 v[kMergeUnits][kMergeSmall];
+                float l[kMergeUnits][kMergeSmall];
+#pragma unroll
+                for (int q = 0; q < kMergeUnits; ++q) {
+                    const int u = u0 + q * kTcThreads;
+                    const bool live = u < K * R * 32;
+                    const int uu = live ? u : u0;
+                    const int k = uu / (R * 32), ri = (uu / 32) % R, c4 = uu & 31;
+                    const int sp0 = k * chunk, sp1 = min(n, sp0 + chunk);
+#pragma unroll
+                    for (int e = 0; e < kMergeSmall; ++e) {
+                        const long prow = (long)(pl.slot0 + min(sp0 + e, sp1 - 1)) * 128 + s + ri * n;
+                        v[q][e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + prow * 128) + c4);
+                        l[q][e] = live && sp0 + e < sp1 ? __ldcg(p.lse_part + prow) : -INFINITY;
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < kMergeUnits; ++q) {
+                    const int u = u0 + q * kTcThreads;
+                    if (u >= K * R * 32) break;
+                    float m_run = l[q][0];
+#pragma unroll
+                    for (int e = 1; e < kMergeSmall; ++e) m_run = fmaxf(m_run, l[q][e]);
+                    float w_run = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (m_run != -INFINITY) {
+#pragma unroll
+                        for (int e = 0; e < kMergeSmall; ++e) {
+                            const float w = __expf(l[q][e] - m_run);   // 0 for an empty or repeated split
+                            w_run += w;
+                            acc.x = fmaf(w, v[q][e].x, acc.x); acc.y = fmaf(w, v[q][e].y, acc.y);
+                            acc.z = fmaf(w, v[q][e].z, acc.z); acc.w = fmaf(w, v[q][e].w, acc.w);
+                        }
+                    }
+                    pacc[u] = acc;
+                    pm[u] = m_run;
+                    pw[u] = w_run;
+                }
+            }
+        } else {
         for (int u = tid; u < K * R * 32; u += kTcThreads) {
             const int k = u / (R * 32), ri = (u / 32) % R, c4 = u & 31;
             const int sp0 = k * chunk, sp1 = min(n, sp0 + chunk);
@@ -349,6 +396,7 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
             pacc[u] = acc;
             pm[u] = m_run;
             pw[u] = w_run;
+        }
         }
         __syncthreads();
         for (int i = tid; i < R * 32; i += kTcThreads) {
