@@ -308,20 +308,55 @@ def config_verify_pass(S, device, stream, n):
 
 
 def profile_case(S, device, args):
-    """One call class alone for a profiler: verify attention of workload 3
-    (8 sequences, ragged contexts) or 5 (4 sequences, 64 query / 8 kv heads,
-    32,768-token contexts), launched --warmup + --steps times on one stream."""
+    """One call class alone for a profiler, launched --warmup + --steps times on
+    one stream: verify attention of workload 3 (8 sequences, ragged contexts)
+    or 5 (4 sequences, 64 query / 8 kv heads, 32,768-token contexts); greedy
+    acceptance over 8 sequences' logits or the sampled rule over 4 (the batched
+    workloads); the projector at prefill (25,119 rows) or for an 8-row append;
+    the latent compressor (16 frames x 576 features, d 4096 -> 64)."""
     import torch
     from serving_sd_verify_gb300 import workloads as W
-    att = W.config(3 if args.profile_case == "cfg3-verify" else 5)["attn"]
-    B_, T_, Hq, D_ = att["q"].shape
-    Hkv = att["k"].shape[2]
-    q, k, v, ctx = (att[x].to(device).contiguous() for x in ("q", "k", "v", "ctx"))
-    out = torch.zeros(B_, T_, Hq, D_, device=device)
-    ws = S.workspace(S.sd_verify_attention_workspace_size(B_, T_, Hq, Hkv, D_, att["max_ctx"]), device)
+    case = args.profile_case
+    if case in ("cfg3-verify", "cfg5-verify"):
+        att = W.config(3 if case == "cfg3-verify" else 5)["attn"]
+        B_, T_, Hq, D_ = att["q"].shape
+        Hkv = att["k"].shape[2]
+        q, k, v, ctx = (att[x].to(device).contiguous() for x in ("q", "k", "v", "ctx"))
+        out = torch.zeros(B_, T_, Hq, D_, device=device)
+        ws = S.workspace(S.sd_verify_attention_workspace_size(B_, T_, Hq, Hkv, D_, att["max_ctx"]), device)
+        call = lambda: S.sd_verify_attention(q, k, v, ctx, att["max_ctx"], out, 1.0, ws)
+    elif case == "accept-greedy-b8":
+        g = W.greedy_inputs(B=8, T=T, V=V, seed=103)
+        d, lg = g["draft"].to(device), g["logits"].to(device)
+        n = torch.zeros(8, dtype=torch.int32, device=device)
+        c = torch.zeros_like(n)
+        ws = S.workspace(S.sd_accept_greedy_workspace_size(8, T, V), device)
+        call = lambda: S.sd_accept_greedy(d, lg, n, c, ws)
+    elif case == "accept-sample-b4":
+        sm = W.sample_inputs(B=4, T=T, V=V, seed=105, draft_seed=1235)
+        d, q, lg = sm["draft"].to(device), sm["q"].to(device), sm["logits"].to(device)
+        n = torch.zeros(4, dtype=torch.int32, device=device)
+        c = torch.zeros_like(n)
+        ws = S.workspace(S.sd_accept_sample_workspace_size(4, T, V), device)
+        call = lambda: S.sd_accept_sample(d, q, lg, 1.0, 1234, 0, n, c, ws)
+    elif case in ("project-prefill", "project-append"):
+        h, wk, wv = W.hidden_and_projector(N=CTX, seed=4)
+        h = h.to(device).contiguous()
+        wk = wk.t().contiguous().to(torch.bfloat16).to(device)
+        wv = wv.t().contiguous().to(torch.bfloat16).to(device)
+        kk = torch.empty(CTX, HKV * D, dtype=torch.bfloat16, device=device)
+        vv = torch.empty_like(kk)
+        r0 = 0 if case == "project-prefill" else CTX - APPEND
+        call = lambda: S.sd_project_kv(h[r0:], wk, wv, kk[r0:], vv[r0:])
+    else:
+        lq, lf = W.latent_inputs(frames=LC_FRAMES, N=LC_N, Cq=LC_C, d=LC_D, seed=16)
+        lq, lf = lq.to(device), lf.to(device)
+        lout = torch.empty(LC_FRAMES, LC_C, LC_D, dtype=torch.bfloat16, device=device)
+        lws = S.workspace(S.sd_latent_compress_workspace_size(LC_FRAMES, LC_N, LC_C, LC_D), device)
+        call = lambda: S.sd_latent_compress(lq, lf, lout, lws)
     torch.cuda.synchronize()
     for _ in range(args.warmup + args.steps):
-        S.sd_verify_attention(q, k, v, ctx, att["max_ctx"], out, 1.0, ws)
+        call()
     torch.cuda.synchronize()
     assert S.sd_fault_word() == 0
 
@@ -707,7 +742,8 @@ def main():
     ap.add_argument("--no-soak", action="store_true", help="no 1.5 s soak before timing (profiling)")
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--cpu-rows", type=int, default=32)
-    ap.add_argument("--profile-case", choices=["cfg3-verify", "cfg5-verify"], default=None,
+    ap.add_argument("--profile-case", choices=["cfg3-verify", "cfg5-verify", "accept-greedy-b8", "accept-sample-b4",
+                                               "project-prefill", "project-append", "latent"], default=None,
                     help="profiling: run only this call, --warmup + --steps times eagerly, print nothing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
