@@ -1076,6 +1076,8 @@ __device__ __forceinline__ FF ff_block_scan(FF v, FF &total) {
 // ex2.approx unit (relative error about 2^-22), y - m rounded once
 constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float exp_rel(float y, float m) { return ex2((y - m) * kLog2e); }
+// e^(x / tau - m), x / tau - m taken with one rounding (FMA)
+__device__ __forceinline__ float exp_scaled(float x, float it, float m) { return ex2(fmaf(x, it, -m) * kLog2e); }
 
 // online (max, sum of exp) of one row's piece: y = l / tau of a new element
 __device__ __forceinline__ void online_add(float &m, FF &z, float y) {
@@ -1150,7 +1152,7 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
                 Vec16<Tin>::unpack(d, f);
                 float w[PV];
 #pragma unroll
-                for (int e = 0; e < PV; ++e) w[e] = exp_rel(f[e] * it, m);
+                for (int e = 0; e < PV; ++e) w[e] = exp_scaled(f[e], it, m);
 #pragma unroll
                 for (int h = PV / 2; h > 0; h >>= 1)
 #pragma unroll
@@ -1171,7 +1173,7 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
                 Vec16<Tin>::unpack(d1, f1);
                 float w[PV];
 #pragma unroll
-                for (int e = 0; e < PV; ++e) w[e] = exp_rel(f0[e] * it, m) + exp_rel(f1[e] * it, m);
+                for (int e = 0; e < PV; ++e) w[e] = exp_scaled(f0[e], it, m) + exp_scaled(f1[e], it, m);
 #pragma unroll
                 for (int h = PV / 2; h > 0; h >>= 1)
 #pragma unroll
