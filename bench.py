@@ -1224,34 +1224,39 @@ def e2e_pass(S, host, ds, device, stream, steps):
     h_acc, d_acc, v_acc = packed(acc_in)
     h_blk_k = a["k"][:, CTX - 1:CTX + T - 1].contiguous().pin_memory()
     h_blk_v = a["v"][:, CTX - 1:CTX + T - 1].contiguous().pin_memory()
-    res = torch.zeros(4, dtype=torch.int32, device=device)
+    # the step's results -- verify output and the four accept ids -- side by
+    # side in one device buffer, read back with one copy
+    out_bytes = 1 * T * HQ * D * 4
+    d_outres = torch.zeros(out_bytes + 256, dtype=torch.uint8, device=device)
+    h_outres = torch.empty(out_bytes + 256, dtype=torch.uint8).pin_memory()
+    res = d_outres[out_bytes:out_bytes + 16].view(torch.int32)
     e2 = types.SimpleNamespace(**vars(ds))
+    e2.out = d_outres[:out_bytes].view(torch.float32).view(1, T, HQ, D)
     e2.q = v_att[0]
     e2.layers = [tuple(v_att[1 + 3 * li: 4 + 3 * li]) for li in range(LAYERS)]
     e2.logits, e2.draft, e2.sq, e2.sdraft = v_acc
     e2.n, e2.c, e2.sn, e2.snx = res[0:1], res[1:2], res[2:3], res[3:4]
-    h_out = torch.empty(1, T, HQ, D).pin_memory()
-    h_res = torch.empty(4, dtype=torch.int32).pin_memory()
     h2d = h_att.numel() + h_acc.numel() + h_blk_k.numel() * 2 + h_blk_v.numel() * 2
-    d2h = h_out.numel() * 4 + h_res.numel() * 4
+    d2h = out_bytes + 16
     side = torch.cuda.Stream(device)
 
     def body():
         cur = torch.cuda.current_stream()
-        # the acceptance inputs (target logits, draft ids and probabilities:
-        # 14.6 of the 15.3 MB) travel on a side stream while the attention
-        # calls run, and join before the acceptance calls
+        # what the drafter layers read goes first on the main stream; the
+        # block's own K/V slots (read from the verify on) and the acceptance
+        # inputs (target logits, draft ids and probabilities: 14.6 of the
+        # 15.3 MB) travel on a side stream while the drafter layers run, and
+        # join before the verify call
         side.wait_stream(cur)
         with torch.cuda.stream(side):
+            ds.k[:, CTX - 1:CTX + T - 1].copy_(h_blk_k, non_blocking=True)
+            ds.v[:, CTX - 1:CTX + T - 1].copy_(h_blk_v, non_blocking=True)
             d_acc.copy_(h_acc, non_blocking=True)
         d_att.copy_(h_att, non_blocking=True)
-        ds.k[:, CTX - 1:CTX + T - 1].copy_(h_blk_k, non_blocking=True)
-        ds.v[:, CTX - 1:CTX + T - 1].copy_(h_blk_v, non_blocking=True)
-        run_step(S, e2, stream, ("draft", "verify"))
+        run_step(S, e2, stream, ("draft",))
         cur.wait_stream(side)
-        run_step(S, e2, stream, ("greedy", "sample"))
-        h_out.copy_(e2.out, non_blocking=True)
-        h_res.copy_(res, non_blocking=True)
+        run_step(S, e2, stream, ("verify", "greedy", "sample"))
+        h_outres.copy_(d_outres, non_blocking=True)
 
     def one():
         body()
@@ -1286,8 +1291,9 @@ def e2e_pass(S, host, ds, device, stream, steps):
     return {"value": steps / sec, "unit": "blocks/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "eager_value": steps / sec_eager,
             "note": "per-block inputs from pinned host memory (two packed buffers plus the block's K/V slots), "
-                    "results read back every step, the host waiting for them; the acceptance inputs copied on "
-                    "a side stream while the attention calls run; the step (copies and C-ABI calls) replayed "
+                    "results read back every step with one copy, the host waiting for them; the block's K/V "
+                    "slots and the acceptance inputs copied on a side stream while the drafter layers run; "
+                    "the step (copies and C-ABI calls) replayed "
                     "from one CUDA graph (eager_value: the same step issued call by call from Python); context "
                     "K/V resident"}
 
