@@ -179,3 +179,29 @@ def test_next_row_workspace_sizes(S):
     a = S.sd_latent_compress_workspace_size(16, 576, 64, 4096)
     b = S.sd_latent_compress_workspace_size(32, 576, 64, 4096)
     assert 0 < a < b
+
+
+def test_path_setters_and_wait_hook_on_the_host(S):
+    """The process-wide selectors return the previous setting and fold
+    unknown values to automatic; the wait-test hook refuses more than 1024
+    extra arrivals and takes (0, 0) back to normal operation.  No launch."""
+    lib = S.load()
+    prev = lib.sd_set_sample_path(1)
+    try:
+        assert lib.sd_set_sample_path(2) == 1
+        assert lib.sd_set_sample_path(7) == 2      # out of range: automatic
+        assert lib.sd_set_sample_path(0) == 0
+    finally:
+        lib.sd_set_sample_path(prev)
+    assert lib.sd_set_wait_test(5000, 0) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_set_wait_test(1, 1_000_000) == S.SD_OK
+    assert lib.sd_set_wait_test(0, 0) == S.SD_OK
+
+
+def test_sample_workspace_covers_both_forms(S):
+    """The sampled rule's workspace holds the two-kernel form and the one-launch
+    form (its records sized for two CTAs per SM), so the call may take either:
+    it grows with the batch and never shrinks below the smaller shapes'."""
+    lib = S.load()
+    sizes = [lib.sd_accept_sample_workspace_size(B, 16, 152_064, S.SD_BF16) for B in (1, 2, 4, 8, 64)]
+    assert all(x > 0 for x in sizes) and sizes == sorted(sizes)
