@@ -596,17 +596,32 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(p.kb);
             const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(p.vb);
             uint8_t *ks = sbase + L::kOffK, *vs = sbase + L::kOffV;
-            for (int idx = lane; idx < kBN * 16; idx += 32) {
-                const int row = idx >> 4, ch = idx & 15;
-                uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
+            // the T <= 16 rows' loads all in flight first (8 pairs per lane), then the stores
+            constexpr int kBlkIters = kMaxT * 16 / 32;
+            uint4 kv4[kBlkIters], vv4[kBlkIters];
+#pragma unroll
+            for (int it = 0; it < kBlkIters; ++it) {
+                const int idx = lane + 32 * it, row = idx >> 4, ch = idx & 15;
+                kv4[it] = make_uint4(0u, 0u, 0u, 0u);
+                vv4[it] = make_uint4(0u, 0u, 0u, 0u);
                 if (row < T) {
                     const long off = (((long)b * T + row) * p.Hkv + g) * 128;
-                    kv4 = __ldg(reinterpret_cast<const uint4 *>(kb + off) + ch);
-                    vv4 = __ldg(reinterpret_cast<const uint4 *>(vb + off) + ch);
+                    kv4[it] = __ldg(reinterpret_cast<const uint4 *>(kb + off) + ch);
+                    vv4[it] = __ldg(reinterpret_cast<const uint4 *>(vb + off) + ch);
                 }
+            }
+#pragma unroll
+            for (int it = 0; it < kBlkIters; ++it) {
+                const int idx = lane + 32 * it, row = idx >> 4, ch = idx & 15;
                 const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
-                *reinterpret_cast<uint4 *>(ks + o) = kv4;
-                *reinterpret_cast<uint4 *>(vs + o) = vv4;
+                *reinterpret_cast<uint4 *>(ks + o) = kv4[it];
+                *reinterpret_cast<uint4 *>(vs + o) = vv4[it];
+            }
+            for (int idx = lane + 32 * kBlkIters; idx < kBN * 16; idx += 32) {   // rows >= 16: zeros
+                const int row = idx >> 4, ch = idx & 15;
+                const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
+                *reinterpret_cast<uint4 *>(ks + o) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(vs + o) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
