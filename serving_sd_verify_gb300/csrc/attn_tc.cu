@@ -761,6 +761,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         // every later wait returns at once) so that no barrier is left short.
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        // this row's tree word, read once (the edge tiles use it)
+        const uint64_t row_tm = tree && row_ok ? p.tree_mask[(long)b * T + j] : 0ull;
         for (int t = 0; t < n_tiles; ++t) {
             const int bi = t % kSP;
             const uint32_t sp_col = tmem + lane_off + 128u + 128u * bi + 64u * wg;
@@ -782,7 +784,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     vis = prefix(T - 64 * wg);
                 } else if (tree) {
                     vis = prefix(min(cend, nb - 1) - key0h);
-                    const uint64_t tm = p.tree_mask[(long)b * T + j];
+                    const uint64_t tm = row_tm;
                     for (int k = 0; k < T; ++k) {
                         const int pos = nb - 1 + k - key0h;
                         if (pos >= 0 && pos < 64 && key0h + pos < cend && ((tm >> k) & 1ull)) vis |= 1ull << pos;
