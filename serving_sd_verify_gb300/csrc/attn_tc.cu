@@ -485,8 +485,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 #if __CUDA_ARCH__ >= 900
+    // inputs of the upstream kernel are visible past the wait; the dependents'
+    // launch is allowed only after it, so that a dependent overlaps this kernel alone
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // inputs of an upstream kernel are visible now
 #endif
 
     // the plan: warp 0 works it out, and its lane 0 starts the Q copy and the
@@ -682,10 +684,30 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const uint32_t idO = idesc_bf16(128, 128, true);
             bool ok = mbar_wait(qready_bar, 0, abort_flag, p.fault);
             // S runs up to kSP tiles ahead of P.V; whichever of the next S and
-            // the next P.V can go is issued, P.V first
+            // the next P.V can go is issued, S first: the tensor pipe runs its
+            // MMAs in issue order, and the softmax waits for the next S, while a
+            // P.V only has to complete before its buffers are reused
             int ns = 0, npv = 0;
             unsigned long long t_last = global_timer();
             for (uint32_t spin = 0; ok && npv < n_tiles;) {
+                if (ns < n_tiles && ns < npv + kSP && mbar_test(kfull_bar(ns % kKSlots), (ns / kKSlots) & 1) &&
+                    (ns < kSP || mbar_test(pempty_bar(ns % kSP), ((ns / kSP) - 1) & 1))) {
+                    // S(ns) into buffer ns % 3, free once P.V(ns - 3) has read it
+                    tc_fence_after();
+                    const uint32_t kb = sK + (ns % kKSlots) * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                        umma_ss(tmem + 128u + 128u * (ns % kSP), sw128_desc(sQ + off, 16, 1024),
+                                sw128_desc(kb + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024), idS,
+                                kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(sfull_bar(ns % kSP));
+                    umma_commit(kempty_bar(ns % kKSlots));
+                    ++ns;
+                    t_last = global_timer();
+                    continue;
+                }
                 if (npv < ns && mbar_test(pfull_bar(npv % kSP), (npv / kSP) & 1) &&
                     mbar_test(vfull_bar(npv % kVSlots), (npv / kVSlots) & 1)) {
                     // P.V(npv): O += P_hi . V (+ P_lo . V when the softmax warps asked
@@ -705,24 +727,6 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     umma_commit(pempty_bar(npv % kSP));
                     umma_commit(vempty_bar(npv % kVSlots));
                     ++npv;
-                    t_last = global_timer();
-                    continue;
-                }
-                if (ns < n_tiles && ns < npv + kSP && mbar_test(kfull_bar(ns % kKSlots), (ns / kKSlots) & 1) &&
-                    (ns < kSP || mbar_test(pempty_bar(ns % kSP), ((ns / kSP) - 1) & 1))) {
-                    // S(ns) into buffer ns % 3, free once P.V(ns - 3) has read it
-                    tc_fence_after();
-                    const uint32_t kb = sK + (ns % kKSlots) * kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-                        umma_ss(tmem + 128u + 128u * (ns % kSP), sw128_desc(sQ + off, 16, 1024),
-                                sw128_desc(kb + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024), idS,
-                                kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(sfull_bar(ns % kSP));
-                    umma_commit(kempty_bar(ns % kKSlots));
-                    ++ns;
                     t_last = global_timer();
                     continue;
                 }

@@ -86,8 +86,10 @@ project_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 #if __CUDA_ARCH__ >= 900
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the dependents may start once this kernel's inputs are complete, so that
+    // a dependent overlaps this kernel alone
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
     tc_fence_before();
     __syncthreads();
