@@ -436,7 +436,8 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kTcThreads, 1)
 attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_kb,
+                     const __grid_constant__ CUtensorMap tmap_vb, const AttnParams p) {
     using L = Layout;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -478,6 +479,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+        if (p.mode == 1) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_kb)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_vb)) : "memory");
+        }
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -512,7 +517,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     // a split's tiles: the cache keys [k0, cend) of its sequence, after the
     // drafter's block tile when it leads the split
     struct Tiles {
-        int nb, k0, cend, n_tiles, first_tma;
+        int nb, k0, cend, n_tiles, lead_blk;
     };
     auto tiles_of = [&](const CtaPlan &q) {
         Tiles r;
@@ -520,25 +525,29 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         r.k0 = q.k0;
         r.cend = p.mode == 1 ? min(q.k1, r.nb) : min(q.k1, r.nb + T - 1);
         const int n_cache = r.cend > r.k0 ? (r.cend - r.k0 + kBN - 1) / kBN : 0;
-        r.first_tma = q.block_tile ? 1 : 0;   // tile 0 of a leading drafter split is the block
-        r.n_tiles = n_cache + r.first_tma;
+        r.lead_blk = q.block_tile ? 1 : 0;   // tile 0 of the drafter's leading split is the block
+        r.n_tiles = n_cache + r.lead_blk;
         return r;
     };
-    // one copy per tile: map coordinates (d within a half, key, half, kv head, sequence)
+    // one copy per tile: map coordinates (d within a half, key, half, kv head,
+    // sequence); the drafter's block tile comes from the [B, T, Hkv, D] block
+    // keys / values, whose rows past T the copy fills with zeros
     auto issue_k = [&](const CtaPlan &q, const Tiles &r, int t) {
         const int sl = t % kKSlots;
         mbar_arrive_expect_tx(kfull_bar(sl), (uint32_t)kTileBytes);
-        tma_load_5d(sK + sl * kTileBytes, &tmap_k, kfull_bar(sl), 0, r.k0 + (t - r.first_tma) * kBN, 0, q.g, q.b);
+        if (t < r.lead_blk) tma_load_5d(sK + sl * kTileBytes, &tmap_kb, kfull_bar(sl), 0, 0, 0, q.g, q.b);
+        else tma_load_5d(sK + sl * kTileBytes, &tmap_k, kfull_bar(sl), 0, r.k0 + (t - r.lead_blk) * kBN, 0, q.g, q.b);
     };
     auto issue_v = [&](const CtaPlan &q, const Tiles &r, int t) {
         const int sl = t % kVSlots;
         mbar_arrive_expect_tx(vfull_bar(sl), (uint32_t)kTileBytes);
-        tma_load_5d(sV + sl * kTileBytes, &tmap_v, vfull_bar(sl), 0, r.k0 + (t - r.first_tma) * kBN, 0, q.g, q.b);
+        if (t < r.lead_blk) tma_load_5d(sV + sl * kTileBytes, &tmap_vb, vfull_bar(sl), 0, 0, 0, q.g, q.b);
+        else tma_load_5d(sV + sl * kTileBytes, &tmap_v, vfull_bar(sl), 0, r.k0 + (t - r.lead_blk) * kBN, 0, q.g, q.b);
     };
     // first wave, before the CTA-wide barrier: every slot of both rings
     if (producer && !pl.idle) {
         const Tiles r = tiles_of(pl);
-        for (int t = r.first_tma; t < min(r.n_tiles, kKSlots); ++t) {
+        for (int t = 0; t < min(r.n_tiles, kKSlots); ++t) {
             issue_k(pl, r, t);
             issue_v(pl, r, t);
         }
@@ -564,16 +573,16 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const bool drafter = p.mode == 1;
     if (tid == 0 && (p.nctx[b] < 1 || p.nctx[b] > p.max_ctx)) set_fault(p.fault, FAULT_BAD_CTX);
     const Tiles tr = tiles_of(pl);
-    const int nb = tr.nb, cend = tr.cend, n_tiles = tr.n_tiles, first_tma = tr.first_tma;
-    const bool has_block_tile = first_tma != 0;
-    auto tile_key0 = [&](int t) { return tr.k0 + (t - first_tma) * kBN; };
+    const int nb = tr.nb, cend = tr.cend, n_tiles = tr.n_tiles, lead_blk = tr.lead_blk;
+    const bool has_block_tile = lead_blk != 0;
+    auto tile_key0 = [&](int t) { return tr.k0 + (t - lead_blk) * kBN; };
     auto is_block_tile = [&](int t) { return has_block_tile && t == 0; };
     // keys every row of the block sees: the drafter's context, the target's
     // cache before the block (before the anchor for a tree)
     const bool tree = p.mode == 2;
     const int all_see = min(cend, tree ? nb - 1 : nb);
     // copies the first wave issued
-    int next_k = max(first_tma, min(n_tiles, kKSlots)), next_v = next_k;
+    int next_k = min(n_tiles, kKSlots), next_v = next_k;
     static_assert(kKSlots == kVSlots, "the first wave fills both rings in step");
     auto issue_k_t = [&](int t) { issue_k(pl, tr, t); };
     auto issue_v_t = [&](int t) { issue_v(pl, tr, t); };
@@ -593,42 +602,6 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
     } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------------ producer
-        if (has_block_tile) {
-            // the T block keys / values from [B, T, Hkv, D] into slot 0 of each ring; rows >= T zero
-            const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(p.kb);
-            const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(p.vb);
-            uint8_t *ks = sbase + L::kOffK, *vs = sbase + L::kOffV;
-            // the T <= 16 rows' loads all in flight first (8 pairs per lane), then the stores
-            constexpr int kBlkIters = kMaxT * 16 / 32;
-            uint4 kv4[kBlkIters], vv4[kBlkIters];
-#pragma unroll
-            for (int it = 0; it < kBlkIters; ++it) {
-                const int idx = lane + 32 * it, row = idx >> 4, ch = idx & 15;
-                kv4[it] = make_uint4(0u, 0u, 0u, 0u);
-                vv4[it] = make_uint4(0u, 0u, 0u, 0u);
-                if (row < T) {
-                    const long off = (((long)b * T + row) * p.Hkv + g) * 128;
-                    kv4[it] = __ldg(reinterpret_cast<const uint4 *>(kb + off) + ch);
-                    vv4[it] = __ldg(reinterpret_cast<const uint4 *>(vb + off) + ch);
-                }
-            }
-#pragma unroll
-            for (int it = 0; it < kBlkIters; ++it) {
-                const int idx = lane + 32 * it, row = idx >> 4, ch = idx & 15;
-                const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
-                *reinterpret_cast<uint4 *>(ks + o) = kv4[it];
-                *reinterpret_cast<uint4 *>(vs + o) = vv4[it];
-            }
-            for (int idx = lane + 32 * kBlkIters; idx < kBN * 16; idx += 32) {   // rows >= 16: zeros
-                const int row = idx >> 4, ch = idx & 15;
-                const uint32_t o = (ch >> 3) * (kBN * 128) + sw128_off(row, ch & 7);
-                *reinterpret_cast<uint4 *>(ks + o) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(vs + o) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) { mbar_arrive(kfull_bar(0)); mbar_arrive(vfull_bar(0)); }
-        }
         if (lane == 0) {
             // whichever ring has a free slot first: a K slot frees when its S has
             // completed, a V slot when its P.V has, so neither waits behind the other
@@ -661,9 +634,9 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // on abort: let the copies already issued land before the CTA exits
             if (*abort_flag) {
                 mbar_wait(qready_bar, 0, nullptr, p.fault);
-                for (int u = max(first_tma, next_k - kKSlots); u < next_k; ++u)
+                for (int u = max(0, next_k - kKSlots); u < next_k; ++u)
                     mbar_wait(kfull_bar(u % kKSlots), (u / kKSlots) & 1, nullptr, p.fault);
-                for (int u = max(first_tma, next_v - kVSlots); u < next_v; ++u)
+                for (int u = max(0, next_v - kVSlots); u < next_v; ++u)
                     mbar_wait(vfull_bar(u % kVSlots), (u / kVSlots) & 1, nullptr, p.fault);
             }
         }
@@ -1060,10 +1033,20 @@ bool make_q_map(CUtensorMap *m, const AttnParams &p) {
 int cache_slots(const AttnParams &p) { return p.mode == 1 ? p.max_ctx : p.max_ctx + p.T - 1; }
 
 cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
-    alignas(64) CUtensorMap mq, mk, mv;
+    alignas(64) CUtensorMap mq, mk, mv, mkb, mvb;
     if (!make_q_map(&mq, p)) return cudaErrorInvalidValue;
     if (!make_map(&mk, p.kc, p.kv, cache_slots(p), p.Hkv, p.B)) return cudaErrorInvalidValue;
     if (!make_map(&mv, p.vc, p.kv, cache_slots(p), p.Hkv, p.B)) return cudaErrorInvalidValue;
+    if (p.mode == 1) {
+        // the drafter's block keys / values [B, T, Hkv, D], contiguous: T slots
+        // per sequence, so a 128-slot box reads rows past T as zeros
+        const sd_strides blk = {(int64_t)p.T * p.Hkv * 128, (int64_t)p.Hkv * 128, 128};
+        if (!make_map(&mkb, p.kb, blk, p.T, p.Hkv, p.B)) return cudaErrorInvalidValue;
+        if (!make_map(&mvb, p.vb, blk, p.T, p.Hkv, p.B)) return cudaErrorInvalidValue;
+    } else {
+        mkb = mk;   // not read
+        mvb = mv;
+    }
     constexpr int smem = Layout::kSmemBytes;
     static std::atomic<bool> opted_in[64];  // per device: shared-memory limit raised
     int dev = 0;
@@ -1094,7 +1077,7 @@ cudaError_t launch_tc(const AttnParams &p, cudaStream_t st) {
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = coop ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, p);
+    return cudaLaunchKernelEx(&cfg, attn_split_tc_kernel, mq, mk, mv, mkb, mvb, p);
 }
 
 }  // namespace
