@@ -244,9 +244,10 @@ __device__ CtaPlan plan_unit(const AttnParams &p) {
 }
 
 // the split's cache keys, from its unit's tiles (one global load)
-__device__ void plan_keys(const AttnParams &p, CtaPlan &pl) {
+// ctx_b: ctx_len of the CTA's sequence, loaded by the caller
+__device__ void plan_keys(const AttnParams &p, CtaPlan &pl, int ctx_b) {
     const int lead = p.mode == 1 ? 1 : 0;
-    pl.nb = max(1, min(p.nctx[pl.b], p.max_ctx));
+    pl.nb = max(1, min(ctx_b, p.max_ctx));
     if (pl.tiles == 0) pl.tiles = ((p.mode == 1 ? pl.nb : pl.nb + p.T - 1) + kBN - 1) / kBN + lead;  // < 2^24
     const int tiles = pl.tiles;
     const int a = pl.s * tiles / pl.n, e = (pl.s + 1) * tiles / pl.n;               // products < 2^31
@@ -504,6 +505,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     CtaPlan pl = {};
     if (warp == kProducerWarp) {
         pl = plan_unit(p);
+        // the sequence's length, loaded ahead of the Q copy so that the two overlap
+        const int ctx_b = pl.idle ? 1 : p.nctx[pl.b];
         if (producer && !pl.idle) {
             // Q first: rows r = (j - j0)*G + hl of this kv head, two 64-column halves;
             // the copy always moves the whole box (out-of-range rows are zero-filled)
@@ -511,7 +514,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tma_load_4d(sQ, &tmap_q, qready_bar, 0, pl.g * G, pl.mb * p.mblk_nodes, pl.b);
             tma_load_4d(sQ + 128 * 128, &tmap_q, qready_bar, 64, pl.g * G, pl.mb * p.mblk_nodes, pl.b);
         }
-        if (!pl.idle) plan_keys(p, pl);
+        if (!pl.idle) plan_keys(p, pl, ctx_b);
         if (lane == 0) *plan_sh = pl;
     }
     // a split's tiles: the cache keys [k0, cend) of its sequence, after the
