@@ -1125,6 +1125,20 @@ def main():
             "chain16_blocks_per_s": 1.0 / (k["us_per_call_back_to_back"] * 1e-6 +
                                            kernels["accept_greedy"]["us_per_call"] * 1e-6),
         })
+        # the same per-call times in SM cycles at the median clock sampled
+        # during the timed step, so that a change can be judged when the
+        # clock differs between runs
+        if clocks and clocks.get("sm_mhz"):
+            mhz = float(clocks["sm_mhz"])
+            roofline["kcycles_at_sampled_clock"] = {
+                "sm_mhz": mhz,
+                "step": ms_per_step * 1e3 * mhz / 1e3,
+                "cfg2_verify": k["us_per_call_back_to_back"] * mhz / 1e3,
+                "cfg5_verify": t5 * 1e6 * mhz / 1e3,
+                "draft_l234": t_l234 * 1e6 * mhz / 1e3,
+                "accept_greedy_b8": tg8 * 1e6 * mhz / 1e3,
+                "accept_sample_b4": ts4 * 1e6 * mhz / 1e3,
+            }
         roofline["acceptance_back_to_back"] = dict(acceptance, note=(
             "acceptance kernels at the batched workloads (greedy over 8 sequences' logits, the sampled rule "
             "over 4; 4 input copies) and for one sequence (32 copies), calls issued back to back in one "

@@ -292,11 +292,20 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
     // every thread's partial (the bulk copies each thread waited for, the
     // log-sum-exps) for whoever acquires the count
     __syncthreads();
+    // every split takes a second ticket once its wait is over, whether or not
+    // it succeeded, so the counter sees exactly 2n increments per launch and
+    // the split holding the last of them returns it to zero (no split reads
+    // it any more by then): a launch whose wait gave up (fault bit set, its
+    // rows left unmerged) still leaves the workspace ready for the next call.
+    // The ticket goes out now and its value is used only when the split ends,
+    // so its round trip overlaps the merge.
+    unsigned int ticket = 0u;
     if (tid == 0) {
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
         const bool ok = wait_count(ctr, (unsigned int)n + p.wt.extra, p.wt.limit_ns);
         if (!ok) set_fault(p.fault, FAULT_WAIT_TIMEOUT);
         *go = ok ? 1 : 0;
+        ticket = atomicAdd(ctr, 1u);
     }
     __syncthreads();
     const int R = s < M ? (M - s + n - 1) / n : 0;   // rows of this split
@@ -421,15 +430,7 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
     }
-    // every split takes a second ticket, whether or not its wait succeeded, so
-    // the counter sees exactly 2n increments per launch and the last of them
-    // returns it to zero: a launch whose wait gave up (fault bit set, its rows
-    // left unmerged) still leaves the workspace ready for the next call
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned int ticket = atomicAdd(ctr, 1u);
-        if (ticket == 2u * (unsigned int)n - 1u) atomicExch(ctr, 0u);
-    }
+    if (tid == 0 && ticket == 2u * (unsigned int)n - 1u) atomicExch(ctr, 0u);
 }
 
 // ---------------------------------------------------------------------------
