@@ -992,11 +992,15 @@ __global__ void __launch_bounds__(kAccThreads) sample_draw_kernel(const SamplePa
 
 // A barrier of `n` CTAs on two counters: thread 0 arrives (a release
 // reduction, after the CTA's writes) and waits, bounded in time, for the count
-// to reach n (acquire loads); each CTA departs once, at its end, and the n-th
-// departure returns both counters to zero -- every CTA has stopped reading
-// them by then, whether or not its wait gave up.  The whole CTA calls the
-// wait; false (and the fault bit) if it gave up.
-__device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int n, const WaitTest &wt, unsigned int *fault) {
+// to reach n (acquire loads).  Once its wait is over, whether or not it
+// succeeded, thread 0 takes a departure ticket on `dep`; the CTA holding ticket
+// n - 1 (every CTA has passed the wait by then, so none reads the counters any
+// more) returns both counters to zero when it ends (barrier_reset).  The
+// ticket goes out right after the wait and is read only at the end, so its
+// round trip overlaps the CTA's work.  The whole CTA calls the wait; false
+// (and the fault bit) if it gave up.
+__device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int *dep, unsigned int n, const WaitTest &wt,
+                                    unsigned int *fault, unsigned int &ticket) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1012,14 +1016,14 @@ __device__ bool barrier_arrive_wait(unsigned int *ctr, unsigned int n, const Wai
         }
         if (!ok) set_fault(fault, FAULT_WAIT_TIMEOUT);
         s_ok = ok;
+        ticket = atomicAdd(dep, 1u);
     }
     __syncthreads();
     return s_ok != 0;
 }
-__device__ __forceinline__ void barrier_depart(unsigned int *arrive, unsigned int *depart, unsigned int n) {
-    if (threadIdx.x == 0) {
-        if (atomicAdd(depart, 1u) == n - 1) { *arrive = 0u; *depart = 0u; }
-    }
+__device__ __forceinline__ void barrier_reset(unsigned int *arrive, unsigned int *dep, unsigned int n,
+                                              unsigned int ticket) {
+    if (threadIdx.x == 0 && ticket == n - 1) { *arrive = 0u; *dep = 0u; }
 }
 
 // two block-wide maxima at once; results valid in every thread
@@ -1251,8 +1255,9 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
     }
 
     // every segment's partials are in (a grid barrier)
-    barrier_arrive_wait(p.counters + 1, C, p.wt, p.fault);
-    auto depart = [&]() { barrier_depart(p.counters + 1, p.counters + 2, C); };
+    unsigned int grid_ticket = 0u, seq_ticket = 0u;
+    barrier_arrive_wait(p.counters + 1, p.counters + 2, C, p.wt, p.fault, grid_ticket);
+    auto depart = [&]() { barrier_reset(p.counters + 1, p.counters + 2, C, grid_ticket); };
     const int b = blockIdx.x / p.n_fchunks, k = blockIdx.x % p.n_fchunks;
     if (b >= p.B) {
         depart();
@@ -1376,7 +1381,8 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
     __shared__ FF s_excl[kAccThreads];
     if (tid == 0) { s_found = INT_MAX; s_lastpos = -1; }
     // ---- 4. every chunk sum of the sequence is in (a barrier of its CTAs)
-    barrier_arrive_wait(p.row_counter + b, (unsigned int)p.n_fchunks, p.wt, p.fault);
+    barrier_arrive_wait(p.row_counter + b, p.row_counter + p.B + b, (unsigned int)p.n_fchunks, p.wt, p.fault,
+                        seq_ticket);
     FF vres = FF{0.f, 0.f}, vp = FF{0.f, 0.f};
     if (tid < p.n_fchunks) {
         const float4 t = __ldcg(p.fs + (long)b * p.n_fchunks + tid);
@@ -1406,7 +1412,7 @@ __global__ void __launch_bounds__(kAccThreads, kSampleFusedPerSm) sample_fused_k
         const int id = search_chunk<Tin, NV>(sr, qs, lg, qn, clo, chi, it, M, Z, res, xl);
         if (tid == 0) p.next_id[b] = id;
     }
-    barrier_depart(p.row_counter + b, p.row_counter + p.B + b, (unsigned int)p.n_fchunks);
+    barrier_reset(p.row_counter + b, p.row_counter + p.B + b, (unsigned int)p.n_fchunks, seq_ticket);
     depart();
 }
 
