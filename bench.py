@@ -1256,17 +1256,18 @@ def e2e_pass(S, host, ds, device, stream, steps):
 
     def body():
         cur = torch.cuda.current_stream()
-        # what the drafter layers read goes first on the main stream; the
-        # block's own K/V slots (read from the verify on) and the acceptance
-        # inputs (target logits, draft ids and probabilities: 14.6 of the
-        # 15.3 MB) travel on a side stream while the drafter layers run, and
-        # join before the verify call
+        # what the attention calls read goes first, alone, on the main stream;
+        # then the block's own K/V slots (read from the verify on) and the
+        # acceptance inputs (target logits, draft ids and probabilities: 14.6
+        # of the 15.3 MB) travel on a side stream while the drafter layers
+        # run, and join before the verify call.  The side copies start after
+        # the first one: started together, they slow it down
+        d_att.copy_(h_att, non_blocking=True)
         side.wait_stream(cur)
         with torch.cuda.stream(side):
             ds.k[:, CTX - 1:CTX + T - 1].copy_(h_blk_k, non_blocking=True)
             ds.v[:, CTX - 1:CTX + T - 1].copy_(h_blk_v, non_blocking=True)
             d_acc.copy_(h_acc, non_blocking=True)
-        d_att.copy_(h_att, non_blocking=True)
         run_step(S, e2, stream, ("draft",))
         cur.wait_stream(side)
         run_step(S, e2, stream, ("verify", "greedy", "sample"))
@@ -1306,7 +1307,8 @@ def e2e_pass(S, host, ds, device, stream, steps):
             "steps": steps, "eager_value": steps / sec_eager,
             "note": "per-block inputs from pinned host memory (two packed buffers plus the block's K/V slots), "
                     "results read back every step with one copy, the host waiting for them; the block's K/V "
-                    "slots and the acceptance inputs copied on a side stream while the drafter layers run; "
+                    "slots and the acceptance inputs copied on a side stream while the drafter layers run, "
+                    "after the attention inputs' copy; "
                     "the step (copies and C-ABI calls) replayed "
                     "from one CUDA graph (eager_value: the same step issued call by call from Python); context "
                     "K/V resident"}
