@@ -243,8 +243,8 @@ __device__ CtaPlan plan_unit(const AttnParams &p) {
     return pl;
 }
 
-// the split's cache keys, from its unit's tiles (one global load)
-// ctx_b: ctx_len of the CTA's sequence, loaded by the caller
+// the split's cache keys, from its unit's tiles; ctx_b: ctx_len of the CTA's
+// sequence, loaded by the caller
 __device__ void plan_keys(const AttnParams &p, CtaPlan &pl, int ctx_b) {
     const int lead = p.mode == 1 ? 1 : 0;
     pl.nb = max(1, min(ctx_b, p.max_ctx));
