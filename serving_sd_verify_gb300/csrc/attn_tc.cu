@@ -498,9 +498,9 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
 
-    // the plan: warp 0 works it out, and its lane 0 starts the Q copy and the
-    // first K/V copies before the CTA-wide barrier; the other warps read the
-    // plan after it
+    // the plan: warp 0 works it out, its lane 0 starts the Q copy and its
+    // lanes the first K/V copies before the CTA-wide barrier; the other warps
+    // read the plan after it
     const int T = p.T, G = p.Hq / p.Hkv;
     const int MQ = G * p.mblk_nodes;  // rows the Q copy writes (those past block row T - 1 as zeros)
     CtaPlan pl = {};
@@ -548,13 +548,13 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         if (t < r.lead_blk) tma_load_5d(sV + sl * kTileBytes, &tmap_vb, vfull_bar(sl), 0, 0, 0, q.g, q.b);
         else tma_load_5d(sV + sl * kTileBytes, &tmap_v, vfull_bar(sl), 0, r.k0 + (t - r.lead_blk) * kBN, 0, q.g, q.b);
     };
-    // first wave, before the CTA-wide barrier: every slot of both rings
-    if (producer && !pl.idle) {
+    // first wave, before the CTA-wide barrier: every slot of both rings, one
+    // copy per lane of the producer warp (issued together, not one by one)
+    if (warp == kProducerWarp && !pl.idle) {
         const Tiles r = tiles_of(pl);
-        for (int t = 0; t < min(r.n_tiles, kKSlots); ++t) {
-            issue_k(pl, r, t);
-            issue_v(pl, r, t);
-        }
+        const int w = min(r.n_tiles, kKSlots);
+        if (lane < w) issue_k(pl, r, lane);
+        else if (lane >= 8 && lane - 8 < w) issue_v(pl, r, lane - 8);
     }
     tc_fence_before();
     __syncthreads();
