@@ -1012,6 +1012,13 @@ def main():
         for n in (3, 5):
             per_config[n] = config_verify_pass(S, device, stream, n)
         per_config["draft"] = drafter_layer_pass(S, sets[0], stream, flush)
+        # the four layers back to back in one graph, as inside the step (the
+        # projected context stays in L2 after the first layer)
+        ds0 = sets[0]
+        per_config["draft_b2b"] = time_back_to_back(
+            [(lambda L=L, li=li: S.sd_draft_block_attention(L[0], ds0.kc, ds0.vc, ds0.nctx, CTX, L[1], L[2],
+                                                            ds0.dout[li], 1.0, ds0.ws_d, stream))
+             for li, L in enumerate(ds0.layers)], LAYERS, stream)
         per_config["tree60"] = tree60_pass(S, device, stream)
         tpk, tsrc = bf16_peak(sustained=False)
         kp = kernels["project_prefill"]
@@ -1115,6 +1122,8 @@ def main():
             "draft_l1_us": t_l1 * 1e6, "draft_l1_frac": BYTES["draft_attention"] / t_l1 / 1e9 / peak,
             "draft_l234_us": t_l234 * 1e6,
             "draft_l234_tensor_frac": draft_flops / t_l234 / 1e12 / tpk_,
+            "draft_layer_us_back_to_back": per_config["draft_b2b"] * 1e6,
+            "draft_layer_tensor_frac_back_to_back": draft_flops / per_config["draft_b2b"] / 1e12 / tpk_,
             "cfg4_draft_blocks_per_s": 1.0 / (t_l1 + (LAYERS - 1) * t_l234),
         })
         t_tv, t_ta, b_tv, b_ta = per_config["tree60"]
