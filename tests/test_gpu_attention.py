@@ -194,6 +194,8 @@ DRAFT_CASES = [
     (1, 16, 4, 1, 64, [300], torch.float32),
     (2, 3, 8, 2, 128, [64, 129], torch.bfloat16),
     (1, 16, 32, 2, 128, [500], torch.bfloat16),   # G*T = 256: two row blocks
+    (1, 1, 28, 4, 128, [300], torch.bfloat16),    # T = 1: a block tile of one row (the copy zero-fills the rest)
+    (3, 16, 28, 4, 128, [10, 2000, 129], torch.bfloat16),  # ragged: the block tile leads each unit's first split
 ]
 
 
