@@ -21,8 +21,11 @@
 // Warp roles (384 threads):
 //   warp 0           TMA producer: Q, then K tiles and V tiles into rings of
 //                    three 32 KB slots each
-//   warp 1           allocates tensor memory; one thread issues every MMA: S
-//                    up to three tiles ahead, and P.V as soon as its P is written
+//   warp 1           allocates tensor memory; one thread issues the S MMAs,
+//                    up to three tiles ahead
+//   warp 2           one thread issues each P.V as soon as its P and V are in
+//                    (two issuing threads, so that neither waits behind the
+//                    other's MMAs: an MMA issue blocks while the pipe is busy)
 //   warps 4-7, 8-11  two softmax warpgroups, both on every tile: warpgroup w
 //                    takes keys [64 w, 64 w + 64) of it; thread = row (=
 //                    tensor-memory lane).  They exchange the row max through
@@ -60,7 +63,8 @@ namespace {
 
 constexpr int kTcThreads = 384;
 constexpr int kProducerWarp = 0;            // TMA producer
-constexpr int kMmaWarp = 1;                 // tensor-memory allocation, MMA issue
+constexpr int kMmaWarp = 1;                 // tensor-memory allocation, S issue
+constexpr int kPvWarp = 2;                  // P.V issue
 constexpr int kSoftmaxWarp0 = 4;            // warps 4-7 and 8-11: the two softmax warpgroups
 constexpr int kBN = kTcTileKeys;            // keys per tile (128)
 constexpr int kTileBytes = 2 * kBN * 128;   // K or V tile: two 64-column blocks of [128 keys x 128 B]
@@ -646,7 +650,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------------ S issuer
         // Q rows past the MQ the copy writes are zero, so the padding rows of S
         // are finite (the copy itself zero-fills rows [M, MQ))
         for (int idx = lane; idx < (128 - MQ) * 16; idx += 32) {
@@ -657,19 +661,20 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+            // S(ns) into S/P buffer ns % 3 as soon as its keys have landed and
+            // P.V(ns - 3) has read the buffer: S runs up to three tiles ahead.
+            // S and P.V go out from two threads, each waiting only for its own
+            // inputs: one thread issuing both held every P.V behind the next S
+            // (an MMA issue blocks while the tensor pipe is busy), and with it
+            // the V slot the P.V frees
             const uint32_t idS = idesc_bf16(128, kBN, false);
-            const uint32_t idO = idesc_bf16(128, 128, true);
             bool ok = mbar_wait(qready_bar, 0, abort_flag, p.fault);
-            // S runs up to kSP tiles ahead of P.V; whichever of the next S and
-            // the next P.V can go is issued, S first: the tensor pipe runs its
-            // MMAs in issue order, and the softmax waits for the next S, while a
-            // P.V only has to complete before its buffers are reused
-            int ns = 0, npv = 0;
             unsigned long long t_last = global_timer();
-            for (uint32_t spin = 0; ok && npv < n_tiles;) {
-                if (ns < n_tiles && ns < npv + kSP && mbar_test(kfull_bar(ns % kKSlots), (ns / kKSlots) & 1) &&
+            int next_s = 0;
+            for (uint32_t spin = 0; ok && next_s < n_tiles;) {
+                const int ns = next_s;
+                if (mbar_test(kfull_bar(ns % kKSlots), (ns / kKSlots) & 1) &&
                     (ns < kSP || mbar_test(pempty_bar(ns % kSP), ((ns / kSP) - 1) & 1))) {
-                    // S(ns) into buffer ns % 3, free once P.V(ns - 3) has read it
                     tc_fence_after();
                     const uint32_t kb = sK + (ns % kKSlots) * kTileBytes;
 #pragma unroll
@@ -681,11 +686,33 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     }
                     umma_commit(sfull_bar(ns % kSP));
                     umma_commit(kempty_bar(ns % kKSlots));
-                    ++ns;
+                    ++next_s;
                     t_last = global_timer();
                     continue;
                 }
-                if (npv < ns && mbar_test(pfull_bar(npv % kSP), (npv / kSP) & 1) &&
+                // nothing ready yet: back off (see the producer), bounded
+                __nanosleep(32);
+                if ((++spin & 15u) == 0) {
+                    if (*abort_flag) ok = false;
+                    else if (global_timer() - t_last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        set_fault(p.fault, FAULT_WAIT_TIMEOUT);
+                        ok = false;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            const uint32_t idO = idesc_bf16(128, 128, true);
+            bool ok = true;
+            unsigned long long t_last = global_timer();
+            int next_pv = 0;
+            for (uint32_t spin = 0; ok && next_pv < n_tiles;) {
+                const int npv = next_pv;
+                if (mbar_test(pfull_bar(npv % kSP), (npv / kSP) & 1) &&
                     mbar_test(vfull_bar(npv % kVSlots), (npv / kVSlots) & 1)) {
                     // P.V(npv): O += P_hi . V (+ P_lo . V when the softmax warps asked
                     // for the two-term P) over the 128 keys
@@ -703,11 +730,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     }
                     umma_commit(pempty_bar(npv % kSP));
                     umma_commit(vempty_bar(npv % kVSlots));
-                    ++npv;
+                    ++next_pv;
                     t_last = global_timer();
                     continue;
                 }
-                // nothing ready yet: back off (see the producer), bounded
                 __nanosleep(32);
                 if ((++spin & 15u) == 0) {
                     if (*abort_flag) ok = false;
@@ -718,7 +744,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     }
                 }
             }
-            // every MMA has completed before tensor memory is freed
+            // every MMA has completed before tensor memory is freed: the last
+            // P.V follows every S (its P needed S), and this thread issued it
             umma_commit(drain_bar);
             mbar_wait(drain_bar, 0, nullptr, p.fault);
         }
@@ -812,7 +839,7 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // where a row's largest weight, in the reference of the tiles before,
             // exceeds kLoFrac of that row's running sum; the vote of all rows is
             // one flag, read after the barrier by every softmax warp and, after
-            // the P arrival, by the MMA issuer
+            // the P arrival, by the P.V issuer
             const bool vote = t == 0 || (row_ok && !(ex2(hmax * qk - m_used) <= kLoFrac * l));
             if (__any_sync(0xffffffffu, vote) && lane == 0) lo_flag[bi] = t + 1;
             xrow[wg * 128 + r] = hmax;
