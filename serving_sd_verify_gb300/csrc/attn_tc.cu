@@ -875,7 +875,11 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const bool live = m_used != -INFINITY;
             const float neg_m = live ? -m_used : 0.f;
             if (!live) vis = 0ull;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            // packed fp32 pairs (one instruction for two lanes' worth of FMA or
+            // add): the argument of each exponential pair, and two pairs of
+            // partial sums
+            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            const float2 qk2 = make_float2(qk, qk), nm2 = make_float2(neg_m, neg_m);
             // the masked keys of an edge tile are cleared in the scores first
             // (-inf gives a weight of 0), so the exponential loop has no selects
             if (!whole || !live) {
@@ -896,9 +900,10 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     uint32_t pk[16], pl[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
-                        ls[c & 3] += p0 + p1;
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sq[2 * c]),
+                                                                __uint_as_float(sq[2 * c + 1])), qk2, nm2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        ls2[c & 1] = __fadd2_rn(ls2[c & 1], make_float2(p0, p1));
                         const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
                         pk[c] = __byte_perm(b0, b1, 0x7632);
                         const uint32_t q0 = __float_as_uint(p0 - __uint_as_float(b0 & 0xffff0000u));
@@ -919,17 +924,19 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sq[2 * c]), qk, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(sq[2 * c + 1]), qk, neg_m));
+                        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sq[2 * c]),
+                                                                __uint_as_float(sq[2 * c + 1])), qk2, nm2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
                         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);   // .x = p0 in the low half
                         const uint32_t h = *reinterpret_cast<const uint32_t *>(&h2);
                         pk[c] = h;
-                        ls[c & 3] += __uint_as_float(h << 16) + __uint_as_float(h & 0xffff0000u);
+                        ls2[c & 1] = __fadd2_rn(ls2[c & 1], make_float2(__uint_as_float(h << 16),
+                                                                        __uint_as_float(h & 0xffff0000u)));
                     }
                     tmem_st16(sp_col + 16u * q, pk);
                 }
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l += (ls2[0].x + ls2[1].x) + (ls2[0].y + ls2[1].y);
             // value rows past the split's last cache key may hold anything (P is
             // zero there, but 0 * NaN is not): each warpgroup zeroes those of
             // its key half once V(t) has landed
