@@ -552,11 +552,14 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         if (t < r.lead_blk) tma_load_5d(sV + sl * kTileBytes, &tmap_vb, vfull_bar(sl), 0, 0, 0, q.g, q.b);
         else tma_load_5d(sV + sl * kTileBytes, &tmap_v, vfull_bar(sl), 0, r.k0 + (t - r.lead_blk) * kBN, 0, q.g, q.b);
     };
-    // first wave, before the CTA-wide barrier: every slot of both rings, one
-    // copy per lane of the producer warp (issued together, not one by one)
+    // first wave, before the CTA-wide barrier: the first tile's K and V, one
+    // copy per lane of the producer warp; the other slots fill after the
+    // barrier (every CTA's first tile then comes back ahead of the rest of
+    // the grid's second and third)
+    constexpr int kFirstWave = 1;
     if (warp == kProducerWarp && !pl.idle) {
         const Tiles r = tiles_of(pl);
-        const int w = min(r.n_tiles, kKSlots);
+        const int w = min(r.n_tiles, kFirstWave);
         if (lane < w) issue_k(pl, r, lane);
         else if (lane >= 8 && lane - 8 < w) issue_v(pl, r, lane - 8);
     }
@@ -590,8 +593,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const bool tree = p.mode == 2;
     const int all_see = min(cend, tree ? nb - 1 : nb);
     // copies the first wave issued
-    int next_k = min(n_tiles, kKSlots), next_v = next_k;
-    static_assert(kKSlots == kVSlots, "the first wave fills both rings in step");
+    int next_k = min(n_tiles, kFirstWave), next_v = next_k;
+    static_assert(kFirstWave <= kKSlots && kFirstWave <= kVSlots, "the first wave fits both rings");
     auto issue_k_t = [&](int t) { issue_k(pl, tr, t); };
     auto issue_v_t = [&](int t) { issue_v(pl, tr, t); };
 
