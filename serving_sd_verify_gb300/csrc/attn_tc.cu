@@ -693,8 +693,8 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     t_last = global_timer();
                     continue;
                 }
-                // nothing ready yet: back off (see the producer), bounded
-                __nanosleep(32);
+                // nothing ready yet: poll again (the bound below still holds); a
+                // back-off here only delays the reaction, the poll costs little
                 if ((++spin & 15u) == 0) {
                     if (*abort_flag) ok = false;
                     else if (global_timer() - t_last > kWaitLimitNs) {
@@ -737,7 +737,6 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     t_last = global_timer();
                     continue;
                 }
-                __nanosleep(32);
                 if ((++spin & 15u) == 0) {
                     if (*abort_flag) ok = false;
                     else if (global_timer() - t_last > kWaitLimitNs) {
@@ -965,17 +964,19 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             if (lane == 0) mbar_arrive(pfull_bar(bi));
         }
         // ---- epilogue: normalise O, write this split's partial (or the output) ----
+        // the row sum first (it needs no MMA), then the wait for the last P.V
+        named_sync(1, 256);
+        xrow[wg * 128 + r] = l;
+        named_sync(1, 256);
         const int last_t = n_tiles - 1;
         ok = __all_sync(0xffffffffu,
                         mbar_wait(pempty_bar(last_t % kSP), (last_t / kSP) & 1, abort_flag, p.fault)) && ok;
-        if (!ok) { m_used = -INFINITY; l = 0.f; }
+        float Lsum = wg == 0 ? l + xrow[128 + r] : xrow[r] + l;  // same order in both
+        if (!ok) { m_used = -INFINITY; l = 0.f; Lsum = 0.f; }
         tc_fence_before();
         // the last P.V, hence every MMA (and every copy they read), is complete
         // past this point: the rings are free for the staging
         named_sync(1, 256);
-        xrow[wg * 128 + r] = l;
-        named_sync(1, 256);
-        const float Lsum = wg == 0 ? l + xrow[128 + r] : xrow[r] + l;  // same order in both
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         const bool abort_seen = *abort_flag != 0;
         // stage the normalised rows in shared memory; warpgroup wg fills output
