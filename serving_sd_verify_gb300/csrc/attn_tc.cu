@@ -345,7 +345,9 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
 #pragma unroll
                     for (int e = 0; e < kMergeSmall; ++e) {
                         const long prow = (long)(pl.slot0 + min(sp0 + e, sp1 - 1)) * 128 + s + ri * n;
-                        v[q][e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + prow * 128) + c4);
+                        v[q][e] = live && sp0 + e < sp1
+                                      ? __ldcg(reinterpret_cast<const float4 *>(p.o_part + prow * 128) + c4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                         l[q][e] = live && sp0 + e < sp1 ? __ldcg(p.lse_part + prow) : -INFINITY;
                     }
                 }
@@ -379,14 +381,17 @@ __device__ void merge_group(const AttnParams &p, const CtaPlan &pl, int j0, int 
             float m_run = -INFINITY, w_run = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int sb = sp0; sb < sp1; sb += kMergeBatch) {
-                // branch-free, so that the batch's loads are all in flight at
-                // once: past the chunk's end, re-read its last split and drop it
+                // every load of the batch is issued before any is used, so
+                // that all are in flight at once; past the chunk's end the
+                // loads are predicated off (no traffic) and the entry carries
+                // weight zero
                 float4 v[kMergeBatch];
                 float l[kMergeBatch];
 #pragma unroll
                 for (int e = 0; e < kMergeBatch; ++e) {
                     const long prow = (long)(pl.slot0 + min(sb + e, sp1 - 1)) * 128 + s + ri * n;  // slot, row
-                    v[e] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + prow * 128) + c4);
+                    v[e] = sb + e < sp1 ? __ldcg(reinterpret_cast<const float4 *>(p.o_part + prow * 128) + c4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                     l[e] = sb + e < sp1 ? __ldcg(p.lse_part + prow) : -INFINITY;
                 }
                 float bm = l[0];
