@@ -108,9 +108,10 @@ struct Layout {
 // unit) and gets n_u = ceil(tiles_u / L) splits, L the smallest load for which
 // sum n_u fits the C slots, so long sequences get more CTAs than short ones and
 // no CTA takes more than L tiles; split s of n takes tiles
-// [s tiles / n, (s + 1) tiles / n).  A unit's CTAs are consecutive: slot0 is
-// its first, and its partial slots are slot0 .. slot0 + n - 1.  CTAs past
-// sum n_u are idle.  Every CTA derives the same plan from ctx_len, so no plan
+// [ceil(s tiles / n), ceil((s + 1) tiles / n)), so that the shorter shares fall
+// to the last splits, the last of which holds the masked edge tile.  A unit's
+// CTAs are consecutive: slot0 is its first, and its partial slots are
+// slot0 .. slot0 + n - 1.  CTAs past sum n_u are idle.  Every CTA derives the same plan from ctx_len, so no plan
 // crosses the host.  With more units than kPlanUnits the grid holds one CTA
 // per unit.
 constexpr int kPlanUnits = 5 * 32;   // units a warp plans with its lanes' registers
@@ -254,7 +255,8 @@ __device__ void plan_keys(const AttnParams &p, CtaPlan &pl, int ctx_b) {
     pl.nb = max(1, min(ctx_b, p.max_ctx));
     if (pl.tiles == 0) pl.tiles = ((p.mode == 1 ? pl.nb : pl.nb + p.T - 1) + kBN - 1) / kBN + lead;  // < 2^24
     const int tiles = pl.tiles;
-    const int a = pl.s * tiles / pl.n, e = (pl.s + 1) * tiles / pl.n;               // products < 2^31
+    const int a = (pl.s * tiles + pl.n - 1) / pl.n;                                 // products < 2^31
+    const int e = ((pl.s + 1) * tiles + pl.n - 1) / pl.n;
     pl.k0 = max(0, a - lead) * kBN;
     pl.k1 = max(0, e - lead) * kBN;
     pl.block_tile = lead && a == 0 && e > 0;   // an empty split [0, 0) takes nothing
