@@ -328,6 +328,21 @@ sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const 
                              const int32_t *path, const int32_t *n_accepted, int B, int T,
                              int max_slots, int Hkv, int D, sd_dtype dtype, void *stream);
 
+/* The results a serving loop reads on the host each cycle (accepted counts and
+ * next ids, the verified rows), stored into pinned host memory by the GPU's
+ * own cores, after the stream's earlier work: for a few hundred KB this ends
+ * sooner than a copy-engine transfer, whose set-up dominates at that size.
+ * Once the stream's work up to this call has completed (an event or stream
+ * synchronisation), host_dst[0, bytes) holds src[0, bytes).
+ *   host_dst  pinned host memory (cudaHostAlloc, or cudaHostRegister'd), read
+ *             by the host only after that synchronisation
+ *   src       device memory
+ *   bytes     a multiple of 16; both addresses 16-byte aligned; the caller
+ *             keeps both ranges inside their allocations
+ * Returns SD_ERR_INVALID_ARG (nothing enqueued) when host_dst is not pinned
+ * host memory, src is not device memory, or the sizes are misaligned. */
+sd_status sd_store_to_host(void *host_dst, const void *src, int64_t bytes, void *stream);
+
 /* The drafter's context append for the committed rows (the incremental
  * append of sd_project_kv with the row count on the device): for r = 0..n
  * (n = n_accepted[b]), hidden row src = 0 (the anchor) or r (chain) or

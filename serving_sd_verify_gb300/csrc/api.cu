@@ -745,6 +745,32 @@ sd_status sd_compact_tree_kv(void *k_cache, void *v_cache, sd_strides kv, const 
     return SD_OK;
 }
 
+sd_status sd_store_to_host(void *host_dst, const void *src, int64_t bytes, void *stream) {
+    if (bytes < 0) return fail(SD_ERR_INVALID_ARG, "bytes must be >= 0");
+    if (bytes == 0) return SD_OK;
+    if (!host_dst || !src) return fail(SD_ERR_INVALID_ARG, "null pointer");
+    if (bytes % 16 != 0 || !aligned16(host_dst) || !aligned16(src))
+        return fail(SD_ERR_INVALID_ARG, "bytes and both addresses must be multiples of 16");
+    cudaPointerAttributes ad = {}, as = {};
+    if (cudaPointerGetAttributes(&ad, host_dst) != cudaSuccess || ad.type != cudaMemoryTypeHost ||
+        !ad.devicePointer) {
+        (void)cudaGetLastError();
+        return fail(SD_ERR_INVALID_ARG, "host_dst must be pinned host memory (cudaHostAlloc / cudaHostRegister)");
+    }
+    if (cudaPointerGetAttributes(&as, src) != cudaSuccess ||
+        (as.type != cudaMemoryTypeDevice && as.type != cudaMemoryTypeManaged)) {
+        (void)cudaGetLastError();
+        return fail(SD_ERR_INVALID_ARG, "src must be device memory");
+    }
+    HostStoreParams p = {};
+    p.src = static_cast<const uint4 *>(src);
+    p.dst = static_cast<uint4 *>(ad.devicePointer);
+    p.n16 = bytes / 16;
+    cudaError_t e = launch_store_to_host(p, device_sm_count(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "host store launch");
+    return SD_OK;
+}
+
 namespace {
 struct LatentLayout {
     int n_splits, ksteps;

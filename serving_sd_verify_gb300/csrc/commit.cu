@@ -10,6 +10,8 @@
 // overwrites the rejected slots once ctx_len has moved past the kept ones.
 // A tree keeps a root path whose nodes sit at scattered block slots, so
 // their K/V rows are first moved to consecutive positions.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace sdv {
@@ -108,6 +110,21 @@ __global__ void __launch_bounds__(kCompactThreads) compact_tree_kv_kernel(const 
     }
 }
 
+// A grid-stride copy of 16-byte vectors.  The stores cross the chip-to-host
+// link one by one, so a handful of CTAs per SM keep enough of them in flight;
+// for the few hundred KB of a step's results this ends sooner than a
+// copy-engine transfer, whose set-up dominates at that size.
+constexpr int kStoreThreads = 256;
+constexpr int kStoreCtasPerSm = 4;
+__global__ void __launch_bounds__(kStoreThreads) store_to_host_kernel(const HostStoreParams p) {
+#if __CUDA_ARCH__ >= 900
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the results of the kernels before
+#endif
+    const int64_t stride = (int64_t)gridDim.x * kStoreThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kStoreThreads + threadIdx.x; i < p.n16; i += stride)
+        p.dst[i] = __ldcg(p.src + i);
+}
+
 template <typename K, typename P>
 cudaError_t launch_pdl_cm(K kern, dim3 grid, dim3 block, cudaStream_t st, const P &args) {
     cudaLaunchConfig_t cfg = {};
@@ -128,6 +145,12 @@ cudaError_t launch_pdl_cm(K kern, dim3 grid, dim3 block, cudaStream_t st, const 
 cudaError_t launch_commit_tokens(const CommitParams &p, cudaStream_t st) {
     const dim3 grid((unsigned)((p.B + kCommitWarps - 1) / kCommitWarps));
     return launch_pdl_cm(commit_tokens_kernel, grid, dim3(kCommitWarps * 32), st, p);
+}
+
+cudaError_t launch_store_to_host(const HostStoreParams &p, int sm_count, cudaStream_t st) {
+    const int64_t need = (p.n16 + kStoreThreads - 1) / kStoreThreads;
+    const int64_t cap = (int64_t)std::max(1, sm_count) * kStoreCtasPerSm;
+    return launch_pdl_cm(store_to_host_kernel, dim3((unsigned)std::min(need, cap)), dim3(kStoreThreads), st, p);
 }
 
 cudaError_t launch_compact_tree_kv(const CompactParams &p, cudaStream_t st) {

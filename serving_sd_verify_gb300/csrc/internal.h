@@ -188,6 +188,15 @@ struct CommitParams {
 };
 cudaError_t launch_commit_tokens(const CommitParams &p, cudaStream_t st);
 
+// Results into pinned host memory by SM stores (16-byte vectors), through the
+// host buffer's device-visible address.
+struct HostStoreParams {
+    const uint4 *src;               // device memory
+    uint4 *dst;                     // device-visible address of pinned host memory
+    int64_t n16;                    // 16-byte vectors
+};
+cudaError_t launch_store_to_host(const HostStoreParams &p, int sm_count, cudaStream_t st);
+
 struct CompactParams {
     void *kc, *vc;                  // [B, S, Hkv, D] with strides kv (elements)
     sd_strides kv;

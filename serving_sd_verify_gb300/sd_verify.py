@@ -31,7 +31,7 @@ SYMBOLS = [
     "sd_fault_word", "sd_set_attention_path", "sd_last_attention_path", "sd_last_attention_launches",
     "sd_project_kv", "sd_set_projector_path", "sd_last_projector_path",
     "sd_set_sample_path", "sd_last_sample_path", "sd_set_wait_test",
-    "sd_commit_tokens", "sd_compact_tree_kv", "sd_project_kv_commit",
+    "sd_commit_tokens", "sd_compact_tree_kv", "sd_store_to_host", "sd_project_kv_commit",
     "sd_latent_compress", "sd_latent_compress_workspace_size",
 ]
 
@@ -111,6 +111,8 @@ def load():
     lib.sd_commit_tokens.restype = _i
     lib.sd_compact_tree_kv.argtypes = [_vp, _vp, Strides, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
     lib.sd_compact_tree_kv.restype = _i
+    lib.sd_store_to_host.argtypes = [_vp, _vp, ctypes.c_int64, _vp]
+    lib.sd_store_to_host.restype = _i
     _i64 = ctypes.c_int64
     lib.sd_project_kv_commit.argtypes = [_vp, _i64, _i64, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp,
                                          _i64, _i64, _i, _i, _vp]
@@ -358,6 +360,21 @@ def sd_compact_tree_kv(k_cache, v_cache, ctx_len, path, n_accepted, stream=None)
     T = path.shape[1]
     _check(load().sd_compact_tree_kv(_p(k_cache), _p(v_cache), _kv_strides(k_cache), _p(ctx_len), _p(path),
                                      _p(n_accepted), B, T, S, Hkv, D, _dt(k_cache), _stream(stream)))
+
+
+def sd_store_to_host(host_dst, src, stream=None):
+    """host_dst: a pinned CPU tensor; src: a CUDA tensor of the same byte size
+    (both contiguous, a multiple of 16 bytes).  Enqueued on the stream; read
+    host_dst after synchronising with it."""
+    if host_dst.is_cuda or not host_dst.is_pinned():
+        raise ValueError("host_dst must be a pinned CPU tensor")
+    _need_cuda(src)
+    if not (host_dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("both tensors must be contiguous")
+    nb = src.numel() * src.element_size()
+    if host_dst.numel() * host_dst.element_size() != nb:
+        raise ValueError("host_dst and src must hold the same number of bytes")
+    _check(load().sd_store_to_host(_p(host_dst), _p(src), nb, _stream(stream)))
 
 
 def sd_project_kv_commit(hidden_block, w_k, w_v, n_accepted, draft_ctx, k_ctx, v_ctx, path=None, stream=None):

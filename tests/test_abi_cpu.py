@@ -90,6 +90,13 @@ def test_host_validation_rejects_bad_arguments(S):
                                 None) == S.SD_ERR_INVALID_ARG
     # philox: negative n
     assert lib.sd_philox4x32_10(fake, 1, fake, -1, None) == S.SD_ERR_INVALID_ARG
+    # host store: negative size, null pointer, a size or address off 16 bytes
+    # (all refused before any CUDA call); an empty store enqueues nothing
+    assert lib.sd_store_to_host(fake, fake, -16, None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_store_to_host(None, fake, 16, None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_store_to_host(fake, fake, 24, None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_store_to_host(ctypes.c_void_p(0x10008), fake, 16, None) == S.SD_ERR_INVALID_ARG
+    assert lib.sd_store_to_host(None, None, 0, None) == S.SD_OK
 
 
 def test_workspace_sizes_are_positive_and_monotone(S):
@@ -119,6 +126,12 @@ def test_binding_refuses_cpu_tensors(S):
     with pytest.raises(ValueError):
         S.sd_verify_attention(q, q, q, torch.zeros(1, dtype=torch.int32), 10, q.float(), 1.0,
                               torch.zeros(8, dtype=torch.uint8))
+
+
+def test_binding_store_to_host_wants_a_pinned_destination(S):
+    import torch
+    with pytest.raises(ValueError):
+        S.sd_store_to_host(torch.zeros(64, dtype=torch.uint8), torch.zeros(64, dtype=torch.uint8))
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
