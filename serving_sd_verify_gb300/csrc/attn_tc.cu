@@ -503,10 +503,11 @@ attn_split_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 #if __CUDA_ARCH__ >= 900
-    // inputs of the upstream kernel are visible past the wait; the dependents'
-    // launch is allowed only after it, so that a dependent overlaps this kernel alone
+    // inputs of the upstream kernel are visible past the wait.  No early
+    // trigger: the dependents launch as this kernel's CTAs exit (an early one
+    // let the next kernel's CTAs occupy the idle SMs only to wait there, and
+    // made a step of the five attention calls and the acceptance slower)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
 
     // the plan: warp 0 works it out, its lane 0 starts the Q copy and its
